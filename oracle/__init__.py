@@ -1,0 +1,210 @@
+"""Python access to the fp64 CPU oracle (``gdn_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the bench's CPU
+baseline / reference arm use this module; the CUDA library and its binding
+never import it.  All arrays crossing into C are contiguous float64 (int32 for
+trims); the layouts are those documented in ``gdn_oracle.h``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Dict, Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C11, IEEE fp64, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(
+            os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "gdn_oracle.h"))):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
+               "-pthread", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Dims(ctypes.Structure):
+    _fields_ = [("n_slots", ctypes.c_int), ("n_qk_heads", ctypes.c_int), ("n_v_heads", ctypes.c_int),
+                ("d_k", ctypes.c_int), ("d_v", ctypes.c_int), ("conv_width", ctypes.c_int),
+                ("n_tokens", ctypes.c_int), ("rms_eps", ctypes.c_double), ("l2_eps", ctypes.c_double),
+                ("q_scale", ctypes.c_double)]
+
+
+_D = ctypes.POINTER(ctypes.c_double)
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(build())
+        _lib.gdno_softplus.restype = ctypes.c_double
+        _lib.gdno_softplus.argtypes = [ctypes.c_double]
+        _lib.gdno_gates.argtypes = [ctypes.c_double] * 4 + [_D, _D]
+        _lib.gdno_l2norm.argtypes = [ctypes.c_int, _D, ctypes.c_double, _D]
+        _lib.gdno_conv_silu.argtypes = [ctypes.c_int] * 3 + [_D, _D, _D]
+        _lib.gdno_delta_step.argtypes = [ctypes.c_int, ctypes.c_int, _D, _D, _D, _D,
+                                         ctypes.c_double, ctypes.c_double, ctypes.c_double, _D]
+        _lib.gdno_rmsnorm_gate.argtypes = [ctypes.c_int, _D, _D, _D, ctypes.c_double, _D]
+        _lib.gdno_verify.argtypes = [ctypes.POINTER(_Dims)] + [_D] * 13 + [ctypes.c_void_p, ctypes.c_int]
+        _lib.gdno_prefill_chunked.argtypes = ([ctypes.POINTER(_Dims), ctypes.c_int] + [_D] * 11 +
+                                              [ctypes.c_void_p, ctypes.c_int])
+        _lib.gdno_rollback.argtypes = [ctypes.POINTER(_Dims), ctypes.c_void_p] + [_D] * 4 + [ctypes.c_void_p]
+    return _lib
+
+
+def _p(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    assert a.dtype == np.float64 and a.flags["C_CONTIGUOUS"], (a.dtype, a.flags)
+    return a.ctypes.data_as(_D)
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def dims(shape, n_tokens: Optional[int] = None, rms_eps=1e-6, l2_eps=1e-6, q_scale=1.0) -> _Dims:
+    return _Dims(shape.n_slots, shape.n_qk_heads, shape.n_v_heads, shape.d_k, shape.d_v,
+                 shape.conv_width, shape.n_tokens if n_tokens is None else n_tokens,
+                 rms_eps, l2_eps, q_scale)
+
+
+# ---- stages ---------------------------------------------------------------
+
+def softplus(x: float) -> float:
+    return lib().gdno_softplus(float(x))
+
+
+def gates(A_log, dt_bias, alpha, beta_raw):
+    g, b = ctypes.c_double(), ctypes.c_double()
+    lib().gdno_gates(float(A_log), float(dt_bias), float(alpha), float(beta_raw),
+                     ctypes.byref(g), ctypes.byref(b))
+    return g.value, b.value
+
+
+def l2norm(x, eps=1e-6):
+    x = _f64(x)
+    out = np.empty_like(x)
+    lib().gdno_l2norm(x.size, _p(x), eps, _p(out))
+    return out
+
+
+def conv_silu(conv_w, win):
+    conv_w, win = _f64(conv_w), _f64(win)
+    W, C = conv_w.shape
+    T = win.shape[0] - (W - 1)
+    y = np.empty((T, C))
+    lib().gdno_conv_silu(W, T, C, _p(conv_w), _p(win), _p(y))
+    return y
+
+
+def delta_step(S, k, v, q, g, beta, q_scale=1.0):
+    """S is logical [d_k][d_v]; returns (S_new, o)."""
+    S = _f64(S).copy()
+    dk, dv = S.shape
+    o = np.empty(dv)
+    lib().gdno_delta_step(dk, dv, _p(S), _p(_f64(k)), _p(_f64(v)), _p(_f64(q)),
+                          float(g), float(beta), float(q_scale), _p(o))
+    return S, o
+
+
+def rmsnorm_gate(o, z, w, eps=1e-6):
+    o, z, w = _f64(o), _f64(z), _f64(w)
+    out = np.empty_like(o)
+    lib().gdno_rmsnorm_gate(o.size, _p(o), _p(z), _p(w), eps, _p(out))
+    return out
+
+
+# ---- composites -----------------------------------------------------------
+
+def _mask(head_mask, n_v_heads):
+    if head_mask is None:
+        return None, None
+    m = np.zeros(n_v_heads, dtype=np.uint8)
+    m[np.asarray(head_mask)] = 1
+    return m, m.ctypes.data_as(ctypes.c_void_p)
+
+
+def verify(shape, x: Dict[str, np.ndarray], capture: bool = True, n_tokens: Optional[int] = None,
+           head_mask=None, n_threads: int = 1, q_scale: float = 1.0,
+           rms_eps: float = 1e-6, l2_eps: float = 1e-6) -> Dict[str, np.ndarray]:
+    """Run the verify forward on fp64 copies of ``x`` (the dict of
+    ``Inputs.as_f64()``).  ``n_tokens`` < shape.n_tokens runs only the first
+    tokens (the prefix re-run).  Returns state, conv_state, out and, with
+    ``capture``, cap_state / cap_conv."""
+    s = shape
+    T = s.n_tokens if n_tokens is None else n_tokens
+    d = dims(s, T, rms_eps, l2_eps, q_scale)
+    B, C, Hv, dk, dv, W = s.n_slots, s.conv_channels, s.n_v_heads, s.d_k, s.d_v, s.conv_width
+    assert x["qkv"].shape[:1] == (B,) and x["qkv"].shape[2] == C and x["qkv"].shape[1] >= T
+    assert x["z"].shape[2] == Hv * dv and x["alpha"].shape[2] == Hv and x["beta_raw"].shape[2] == Hv
+    assert x["state"].shape == (B, Hv, dv, dk) and x["conv_state"].shape == (B, W - 1, C)
+    assert x["conv_w"].shape == (W, C) and x["A_log"].shape == (Hv,) and x["norm_w"].shape == (dv,)
+    qkv = _f64(x["qkv"][:, :T])
+    z = _f64(x["z"][:, :T])
+    alpha = _f64(x["alpha"][:, :T])
+    beta_raw = _f64(x["beta_raw"][:, :T])
+    state = _f64(x["state"]).copy()
+    conv_state = _f64(x["conv_state"]).copy()
+    out = np.zeros((B, T, Hv * dv))
+    cap_state = np.zeros((B, T, Hv, dv, dk)) if capture else None
+    cap_conv = np.zeros((B, W - 1 + T, C)) if capture else None
+    m, mp = _mask(head_mask, Hv)
+    rc = lib().gdno_verify(ctypes.byref(d), _p(_f64(x["conv_w"])), _p(_f64(x["A_log"])),
+                           _p(_f64(x["dt_bias"])), _p(_f64(x["norm_w"])), _p(qkv), _p(z),
+                           _p(alpha), _p(beta_raw), _p(state), _p(conv_state), _p(cap_state),
+                           _p(cap_conv), _p(out), mp, int(n_threads))
+    assert rc == 0
+    res = {"state": state, "conv_state": conv_state, "out": out}
+    if capture:
+        res["cap_state"], res["cap_conv"] = cap_state, cap_conv
+    return res
+
+
+def rollback(shape, trim, state, conv_state, cap_state, cap_conv, n_tokens: Optional[int] = None):
+    """Returns (state, conv_state, slot_status) after rolling back copies."""
+    T = shape.n_tokens if n_tokens is None else n_tokens
+    d = dims(shape, T)
+    s = shape
+    B, C = s.n_slots, s.conv_channels
+    assert np.shape(state) == (B, s.n_v_heads, s.d_v, s.d_k)
+    assert np.shape(conv_state) == (B, s.conv_width - 1, C)
+    assert np.shape(cap_state) == (B, T, s.n_v_heads, s.d_v, s.d_k)
+    assert np.shape(cap_conv) == (B, s.conv_width - 1 + T, C)
+    assert np.size(trim) == B
+    st, cs = _f64(state).copy(), _f64(conv_state).copy()
+    tr = np.ascontiguousarray(trim, dtype=np.int32)
+    status = np.zeros(shape.n_slots, dtype=np.int32)
+    lib().gdno_rollback(ctypes.byref(d), tr.ctypes.data_as(ctypes.c_void_p), _p(st), _p(cs),
+                        _p(_f64(cap_state)), _p(_f64(cap_conv)), status.ctypes.data_as(ctypes.c_void_p))
+    return st, cs, status
+
+
+def prefill_chunked(shape, x: Dict[str, np.ndarray], chunk: int, n_tokens: Optional[int] = None,
+                    head_mask=None, n_threads: int = 1, q_scale: float = 1.0,
+                    rms_eps: float = 1e-6, l2_eps: float = 1e-6) -> Dict[str, np.ndarray]:
+    s = shape
+    T = s.n_tokens if n_tokens is None else n_tokens
+    d = dims(s, T, rms_eps, l2_eps, q_scale)
+    state = _f64(x["state"]).copy()
+    conv_state = _f64(x["conv_state"]).copy()
+    out = np.zeros((s.n_slots, T, s.n_v_heads * s.d_v))
+    m, mp = _mask(head_mask, s.n_v_heads)
+    rc = lib().gdno_prefill_chunked(ctypes.byref(d), int(chunk), _p(_f64(x["conv_w"])),
+                                    _p(_f64(x["A_log"])), _p(_f64(x["dt_bias"])),
+                                    _p(_f64(x["norm_w"])), _p(_f64(x["qkv"][:, :T])),
+                                    _p(_f64(x["z"][:, :T])), _p(_f64(x["alpha"][:, :T])),
+                                    _p(_f64(x["beta_raw"][:, :T])), _p(state), _p(conv_state),
+                                    _p(out), mp, int(n_threads))
+    assert rc == 0
+    return {"state": state, "conv_state": conv_state, "out": out}
