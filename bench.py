@@ -1,0 +1,597 @@
+#!/usr/bin/env python3
+"""Benchmark of the GDN verify hot path on GB300.
+
+One step = one verify forward (conv + SiLU, q/k L2 norm, gates, gated
+delta-rule recurrence with per-position state capture, gated RMSNorm,
+conv-state advance) followed by one rollback, over one batch of seeded
+synthetic inputs already resident in HBM.  Default workload: one GDN layer of
+a 64-layer hybrid target, 1 slot, 16 QK / 48 V heads, d_k = d_v = 128, K+1 =
+16 verify tokens, bf16 activations, fp32 state.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+                    [--workload layer_verify|multislot_verify|stack_verify|prefill]
+
+Prints one JSON line.  ``value`` = verified tokens/s over all ranks (device
+time, CUDA events, steps replayed from CUDA graphs over rotating buffer sets
+whose total exceeds 3x L2).  ``roofline`` is for the dominant kernel
+(verify): algorithmic bytes per launch / its average launch duration.
+``e2e`` = the same metric through the public API with pinned host buffers,
+host->device copies of each step's activations and a device->host read of
+its output inside the timed region.  ``cpu_baseline`` = the fp64 oracle on
+the host cores on a bounded sample.  ``--impl reference`` times the oracle
+alone (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads.synth import WORKLOADS, make_inputs, randint  # noqa: E402
+
+METRIC = "GDN verify tokens/sec at 1 GB300; achieved HBM GB/s vs roofline"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (compulsory traffic) per launch
+# ---------------------------------------------------------------------------
+
+def verify_bytes(s, capture=True) -> int:
+    a = 2 if s.act == "bf16" else 4
+    B, T, C, Hv, dk, dv, W = s.n_slots, s.n_tokens, s.conv_channels, s.n_v_heads, s.d_k, s.d_v, s.conv_width
+    st = B * Hv * dv * dk * 4
+    n = st * 2                                            # state read once, final state written once
+    if capture:
+        n += T * st                                       # one captured state per position
+        n += B * (W - 1 + T) * C * 4                      # conv window capture
+    n += B * T * C * a + B * T * Hv * dv * a * 2          # qkv in, z in, out
+    n += 2 * B * T * Hv * a                               # alpha, beta_raw
+    n += 2 * B * (W - 1) * C * 4                          # conv state read + write
+    n += W * C * 4 + 2 * Hv * 4 + dv * 4                  # parameters
+    return n
+
+
+def rollback_bytes(s, trims) -> int:
+    per_slot = 2 * (s.n_v_heads * s.d_v * s.d_k * 4 + (s.conv_width - 1) * s.conv_channels * 4)
+    return int(np.count_nonzero(np.asarray(trims))) * per_slot + 4 * s.n_slots
+
+
+def prefill_bytes(s) -> int:
+    return verify_bytes(s, capture=False)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha(names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "gated_deltanet_verify_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, sha: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    this exact kernel source and workload; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel, {}).get(workload)
+    if not e or e.get("source_sha") != sha:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def _parse(self, line):
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 8:
+            return None
+        try:
+            return {"sm": float(parts[0]), "max": float(parts[1]), "hw": parts[4], "hw_thermal": parts[5],
+                    "sw_thermal": parts[6], "sw_power": parts[7], "t": time.time()}
+        except ValueError:
+            return None
+
+    def once(self):
+        try:
+            r = subprocess.run(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20)
+            s = self._parse(r.stdout.strip().splitlines()[0]) if r.stdout.strip() else None
+            if s:
+                self.samples.append(s)
+        except Exception:
+            pass
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                s = self._parse(line)
+                if s:
+                    self.samples.append(s)
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s["t"] <= t1] or self.samples
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        reasons = set()
+        for s in inside:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if s[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([s["sm"] for s in inside])),
+                "sm_max_mhz": float(max(s["max"] for s in inside)), "reasons": sorted(reasons),
+                "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# the CUDA arm
+# ---------------------------------------------------------------------------
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class VerifyWorkload:
+    """Rotating buffer sets of one verify+rollback workload (one or more layers)."""
+
+    def __init__(self, shape, device, l2_bytes):
+        import torch
+        import gated_deltanet_verify_gb300 as gdn
+        from workloads.device import empty_outputs, to_device
+        self.gdn, self.torch = gdn, torch
+        self.shape = s = shape
+        self.layers = s.n_layers
+        per_set = verify_bytes(s) * self.layers
+        self.n_sets = 1 if per_set > 3 * l2_bytes else int(min(64, -(-3 * l2_bytes // per_set) + 1))
+        self.dims = gdn.make_dims(s.n_slots, s.n_qk_heads, s.n_v_heads, s.d_k, s.d_v, s.n_tokens,
+                                  gdn.GDN_BF16 if s.act == "bf16" else gdn.GDN_F32)
+        self.sets = []
+        self.host_inputs = []
+        n_layer_inputs = self.layers if self.layers > 1 else 1
+        for li in range(n_layer_inputs):
+            inp = make_inputs(s, layer=li)
+            self.host_inputs.append(inp)
+        trims = randint(s.seed, 12, self.n_sets * self.layers * s.n_slots, s.n_tokens).reshape(
+            self.n_sets, self.layers, s.n_slots)
+        self.trims = trims
+        for k in range(self.n_sets):
+            layers = []
+            for li in range(self.layers):
+                x = to_device(self.host_inputs[li if self.layers > 1 else 0], device)
+                x["trim"] = torch.from_numpy(trims[k, li].astype(np.int32)).to(device)
+                x.update(empty_outputs(s, device))
+                x["status"] = torch.zeros(1, dtype=torch.int32, device=device)
+                x["params"] = gdn.layer_params(x["conv_w"], x["A_log"], x["dt_bias"], x["norm_w"])
+                layers.append(x)
+            self.sets.append(layers)
+        self.tokens_per_step = s.n_slots * s.n_tokens
+        self.kernels_per_step = 2 * self.layers
+
+    def verify(self, k, li, stream):
+        x = self.sets[k][li]
+        self.gdn.gdn_verify_forward(self.dims, x["params"], x["qkv"], x["z"], x["alpha"], x["beta_raw"], x["state"],
+                                    x["conv_state"], x["cap_state"], x["cap_conv"], x["out"], x["status"], stream)
+
+    def rollback(self, k, li, stream):
+        x = self.sets[k][li]
+        self.gdn.gdn_rollback(self.dims, x["trim"], x["state"], x["conv_state"], x["cap_state"], x["cap_conv"],
+                              x["status"], stream)
+
+    def step(self, k, stream):
+        for li in range(self.layers):
+            self.verify(k, li, stream)
+            self.rollback(k, li, stream)
+
+    def step_bytes(self, k):
+        return sum(verify_bytes(self.shape) + rollback_bytes(self.shape, self.trims[k, li])
+                   for li in range(self.layers))
+
+    def e2e(self, steps, device):
+        """Public-API loop with host buffers: H2D activations + trims, verify, rollback, D2H out."""
+        torch = self.torch
+        from workloads.device import act_host
+        s = self.shape
+        inp = self.host_inputs[0]
+        host = {"qkv": act_host(inp.qkv, s).pin_memory(), "z": act_host(inp.z, s).pin_memory(),
+                "alpha": act_host(inp.alpha, s).pin_memory(), "beta_raw": act_host(inp.beta_raw, s).pin_memory(),
+                "trim": torch.from_numpy(self.trims[0, 0].astype(np.int32)).pin_memory()}
+        out_host = torch.empty(self.sets[0][0]["out"].shape, dtype=self.sets[0][0]["out"].dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+        stream = torch.cuda.current_stream()
+        sp = stream.cuda_stream
+
+        def one(k):
+            x = self.sets[k % self.n_sets][0]
+            for key, t in host.items():
+                x[key].copy_(t, non_blocking=True)
+            self.verify(k % self.n_sets, 0, sp)
+            self.rollback(k % self.n_sets, 0, sp)
+            out_host.copy_(x["out"], non_blocking=True)
+            stream.synchronize()
+
+        for k in range(10):
+            one(k)
+        t0 = time.perf_counter()
+        for k in range(steps):
+            one(k)
+        dt = time.perf_counter() - t0
+        return dt, h2d * self.layers, d2h * self.layers
+
+
+class PrefillWorkload:
+    def __init__(self, shape, device, l2_bytes):
+        import torch
+        import gated_deltanet_verify_gb300 as gdn
+        from workloads.device import act_torch_dtype, to_device
+        self.gdn, self.torch = gdn, torch
+        self.shape = s = shape
+        self.layers = 1
+        self.dims = gdn.make_dims(s.n_slots, s.n_qk_heads, s.n_v_heads, s.d_k, s.d_v, s.n_tokens,
+                                  gdn.GDN_BF16 if s.act == "bf16" else gdn.GDN_F32)
+        per_set = prefill_bytes(s)
+        self.n_sets = 1 if per_set > 3 * l2_bytes else 2
+        inp = make_inputs(s)
+        self.host_inputs = [inp]
+        self.ws_bytes = gdn.gdn_prefill_workspace_bytes(self.dims)
+        self.sets = []
+        for _ in range(self.n_sets):
+            x = to_device(inp, device)
+            x["out"] = torch.empty((s.n_slots, s.n_tokens, s.n_v_heads * s.d_v), dtype=act_torch_dtype(s),
+                                   device=device)
+            x["ws"] = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
+            x["status"] = torch.zeros(1, dtype=torch.int32, device=device)
+            x["params"] = gdn.layer_params(x["conv_w"], x["A_log"], x["dt_bias"], x["norm_w"])
+            self.sets.append([x])
+        self.tokens_per_step = s.n_slots * s.n_tokens
+        self.kernels_per_step = None
+
+    def prefill(self, k, li, stream):
+        x = self.sets[k][0]
+        self.gdn.gdn_prefill_chunked(self.dims, x["params"], x["qkv"], x["z"], x["alpha"], x["beta_raw"],
+                                     x["state"], x["conv_state"], x["out"], x["ws"], self.ws_bytes, x["status"],
+                                     stream)
+
+    def step(self, k, stream):
+        self.prefill(k, 0, stream)
+
+    def step_bytes(self, k):
+        return prefill_bytes(self.shape)
+
+
+def capture_graph(torch, fn_list):
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        sp = cs.cuda_stream
+        for f in fn_list:          # one eager pass on the capture stream first (lazy init, attributes)
+            f(sp)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=cs):
+        sp = torch.cuda.current_stream().cuda_stream
+        for f in fn_list:
+            f(sp)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph_steps(torch, wl, steps, graph_len):
+    """Replay graphs of `graph_len` steps (rotating buffer sets) covering exactly `steps` steps."""
+    n_full, rem = divmod(steps, graph_len)
+    fns = [lambda sp, k=k: wl.step(k % wl.n_sets, sp) for k in range(graph_len)]
+    g_full = capture_graph(torch, fns) if n_full else None
+    g_rem = capture_graph(torch, fns[:rem]) if rem else None
+    return g_full, n_full, g_rem
+
+
+def kernel_duration(torch, wl, which, n_launch):
+    """Average duration of one kernel kind: CUDA events around a graph of n_launch back-to-back launches."""
+    fns = []
+    for k in range(n_launch):
+        kk, li = k % wl.n_sets, (k // wl.n_sets) % wl.layers
+        fns.append(lambda sp, kk=kk, li=li: getattr(wl, which)(kk, li, sp))
+    g = capture_graph(torch, fns)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / (reps * n_launch)
+
+
+def run_cuda(args):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    import gated_deltanet_verify_gb300 as gdn
+    gdn.lib()
+
+    shape = WORKLOADS[args.workload]
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
+    wl = PrefillWorkload(shape, device, l2) if args.workload == "prefill" else VerifyWorkload(shape, device, l2)
+    torch.cuda.synchronize()
+
+    graph_len = max(1, min(args.graph_len, args.steps))
+    if args.workload in ("stack_verify", "prefill"):
+        graph_len = 1
+    g_full, n_full, g_rem = time_graph_steps(torch, wl, args.steps, graph_len)
+    g_warm, nw_full, g_wrem = time_graph_steps(torch, wl, args.warmup, graph_len)
+
+    vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    clocks = ClockSampler(int(vis[local]) if len(vis) > local and vis[local].strip().isdigit() else local)
+    clocks.start()
+    # warm-up steps (untimed)
+    for _ in range(nw_full):
+        g_warm.replay()
+    if g_wrem:
+        g_wrem.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks.once()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(n_full):
+        g_full.replay()
+    if g_rem:
+        g_rem.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    clocks.once()
+    dt = e0.elapsed_time(e1) / 1e3
+    # the status words must still read GDN_OK
+    bad = [int(x["status"].item()) for layers in wl.sets for x in layers if int(x["status"].item()) != 0]
+
+    # per-kernel durations (own timed regions, graphs of back-to-back launches)
+    n_launch = max(1, min(64, 8 * wl.n_sets * wl.layers))
+    if args.workload == "prefill":
+        kdur = {"prefill": kernel_duration(torch, wl, "prefill", 2)}
+    else:
+        kdur = {"verify": kernel_duration(torch, wl, "verify", n_launch),
+                "rollback": kernel_duration(torch, wl, "rollback", n_launch)}
+    clocks.stop()
+
+    if world > 1:
+        t = torch.tensor([dt], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt = float(t.item())
+    tokens = wl.tokens_per_step * args.steps * world
+    value = tokens / dt
+    hbm, peak_kind = peaks()
+    if args.workload == "prefill":
+        dom, dom_bytes, dom_src = "prefill", prefill_bytes(shape), ["prefill.cu", "verify.cu", "internal.cuh"]
+    else:
+        dom, dom_bytes, dom_src = "verify", verify_bytes(shape), ["verify.cu", "internal.cuh"]
+    achieved = dom_bytes / kdur[dom] / 1e9
+    sha = kernel_source_sha(dom_src)
+    traffic = recorded_traffic(dom, sha, args.workload)
+
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded splitmix64/Box-Muller)",
+        "config": {
+            "workload": (f"{shape.name}: {shape.n_layers} layer(s) x {shape.n_slots} slot(s), "
+                         f"{shape.n_qk_heads} QK / {shape.n_v_heads} V heads, d_k=d_v={shape.d_k}, "
+                         f"{shape.n_tokens} tokens"),
+            "act_dtype": shape.act, "state_dtype": "f32",
+            "step": "verify+rollback" if args.workload != "prefill" else "chunked prefill",
+            "l2": (f"rotating {wl.n_sets} buffer sets, {wl.n_sets * wl.step_bytes(0) / 1e6:.0f} MB "
+                   f"touched per rotation (> 3x L2 {l2 / 2**20:.0f} MiB)"),
+            "timing": f"CUDA events around CUDA-graph replays of {graph_len} steps",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic, "kernel": dom,
+                     "bytes_per_launch": dom_bytes, "launch_us": kdur[dom] * 1e6,
+                     "peak_source": f"{peak_kind} hbm_gbs" + (" (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                                                               else " (recipe fallback)")},
+        "kernels_us": {k: v * 1e6 for k, v in kdur.items()},
+        "step_bytes": wl.step_bytes(0),
+        "step_gbs": wl.step_bytes(0) * args.steps / dt / 1e9,
+        "gpu_launches": (wl.kernels_per_step * args.steps if wl.kernels_per_step is not None
+                         else args.steps * int(-(-shape.n_tokens // 64))),
+        "clocks": clocks.summary(t_wall0 - 0.5, t_wall1 + 0.5),
+    }
+    if bad:
+        res["device_status_errors"] = bad
+    if args.workload != "prefill" and not args.no_e2e:
+        e_steps = max(20, min(args.steps, 500))
+        edt, h2d, d2h = wl.e2e(e_steps, device)
+        res["e2e"] = {"value": wl.tokens_per_step * e_steps * world / edt, "unit": "tokens/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+                      "timing": "wall clock, host sync per step"}
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(shape, args.cpu_seconds)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res))
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def _oracle_pass(shape, x, heads, n_threads, trims):
+    import oracle
+    if shape.name == "prefill":
+        oracle.verify(shape, x, capture=False, head_mask=heads, n_threads=n_threads)
+        return
+    r = oracle.verify(shape, x, head_mask=heads, n_threads=n_threads)
+    oracle.rollback(shape, trims, r["state"], r["conv_state"], r["cap_state"], r["cap_conv"])
+
+
+def cpu_baseline(shape, seconds):
+    """fp64 oracle, all host cores, on whole value heads of the same workload
+    until about `seconds` of CPU work; tokens/s scaled by the fraction of heads."""
+    import oracle
+    oracle.build()
+    one = shape.with_(n_layers=1)
+    inp = make_inputs(one)
+    x = inp.as_f64()
+    cores = os.cpu_count() or 1
+    heads = list(range(min(cores, shape.n_v_heads)))
+    t0 = time.perf_counter()
+    _oracle_pass(one, x, heads, cores, inp.trim)
+    t_pass = time.perf_counter() - t0
+    reps = max(1, int(seconds / max(t_pass, 1e-3)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        _oracle_pass(one, x, heads, cores, inp.trim)
+    dt = time.perf_counter() - t0
+    frac = len(heads) / shape.n_v_heads
+    tok = one.n_slots * one.n_tokens * frac * reps / shape.n_layers
+    return {"value": tok / dt, "unit": "tokens/s", "cores": min(cores, len(heads)) if shape.n_slots == 1 else cores,
+            "kind": "oracle",
+            "sample": (f"{reps} passes of verify+rollback over {len(heads)} of {shape.n_v_heads} value heads "
+                       f"(all {one.n_slots} slot(s), {one.n_tokens} tokens, 1 layer) of the same workload, fp64, "
+                       f"{dt:.1f} s")}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    shape = WORKLOADS[args.workload]
+    one = shape.with_(n_layers=1)
+    inp = make_inputs(one)
+    x = inp.as_f64()
+    cores = os.cpu_count() or 1
+    # size each step so the whole run stays within ~2 minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    t0 = time.perf_counter()
+    _oracle_pass(one, x, [0], 1, inp.trim)
+    t_head = time.perf_counter() - t0
+    n_heads = int(max(1, min(shape.n_v_heads, cores * max(1.0, budget / max(t_head, 1e-4)))))
+    n_heads = min(n_heads, shape.n_v_heads)
+    heads = list(range(n_heads))
+    for _ in range(args.warmup):
+        _oracle_pass(one, x, heads, cores, inp.trim)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_pass(one, x, heads, cores, inp.trim)
+    dt = time.perf_counter() - t0
+    tok = one.n_slots * one.n_tokens * (n_heads / shape.n_v_heads) * args.steps / shape.n_layers
+    value = tok / dt
+    sample = (f"each step: verify+rollback over {n_heads} of {shape.n_v_heads} value heads of {shape.name} "
+              f"(fp64 oracle, {min(cores, n_heads * one.n_slots)} threads)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded splitmix64/Box-Muller)",
+        "config": {"workload": shape.name, "act_dtype": shape.act, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="layer_verify")
+    ap.add_argument("--graph-len", type=int, default=64)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.workload == "tiny":
+        ap.error("the tiny workload is a parity case, not a bench workload")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cuda(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,149 @@
+"""Python binding of the GB300 Gated DeltaNet verify library (C ABI in
+``include/gdn_verify.h``).
+
+Argument marshalling only: every step runs in the CUDA kernels of
+``libgdn_verify.so``.  Buffers are passed as torch tensors (their
+``data_ptr()``) or raw integer device addresses; the stream defaults to
+torch's current stream.  If the library has not been built the import of
+``lib()`` raises -- there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdn_verify.so")
+
+GDN_OK = 0
+GDN_ERR_ARG = 1
+GDN_ERR_SHAPE = 2
+GDN_ERR_ALIGN = 3
+GDN_ERR_DTYPE = 4
+GDN_ERR_TRIM_RANGE = 5
+GDN_ERR_NO_CAPTURE = 6
+GDN_ERR_LAUNCH = 7
+GDN_ERR_TIMEOUT = 8
+GDN_ERR_WORKSPACE = 9
+STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_ALIGN", 4: "GDN_ERR_DTYPE",
+                5: "GDN_ERR_TRIM_RANGE", 6: "GDN_ERR_NO_CAPTURE", 7: "GDN_ERR_LAUNCH", 8: "GDN_ERR_TIMEOUT",
+                9: "GDN_ERR_WORKSPACE"}
+
+GDN_F32 = 0
+GDN_BF16 = 1
+
+EXPORTED_SYMBOLS = ("gdn_verify_forward", "gdn_rollback", "gdn_prefill_workspace_bytes",
+                    "gdn_prefill_chunked", "gdn_last_error", "gdn_version")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("n_slots", ctypes.c_int), ("n_qk_heads", ctypes.c_int), ("n_v_heads", ctypes.c_int),
+                ("d_k", ctypes.c_int), ("d_v", ctypes.c_int), ("conv_width", ctypes.c_int),
+                ("n_tokens", ctypes.c_int), ("act_dtype", ctypes.c_int), ("rms_eps", ctypes.c_float),
+                ("l2_eps", ctypes.c_float), ("q_scale", ctypes.c_float)]
+
+
+class LayerParams(ctypes.Structure):
+    _fields_ = [("conv_w", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+                ("norm_w", ctypes.c_void_p)]
+
+
+def make_dims(n_slots: int, n_qk_heads: int, n_v_heads: int, d_k: int, d_v: int, n_tokens: int,
+              act_dtype: int = GDN_BF16, conv_width: int = 4, rms_eps: float = 1e-6,
+              l2_eps: float = 1e-6, q_scale: float = 1.0) -> Dims:
+    return Dims(n_slots, n_qk_heads, n_v_heads, d_k, d_v, conv_width, n_tokens, act_dtype,
+                rms_eps, l2_eps, q_scale)
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it was not built (no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, ip = ctypes.c_void_p, ctypes.c_int
+        L.gdn_verify_forward.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 11
+        L.gdn_verify_forward.restype = ip
+        L.gdn_rollback.argtypes = [ctypes.POINTER(Dims)] + [vp] * 7
+        L.gdn_rollback.restype = ip
+        L.gdn_prefill_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
+        L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
+        L.gdn_prefill_chunked.argtypes = ([ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 8 +
+                                          [ctypes.c_size_t, vp, vp])
+        L.gdn_prefill_chunked.restype = ip
+        L.gdn_last_error.restype = ctypes.c_char_p
+        L.gdn_version.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int) -> None:
+    if rc != GDN_OK:
+        raise GdnError(rc, gdn_last_error())
+
+
+def layer_params(conv_w, A_log, dt_bias, norm_w) -> LayerParams:
+    return LayerParams(_ptr(conv_w), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w))
+
+
+def gdn_last_error() -> str:
+    return lib().gdn_last_error().decode()
+
+
+def gdn_version() -> str:
+    return lib().gdn_version().decode()
+
+
+def gdn_verify_forward(dims: Dims, params: LayerParams, qkv, z, alpha, beta_raw, state, conv_state,
+                       cap_state=None, cap_conv=None, out=None, d_status=None, stream=None) -> None:
+    _check(lib().gdn_verify_forward(ctypes.byref(dims), ctypes.byref(params), _ptr(qkv), _ptr(z),
+                                    _ptr(alpha), _ptr(beta_raw), _ptr(state), _ptr(conv_state),
+                                    _ptr(cap_state), _ptr(cap_conv), _ptr(out), _ptr(d_status),
+                                    _stream(stream)))
+
+
+def gdn_rollback(dims: Dims, d_trim, state, conv_state, cap_state, cap_conv, d_status=None,
+                 stream=None) -> None:
+    _check(lib().gdn_rollback(ctypes.byref(dims), _ptr(d_trim), _ptr(state), _ptr(conv_state),
+                              _ptr(cap_state), _ptr(cap_conv), _ptr(d_status), _stream(stream)))
+
+
+def gdn_prefill_workspace_bytes(dims: Dims) -> int:
+    return int(lib().gdn_prefill_workspace_bytes(ctypes.byref(dims)))
+
+
+def gdn_prefill_chunked(dims: Dims, params: LayerParams, qkv, z, alpha, beta_raw, state, conv_state, out,
+                        workspace=None, ws_bytes: int = 0, d_status=None, stream=None) -> None:
+    _check(lib().gdn_prefill_chunked(ctypes.byref(dims), ctypes.byref(params), _ptr(qkv), _ptr(z),
+                                     _ptr(alpha), _ptr(beta_raw), _ptr(state), _ptr(conv_state), _ptr(out),
+                                     _ptr(workspace), ctypes.c_size_t(ws_bytes), _ptr(d_status),
+                                     _stream(stream)))

@@ -1,0 +1,210 @@
+// gdn_api.cu -- the C ABI declared in include/gdn_verify.h: argument
+// validation, launch-shape choice and error reporting.  No allocation, no
+// synchronisation: every call only enqueues work on the caller's stream.
+#include "internal.cuh"
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <string>
+
+namespace gdn {
+size_t verify_smem_bytes(int T, int dk, int dv, int P, int act_bytes);
+size_t prefill_workspace_bytes(const gdn_dims &d);
+int prefill_check(const gdn_dims &d, std::string &why);
+cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const void *qkv, const void *z,
+                           const void *alpha, const void *beta_raw, float *state, float *conv_state,
+                           void *out, void *workspace, int *d_status, cudaStream_t stream);
+}  // namespace gdn
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DevInfo {
+    int sms = 0, smem_optin = 0;
+};
+
+DevInfo dev_info() {
+    int dev = 0;
+    DevInfo d;
+    if (cudaGetDevice(&dev) != cudaSuccess) return d;
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    return d;
+}
+
+// Basic shape checks common to every call.
+int check_common(const gdn_dims *d) {
+    if (!d) return fail(GDN_ERR_ARG, "dims is NULL");
+    if (d->n_slots < 1 || d->n_qk_heads < 1 || d->n_v_heads < 1 || d->d_k < 1 || d->d_v < 1 ||
+        d->n_tokens < 1)
+        return fail(GDN_ERR_SHAPE, "dims must be positive (slots %d, H_k %d, H_v %d, d_k %d, d_v %d, T %d)",
+                    d->n_slots, d->n_qk_heads, d->n_v_heads, d->d_k, d->d_v, d->n_tokens);
+    if (d->n_v_heads % d->n_qk_heads != 0)
+        return fail(GDN_ERR_SHAPE, "n_v_heads (%d) must be a multiple of n_qk_heads (%d)", d->n_v_heads,
+                    d->n_qk_heads);
+    if (d->conv_width != 4) return fail(GDN_ERR_SHAPE, "conv_width must be 4 (got %d)", d->conv_width);
+    if (d->act_dtype != GDN_F32 && d->act_dtype != GDN_BF16)
+        return fail(GDN_ERR_DTYPE, "act_dtype %d is neither GDN_F32 nor GDN_BF16", int(d->act_dtype));
+    if (!(d->rms_eps >= 0.f) || !(d->l2_eps >= 0.f)) return fail(GDN_ERR_ARG, "eps must be >= 0");
+    return GDN_OK;
+}
+
+long long conv_channels(const gdn_dims *d) {
+    return 2LL * d->n_qk_heads * d->d_k + (long long)d->n_v_heads * d->d_v;
+}
+
+int check_params(const gdn_layer_params *p) {
+    if (!p) return fail(GDN_ERR_ARG, "params is NULL");
+    if (!p->conv_w || !p->A_log || !p->dt_bias || !p->norm_w)
+        return fail(GDN_ERR_ARG, "a layer parameter pointer is NULL");
+    if (!aligned16(p->conv_w) || !aligned16(p->A_log) || !aligned16(p->dt_bias) || !aligned16(p->norm_w))
+        return fail(GDN_ERR_ALIGN, "layer parameter pointers must be 16-byte aligned");
+    return GDN_OK;
+}
+
+}  // namespace
+
+namespace gdn {
+
+// CTAs per value head: as many as the cluster allows (portable size 8) while a
+// CTA keeps at most 16 warps of 8 rows; more CTAs spread a small batch over
+// more SMs, whose store bandwidth is what the capture needs.
+int verify_parts_per_head(int B, int Hv, int r, int dv, int sm_count) {
+    (void)B; (void)Hv; (void)sm_count;
+    const int warps_head = dv / 8;
+    int best = 0;
+    for (int P = 1; P <= warps_head; P *= 2) {
+        if (warps_head % P) continue;
+        if (warps_head / P > 16) continue;
+        if (r * P <= 8) best = P;
+    }
+    if (best) return best;
+    for (int P = 1; P <= warps_head; P *= 2) {             // non-portable cluster sizes up to 16
+        if (warps_head % P || warps_head / P > 16) continue;
+        if (r * P <= 16) return P;
+    }
+    return 0;
+}
+
+}  // namespace gdn
+
+extern "C" {
+
+const char *gdn_last_error(void) { return g_err.c_str(); }
+
+const char *gdn_version(void) { return "gdn-verify 0.1.0 (sm_103a)"; }
+
+int gdn_verify_forward(const gdn_dims *dims, const gdn_layer_params *params, const void *qkv,
+                       const void *z, const void *alpha, const void *beta_raw, float *state,
+                       float *conv_state, float *cap_state, float *cap_conv, void *out, int *d_status,
+                       void *stream) {
+    (void)d_status;
+    g_err.clear();
+    int rc = check_common(dims);
+    if (rc) return rc;
+    if ((rc = check_params(params))) return rc;
+    const gdn_dims &d = *dims;
+    if (d.d_k != 32 && d.d_k != 64 && d.d_k != 128)
+        return fail(GDN_ERR_SHAPE, "d_k must be 32, 64 or 128 (got %d)", d.d_k);
+    if (d.d_v % 8 || d.d_v > 256) return fail(GDN_ERR_SHAPE, "d_v must be a multiple of 8 up to 256 (got %d)", d.d_v);
+    if (d.n_tokens > 64) return fail(GDN_ERR_SHAPE, "n_tokens must be <= 64 for verify (got %d)", d.n_tokens);
+    if (d.n_slots > 65535) return fail(GDN_ERR_SHAPE, "n_slots must be <= 65535");
+    if (!qkv || !z || !alpha || !beta_raw || !state || !conv_state || !out)
+        return fail(GDN_ERR_ARG, "a required buffer pointer is NULL");
+    const void *ptrs[] = {qkv, z, alpha, beta_raw, state, conv_state, cap_state, cap_conv, out};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return fail(GDN_ERR_ALIGN, "buffer %p is not 16-byte aligned", p);
+    const int r = d.n_v_heads / d.n_qk_heads;
+    const DevInfo info = dev_info();
+    const int P = gdn::verify_parts_per_head(d.n_slots, d.n_v_heads, r, d.d_v, info.sms);
+    if (P == 0) return fail(GDN_ERR_SHAPE, "H_v/H_k = %d is too large for one thread-block cluster", r);
+    const int act_bytes = d.act_dtype == GDN_BF16 ? 2 : 4;
+    const size_t smem = gdn::verify_smem_bytes(d.n_tokens, d.d_k, d.d_v, P, act_bytes);
+    if (info.smem_optin > 0 && smem > size_t(info.smem_optin))
+        return fail(GDN_ERR_SHAPE, "verify needs %zu bytes of shared memory per CTA (max %d)", smem,
+                    info.smem_optin);
+
+    gdn::VerifyArgs a{};
+    a.B = d.n_slots; a.Hk = d.n_qk_heads; a.Hv = d.n_v_heads; a.dk = d.d_k; a.dv = d.d_v;
+    a.T = d.n_tokens; a.Ts = d.n_tokens; a.C = int(conv_channels(&d)); a.r = r; a.P = P;
+    a.rms_eps = d.rms_eps; a.l2_eps = d.l2_eps; a.q_scale = d.q_scale;
+    a.conv_w = params->conv_w; a.A_log = params->A_log; a.dt_bias = params->dt_bias; a.norm_w = params->norm_w;
+    a.qkv = qkv; a.z = z; a.alpha = alpha; a.beta_raw = beta_raw;
+    a.state = state; a.conv_state = conv_state; a.cap_state = cap_state; a.cap_conv = cap_conv; a.out = out;
+    cudaError_t e = gdn::launch_verify(a, d.act_dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "verify launch failed: %s", cudaGetErrorString(e));
+    return GDN_OK;
+}
+
+int gdn_rollback(const gdn_dims *dims, const int32_t *d_trim, float *state, float *conv_state,
+                 const float *cap_state, const float *cap_conv, int *d_status, void *stream) {
+    g_err.clear();
+    int rc = check_common(dims);
+    if (rc) return rc;
+    const gdn_dims &d = *dims;
+    if (d.n_slots > 65535) return fail(GDN_ERR_SHAPE, "n_slots must be <= 65535");
+    if ((d.d_k % 4) || (d.d_v % 8)) return fail(GDN_ERR_SHAPE, "d_k must be a multiple of 4 and d_v of 8");
+    if (!d_trim || !state || !conv_state) return fail(GDN_ERR_ARG, "trim, state or conv_state is NULL");
+    if (!cap_state || !cap_conv) return fail(GDN_ERR_NO_CAPTURE, "rollback needs both capture buffers");
+    const void *ptrs[] = {d_trim, state, conv_state, cap_state, cap_conv};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(GDN_ERR_ALIGN, "buffer %p is not 16-byte aligned", p);
+    gdn::RollbackArgs a{};
+    a.B = d.n_slots; a.T = d.n_tokens; a.W1 = d.conv_width - 1;
+    a.C = conv_channels(&d);
+    a.state_elems = (long long)d.n_v_heads * d.d_v * d.d_k;
+    a.conv_elems = (long long)a.W1 * a.C;
+    a.trim = d_trim; a.state = state; a.conv_state = conv_state; a.cap_state = cap_state; a.cap_conv = cap_conv;
+    a.d_status = d_status;
+    cudaError_t e = gdn::launch_rollback(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "rollback launch failed: %s", cudaGetErrorString(e));
+    return GDN_OK;
+}
+
+size_t gdn_prefill_workspace_bytes(const gdn_dims *dims) {
+    if (!dims) return 0;
+    std::string why;
+    if (check_common(dims) != GDN_OK || gdn::prefill_check(*dims, why) != GDN_OK) return 0;
+    return gdn::prefill_workspace_bytes(*dims);
+}
+
+int gdn_prefill_chunked(const gdn_dims *dims, const gdn_layer_params *params, const void *qkv, const void *z,
+                        const void *alpha, const void *beta_raw, float *state, float *conv_state, void *out,
+                        void *workspace, size_t ws_bytes, int *d_status, void *stream) {
+    g_err.clear();
+    int rc = check_common(dims);
+    if (rc) return rc;
+    if ((rc = check_params(params))) return rc;
+    std::string why;
+    if ((rc = gdn::prefill_check(*dims, why))) return fail(rc, "%s", why.c_str());
+    if (!qkv || !z || !alpha || !beta_raw || !state || !conv_state || !out)
+        return fail(GDN_ERR_ARG, "a required buffer pointer is NULL");
+    const void *ptrs[] = {qkv, z, alpha, beta_raw, state, conv_state, out};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(GDN_ERR_ALIGN, "buffer %p is not 16-byte aligned", p);
+    const size_t need = gdn::prefill_workspace_bytes(*dims);
+    if (need > 0 && (!workspace || ws_bytes < need))
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need, ws_bytes);
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(GDN_ERR_ALIGN, "workspace must be 256-byte aligned");
+    cudaError_t e = gdn::launch_prefill(*dims, *params, qkv, z, alpha, beta_raw, state, conv_state, out,
+                                        workspace, d_status, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "prefill launch failed: %s", cudaGetErrorString(e));
+    return GDN_OK;
+}
+
+}  // extern "C"

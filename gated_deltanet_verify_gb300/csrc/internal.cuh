@@ -1,0 +1,43 @@
+// internal.cuh -- argument blocks shared by the C-ABI layer and the kernels.
+// Not part of the public interface (that is include/gdn_verify.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "gdn_verify.h"
+
+namespace gdn {
+
+// Everything one verify launch needs, validated on the host.
+struct VerifyArgs {
+    int B, Hk, Hv, dk, dv, T, C, r;   // C: conv channels; r = Hv / Hk
+    int Ts;                           // tokens per slot in the activation buffers (>= T)
+    int P;                            // CTAs per value head (each owns d_v / P rows)
+    float rms_eps, l2_eps, q_scale;
+    const float *conv_w, *A_log, *dt_bias, *norm_w;
+    const void *qkv, *z, *alpha, *beta_raw;
+    float *state, *conv_state, *cap_state, *cap_conv;
+    void *out;
+};
+
+struct RollbackArgs {
+    int B, T, W1;                 // W1 = conv_width - 1
+    long long state_elems;        // floats per slot state (H_v * d_v * d_k)
+    long long conv_elems;         // floats per slot conv state (W1 * C)
+    long long C;
+    const int32_t *trim;
+    float *state, *conv_state;
+    const float *cap_state, *cap_conv;
+    int *d_status;
+};
+
+// Returns a cudaError_t of the launch (cudaSuccess when enqueued).
+cudaError_t launch_verify(const VerifyArgs &a, gdn_dtype act, cudaStream_t stream);
+cudaError_t launch_rollback(const RollbackArgs &a, cudaStream_t stream);
+
+// Choice of CTAs per value head for a verify launch (host heuristic).
+int verify_parts_per_head(int B, int Hv, int r, int dv, int sm_count);
+
+}  // namespace gdn

@@ -1,0 +1,73 @@
+// rollback.cu -- per-slot rollback of the GDN state to the last accepted token.
+//
+// hf2q qwen35_target.rs, DFlashTarget::rollback_kv: trim 0 is a no-op and
+// accepted_idx = n_tokens_max - 1 - trim.  internal.h, DeltaNetCapture: the
+// state comes from capture element accepted_idx and the conv state from
+// window rows [commit_n .. commit_n + kernel - 2], commit_n = accepted_idx + 1.
+//
+// A pure copy, so HBM-bound: grid (blocks_per_slot, B); every block reads the
+// slot's trim from device memory (the call can live in a CUDA graph), and
+// copies its share of the 16-byte vectors with several loads in flight per
+// thread.  A slot with an invalid trim is left untouched and reported through
+// the status word.
+#include "internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+__device__ __forceinline__ float4 ld_nc4(const float4 *p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__global__ void __launch_bounds__(kThreads) rollback_kernel(const RollbackArgs a) {
+    const int s = blockIdx.y;
+    const int trim = __ldg(a.trim + s);
+    if (trim == 0) return;                                   // nothing to discard
+    if (trim < 0 || trim >= a.T) {                           // more than was verified
+        if (blockIdx.x == 0 && threadIdx.x == 0 && a.d_status)
+            atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TRIM_RANGE));
+        return;
+    }
+    const int accepted_idx = a.T - 1 - trim;
+    const long long n4_state = a.state_elems / 4, n4_conv = a.conv_elems / 4;
+    const float4 *src_s = reinterpret_cast<const float4 *>(a.cap_state + (size_t(s) * a.T + accepted_idx) * a.state_elems);
+    float4 *dst_s = reinterpret_cast<float4 *>(a.state + size_t(s) * a.state_elems);
+    const float4 *src_c = reinterpret_cast<const float4 *>(
+        a.cap_conv + (size_t(s) * (a.W1 + a.T) + accepted_idx + 1) * a.C);
+    float4 *dst_c = reinterpret_cast<float4 *>(a.conv_state + size_t(s) * a.conv_elems);
+
+    const long long total = n4_state + n4_conv;
+    const long long stride = (long long)gridDim.x * kThreads;
+    long long i = (long long)blockIdx.x * kThreads + threadIdx.x;
+    for (; i + (kUnroll - 1) * stride < n4_state; i += kUnroll * stride) {
+        float4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = ld_nc4(src_s + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) dst_s[i + u * stride] = v[u];
+    }
+    for (; i < total; i += stride) {
+        if (i < n4_state) dst_s[i] = ld_nc4(src_s + i);
+        else dst_c[i - n4_state] = ld_nc4(src_c + (i - n4_state));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_rollback(const RollbackArgs &a, cudaStream_t stream) {
+    const long long n4 = (a.state_elems + a.conv_elems) / 4;
+    long long per_slot = (n4 + (long long)kThreads * kUnroll - 1) / ((long long)kThreads * kUnroll);
+    if (per_slot < 1) per_slot = 1;
+    if (per_slot > 65535) per_slot = 65535;
+    rollback_kernel<<<dim3(unsigned(per_slot), unsigned(a.B), 1), kThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

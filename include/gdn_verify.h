@@ -1,0 +1,160 @@
+/*
+ * gdn_verify.h -- C ABI of the GB300 (sm_103a) Gated DeltaNet verify library.
+ *
+ * The library runs the Gated DeltaNet linear-attention block of a hybrid
+ * (full-attention + GDN) model over a speculative-decode verify batch of T =
+ * K+1 tokens, captures the recurrent and conv state after every position, and
+ * rolls a slot back to the state after its last accepted token.  It also runs
+ * a chunkwise prefill of the same block over a long prompt.
+ *
+ * Math (gated delta rule; Yang, Kautz & Hatamizadeh, "Gated Delta Networks",
+ * ICLR 2025), per slot and value head h with key head kh = h / (H_v / H_k):
+ *   window  = concat(conv_state, qkv tokens); y_t = SiLU(sum_j conv_w[j] * window[t+j])
+ *   q^, k^  = L2-normalised (eps l2_eps) key-head slices of y_t; v = value-head slice
+ *   g_t     = exp(-exp(A_log[h]) * softplus(alpha_t + dt_bias[h])), beta_t = sigmoid(beta_raw_t)
+ *   S_t     = g_t S_{t-1} + beta_t k^ (v - (g_t S_{t-1})^T k^)^T,   o_t = q_scale * S_t^T q^
+ *   out_t   = o_t / sqrt(mean(o_t^2) + rms_eps) * norm_w * SiLU(z_t)
+ *
+ * Structure and storage follow the lucebox-hub page server/src/internal.h:
+ * "Target cache" (GDN recurrent state [S_v,S_v,H_v] f32 and conv state
+ * [(kernel-1), conv_channels] f32 per layer, persistent and pre-allocated),
+ * the per-step capture buffers ssm_intermediate / conv_input_cache (state
+ * after verify token t; the concatenated conv window), TargetWeights GDN dims
+ * (ssm_d_conv 4, rms_eps 1e-6), and TargetLayer's GDN tensors (fused wqkv
+ * stream, z gate, ssm_conv1d [kernel,dim], per-head A and dt bias, ssm_norm
+ * [head_v_dim]).  Rollback follows the hf2q page qwen35_target.rs,
+ * DFlashTarget::rollback_kv (trim 0 is a no-op; accepted_idx = n_tokens_max
+ * - 1 - trim; per-slot isolation).
+ *
+ * Conventions
+ *  - Every buffer is caller-owned device memory (except the dims / params
+ *    structs, which are host memory read during the call).  The library never
+ *    allocates, frees or synchronises; work is enqueued on `stream` (a
+ *    cudaStream_t passed as void*; NULL = the legacy default stream) and the
+ *    call returns as soon as it is enqueued.  Calls may be captured into a
+ *    CUDA graph.
+ *  - Every device pointer must be 16-byte aligned (GDN_ERR_ALIGN otherwise).
+ *  - A non-OK return means nothing was enqueued; gdn_last_error() (per
+ *    thread) then describes the problem.  Problems only the device can see
+ *    are written to *d_status (a device int the caller zeroes; may be NULL):
+ *    the first error code wins.  No kernel traps, asserts or waits unbounded.
+ *
+ * Layouts (row-major, last index fastest; B = n_slots, T = n_tokens,
+ * C = 2*H_k*d_k + H_v*d_v conv channels ordered [q | k | v], head-major):
+ *   qkv        [B][T][C]            act_dtype   (projected, pre-conv)
+ *   z          [B][T][H_v*d_v]      act_dtype
+ *   alpha      [B][T][H_v]          act_dtype
+ *   beta_raw   [B][T][H_v]          act_dtype
+ *   out        [B][T][H_v*d_v]      act_dtype
+ *   conv_w     [W][C] f32, A_log [H_v] f32, dt_bias [H_v] f32, norm_w [d_v] f32
+ *   state      [B][H_v][d_v][d_k] f32   (element (j,i) = S[i][j]; d_k contiguous)
+ *   conv_state [B][W-1][C] f32          (last W-1 raw qkv inputs per channel)
+ *   cap_state  [B][T][H_v][d_v][d_k] f32   (state after token t)
+ *   cap_conv   [B][W-1+T][C] f32        (concat(conv_state, qkv) window)
+ */
+#ifndef GDN_VERIFY_H
+#define GDN_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_ARG = 1,         /* a required pointer is NULL or an enum is invalid */
+    GDN_ERR_SHAPE = 2,       /* dims outside what the kernels support (see each call) */
+    GDN_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned */
+    GDN_ERR_DTYPE = 4,       /* act_dtype not supported for this call */
+    GDN_ERR_TRIM_RANGE = 5,  /* (device) a slot's trim is outside [0, T-1]; slot left untouched */
+    GDN_ERR_NO_CAPTURE = 6,  /* rollback asked without capture buffers */
+    GDN_ERR_LAUNCH = 7,      /* the CUDA launch itself failed (message in gdn_last_error) */
+    GDN_ERR_TIMEOUT = 8,     /* (device) a bounded wait gave up */
+    GDN_ERR_WORKSPACE = 9    /* workspace missing or smaller than the query returned */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+typedef struct {
+    int n_slots;       /* B >= 1: independent sequences ("slots"), each with its own state */
+    int n_qk_heads;    /* H_k >= 1 */
+    int n_v_heads;     /* H_v, a multiple of H_k; value head h reads key head h / (H_v/H_k) */
+    int d_k;           /* key head dim: 32, 64 or 128 */
+    int d_v;           /* value head dim: a multiple of 8, 8..256 */
+    int conv_width;    /* W: must be 4 (ssm_d_conv) */
+    int n_tokens;      /* T: verify positions (K+1), or prompt length for prefill */
+    gdn_dtype act_dtype;
+    float rms_eps;     /* gated RMSNorm epsilon (1e-6) */
+    float l2_eps;      /* q/k L2-norm epsilon (1e-6) */
+    float q_scale;     /* read-out scale on q (1.0 = none; 1/sqrt(d_k) is common) */
+} gdn_dims;
+
+typedef struct {
+    const float *conv_w;   /* [W][C] depthwise conv weights, tap W-1 meets the current token */
+    const float *A_log;    /* [H_v] log of the decay rate magnitude */
+    const float *dt_bias;  /* [H_v] bias added to alpha before softplus */
+    const float *norm_w;   /* [d_v] RMSNorm weight shared by all value heads */
+} gdn_layer_params;
+
+/*
+ * Verify forward over T positions.  Reads qkv/z/alpha/beta_raw and the layer
+ * params; updates state and conv_state IN PLACE to "after all T tokens";
+ * writes out.  If cap_state is non-NULL it receives, for every position t,
+ * the state after token t (internal.h, ssm_intermediate: "element t ... holds
+ * the DeltaNet recurrent state after processing verify token t"), so
+ * cap_state[:, T-1] equals the new state bit for bit.  If cap_conv is non-NULL
+ * it receives the concat(old conv_state, qkv) window (internal.h,
+ * conv_input_cache).  Supported: 1 <= T <= 64, d_k in {32,64,128}, d_v % 8 ==
+ * 0 and d_v <= 256, H_v/H_k <= 16, W == 4, act_dtype f32 or bf16.
+ * d_status may be NULL (the verify kernel reports nothing through it).
+ */
+int gdn_verify_forward(const gdn_dims *dims, const gdn_layer_params *params,
+                       const void *qkv, const void *z, const void *alpha, const void *beta_raw,
+                       float *state, float *conv_state, float *cap_state, float *cap_conv,
+                       void *out, int *d_status, void *stream);
+
+/*
+ * Rollback after a verify of T = dims->n_tokens positions (hf2q qwen35_target.rs,
+ * rollback_kv).  d_trim is a DEVICE int32[B] (so the call can sit in a CUDA
+ * graph).  Per slot s: trim 0 = no-op (no bytes moved); 1 <= trim <= T-1:
+ * accepted_idx = T-1-trim, state[s] = cap_state[s][accepted_idx] and
+ * conv_state[s] = cap_conv[s][accepted_idx+1 .. accepted_idx+W-1] (the window
+ * rows [commit_n .. commit_n+kernel-2] of internal.h with commit_n =
+ * accepted_idx+1); any other trim leaves the slot untouched and writes
+ * GDN_ERR_TRIM_RANGE to *d_status.  Slots are independent.  cap_state or
+ * cap_conv NULL -> GDN_ERR_NO_CAPTURE (the page skips silently; this ABI
+ * reports).  Only state/conv_state of the rolled-back slots change.
+ */
+int gdn_rollback(const gdn_dims *dims, const int32_t *d_trim, float *state, float *conv_state,
+                 const float *cap_state, const float *cap_conv, int *d_status, void *stream);
+
+/* Bytes of device workspace gdn_prefill_chunked needs for these dims (0 on bad dims). */
+size_t gdn_prefill_workspace_bytes(const gdn_dims *dims);
+
+/*
+ * Chunkwise prefill of a prompt of L = dims->n_tokens tokens per slot (any
+ * L >= 1; chunks of 64, the last one may be partial).  Same inputs/outputs as
+ * gdn_verify_forward with T = L, no capture (a prefill-only cache skips the
+ * rollback tensors: internal.h, create_target_cache, prefill_only).  Updates
+ * state and conv_state in place.  workspace: caller-owned device scratch of
+ * at least gdn_prefill_workspace_bytes(dims) bytes, 256-byte aligned; its
+ * contents need no initialisation and are garbage afterwards.  Supported:
+ * d_k == d_v == 128, W == 4, act_dtype bf16 or f32.
+ */
+int gdn_prefill_chunked(const gdn_dims *dims, const gdn_layer_params *params,
+                        const void *qkv, const void *z, const void *alpha, const void *beta_raw,
+                        float *state, float *conv_state, void *out,
+                        void *workspace, size_t ws_bytes, int *d_status, void *stream);
+
+/* Message for the last non-OK return on this thread ("" if none). */
+const char *gdn_last_error(void);
+
+/* Library version string. */
+const char *gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_VERIFY_H */

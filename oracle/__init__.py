@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 from typing import Dict, Optional
 
@@ -21,15 +22,23 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 
+def _foreign() -> bool:
+    """True if the existing library was built for another host architecture."""
+    marker = _LIB + ".machine"
+    return not os.path.exists(marker) or open(marker).read().strip() != platform.machine()
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (plain C11, IEEE fp64, no FMA contraction)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(
+    if force or _foreign() or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(
             os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "gdn_oracle.h"))):
         tmp = _LIB + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
                "-pthread", "-o", tmp, _SRC, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
+        with open(_LIB + ".machine", "w") as fh:
+            fh.write(platform.machine() + "\n")
     return _LIB
 
 
