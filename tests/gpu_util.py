@@ -24,7 +24,7 @@ def prefix(x: Dict[str, torch.Tensor], n_tokens: int) -> Dict[str, torch.Tensor]
     """The first n_tokens positions of every slot's activations (contiguous copies)."""
     y = dict(x)
     for k in ("qkv", "z", "alpha", "beta_raw"):
-        y[k] = x[k][:, :n_tokens].contiguous()
+        y[k] = x[k][:, :n_tokens].clone(memory_format=torch.contiguous_format)
     y["state"] = x["state"].clone()
     y["conv_state"] = x["conv_state"].clone()
     return y

@@ -103,7 +103,8 @@ def test_slot_isolation_bitwise():
     full = as_f64(run_verify(shape, {k: v.clone() for k, v in x.items()}))
     one = shape.with_(n_slots=1)
     for b in range(4):
-        xb = {k: (v[b:b + 1].contiguous() if k in ("qkv", "z", "alpha", "beta_raw", "state", "conv_state", "trim")
+        # fresh allocations: a slice of a slot would not be 16-byte aligned in general
+        xb = {k: (v[b:b + 1].clone() if k in ("qkv", "z", "alpha", "beta_raw", "state", "conv_state", "trim")
                   else v) for k, v in x.items()}
         rb = as_f64(run_verify(one, xb))
         for k in ("state", "conv_state", "out", "cap_state", "cap_conv"):
@@ -140,7 +141,7 @@ def test_rollback_bit_identical_to_capture_and_prefix_rerun():
         assert np.array_equal(cs[b], capc[b, idx + 1: idx + 4])
         # a GPU re-run of only the accepted prefix from the pre-verify state
         one = shape.with_(n_slots=1)
-        xb = {k: (v[b:b + 1].contiguous() if k in ("qkv", "z", "alpha", "beta_raw", "state", "conv_state")
+        xb = {k: (v[b:b + 1].clone() if k in ("qkv", "z", "alpha", "beta_raw", "state", "conv_state")
                   else v) for k, v in x0.items()}
         rr = as_f64(run_verify(one, prefix(xb, idx + 1), capture=False, n_tokens=idx + 1))
         assert np.array_equal(rr["state"][0], st[b]), f"slot {b}: prefix re-run differs"
