@@ -27,6 +27,10 @@ __device__ __forceinline__ float4 ld_nc4(const float4 *p) {
 }
 
 __global__ void __launch_bounds__(kThreads) rollback_kernel(const RollbackArgs a) {
+    // programmatic dependent launch: wait for the previous kernel's writes
+    // (captures, trims), then let the next kernel start launching
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int s = blockIdx.y;
     const int trim = __ldg(a.trim + s);
     if (trim == 0) return;                                   // nothing to discard
@@ -66,8 +70,16 @@ cudaError_t launch_rollback(const RollbackArgs &a, cudaStream_t stream) {
     long long per_slot = (n4 + (long long)kThreads * kUnroll - 1) / ((long long)kThreads * kUnroll);
     if (per_slot < 1) per_slot = 1;
     if (per_slot > 65535) per_slot = 65535;
-    rollback_kernel<<<dim3(unsigned(per_slot), unsigned(a.B), 1), kThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(per_slot), unsigned(a.B), 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, rollback_kernel, a);
 }
 
 }  // namespace gdn
