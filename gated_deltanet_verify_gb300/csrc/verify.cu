@@ -14,12 +14,15 @@
 //     one cluster barrier, which also orders the in-place conv_state update:
 //     the q/k conv channels are read by every CTA of the group and are
 //     rewritten only after that barrier.
-//   * Inside a CTA each warp owns 8 value rows j, four lanes per row; lane
-//     quarter q holds S[i][j] for the 16-byte chunks i/4 = q + 4m, m <
-//     d_k/16.  The reductions k^T S and q^T S over d_k are then in-thread
-//     FMA chains plus two shuffle levels, the rank-one update needs no
-//     broadcast (each lane has its own row's w), and one 16-byte store per
-//     lane writes 64 contiguous bytes of each of the warp's 8 captured rows.
+//   * Inside a CTA each warp owns 8 value rows j, split into row groups of
+//     RPG rows served by LR lanes (LR = 16, RPG = 4 for d_k >= 64; LR = 8,
+//     RPG = 2 for d_k = 32).  Lane b of a group holds S[i][j] of its RPG rows
+//     for the 16-byte chunks i/4 = b + LR*m.  Per token a lane reads only its
+//     own chunks of k and q (each chunk is shared by the 32/LR groups, so
+//     shared-memory traffic stays low), the dot products over d_k are FMA
+//     chains plus a reduce-scatter over the LR lanes (log2(LR) shuffle
+//     levels, 2*RPG values), and one 16-byte store per lane writes LR*16
+//     contiguous bytes of a captured row.
 //   * Per token both reductions are taken on the state before the update:
 //     u = g S^T k, w = beta (v - u), and the read-out S_t^T q = g S^T q +
 //     (k.q) w, so a token costs one reduction phase.
@@ -133,7 +136,6 @@ struct Smem {
 
 template <int DK, typename Act>
 __global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
-    constexpr int NCHUNK = DK / 16;       // 16-byte chunks of a row held by one lane
     constexpr int EPL = DK / 32;          // q (and k) channels per lane in the conv phase
     static_assert(DK == 32 || DK == 64 || DK == 128, "d_k must be 32, 64 or 128");
 
@@ -186,16 +188,27 @@ __global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
     grid_dependency_wait();
 
     // ---------------------------------------------------------------- loads
-    const int rloc = lane >> 2, q4 = lane & 3;                 // row within warp, lane quarter
-    const int row = wid * kRowsPerWarp + rloc;                 // row within CTA
-    float S[NCHUNK][4];
+    // (1) this warp's state rows, straight into registers (recurrence lane layout)
+    constexpr int LR = DK >= 64 ? 16 : 8;          // lanes per row group
+    constexpr int NG = 32 / LR;                    // row groups per warp
+    constexpr int RPG = kRowsPerWarp / NG;         // rows per group
+    constexpr int NV = 2 * RPG;                    // k- and q-dot values per lane (== LR / 2)
+    constexpr int NCL = DK / (4 * LR);             // 16-byte chunks per lane per row
+    static_assert(NV == LR / 2, "lane layout");
+    const int grp = lane / LR, b = lane % LR;
+    const int row0 = wid * kRowsPerWarp + grp * RPG;           // first row (within CTA) of this group
+    const int my_kind = (b & NV) ? 1 : 0;                       // after the reduce-scatter
+    const int my_rho = (b >> 1) & (RPG - 1);
+    float S[RPG][NCL][4];
     {
-        const float *src = a.state + ((size_t(s) * Hv + h) * DV + j0 + row) * DK + 4 * q4;
+        const float *src = a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b;
 #pragma unroll
-        for (int m = 0; m < NCHUNK; ++m) {
-            const float4 v = ld_na4(src + 16 * m);
-            S[m][0] = v.x; S[m][1] = v.y; S[m][2] = v.z; S[m][3] = v.w;
-        }
+        for (int rho = 0; rho < RPG; ++rho)
+#pragma unroll
+            for (int m = 0; m < NCL; ++m) {
+                const float4 v = ld_na4(src + size_t(rho) * DK + 4 * LR * m);
+                S[rho][m][0] = v.x; S[rho][m][1] = v.y; S[rho][m][2] = v.z; S[rho][m][3] = v.w;
+            }
     }
     {
         constexpr int kPer16 = 16 / sizeof(Act);
@@ -248,7 +261,7 @@ __global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
     __syncthreads();
 
     // ------------------------------------ conv + SiLU, q/k L2 norm, k.q per token
-    // q and k: one warp per token, EPL consecutive channels per lane
+    // q and k: one warp per token, EPL consecutive channels per lane (vector loads)
     for (int t = wid; t < T; t += WARPS) {
         float qv[EPL], kv[EPL];
         float sq = 0.f, sk = 0.f;
@@ -258,11 +271,17 @@ __global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
             float acc[EPL];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+                float wv[EPL], xv[EPL];
+                if constexpr (EPL == 4) {
+                    const float4 w4 = load4(cw + j * NCH + c), x4 = win4(t + j, c);
+                    wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
+                    xv[0] = x4.x; xv[1] = x4.y; xv[2] = x4.z; xv[3] = x4.w;
+                } else {
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) {
-                    const float wv = cw[j * NCH + c + e], xv = win(t + j, c + e);
-                    acc[e] = j == 0 ? wv * xv : fmaf(wv, xv, acc[e]);
+                    for (int e = 0; e < EPL; ++e) { wv[e] = cw[j * NCH + c + e]; xv[e] = win(t + j, c + e); }
                 }
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[e] = j == 0 ? wv[e] * xv[e] : fmaf(wv[e], xv[e], acc[e]);
             }
 #pragma unroll
             for (int e = 0; e < EPL; ++e) {
@@ -282,9 +301,14 @@ __global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
             qv[e] *= iq; kv[e] *= ik;
-            yt[lane * EPL + e] = qv[e];
-            yt[DK + lane * EPL + e] = kv[e];
             kq = fmaf(kv[e], qv[e], kq);
+        }
+        if constexpr (EPL == 4) {
+            store4(yt + lane * 4, make_float4(qv[0], qv[1], qv[2], qv[3]));
+            store4(yt + DK + lane * 4, make_float4(kv[0], kv[1], kv[2], kv[3]));
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) { yt[lane * EPL + e] = qv[e]; yt[DK + lane * EPL + e] = kv[e]; }
         }
 #pragma unroll
         for (int m = 16; m >= 1; m >>= 1) kq += __shfl_xor_sync(kFull, kq, m);
@@ -317,71 +341,102 @@ __global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
 
     // ------------------------------------------------------------ recurrence
     const bool capture = a.cap_state != nullptr;
-    float *cap_row = capture ? a.cap_state + (size_t(h) * DV + j0 + row) * DK + 4 * q4 : nullptr;
+    float *cap_row = capture ? a.cap_state + (size_t(h) * DV + j0 + row0) * DK + 4 * b : nullptr;
     const size_t cap_token_stride = size_t(Hv) * DV * DK;
     const float q_scale = a.q_scale;
 
     for (int t = 0; t < T; ++t) {
         const float *yt = ys + size_t(t) * NCH;
         const float g = gs[t], beta = bs[t], kq = kqs[t];
-        const float vj = yt[2 * DK + row];
-        float ka[4] = {0.f, 0.f, 0.f, 0.f}, qa[4] = {0.f, 0.f, 0.f, 0.f};
-        float kk[NCHUNK][4];
+        float kk[NCL][4], qq[NCL][4];
 #pragma unroll
-        for (int m = 0; m < NCHUNK; ++m) {
-            const float4 k4 = load4(yt + DK + 16 * m + 4 * q4);
-            const float4 qv = load4(yt + 16 * m + 4 * q4);
+        for (int m = 0; m < NCL; ++m) {
+            const float4 k4 = load4(yt + DK + 4 * (b + LR * m));
+            const float4 q4 = load4(yt + 4 * (b + LR * m));
             kk[m][0] = k4.x; kk[m][1] = k4.y; kk[m][2] = k4.z; kk[m][3] = k4.w;
-            ka[0] = fmaf(S[m][0], k4.x, ka[0]); qa[0] = fmaf(S[m][0], qv.x, qa[0]);
-            ka[1] = fmaf(S[m][1], k4.y, ka[1]); qa[1] = fmaf(S[m][1], qv.y, qa[1]);
-            ka[2] = fmaf(S[m][2], k4.z, ka[2]); qa[2] = fmaf(S[m][2], qv.z, qa[2]);
-            ka[3] = fmaf(S[m][3], k4.w, ka[3]); qa[3] = fmaf(S[m][3], qv.w, qa[3]);
+            qq[m][0] = q4.x; qq[m][1] = q4.y; qq[m][2] = q4.z; qq[m][3] = q4.w;
         }
-        float kd = (ka[0] + ka[1]) + (ka[2] + ka[3]);
-        float qd = (qa[0] + qa[1]) + (qa[2] + qa[3]);
-        kd += __shfl_xor_sync(kFull, kd, 1);
-        qd += __shfl_xor_sync(kFull, qd, 1);
-        kd += __shfl_xor_sync(kFull, kd, 2);
-        qd += __shfl_xor_sync(kFull, qd, 2);
-        const float w = beta * (vj - g * kd);                    // beta (v - (g S)^T k)
-        if (q4 == 0) os[size_t(t) * ROWS + row] = q_scale * fmaf(g, qd, kq * w);
-        // S <- g S + k w^T
+        const float vj = yt[2 * DK + row0 + my_rho];
+        // partial dot products of this lane's chunks: vals[kind * RPG + rho]
+        float vals[NV];
 #pragma unroll
-        for (int m = 0; m < NCHUNK; ++m)
+        for (int rho = 0; rho < RPG; ++rho) {
+            float dk_ = S[rho][0][0] * kk[0][0], dq_ = S[rho][0][0] * qq[0][0];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) S[m][e] = fmaf(kk[m][e], w, g * S[m][e]);
+            for (int m = 0; m < NCL; ++m)
+#pragma unroll
+                for (int e = (m == 0 ? 1 : 0); e < 4; ++e) {
+                    dk_ = fmaf(S[rho][m][e], kk[m][e], dk_);
+                    dq_ = fmaf(S[rho][m][e], qq[m][e], dq_);
+                }
+            vals[rho] = dk_;
+            vals[RPG + rho] = dq_;
+        }
+        // reduce-scatter over the LR lanes of the group: masks NV, NV/2, ..., 2 halve
+        // the value set; mask 1 completes the sum (lane pairs hold equal values)
+#pragma unroll
+        for (int half = NV / 2, msk = NV; half >= 1; half >>= 1, msk >>= 1) {
+            const bool up = (b & msk) != 0;
+#pragma unroll
+            for (int i = 0; i < half; ++i) {
+                const float keep = up ? vals[i + half] : vals[i];
+                const float send = up ? vals[i] : vals[i + half];
+                vals[i] = keep + __shfl_xor_sync(kFull, send, msk);
+            }
+        }
+        const float mine = vals[0] + __shfl_xor_sync(kFull, vals[0], 1);
+        const float other = __shfl_xor_sync(kFull, mine, NV);
+        const float kd = my_kind ? other : mine;       // (S^T k)_j of row my_rho
+        const float qd = my_kind ? mine : other;       // (S^T q)_j of row my_rho
+        const float w = beta * (vj - g * kd);           // beta (v - (g S)^T k)
+        if (my_kind == 0 && (b & 1) == 0) os[size_t(t) * ROWS + row0 + my_rho] = q_scale * fmaf(g, qd, kq * w);
+        // S <- g S + k w^T for the group's rows
+#pragma unroll
+        for (int rho = 0; rho < RPG; ++rho) {
+            const float wr = __shfl_sync(kFull, w, grp * LR + 2 * rho);
+#pragma unroll
+            for (int m = 0; m < NCL; ++m)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) S[rho][m][e] = fmaf(kk[m][e], wr, g * S[rho][m][e]);
+        }
         if (capture) {
             float *dst = cap_row + (size_t(s) * T + t) * cap_token_stride;
 #pragma unroll
-            for (int m = 0; m < NCHUNK; ++m) st_stream4(dst + 16 * m, S[m][0], S[m][1], S[m][2], S[m][3]);
+            for (int rho = 0; rho < RPG; ++rho)
+#pragma unroll
+                for (int m = 0; m < NCL; ++m)
+                    st_stream4(dst + size_t(rho) * DK + 4 * LR * m, S[rho][m][0], S[rho][m][1], S[rho][m][2],
+                               S[rho][m][3]);
         }
     }
     // the next kernel in the stream may start launching (it waits for this grid's completion itself)
     grid_launch_dependents();
 
     // ------------------------------------------------------------- epilogue
-    {
-        float *dst = a.state + ((size_t(s) * Hv + h) * DV + j0 + row) * DK + 4 * q4;
-#pragma unroll
-        for (int m = 0; m < NCHUNK; ++m) store4(dst + 16 * m, make_float4(S[m][0], S[m][1], S[m][2], S[m][3]));
-    }
-    __syncthreads();
+    // this warp's sums of o^2 per token, pushed into the allp table of every CTA of this head
+    __syncwarp();
     cluster_wait_acquire();                        // all peers have started: their smem may be written
     {
-        // per-warp sums of o^2, pushed into the allp table of every CTA of this head
         const int first_rank = (h - kh * a.r) * P;
-        const int per = T * WARPS;
-        for (int i = tid; i < per * P; i += nthr) {
-            const int dst_p = i / per, rem = i % per, t = rem / WARPS, w = rem % WARPS;
-            const float *o = os + size_t(t) * ROWS + w * kRowsPerWarp;
+        for (int i = lane; i < T * P; i += 32) {
+            const int t = i % T, dst_p = i / T;
+            const float *o = os + size_t(t) * ROWS + wid * kRowsPerWarp;
             float acc = o[0] * o[0];
 #pragma unroll
             for (int r = 1; r < kRowsPerWarp; ++r) acc = fmaf(o[r], o[r], acc);
             float *peer = cluster.map_shared_rank(allp, first_rank + dst_p);
-            peer[size_t(t) * P * WARPS + p * WARPS + w] = acc;
+            peer[size_t(t) * P * WARPS + p * WARPS + wid] = acc;
         }
     }
-    // every CTA of the cluster has read the old conv state and pushed its partials
+    {
+        float *dst = a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b;
+#pragma unroll
+        for (int rho = 0; rho < RPG; ++rho)
+#pragma unroll
+            for (int m = 0; m < NCL; ++m)
+                store4(dst + size_t(rho) * DK + 4 * LR * m,
+                       make_float4(S[rho][m][0], S[rho][m][1], S[rho][m][2], S[rho][m][3]));
+    }
     cluster_arrive_release();
     cluster_wait_acquire();
     for (int t = tid; t < T; t += nthr) {
