@@ -81,20 +81,20 @@ int check_params(const gdn_layer_params *p) {
 namespace gdn {
 
 // CTAs per value head: as many as the cluster allows (portable size 8) while a
-// CTA keeps at most 16 warps of 8 rows; more CTAs spread a small batch over
-// more SMs, whose store bandwidth is what the capture needs.
+// CTA keeps at most 8 consumer warps of 8 rows; more CTAs spread a small
+// batch over more SMs.
 int verify_parts_per_head(int B, int Hv, int r, int dv, int sm_count) {
     (void)B; (void)Hv; (void)sm_count;
     const int warps_head = dv / 8;
     int best = 0;
     for (int P = 1; P <= warps_head; P *= 2) {
         if (warps_head % P) continue;
-        if (warps_head / P > 16) continue;
+        if (warps_head / P > 8) continue;
         if (r * P <= 8) best = P;
     }
     if (best) return best;
     for (int P = 1; P <= warps_head; P *= 2) {             // non-portable cluster sizes up to 16
-        if (warps_head % P || warps_head / P > 16) continue;
+        if (warps_head % P || warps_head / P > 8) continue;
         if (r * P <= 16) return P;
     }
     return 0;
@@ -112,7 +112,6 @@ int gdn_verify_forward(const gdn_dims *dims, const gdn_layer_params *params, con
                        const void *z, const void *alpha, const void *beta_raw, float *state,
                        float *conv_state, float *cap_state, float *cap_conv, void *out, int *d_status,
                        void *stream) {
-    (void)d_status;
     g_err.clear();
     int rc = check_common(dims);
     if (rc) return rc;
@@ -145,6 +144,7 @@ int gdn_verify_forward(const gdn_dims *dims, const gdn_layer_params *params, con
     a.conv_w = params->conv_w; a.A_log = params->A_log; a.dt_bias = params->dt_bias; a.norm_w = params->norm_w;
     a.qkv = qkv; a.z = z; a.alpha = alpha; a.beta_raw = beta_raw;
     a.state = state; a.conv_state = conv_state; a.cap_state = cap_state; a.cap_conv = cap_conv; a.out = out;
+    a.d_status = d_status;
     cudaError_t e = gdn::launch_verify(a, d.act_dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "verify launch failed: %s", cudaGetErrorString(e));
     return GDN_OK;

@@ -20,6 +20,7 @@ struct VerifyArgs {
     const void *qkv, *z, *alpha, *beta_raw;
     float *state, *conv_state, *cap_state, *cap_conv;
     void *out;
+    int *d_status;                    // device status word (may be NULL)
 };
 
 struct RollbackArgs {

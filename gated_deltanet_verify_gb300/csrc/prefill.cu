@@ -45,7 +45,7 @@ size_t prefill_workspace_bytes(const gdn_dims &d) {
 cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const void *qkv, const void *z,
                            const void *alpha, const void *beta_raw, float *state, float *conv_state,
                            void *out, void *workspace, int *d_status, cudaStream_t stream) {
-    (void)workspace; (void)d_status;
+    (void)workspace;
     const int act_bytes = d.act_dtype == GDN_BF16 ? 2 : 4;
     const int r = d.n_v_heads / d.n_qk_heads;
     VerifyArgs a{};
@@ -56,6 +56,7 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
     a.rms_eps = d.rms_eps; a.l2_eps = d.l2_eps; a.q_scale = d.q_scale;
     a.conv_w = p.conv_w; a.A_log = p.A_log; a.dt_bias = p.dt_bias; a.norm_w = p.norm_w;
     a.state = state; a.conv_state = conv_state; a.cap_state = nullptr; a.cap_conv = nullptr;
+    a.d_status = d_status;
     const size_t Cb = size_t(a.C) * act_bytes, Zb = size_t(d.n_v_heads) * d.d_v * act_bytes,
                  Gb = size_t(d.n_v_heads) * act_bytes;
     for (int t0 = 0; t0 < d.n_tokens; t0 += kSegment) {

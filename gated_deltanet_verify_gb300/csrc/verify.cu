@@ -10,10 +10,9 @@
 //     value heads that share key head kh, each split into P CTAs along d_v.
 //     Columns j of S (value dims) evolve independently, so a CTA owns d_v/P
 //     of them; only the per-head RMSNorm needs all d_v.  Its partial sums are
-//     pushed into the peers' shared memory (distributed shared memory) before
-//     one cluster barrier, which also orders the in-place conv_state update:
-//     the q/k conv channels are read by every CTA of the group and are
-//     rewritten only after that barrier.
+//     exchanged through distributed shared memory inside the cluster; the
+//     q/k conv channels are read by every CTA of the group, and the cluster
+//     also orders their in-place conv_state rewrite after all those reads.
 //   * Inside a CTA each warp owns 8 value rows j, split into row groups of
 //     RPG rows served by LR lanes (LR = 16, RPG = 4 for d_k >= 64; LR = 8,
 //     RPG = 2 for d_k = 32).  Lane b of a group holds S[i][j] of its RPG rows
@@ -29,22 +28,34 @@
 //   * Reduction orders depend only on the lane layout, never on P or T: the
 //     state after token t is bit-identical whatever the launch shape and
 //     however many tokens follow it (the rollback contract relies on this).
+//   * Conv + SiLU + L2 norm run before the recurrence with one thread per
+//     (token, q|k, 16-channel chunk); a chunk's channels are interleaved
+//     (4 channels every 4*chunks) so the vector loads of a warp are
+//     conflict-free, and the sums of squares need three shuffle levels.
+//   * The RMSNorm partials travel by st.async into the peers' shared memory,
+//     completing a transaction-counted mbarrier there; no release fence has
+//     to wait behind the capture stores still in flight.  The one cluster
+//     barrier sits right after the loads: it orders every CTA's read of the
+//     old conv state before the in-place rewrite, and publishes the
+//     initialised mbarriers before any peer writes to them.
+//   * Every wait is bounded; a wait that gives up writes GDN_ERR_TIMEOUT to
+//     the caller's status word instead of hanging.
 //   * Programmatic dependent launch: the kernel waits on its predecessor only
 //     right before its first global read, so its launch overlaps the tail of
 //     the previous kernel in the stream.
 #include "internal.cuh"
 
-#include <cooperative_groups.h>
 #include <cuda_bf16.h>
-
-namespace cg = cooperative_groups;
 
 namespace gdn {
 namespace {
 
 constexpr int kRowsPerWarp = 8;
+constexpr int kMaxWarps = 8;
+constexpr int kMaxThreads = 32 * kMaxWarps;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxDevices = 64;
+constexpr int kSpinLimit = 1 << 22;     // try_wait rounds before a wait gives up
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -102,6 +113,50 @@ __device__ __forceinline__ void cluster_arrive_release() {
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], %1;\n\t}\n" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}\n"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+// Bounded waits: after kSpinLimit rounds the wait gives up and reports.
+__device__ __forceinline__ void report_timeout(int *status) {
+    if (status) atomicCAS(status, int(GDN_OK), int(GDN_ERR_TIMEOUT));
+}
+__device__ __forceinline__ void mbar_wait_cluster(uint32_t bar, uint32_t parity, int *status) {
+    for (int i = 0; i < kSpinLimit; ++i)
+        if (mbar_try_wait_cluster(bar, parity)) return;
+    report_timeout(status);
+}
+__device__ __forceinline__ void fence_mbarrier_init_cluster() {
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+// shared::cluster address of `local` in the CTA of cluster rank `rank`
+__device__ __forceinline__ uint32_t map_cluster(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+// 4-byte store into a peer CTA's shared memory that completes 4 bytes of its mbarrier's transaction
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];\n" ::"r"(remote_addr),
+                 "r"(__float_as_uint(v)), "r"(remote_bar)
+                 : "memory");
+}
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -110,7 +165,7 @@ __device__ __forceinline__ void grid_launch_dependents() {
 // Shared-memory carve-up; identical on host and device.
 struct Smem {
     int NCH;
-    size_t xs, zs, cw, cs, nw, ys, os, gs, bs, kqs, rinv, allp, total;
+    size_t xs, zs, cw, cs, nw, ys, os, gs, bs, kqs, rinv, allp, redbar, total;
     __host__ __device__ Smem(int T, int dk, int rows, int warps, int P, int act_bytes) : NCH(2 * dk + rows) {
         size_t off = 0;
         auto take = [&](size_t bytes) {
@@ -130,20 +185,26 @@ struct Smem {
         kqs = take(size_t(T) * 4);
         rinv = take(size_t(T) * 4);
         allp = take(size_t(T) * P * warps * 4);     // per-warp sums of o^2 of the whole head
+        redbar = take(8);                           // all RMSNorm partials of the head arrived
         total = off;
     }
 };
 
 template <int DK, typename Act>
-__global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
-    constexpr int EPL = DK / 32;          // q (and k) channels per lane in the conv phase
+__global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs a) {
     static_assert(DK == 32 || DK == 64 || DK == 128, "d_k must be 32, 64 or 128");
+    constexpr int LR = DK >= 64 ? 16 : 8;          // lanes per row group
+    constexpr int NG = 32 / LR;                    // row groups per warp
+    constexpr int RPG = kRowsPerWarp / NG;         // rows per group
+    constexpr int NV = 2 * RPG;                    // k- and q-dot values per lane (== LR / 2)
+    constexpr int NCL = DK / (4 * LR);             // 16-byte chunks per lane per row
+    static_assert(NV == LR / 2, "lane layout");
 
-    cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ __align__(16) unsigned char smem_raw[];
 
     const int tid = threadIdx.x, nthr = blockDim.x;
-    const int lane = tid & 31, wid = tid >> 5, WARPS = nthr >> 5;
+    const int lane = tid & 31, wid = tid >> 5;
+    const int WARPS = nthr >> 5;
     const int ROWS = WARPS * kRowsPerWarp;
     const int T = a.T, Hv = a.Hv, Hk = a.Hk, DV = a.dv, C = a.C, P = a.P;
     const int s = blockIdx.y;
@@ -165,6 +226,7 @@ __global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
     float *kqs = reinterpret_cast<float *>(smem_raw + L.kqs);
     float *rinv = reinterpret_cast<float *>(smem_raw + L.rinv);
     float *allp = reinterpret_cast<float *>(smem_raw + L.allp);
+    const uint32_t redbar = smem_u32(smem_raw + L.redbar);
     const int NCH = L.NCH;
 
     // local channel c -> global conv channel
@@ -181,20 +243,17 @@ __global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
         return rho < 3 ? load4(cs + rho * NCH + c) : load4(xs + size_t(rho - 3) * NCH + c);
     };
 
-    // announce that this CTA has started (peers write into its shared memory
-    // later); the matching wait comes after the recurrence
-    cluster_arrive_relaxed();
+    if (tid == 0) {
+        mbar_init(redbar, 1);
+        fence_mbarrier_init_cluster();
+        // the single arrival; the phase completes once every partial of the head has landed
+        mbar_arrive_expect_tx(redbar, uint32_t(T * P * WARPS * 4));
+    }
     // everything below may read what the previous kernel in the stream wrote
     grid_dependency_wait();
 
     // ---------------------------------------------------------------- loads
     // (1) this warp's state rows, straight into registers (recurrence lane layout)
-    constexpr int LR = DK >= 64 ? 16 : 8;          // lanes per row group
-    constexpr int NG = 32 / LR;                    // row groups per warp
-    constexpr int RPG = kRowsPerWarp / NG;         // rows per group
-    constexpr int NV = 2 * RPG;                    // k- and q-dot values per lane (== LR / 2)
-    constexpr int NCL = DK / (4 * LR);             // 16-byte chunks per lane per row
-    static_assert(NV == LR / 2, "lane layout");
     const int grp = lane / LR, b = lane % LR;
     const int row0 = wid * kRowsPerWarp + grp * RPG;           // first row (within CTA) of this group
     const int my_kind = (b & NV) ? 1 : 0;                       // after the reduce-scatter
@@ -210,6 +269,7 @@ __global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
                 S[rho][m][0] = v.x; S[rho][m][1] = v.y; S[rho][m][2] = v.z; S[rho][m][3] = v.w;
             }
     }
+    // (2) activations, conv weights / state, norm weight: 16-byte async copies to smem
     {
         constexpr int kPer16 = 16 / sizeof(Act);
         const int vq = DK / kPer16, vv = ROWS / kPer16;     // 16-byte vectors per segment
@@ -247,7 +307,7 @@ __global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
         }
         for (int i = tid; i < ROWS / 4; i += nthr) cp_async16(nw + i * 4, a.norm_w + j0 + i * 4);
     }
-    // gates for this head, one token per thread
+    // (3) gates for this head, one token per thread
     for (int t = tid; t < T; t += nthr) {
         const size_t idx = (size_t(s) * a.Ts + t) * Hv + h;
         const float al = to_f32(static_cast<const Act *>(a.alpha)[idx]);
@@ -259,60 +319,64 @@ __global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
     }
     cp_async_wait_all();
     __syncthreads();
+    // cluster phase 1: this CTA has read the old conv state and initialised its mbarriers
+    cluster_arrive_release();
 
     // ------------------------------------ conv + SiLU, q/k L2 norm, k.q per token
-    // q and k: one warp per token, EPL consecutive channels per lane (vector loads)
-    for (int t = wid; t < T; t += WARPS) {
-        float qv[EPL], kv[EPL];
-        float sq = 0.f, sk = 0.f;
+    {
+        constexpr int QC = DK / 16;                 // 16-channel chunks per q (or k) vector
+        constexpr int PER_T = 2 * QC;               // q and k items per token (divides 32)
+        const int n_items = T * PER_T;
+        const int n_round = (n_items + 31) & ~31;   // whole warps, so every lane joins the shuffles
+        for (int base = wid * 32; base < n_round; base += nthr) {
+            const int i = base + lane;
+            const bool valid = i < n_items;
+            const int t = valid ? i / PER_T : 0, part = (i % PER_T) / QC, c = i % QC;
+            float y[4][4];
+            float ss = 0.f;
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            const int c = part * DK + lane * EPL;
-            float acc[EPL];
+            for (int m = 0; m < 4; ++m) {
+                const int ch = part * DK + 4 * (c + QC * m);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (valid) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float wv[EPL], xv[EPL];
-                if constexpr (EPL == 4) {
-                    const float4 w4 = load4(cw + j * NCH + c), x4 = win4(t + j, c);
-                    wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
-                    xv[0] = x4.x; xv[1] = x4.y; xv[2] = x4.z; xv[3] = x4.w;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) { wv[e] = cw[j * NCH + c + e]; xv[e] = win(t + j, c + e); }
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 w4 = load4(cw + j * NCH + ch), x4 = win4(t + j, ch);
+                        if (j == 0) acc = make_float4(w4.x * x4.x, w4.y * x4.y, w4.z * x4.z, w4.w * x4.w);
+                        else acc = make_float4(fmaf(w4.x, x4.x, acc.x), fmaf(w4.y, x4.y, acc.y),
+                                               fmaf(w4.z, x4.z, acc.z), fmaf(w4.w, x4.w, acc.w));
+                    }
                 }
+                y[m][0] = silu(acc.x); y[m][1] = silu(acc.y); y[m][2] = silu(acc.z); y[m][3] = silu(acc.w);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[e] = j == 0 ? wv[e] * xv[e] : fmaf(wv[e], xv[e], acc[e]);
+                for (int e = 0; e < 4; ++e) ss = fmaf(y[m][e], y[m][e], ss);
             }
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) {
-                const float y = silu(acc[e]);
-                if (part == 0) { qv[e] = y; sq = fmaf(y, y, sq); }
-                else { kv[e] = y; sk = fmaf(y, y, sk); }
+            for (int msk = 1; msk < QC; msk <<= 1) ss += __shfl_xor_sync(kFull, ss, msk);
+            const float inv = 1.0f / sqrtf(ss + a.l2_eps);
+            float *yt = ys + size_t(t) * NCH;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) y[m][e] *= inv;
+                if (valid) store4(yt + part * DK + 4 * (c + QC * m), make_float4(y[m][0], y[m][1], y[m][2], y[m][3]));
             }
-        }
+            __syncwarp();
+            // k.q of the token: the q threads read k^ back for their channels
+            float kq = 0.f;
+            if (valid && part == 0) {
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) {
-            sq += __shfl_xor_sync(kFull, sq, m);
-            sk += __shfl_xor_sync(kFull, sk, m);
-        }
-        const float iq = 1.0f / sqrtf(sq + a.l2_eps), ik = 1.0f / sqrtf(sk + a.l2_eps);
-        float kq = 0.f;
-        float *yt = ys + size_t(t) * NCH;
+                for (int m = 0; m < 4; ++m) {
+                    const float4 k4 = load4(yt + DK + 4 * (c + QC * m));
+                    kq = fmaf(y[m][0], k4.x, kq); kq = fmaf(y[m][1], k4.y, kq);
+                    kq = fmaf(y[m][2], k4.z, kq); kq = fmaf(y[m][3], k4.w, kq);
+                }
+            }
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            qv[e] *= iq; kv[e] *= ik;
-            kq = fmaf(kv[e], qv[e], kq);
+            for (int msk = 1; msk < QC; msk <<= 1) kq += __shfl_xor_sync(kFull, kq, msk);
+            if (valid && part == 0 && c == 0) kqs[t] = kq;
+            __syncwarp();
         }
-        if constexpr (EPL == 4) {
-            store4(yt + lane * 4, make_float4(qv[0], qv[1], qv[2], qv[3]));
-            store4(yt + DK + lane * 4, make_float4(kv[0], kv[1], kv[2], kv[3]));
-        } else {
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) { yt[lane * EPL + e] = qv[e]; yt[DK + lane * EPL + e] = kv[e]; }
-        }
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) kq += __shfl_xor_sync(kFull, kq, m);
-        if (lane == 0) kqs[t] = kq;
     }
     // v: four channels of one token per item
     for (int i = tid; i < T * (ROWS / 4); i += nthr) {
@@ -339,107 +403,111 @@ __global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
     }
     __syncthreads();
 
-    // ------------------------------------------------------------ recurrence
-    const bool capture = a.cap_state != nullptr;
-    float *cap_row = capture ? a.cap_state + (size_t(h) * DV + j0 + row0) * DK + 4 * b : nullptr;
-    const size_t cap_token_stride = size_t(Hv) * DV * DK;
-    const float q_scale = a.q_scale;
+    {
+        // ------------------------------------------------------------ recurrence
+        const bool capture = a.cap_state != nullptr;
+        float *cap_row = capture ? a.cap_state + (size_t(h) * DV + j0 + row0) * DK + 4 * b : nullptr;
+        const size_t cap_token_stride = size_t(Hv) * DV * DK;
+        const float q_scale = a.q_scale;
 
-    for (int t = 0; t < T; ++t) {
-        const float *yt = ys + size_t(t) * NCH;
-        const float g = gs[t], beta = bs[t], kq = kqs[t];
-        float kk[NCL][4], qq[NCL][4];
+        for (int t = 0; t < T; ++t) {
+            const float *yt = ys + size_t(t) * NCH;
+            const float g = gs[t], beta = bs[t], kq = kqs[t];
+            float kk[NCL][4], qq[NCL][4];
 #pragma unroll
-        for (int m = 0; m < NCL; ++m) {
-            const float4 k4 = load4(yt + DK + 4 * (b + LR * m));
-            const float4 q4 = load4(yt + 4 * (b + LR * m));
-            kk[m][0] = k4.x; kk[m][1] = k4.y; kk[m][2] = k4.z; kk[m][3] = k4.w;
-            qq[m][0] = q4.x; qq[m][1] = q4.y; qq[m][2] = q4.z; qq[m][3] = q4.w;
-        }
-        const float vj = yt[2 * DK + row0 + my_rho];
-        // partial dot products of this lane's chunks: vals[kind * RPG + rho]
-        float vals[NV];
+            for (int m = 0; m < NCL; ++m) {
+                const float4 k4 = load4(yt + DK + 4 * (b + LR * m));
+                const float4 q4 = load4(yt + 4 * (b + LR * m));
+                kk[m][0] = k4.x; kk[m][1] = k4.y; kk[m][2] = k4.z; kk[m][3] = k4.w;
+                qq[m][0] = q4.x; qq[m][1] = q4.y; qq[m][2] = q4.z; qq[m][3] = q4.w;
+            }
+            const float vj = yt[2 * DK + row0 + my_rho];
+            // partial dot products of this lane's chunks: vals[kind * RPG + rho]
+            float vals[NV];
 #pragma unroll
-        for (int rho = 0; rho < RPG; ++rho) {
-            float dk_ = S[rho][0][0] * kk[0][0], dq_ = S[rho][0][0] * qq[0][0];
+            for (int rho = 0; rho < RPG; ++rho) {
+                float dk_ = S[rho][0][0] * kk[0][0], dq_ = S[rho][0][0] * qq[0][0];
 #pragma unroll
-            for (int m = 0; m < NCL; ++m)
+                for (int m = 0; m < NCL; ++m)
 #pragma unroll
-                for (int e = (m == 0 ? 1 : 0); e < 4; ++e) {
-                    dk_ = fmaf(S[rho][m][e], kk[m][e], dk_);
-                    dq_ = fmaf(S[rho][m][e], qq[m][e], dq_);
+                    for (int e = (m == 0 ? 1 : 0); e < 4; ++e) {
+                        dk_ = fmaf(S[rho][m][e], kk[m][e], dk_);
+                        dq_ = fmaf(S[rho][m][e], qq[m][e], dq_);
+                    }
+                vals[rho] = dk_;
+                vals[RPG + rho] = dq_;
+            }
+            // reduce-scatter over the LR lanes of the group: masks NV, NV/2, ..., 2 halve
+            // the value set; mask 1 completes the sum (lane pairs hold equal values)
+#pragma unroll
+            for (int half = NV / 2, msk = NV; half >= 1; half >>= 1, msk >>= 1) {
+                const bool up = (b & msk) != 0;
+#pragma unroll
+                for (int i = 0; i < half; ++i) {
+                    const float keep = up ? vals[i + half] : vals[i];
+                    const float send = up ? vals[i] : vals[i + half];
+                    vals[i] = keep + __shfl_xor_sync(kFull, send, msk);
                 }
-            vals[rho] = dk_;
-            vals[RPG + rho] = dq_;
-        }
-        // reduce-scatter over the LR lanes of the group: masks NV, NV/2, ..., 2 halve
-        // the value set; mask 1 completes the sum (lane pairs hold equal values)
+            }
+            const float mine = vals[0] + __shfl_xor_sync(kFull, vals[0], 1);
+            const float other = __shfl_xor_sync(kFull, mine, NV);
+            const float kd = my_kind ? other : mine;       // (S^T k)_j of row my_rho
+            const float qd = my_kind ? mine : other;       // (S^T q)_j of row my_rho
+            const float w = beta * (vj - g * kd);           // beta (v - (g S)^T k)
+            if (my_kind == 0 && (b & 1) == 0) os[size_t(t) * ROWS + row0 + my_rho] = q_scale * fmaf(g, qd, kq * w);
+            // S <- g S + k w^T for the group's rows
 #pragma unroll
-        for (int half = NV / 2, msk = NV; half >= 1; half >>= 1, msk >>= 1) {
-            const bool up = (b & msk) != 0;
+            for (int rho = 0; rho < RPG; ++rho) {
+                const float wr = __shfl_sync(kFull, w, grp * LR + 2 * rho);
 #pragma unroll
-            for (int i = 0; i < half; ++i) {
-                const float keep = up ? vals[i + half] : vals[i];
-                const float send = up ? vals[i] : vals[i + half];
-                vals[i] = keep + __shfl_xor_sync(kFull, send, msk);
+                for (int m = 0; m < NCL; ++m)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) S[rho][m][e] = fmaf(kk[m][e], wr, g * S[rho][m][e]);
+            }
+            if (capture) {
+                float *dst = cap_row + (size_t(s) * T + t) * cap_token_stride;
+#pragma unroll
+                for (int rho = 0; rho < RPG; ++rho)
+#pragma unroll
+                    for (int m = 0; m < NCL; ++m)
+                        st_stream4(dst + size_t(rho) * DK + 4 * LR * m, S[rho][m][0], S[rho][m][1], S[rho][m][2],
+                                   S[rho][m][3]);
             }
         }
-        const float mine = vals[0] + __shfl_xor_sync(kFull, vals[0], 1);
-        const float other = __shfl_xor_sync(kFull, mine, NV);
-        const float kd = my_kind ? other : mine;       // (S^T k)_j of row my_rho
-        const float qd = my_kind ? mine : other;       // (S^T q)_j of row my_rho
-        const float w = beta * (vj - g * kd);           // beta (v - (g S)^T k)
-        if (my_kind == 0 && (b & 1) == 0) os[size_t(t) * ROWS + row0 + my_rho] = q_scale * fmaf(g, qd, kq * w);
-        // S <- g S + k w^T for the group's rows
+        // the next kernel in the stream may start launching (it waits for this grid's completion itself)
+        grid_launch_dependents();
+        __syncwarp();
+        cluster_wait_acquire();            // phase 1: every peer's mbarrier is initialised
+        {
+            // this warp's sums of o^2 per token, sent to the allp table of every CTA of this head
+            const int first_rank = (h - kh * a.r) * P;
+            const uint32_t allp_local = smem_u32(allp);
+            for (int i = lane; i < T * P; i += 32) {
+                const int t = i % T, dst_p = i / T;
+                const float *o = os + size_t(t) * ROWS + wid * kRowsPerWarp;
+                float acc = o[0] * o[0];
 #pragma unroll
-        for (int rho = 0; rho < RPG; ++rho) {
-            const float wr = __shfl_sync(kFull, w, grp * LR + 2 * rho);
-#pragma unroll
-            for (int m = 0; m < NCL; ++m)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) S[rho][m][e] = fmaf(kk[m][e], wr, g * S[rho][m][e]);
+                for (int r = 1; r < kRowsPerWarp; ++r) acc = fmaf(o[r], o[r], acc);
+                const uint32_t rank = uint32_t(first_rank + dst_p);
+                const uint32_t off = uint32_t((size_t(t) * P * WARPS + p * WARPS + wid) * 4);
+                st_async_f32(map_cluster(allp_local + off, rank), acc, map_cluster(redbar, rank));
+            }
         }
-        if (capture) {
-            float *dst = cap_row + (size_t(s) * T + t) * cap_token_stride;
+        {
+            float *dst = a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b;
 #pragma unroll
             for (int rho = 0; rho < RPG; ++rho)
 #pragma unroll
                 for (int m = 0; m < NCL; ++m)
-                    st_stream4(dst + size_t(rho) * DK + 4 * LR * m, S[rho][m][0], S[rho][m][1], S[rho][m][2],
-                               S[rho][m][3]);
+                    store4(dst + size_t(rho) * DK + 4 * LR * m,
+                           make_float4(S[rho][m][0], S[rho][m][1], S[rho][m][2], S[rho][m][3]));
         }
     }
-    // the next kernel in the stream may start launching (it waits for this grid's completion itself)
-    grid_launch_dependents();
 
     // ------------------------------------------------------------- epilogue
-    // this warp's sums of o^2 per token, pushed into the allp table of every CTA of this head
-    __syncwarp();
-    cluster_wait_acquire();                        // all peers have started: their smem may be written
-    {
-        const int first_rank = (h - kh * a.r) * P;
-        for (int i = lane; i < T * P; i += 32) {
-            const int t = i % T, dst_p = i / T;
-            const float *o = os + size_t(t) * ROWS + wid * kRowsPerWarp;
-            float acc = o[0] * o[0];
-#pragma unroll
-            for (int r = 1; r < kRowsPerWarp; ++r) acc = fmaf(o[r], o[r], acc);
-            float *peer = cluster.map_shared_rank(allp, first_rank + dst_p);
-            peer[size_t(t) * P * WARPS + p * WARPS + wid] = acc;
-        }
-    }
-    {
-        float *dst = a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b;
-#pragma unroll
-        for (int rho = 0; rho < RPG; ++rho)
-#pragma unroll
-            for (int m = 0; m < NCL; ++m)
-                store4(dst + size_t(rho) * DK + 4 * LR * m,
-                       make_float4(S[rho][m][0], S[rho][m][1], S[rho][m][2], S[rho][m][3]));
-    }
-    cluster_arrive_release();
-    cluster_wait_acquire();
-    for (int t = tid; t < T; t += nthr) {
+    if (tid < T) {
+        mbar_wait_cluster(redbar, 0, a.d_status);   // every partial of this head has landed
+        const int t = tid;
         const float *ap = allp + size_t(t) * P * WARPS;
         float tot = 0.f;
         for (int i = 0; i < P * WARPS; ++i) tot += ap[i];              // head-level warp order: fixed
@@ -461,7 +529,7 @@ __global__ void __launch_bounds__(512) verify_kernel(const VerifyArgs a) {
         }
     }
     {
-        // conv state <- window rows T .. T+2 (after the cluster barrier: every reader is done)
+        // conv state <- window rows T .. T+2 (after cluster phase 1: every reader is done)
         const int c_first = qk_writer ? 0 : 2 * DK;
         const int n4 = (NCH - c_first) / 4;
         float *base = a.conv_state + size_t(s) * 3 * C;
