@@ -319,8 +319,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     }
     cp_async_wait_all();
     __syncthreads();
-    // cluster phase 1: this CTA has read the old conv state and initialised its mbarriers
-    cluster_arrive_release();
+    // cluster phase 1: this CTA has read the old conv state (the copies above have
+    // landed) and initialised its mbarrier (published by fence.mbarrier_init)
+    cluster_arrive_relaxed();
 
     // ------------------------------------ conv + SiLU, q/k L2 norm, k.q per token
     {
@@ -390,16 +391,6 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
                                    fmaf(w4.w, x4.w, acc.w));
         }
         store4(ys + size_t(t) * NCH + c, make_float4(silu(acc.x), silu(acc.y), silu(acc.z), silu(acc.w)));
-    }
-    // conv window capture: concat(old conv state, new tokens) of the channels this CTA owns
-    if (a.cap_conv) {
-        const int c_first = qk_writer ? 0 : 2 * DK;
-        const int n4 = (NCH - c_first) / 4;
-        float *base = a.cap_conv + size_t(s) * (3 + T) * C;
-        for (int i = tid; i < (3 + T) * n4; i += nthr) {
-            const int rho = i / n4, c = c_first + 4 * (i % n4);
-            store4(base + size_t(rho) * C + gchan(c), win4(rho, c));
-        }
     }
     __syncthreads();
 
@@ -476,6 +467,16 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         }
         // the next kernel in the stream may start launching (it waits for this grid's completion itself)
         grid_launch_dependents();
+        // conv window capture: concat(old conv state, new tokens) of the channels this CTA owns
+        if (a.cap_conv) {
+            const int c_first = qk_writer ? 0 : 2 * DK;
+            const int n4 = (NCH - c_first) / 4;
+            float *base = a.cap_conv + size_t(s) * (3 + T) * C;
+            for (int i = tid; i < (3 + T) * n4; i += nthr) {
+                const int rho = i / n4, c = c_first + 4 * (i % n4);
+                store4(base + size_t(rho) * C + gchan(c), win4(rho, c));
+            }
+        }
         __syncwarp();
         cluster_wait_acquire();            // phase 1: every peer's mbarrier is initialised
         {
