@@ -382,10 +382,19 @@ def run_cuda(args):
     gdn.lib()
 
     shape = WORKLOADS[args.workload]
+    if args.slots:
+        shape = shape.with_(n_slots=args.slots)
     props = torch.cuda.get_device_properties(local)
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
     wl = PrefillWorkload(shape, device, l2) if args.workload == "prefill" else VerifyWorkload(shape, device, l2)
     torch.cuda.synchronize()
+    if args.profile:
+        # profiling mode (for ncu): eager steps on the current stream, no timing, no output
+        sp = torch.cuda.current_stream().cuda_stream
+        for k in range(args.profile):
+            wl.step(k % wl.n_sets, sp)
+        torch.cuda.synchronize()
+        return
 
     graph_len = max(1, min(args.graph_len, args.steps))
     if args.workload in ("stack_verify", "prefill"):
@@ -582,6 +591,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--slots", type=int, default=0, help="override the workload's slot count (profiling cases)")
+    ap.add_argument("--profile", type=int, default=0, metavar="K",
+                    help="run K untimed eager steps and exit (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
