@@ -190,6 +190,23 @@ def _dist():
     return world, rank, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The slowest rank's time: replicas run the same work, so the job's clock
+    is the maximum over ranks.  No-op without an initialised process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step: float, steps: int, world: int, seconds: float) -> float:
+    """Whole-job throughput: every rank processes its own units (weak scaling)."""
+    return units_per_rank_step * steps * world / seconds
+
+
 class VerifyWorkload:
     """Rotating buffer sets of one verify+rollback workload (one or more layers)."""
 
@@ -441,12 +458,8 @@ def run_cuda(args):
                 "rollback": kernel_duration(torch, wl, "rollback", n_launch)}
     clocks.stop()
 
-    if world > 1:
-        t = torch.tensor([dt], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt = float(t.item())
-    tokens = wl.tokens_per_step * args.steps * world
-    value = tokens / dt
+    dt = max_over_ranks(dt, device)
+    value = job_throughput(wl.tokens_per_step, args.steps, world, dt)
     hbm, peak_kind = peaks()
     if args.workload == "prefill":
         dom, dom_bytes, dom_src = "prefill", prefill_bytes(shape), ["prefill.cu", "verify.cu", "internal.cuh"]

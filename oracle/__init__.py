@@ -52,22 +52,27 @@ class _Dims(ctypes.Structure):
 _D = ctypes.POINTER(ctypes.c_double)
 
 
+def configure(L: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the C signatures on a loaded oracle library."""
+    L.gdno_softplus.restype = ctypes.c_double
+    L.gdno_softplus.argtypes = [ctypes.c_double]
+    L.gdno_gates.argtypes = [ctypes.c_double] * 4 + [_D, _D]
+    L.gdno_l2norm.argtypes = [ctypes.c_int, _D, ctypes.c_double, _D]
+    L.gdno_conv_silu.argtypes = [ctypes.c_int] * 3 + [_D, _D, _D]
+    L.gdno_delta_step.argtypes = [ctypes.c_int, ctypes.c_int, _D, _D, _D, _D,
+                                         ctypes.c_double, ctypes.c_double, ctypes.c_double, _D]
+    L.gdno_rmsnorm_gate.argtypes = [ctypes.c_int, _D, _D, _D, ctypes.c_double, _D]
+    L.gdno_verify.argtypes = [ctypes.POINTER(_Dims)] + [_D] * 13 + [ctypes.c_void_p, ctypes.c_int]
+    L.gdno_prefill_chunked.argtypes = ([ctypes.POINTER(_Dims), ctypes.c_int] + [_D] * 11 +
+                                              [ctypes.c_void_p, ctypes.c_int])
+    L.gdno_rollback.argtypes = [ctypes.POINTER(_Dims), ctypes.c_void_p] + [_D] * 4 + [ctypes.c_void_p]
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
-        _lib = ctypes.CDLL(build())
-        _lib.gdno_softplus.restype = ctypes.c_double
-        _lib.gdno_softplus.argtypes = [ctypes.c_double]
-        _lib.gdno_gates.argtypes = [ctypes.c_double] * 4 + [_D, _D]
-        _lib.gdno_l2norm.argtypes = [ctypes.c_int, _D, ctypes.c_double, _D]
-        _lib.gdno_conv_silu.argtypes = [ctypes.c_int] * 3 + [_D, _D, _D]
-        _lib.gdno_delta_step.argtypes = [ctypes.c_int, ctypes.c_int, _D, _D, _D, _D,
-                                         ctypes.c_double, ctypes.c_double, ctypes.c_double, _D]
-        _lib.gdno_rmsnorm_gate.argtypes = [ctypes.c_int, _D, _D, _D, ctypes.c_double, _D]
-        _lib.gdno_verify.argtypes = [ctypes.POINTER(_Dims)] + [_D] * 13 + [ctypes.c_void_p, ctypes.c_int]
-        _lib.gdno_prefill_chunked.argtypes = ([ctypes.POINTER(_Dims), ctypes.c_int] + [_D] * 11 +
-                                              [ctypes.c_void_p, ctypes.c_int])
-        _lib.gdno_rollback.argtypes = [ctypes.POINTER(_Dims), ctypes.c_void_p] + [_D] * 4 + [ctypes.c_void_p]
+        _lib = configure(ctypes.CDLL(build()))
     return _lib
 
 
