@@ -10,11 +10,6 @@
 
 namespace gdn {
 size_t verify_smem_bytes(int T, int dk, int dv, int P, int act_bytes);
-size_t prefill_workspace_bytes(const gdn_dims &d);
-int prefill_check(const gdn_dims &d, std::string &why);
-cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const void *qkv, const void *z,
-                           const void *alpha, const void *beta_raw, float *state, float *conv_state,
-                           void *out, void *workspace, int *d_status, cudaStream_t stream);
 }  // namespace gdn
 
 namespace {

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <string>
 
 #include "gdn_verify.h"
 
@@ -34,9 +35,29 @@ struct RollbackArgs {
     int *d_status;
 };
 
+// Everything one chunkwise prefill launch needs (d_k = d_v = 128, W = 4).
+struct PrefillArgs {
+    int B, Hk, Hv, L, C, r;           // L: prompt tokens per slot; C: conv channels; r = Hv / Hk
+    float rms_eps, l2_eps, q_scale;
+    const float *conv_w, *A_log, *dt_bias, *norm_w;
+    const void *qkv, *z, *alpha, *beta_raw;
+    float *state, *conv_state;
+    void *out;
+    float *scratch;                   // per-(slot, value head) scratch, prefill_workspace_bytes in total
+    int *d_status;
+};
+
 // Returns a cudaError_t of the launch (cudaSuccess when enqueued).
 cudaError_t launch_verify(const VerifyArgs &a, gdn_dtype act, cudaStream_t stream);
 cudaError_t launch_rollback(const RollbackArgs &a, cudaStream_t stream);
+
+// Prefill: shape check (GDN_OK or a status, reason in why), workspace size,
+// and the launch.
+int prefill_check(const gdn_dims &d, std::string &why);
+size_t prefill_workspace_bytes(const gdn_dims &d);
+cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const void *qkv, const void *z,
+                           const void *alpha, const void *beta_raw, float *state, float *conv_state,
+                           void *out, void *workspace, int *d_status, cudaStream_t stream);
 
 // Choice of CTAs per value head for a verify launch (host heuristic).
 int verify_parts_per_head(int B, int Hv, int r, int dv, int sm_count);

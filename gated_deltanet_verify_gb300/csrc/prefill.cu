@@ -1,75 +1,607 @@
-// prefill.cu -- prefill of a long prompt through the same GDN block.
+// prefill.cu -- chunkwise (WY / UT-transform) prefill of the Gated DeltaNet
+// block on sm_103a tensor cores.
 //
-// First correct path: the prompt is processed as consecutive 64-token
-// segments by the fused verify kernel with capture disabled; state and conv
-// state are carried in place from one segment to the next.  This is the
-// sequential recurrence (bit-for-bit what verify computes), launched L/64
-// times.  No workspace is needed.
+// For a chunk of C = 64 tokens with decays accumulated inside the chunk,
+// Gamma_r = prod_{u<=r} g_u, and the state S0 at the chunk start, the gated
+// delta rule unrolls to (Yang et al., "Parallelizing Linear Transformers with
+// the Delta Rule over Sequence Length", 2024; Yang, Kautz & Hatamizadeh,
+// "Gated Delta Networks", 2025):
+//   A[r][s] = beta_r (Gamma_r / Gamma_s) k_r . k_s   (s < r),   T = (I + A)^-1
+//   W = T diag(beta Gamma) K,   U~ = T diag(beta) V,   U = U~ - W S0
+//   O = diag(Gamma) Q S0 + (Q K^T (.) M) U,   M[r][s] = Gamma_r / Gamma_s (s <= r)
+//   S = Gamma_C S0 + (diag(Gamma_C / Gamma) K)^T U
+// Every dense product runs on tcgen05.mma (kind::tf32, fp32 accumulators in
+// tensor memory) with 3xTF32 operands: each fp32 operand is split into a
+// tf32-exact high part and the remainder, and A.B is taken as hi.hi + hi.lo +
+// lo.hi.  Single-pass tf32 (or bf16) operands are not accurate enough here:
+// the delta rule subtracts nearly equal predictions (U~ against W S0) and the
+// per-token RMSNorm rescales small outputs, so an operand rounding of 2^-11
+// becomes an error of 10-60 % in the outputs; with the split it is ~1e-5.
+//
+// Layout of the work: one CTA per (value head, slot), 256 threads, the fp32
+// state held in registers (thread (j, half) owns S[i][j] for 64 values of i),
+// chunks processed in order.  The products use transposed forms so that the
+// MMA M dimension is always 128 (d_k or d_v):
+//   G   = [K; Q] K^T                               (N 64, K 128) -> A and masked P
+//   W^T = (diag(beta Gamma) K)^T T^T,  U~^T = (diag(beta) V)^T T^T   (N 64, K 64)
+//   U^T = U~^T - S0^T W^T                          (N 64, K 128)
+//   O^T = S0^T (diag(Gamma) Q)^T + U^T P^T         (N 64)
+//   D2  = U^T (diag(Gamma_C / Gamma) K)            (N 128, K 64);  S^T <- Gamma_C S^T + D2
+// Operands are written into shared memory in the canonical K-major,
+// no-swizzle layout (core matrix = 8 rows x 16 bytes); accumulators are read
+// back with tcgen05.ld.  The conv outputs of a chunk and the masked P matrix
+// pass through a per-CTA scratch area of the caller's workspace (it stays in
+// L2).  T = (I + A)^-1 is formed on the CUDA cores by 16 x 16 block inversion.
+// A thread-block cluster spans the value heads of one key head, so the q/k
+// conv channels they all read are rewritten only after a cluster barrier.
 #include "internal.cuh"
 
+#include <cuda_bf16.h>
 #include <string>
 
 namespace gdn {
-size_t verify_smem_bytes(int T, int dk, int dv, int P, int act_bytes);
-
 namespace {
-constexpr int kSegment = 64;
+
+constexpr int kC = 64;                 // chunk length
+constexpr int kD = 128;                // d_k = d_v
+constexpr int kCh = 3 * kD;            // conv channels of one value head: q | k | v
+constexpr int kThreads = 256;
+constexpr int kSpinLimit = 1 << 20;
+constexpr int kTmemCols = 512;
+
+// dynamic shared memory carve-up (bytes)
+constexpr uint32_t kRA = 0;                    // 128 KB: A operand planes; raw chunk inputs at chunk start
+constexpr uint32_t kRB = 128 * 1024;           // 64 KB: B operand planes; T and block temporaries
+constexpr uint32_t kAM = 192 * 1024;           // 16 KB: the A matrix (fp32, 64 x 64)
+constexpr uint32_t kMisc = 208 * 1024;
+constexpr uint32_t kMbar = kMisc;              // 8 B
+constexpr uint32_t kTmemSlot = kMisc + 16;     // 4 B
+constexpr uint32_t kLogG = kMisc + 32;         // 64 floats each
+constexpr uint32_t kBeta = kLogG + 256;
+constexpr uint32_t kGam = kBeta + 256;
+constexpr uint32_t kRinv = kGam + 256;
+constexpr uint32_t kRed = kRinv + 256;         // 4 lane quarters x 64 tokens
+constexpr uint32_t kSmemBytes = kRed + 4 * 64 * 4;
+static_assert(kC + 3 <= 67 && 67 * kCh * 4 <= 128 * 1024, "raw chunk staging fits the A region");
+
+// TMEM columns of the accumulators
+constexpr uint32_t kColG = 0, kColWT = 64, kColUT = 128, kColOT = 192, kColD2 = 256;
+
+// per-CTA scratch (floats): q^, k^, v of the chunk (64 x 128 each), P (64 x 64)
+constexpr size_t kScrQ = 0, kScrK = 64 * 128, kScrV = 2 * 64 * 128, kScrP = 3 * 64 * 128;
+constexpr size_t kScrFloats = 3 * 64 * 128 + 64 * 64;
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float4 load4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+template <typename Act> __device__ __forceinline__ Act from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-int prefill_check(const gdn_dims &d, std::string &why) {
-    if (d.d_k != 32 && d.d_k != 64 && d.d_k != 128) {
-        why = "prefill: d_k must be 32, 64 or 128";
-        return GDN_ERR_SHAPE;
+// ---- 3xTF32 operand planes: canonical K-major, no swizzle -----------------
+// 16-byte group (r, k4) of an R x K operand: core matrix (r/8, k4) of 8 rows x 16 B
+__device__ __forceinline__ uint32_t plane_off(int r, int k4, int K) {
+    return (uint32_t)((((r >> 3) * (K >> 2) + k4) << 7) + ((r & 7) << 4));
+}
+__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+// 4 consecutive k of row r: the tf32 part into the hi plane, the remainder into the lo plane
+__device__ __forceinline__ void put4(unsigned char *hi, unsigned char *lo, int r, int k4, int K, float4 v) {
+    const float4 h = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
+    const float4 l = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
+    const uint32_t off = plane_off(r, k4, K);
+    *reinterpret_cast<float4 *>(hi + off) = h;
+    *reinterpret_cast<float4 *>(lo + off) = l;
+}
+__device__ __forceinline__ void put1(unsigned char *hi, unsigned char *lo, int r, int k, int K, float v) {
+    const float h = tf32_hi(v);
+    const uint32_t off = plane_off(r, k >> 2, K) + ((k & 3) << 2);
+    *reinterpret_cast<float *>(hi + off) = h;
+    *reinterpret_cast<float *>(lo + off) = v - h;
+}
+// item -> (row, 16-byte group) so that consecutive items fill consecutive 16-byte slots
+__device__ __forceinline__ void item_rc(int it, int K, int &r, int &k4) {
+    const int cm = it >> 3, groups = K >> 2;
+    r = (cm / groups) * 8 + (it & 7);
+    k4 = cm % groups;
+}
+
+// ---- tcgen05 ---------------------------------------------------------------
+__device__ __forceinline__ uint64_t make_desc(uint32_t saddr, int K) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)(128 >> 4) << 16;                          // LBO: next core matrix along K
+    d |= (uint64_t)((((uint32_t)K >> 2) * 128) >> 4) << 32;   // SBO: next 8-row group
+    d |= (uint64_t)1 << 46;                                    // descriptor version (sm_100 family)
+    return d;                                                  // no swizzle, base offset 0
+}
+__host__ __device__ constexpr uint32_t idesc_tf32(int N) {
+    // D f32, A and B tf32, both K-major, N >> 3, M = 128 >> 4
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+                 "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+// D (128 x N, fp32 in TMEM) (+)= A (128 x K) . B (N x K)^T with 3xTF32 planes
+__device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo, int K,
+                                     int N, bool accumulate) {
+    const uint32_t id = idesc_tf32(N);
+    for (int ks = 0; ks < K / 8; ++ks) {
+        const uint32_t o = (uint32_t)ks * 256u;                // 8 tf32 = two core matrices along K
+        const uint64_t ah = make_desc(a_hi + o, K), al = make_desc(a_lo + o, K);
+        const uint64_t bh = make_desc(b_hi + o, K), bl = make_desc(b_lo + o, K);
+        mma_tf32(d, ah, bh, id, (ks > 0 || accumulate) ? 1u : 0u);
+        mma_tf32(d, ah, bl, id, 1u);
+        mma_tf32(d, al, bh, id, 1u);
     }
-    if (d.d_v % 8 || d.d_v > 256) {
-        why = "prefill: d_v must be a multiple of 8 up to 256";
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+// 16 fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}\n"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+template <typename Act>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs a) {
+    extern __shared__ __align__(1024) unsigned char sm[];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int tl = tid & 127, half = tid >> 7;          // TMEM lane of this thread, column half
+    const int h = blockIdx.x, s = blockIdx.y;
+    const int Hk = a.Hk, Hv = a.Hv, L = a.L, C = a.C;
+    const int kh = h / a.r;
+    const bool qk_writer = (h % a.r) == 0;
+    const Act *qkv = static_cast<const Act *>(a.qkv);
+    float *scr = a.scratch + ((size_t)s * Hv + h) * kScrFloats;
+    float *qs = scr + kScrQ, *ks = scr + kScrK, *vs = scr + kScrV, *ps = scr + kScrP;
+    float *raw = reinterpret_cast<float *>(sm + kRA);                 // [67][384] raw window of the chunk
+    float *AM = reinterpret_cast<float *>(sm + kAM);
+    float *Tm = reinterpret_cast<float *>(sm + kRB + 32 * 1024);      // T (fp32, 64 x 64)
+    float *Xb = reinterpret_cast<float *>(sm + kRB + 48 * 1024);      // block-inversion temporaries
+    float *logG = reinterpret_cast<float *>(sm + kLogG);
+    float *betas = reinterpret_cast<float *>(sm + kBeta);
+    float *gam = reinterpret_cast<float *>(sm + kGam);
+    float *rinv = reinterpret_cast<float *>(sm + kRinv);
+    float *red = reinterpret_cast<float *>(sm + kRed);
+    unsigned char *RA = sm + kRA, *RB = sm + kRB;
+    const uint32_t sRA = smem_u32(RA), sRB = smem_u32(RB);
+    const uint32_t mbar = smem_u32(sm + kMbar);
+    uint32_t phase = 0;
+    bool timed_out = false;
+
+    // global conv channel of local channel ch (q 0..127, k 128..255, v 256..383)
+    auto gch = [&](int ch) -> int {
+        if (ch < kD) return kh * kD + ch;
+        if (ch < 2 * kD) return Hk * kD + kh * kD + (ch - kD);
+        return 2 * Hk * kD + h * kD + (ch - 2 * kD);
+    };
+
+    // ---- set-up: TMEM, mbarrier, state rows into registers
+    if (wid == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                         smem_u32(sm + kTmemSlot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+    }
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(mbar));
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + kTmemSlot);
+    const uint32_t tq = (uint32_t)(32 * (wid & 3)) << 16;         // this warp's TMEM lane quarter
+
+    // thread (j = tl, half) keeps S^T[j][64 half .. 64 half + 63] = S[i][j]
+    float St[64];
+    {
+        const float *src = a.state + (((size_t)s * Hv + h) * kD + tl) * kD + 64 * half;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const float4 v = *reinterpret_cast<const float4 *>(src + 4 * q);
+            St[4 * q] = v.x; St[4 * q + 1] = v.y; St[4 * q + 2] = v.z; St[4 * q + 3] = v.w;
+        }
+    }
+
+    auto commit_wait = [&]() {
+        if (tid == 0) mma_commit(mbar);
+        bool ok = timed_out;           // after one timeout the rest of the launch only drains
+        for (int it = 0; it < kSpinLimit && !ok; ++it) ok = mbar_try(mbar, phase & 1u);
+        if (!ok) timed_out = true;
+        phase ^= 1u;
+        fence_after_sync();
+    };
+    auto publish = [&]() {              // generic-proxy smem writes -> visible to the tensor core
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    };
+
+    const int n_chunks = (L + kC - 1) / kC;
+    for (int c = 0; c < n_chunks; ++c) {
+        const int t0 = c * kC, n = min(kC, L - t0);
+
+        // ---------------- (a) raw window rows t0-3 .. t0+63 -> smem (fp32), gates
+        for (int it = tid; it < (kC + 3) * (kCh / 4); it += kThreads) {
+            const int row = it / (kCh / 4), ch = 4 * (it % (kCh / 4));
+            const int t = t0 - 3 + row;
+            const int g = gch(ch);
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < 0) v = load4(a.conv_state + ((size_t)s * 3 + (3 + t)) * C + g);   // before the prompt
+            else if (t < L) v = load4(qkv + ((size_t)s * L + t) * C + g);
+            *reinterpret_cast<float4 *>(raw + row * kCh + ch) = v;
+        }
+        if (tid < kC) {                    // gates; padded tokens: no decay, no write
+            float lg = 0.f, b = 0.f;
+            if (tid < n) {
+                const size_t idx = ((size_t)s * L + t0 + tid) * Hv + h;
+                const float x = to_f32(static_cast<const Act *>(a.alpha)[idx]) + __ldg(a.dt_bias + h);
+                const float sp = x > 20.0f ? x : log1pf(expf(x));
+                lg = -expf(__ldg(a.A_log + h)) * sp;
+                b = 1.0f / (1.0f + expf(-to_f32(static_cast<const Act *>(a.beta_raw)[idx])));
+            }
+            logG[tid] = lg;
+            betas[tid] = b;
+        }
+        __syncthreads();
+        if (c == 0) {
+            // every CTA of the cluster has read the old conv state (q/k channels are shared)
+            asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+        }
+        if (tid == 0) {                    // Gamma = exp(cumsum(log g)) inside the chunk
+            float acc = 0.f;
+            for (int t = 0; t < kC; ++t) {
+                acc += logG[t];
+                logG[t] = acc;
+                gam[t] = expf(acc);
+            }
+        }
+        // conv + SiLU: thread per channel, sliding window over the 64 tokens; into scratch
+        for (int ch = tid; ch < kCh; ch += kThreads) {
+            const int g = gch(ch);
+            const float w0 = __ldg(a.conv_w + g), w1 = __ldg(a.conv_w + C + g), w2 = __ldg(a.conv_w + 2 * C + g),
+                        w3 = __ldg(a.conv_w + 3 * C + g);
+            float x0 = raw[ch], x1 = raw[kCh + ch], x2 = raw[2 * kCh + ch];
+            float *dst = ch < kD ? qs + ch : (ch < 2 * kD ? ks + (ch - kD) : vs + (ch - 2 * kD));
+            for (int t = 0; t < kC; ++t) {
+                const float x3 = raw[(t + 3) * kCh + ch];
+                const float y = silu(fmaf(w3, x3, fmaf(w2, x2, fmaf(w1, x1, w0 * x0))));
+                dst[t * kD] = t < n ? y : 0.f;
+                x0 = x1; x1 = x2; x2 = x3;
+            }
+        }
+        __syncthreads();
+        // L2 norms of q and k rows (a zero padded row stays zero)
+        for (int t = wid; t < kC; t += kThreads / 32) {
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                float *row = (part ? ks : qs) + t * kD + 4 * lane;
+                float4 v = *reinterpret_cast<float4 *>(row);
+                float ss = v.x * v.x;
+                ss = fmaf(v.y, v.y, ss); ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+                const float inv = 1.0f / sqrtf(ss + a.l2_eps);
+                v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
+                *reinterpret_cast<float4 *>(row) = v;
+            }
+        }
+        __syncthreads();
+
+        // ---------------- (b) G = [K; Q] K^T
+        for (int it = tid; it < 128 * 32; it += kThreads) {
+            int m, k4;
+            item_rc(it, 128, m, k4);
+            const float *src = (m < kC ? ks + m * kD : qs + (m - kC) * kD) + 4 * k4;
+            put4(RA, RA + 64 * 1024, m, k4, 128, *reinterpret_cast<const float4 *>(src));
+        }
+        publish();
+        if (tid == 0) mma3(tmem + kColG, sRA, sRA + 64 * 1024, sRA, sRA + 64 * 1024, 128, 64, false);
+        commit_wait();
+        {
+            float g32[32];
+            tmem_ld16(tmem + tq + kColG + 32 * half, g32);
+            tmem_ld16(tmem + tq + kColG + 32 * half + 16, g32 + 16);
+            if (tl < kC) {                 // A[r][s] = beta_r Gamma_r / Gamma_s k_r.k_s for s < r
+                const int r = tl;
+                for (int q = 0; q < 32; ++q) {
+                    const int sc = 32 * half + q;
+                    AM[r * kC + sc] = sc < r ? betas[r] * expf(logG[r] - logG[sc]) * g32[q] : 0.f;
+                }
+            } else {                       // P[r][s] = q_r.k_s Gamma_r / Gamma_s for s <= r
+                const int r = tl - kC;
+                for (int q = 0; q < 32; ++q) {
+                    const int sc = 32 * half + q;
+                    ps[r * kC + sc] = sc <= r ? expf(logG[r] - logG[sc]) * g32[q] : 0.f;
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---------------- (c) T = (I + A)^-1, 16 x 16 blocks
+        // diagonal blocks: forward substitution, one column per thread
+        if (tid < kC) {
+            const int b = tid >> 4, col = tid & 15, o = 16 * b;
+            for (int r = 0; r < 16; ++r) {
+                float acc = r == col ? 1.f : 0.f;
+                for (int m = col; m < r; ++m) acc = fmaf(-AM[(o + r) * kC + o + m], Tm[(o + m) * kC + o + col], acc);
+                Tm[(o + r) * kC + o + col] = acc;
+            }
+            for (int r = 0; r < 16; ++r)          // the strictly upper blocks of this block column are zero
+                for (int bb = 0; bb < b; ++bb) Tm[(16 * bb + r) * kC + o + col] = 0.f;
+        }
+        __syncthreads();
+        // off-diagonal blocks by distance: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
+        for (int dist = 1; dist < 4; ++dist) {
+            const int nb = 4 - dist;               // blocks (j + dist, j), j < nb
+            for (int e = tid; e < nb * 256; e += kThreads) {
+                const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15, i = j + dist;
+                float x = 0.f;
+                for (int kb = j; kb < i; ++kb)
+                    for (int m = 0; m < 16; ++m)
+                        x = fmaf(AM[(16 * i + rr) * kC + 16 * kb + m], Tm[(16 * kb + m) * kC + 16 * j + cc], x);
+                Xb[e] = x;
+            }
+            __syncthreads();
+            for (int e = tid; e < nb * 256; e += kThreads) {
+                const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15, i = j + dist;
+                float t = 0.f;
+                for (int m = 0; m < 16; ++m) t = fmaf(Tm[(16 * i + rr) * kC + 16 * i + m], Xb[(j << 8) + m * 16 + cc], t);
+                Tm[(16 * i + rr) * kC + 16 * j + cc] = -t;
+            }
+            __syncthreads();
+        }
+        // B = T (64 x 64) in RB[0, 32K); A1 = (diag(beta Gamma) K)^T, A2 = (diag(beta) V)^T in RA
+        for (int it = tid; it < 64 * 16; it += kThreads) {
+            int r, k4;
+            item_rc(it, 64, r, k4);
+            put4(RB, RB + 16 * 1024, r, k4, 64, *reinterpret_cast<const float4 *>(Tm + r * kC + 4 * k4));
+        }
+        for (int it = tid; it < 128 * 16; it += kThreads) {
+            int i, k4;
+            item_rc(it, 64, i, k4);
+            float kv[4], vv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int sr = 4 * k4 + e;
+                kv[e] = betas[sr] * gam[sr] * ks[sr * kD + i];
+                vv[e] = betas[sr] * vs[sr * kD + i];
+            }
+            put4(RA, RA + 32 * 1024, i, k4, 64, make_float4(kv[0], kv[1], kv[2], kv[3]));
+            put4(RA + 64 * 1024, RA + 96 * 1024, i, k4, 64, make_float4(vv[0], vv[1], vv[2], vv[3]));
+        }
+        publish();
+        if (tid == 0) {
+            mma3(tmem + kColWT, sRA, sRA + 32 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
+            mma3(tmem + kColUT, sRA + 64 * 1024, sRA + 96 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
+        }
+        commit_wait();
+
+        // ---------------- (d) U^T = U~^T - S0^T W^T
+        {
+            // B = -W (64 x 128): this thread holds W[r][i = tl] for its 32 values of r
+            float w32[32];
+            tmem_ld16(tmem + tq + kColWT + 32 * half, w32);
+            tmem_ld16(tmem + tq + kColWT + 32 * half + 16, w32 + 16);
+            for (int q = 0; q < 32; ++q) put1(RB, RB + 32 * 1024, 32 * half + q, tl, 128, -w32[q]);
+            // A = S0^T (128 x 128) from the registers
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                put4(RA, RA + 64 * 1024, tl, 16 * half + q, 128,
+                     make_float4(St[4 * q], St[4 * q + 1], St[4 * q + 2], St[4 * q + 3]));
+        }
+        publish();
+        if (tid == 0) mma3(tmem + kColUT, sRA, sRA + 64 * 1024, sRB, sRB + 32 * 1024, 128, 64, true);
+        commit_wait();
+
+        // ---------------- (e) O^T = S0^T (diag(Gamma) Q)^T
+        for (int it = tid; it < 64 * 32; it += kThreads) {
+            int r, k4;
+            item_rc(it, 128, r, k4);
+            float4 v = *reinterpret_cast<const float4 *>(qs + r * kD + 4 * k4);
+            const float gr = gam[r];
+            v.x *= gr; v.y *= gr; v.z *= gr; v.w *= gr;
+            put4(RB, RB + 32 * 1024, r, k4, 128, v);
+        }
+        publish();
+        if (tid == 0) mma3(tmem + kColOT, sRA, sRA + 64 * 1024, sRB, sRB + 32 * 1024, 128, 64, false);
+        commit_wait();
+
+        // ---------------- (f) O^T += U^T P^T;  D2 = U^T (diag(Gamma_C / Gamma) K)
+        {
+            float u32[32];
+            tmem_ld16(tmem + tq + kColUT + 32 * half, u32);
+            tmem_ld16(tmem + tq + kColUT + 32 * half + 16, u32 + 16);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                put4(RA, RA + 32 * 1024, tl, 8 * half + q, 64,
+                     make_float4(u32[4 * q], u32[4 * q + 1], u32[4 * q + 2], u32[4 * q + 3]));
+        }
+        for (int it = tid; it < 64 * 16; it += kThreads) {
+            int r, k4;
+            item_rc(it, 64, r, k4);
+            put4(RB, RB + 16 * 1024, r, k4, 64, *reinterpret_cast<const float4 *>(ps + r * kC + 4 * k4));
+        }
+        for (int it = tid; it < 128 * 16; it += kThreads) {
+            int i, k4;
+            item_rc(it, 64, i, k4);
+            float kv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int sr = 4 * k4 + e;
+                kv[e] = expf(logG[kC - 1] - logG[sr]) * ks[sr * kD + i];
+            }
+            put4(RA + 64 * 1024, RA + 96 * 1024, i, k4, 64, make_float4(kv[0], kv[1], kv[2], kv[3]));
+        }
+        publish();
+        if (tid == 0) {
+            mma3(tmem + kColOT, sRA, sRA + 32 * 1024, sRB, sRB + 16 * 1024, 64, 64, true);
+            mma3(tmem + kColD2, sRA, sRA + 32 * 1024, sRA + 64 * 1024, sRA + 96 * 1024, 64, 128, false);
+        }
+        commit_wait();
+
+        // ---------------- (g) outputs (gated RMSNorm) and the state update
+        {
+            float o32[32];
+            tmem_ld16(tmem + tq + kColOT + 32 * half, o32);
+            tmem_ld16(tmem + tq + kColOT + 32 * half + 16, o32 + 16);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                o32[q] *= a.q_scale;
+                float sq = o32[q] * o32[q];
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, m);
+                if (lane == 0) red[(wid & 3) * 64 + 32 * half + q] = sq;     // lane quarter x token
+            }
+            __syncthreads();
+            if (tid < kC) {
+                const float tot = (red[tid] + red[64 + tid]) + (red[128 + tid] + red[192 + tid]);
+                rinv[tid] = 1.0f / sqrtf(tot / float(kD) + a.rms_eps);
+            }
+            __syncthreads();
+            Act *out = static_cast<Act *>(a.out);
+            const Act *z = static_cast<const Act *>(a.z);
+            const float nw = __ldg(a.norm_w + tl);
+            for (int q = 0; q < 32; ++q) {
+                const int t = 32 * half + q;
+                if (t < n) {
+                    const size_t o_idx = ((size_t)s * L + t0 + t) * Hv * kD + (size_t)h * kD + tl;
+                    out[o_idx] = from_f32<Act>(o32[q] * rinv[t] * nw * silu(to_f32(z[o_idx])));
+                }
+            }
+            // S^T <- Gamma_C S^T + D2
+            const float gc = gam[kC - 1];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float d16[16];
+                tmem_ld16(tmem + tq + kColD2 + 64 * half + 16 * q4, d16);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) St[16 * q4 + e] = fmaf(gc, St[16 * q4 + e], d16[e]);
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- final state, conv state, TMEM release
+    {
+        float *dst = a.state + (((size_t)s * Hv + h) * kD + tl) * kD + 64 * half;
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            *reinterpret_cast<float4 *>(dst + 4 * q) =
+                make_float4(St[4 * q], St[4 * q + 1], St[4 * q + 2], St[4 * q + 3]);
+    }
+    // the new conv state is the last 3 window rows; rows before the prompt are old conv-state rows
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+    for (int ch = tid; ch < kCh; ch += kThreads) {
+        if (ch < 2 * kD && !qk_writer) continue;
+        const int g = gch(ch);
+        float *cs = a.conv_state + (size_t)s * 3 * C + g;
+        float nv[3];
+        for (int rr = 0; rr < 3; ++rr) {
+            const int t = L - 3 + rr;
+            nv[rr] = t >= 0 ? to_f32(qkv[((size_t)s * L + t) * C + g]) : cs[(size_t)(3 + t) * C];
+        }
+        for (int rr = 0; rr < 3; ++rr) cs[(size_t)rr * C] = nv[rr];
+    }
+    if (timed_out && tid == 0 && a.d_status) atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TIMEOUT));
+    fence_before_sync();
+    __syncthreads();
+    if (wid == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
+}
+
+}  // namespace
+
+int prefill_check(const gdn_dims &d, std::string &why) {
+    if (d.d_k != kD || d.d_v != kD) {
+        why = "prefill: d_k and d_v must be 128";
         return GDN_ERR_SHAPE;
     }
     if (d.n_slots > 65535) {
         why = "prefill: n_slots must be <= 65535";
         return GDN_ERR_SHAPE;
     }
-    const int r = d.n_v_heads / d.n_qk_heads;
-    if (verify_parts_per_head(d.n_slots, d.n_v_heads, r, d.d_v, 0) == 0) {
-        why = "prefill: H_v/H_k too large for one thread-block cluster";
+    if (d.n_v_heads / d.n_qk_heads > 8) {
+        why = "prefill: at most 8 value heads per key head (one thread-block cluster)";
         return GDN_ERR_SHAPE;
     }
     return GDN_OK;
 }
 
 size_t prefill_workspace_bytes(const gdn_dims &d) {
-    (void)d;
-    return 0;
+    return (size_t)d.n_slots * d.n_v_heads * kScrFloats * sizeof(float);
+}
+
+static cudaError_t launch_prefill_args(const PrefillArgs &a, gdn_dtype act, cudaStream_t stream) {
+    const bool bf = act == GDN_BF16;
+    void (*kern)(PrefillArgs) = bf ? prefill_kernel<__nv_bfloat16> : prefill_kernel<float>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.Hv, a.B, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = a.r;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const void *qkv, const void *z,
                            const void *alpha, const void *beta_raw, float *state, float *conv_state,
                            void *out, void *workspace, int *d_status, cudaStream_t stream) {
-    (void)workspace;
-    const int act_bytes = d.act_dtype == GDN_BF16 ? 2 : 4;
-    const int r = d.n_v_heads / d.n_qk_heads;
-    VerifyArgs a{};
-    a.B = d.n_slots; a.Hk = d.n_qk_heads; a.Hv = d.n_v_heads; a.dk = d.d_k; a.dv = d.d_v;
-    a.C = 2 * d.n_qk_heads * d.d_k + d.n_v_heads * d.d_v; a.r = r;
-    a.P = verify_parts_per_head(d.n_slots, d.n_v_heads, r, d.d_v, 0);
-    a.Ts = d.n_tokens;
+    PrefillArgs a{};
+    a.B = d.n_slots; a.Hk = d.n_qk_heads; a.Hv = d.n_v_heads; a.L = d.n_tokens;
+    a.C = 2 * d.n_qk_heads * kD + d.n_v_heads * kD; a.r = d.n_v_heads / d.n_qk_heads;
     a.rms_eps = d.rms_eps; a.l2_eps = d.l2_eps; a.q_scale = d.q_scale;
     a.conv_w = p.conv_w; a.A_log = p.A_log; a.dt_bias = p.dt_bias; a.norm_w = p.norm_w;
-    a.state = state; a.conv_state = conv_state; a.cap_state = nullptr; a.cap_conv = nullptr;
+    a.qkv = qkv; a.z = z; a.alpha = alpha; a.beta_raw = beta_raw;
+    a.state = state; a.conv_state = conv_state; a.out = out;
+    a.scratch = static_cast<float *>(workspace);
     a.d_status = d_status;
-    const size_t Cb = size_t(a.C) * act_bytes, Zb = size_t(d.n_v_heads) * d.d_v * act_bytes,
-                 Gb = size_t(d.n_v_heads) * act_bytes;
-    for (int t0 = 0; t0 < d.n_tokens; t0 += kSegment) {
-        a.T = (d.n_tokens - t0 < kSegment) ? d.n_tokens - t0 : kSegment;
-        a.qkv = static_cast<const char *>(qkv) + t0 * Cb;
-        a.z = static_cast<const char *>(z) + t0 * Zb;
-        a.alpha = static_cast<const char *>(alpha) + t0 * Gb;
-        a.beta_raw = static_cast<const char *>(beta_raw) + t0 * Gb;
-        a.out = static_cast<char *>(out) + t0 * Zb;
-        cudaError_t e = launch_verify(a, d.act_dtype, stream);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    return launch_prefill_args(a, d.act_dtype, stream);
 }
 
 }  // namespace gdn
