@@ -34,7 +34,10 @@ GDN_F32 = 0
 GDN_BF16 = 1
 
 EXPORTED_SYMBOLS = ("gdn_verify_forward", "gdn_rollback", "gdn_prefill_workspace_bytes",
-                    "gdn_prefill_chunked", "gdn_last_error", "gdn_version")
+                    "gdn_prefill_chunked", "gdn_prefill_chunked_static", "gdn_last_error", "gdn_version")
+
+# size of the library's built-in prefill scratch (GDN_PREFILL_STATIC_SCRATCH_BYTES)
+PREFILL_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class GdnError(RuntimeError):
@@ -83,6 +86,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_prefill_chunked.argtypes = ([ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 8 +
                                           [ctypes.c_size_t, vp, vp])
         L.gdn_prefill_chunked.restype = ip
+        L.gdn_prefill_chunked_static.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 9
+        L.gdn_prefill_chunked_static.restype = ip
         L.gdn_last_error.restype = ctypes.c_char_p
         L.gdn_version.restype = ctypes.c_char_p
         _lib = L
@@ -147,3 +152,11 @@ def gdn_prefill_chunked(dims: Dims, params: LayerParams, qkv, z, alpha, beta_raw
                                      _ptr(alpha), _ptr(beta_raw), _ptr(state), _ptr(conv_state), _ptr(out),
                                      _ptr(workspace), ctypes.c_size_t(ws_bytes), _ptr(d_status),
                                      _stream(stream)))
+
+
+def gdn_prefill_chunked_static(dims: Dims, params: LayerParams, qkv, z, alpha, beta_raw, state, conv_state, out,
+                               d_status=None, stream=None) -> None:
+    """gdn_prefill_chunked with the library's built-in scratch instead of a workspace."""
+    _check(lib().gdn_prefill_chunked_static(ctypes.byref(dims), ctypes.byref(params), _ptr(qkv), _ptr(z),
+                                            _ptr(alpha), _ptr(beta_raw), _ptr(state), _ptr(conv_state),
+                                            _ptr(out), _ptr(d_status), _stream(stream)))

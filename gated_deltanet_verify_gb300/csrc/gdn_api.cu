@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 namespace gdn {
@@ -96,6 +97,33 @@ int verify_parts_per_head(int B, int Hv, int r, int dv, int sm_count) {
 }
 
 }  // namespace gdn
+
+// ---- prefill with library-owned scratch -----------------------------------
+// One fixed scratch array per device (the module's device globals are per
+// context); its device address is looked up once per device and cached.
+namespace {
+__device__ __align__(256) unsigned char g_prefill_scratch[GDN_PREFILL_STATIC_SCRATCH_BYTES];
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices];
+
+int static_scratch(void **addr) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(GDN_ERR_ARG, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_prefill_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(GDN_ERR_LAUNCH, "looking up the prefill scratch array failed: %s", cudaGetErrorString(e));
+        g_scratch_addr[dev] = p;
+    }
+    *addr = g_scratch_addr[dev];
+    return GDN_OK;
+}
+}  // namespace
 
 extern "C" {
 
@@ -200,6 +228,24 @@ int gdn_prefill_chunked(const gdn_dims *dims, const gdn_layer_params *params, co
                                         workspace, d_status, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "prefill launch failed: %s", cudaGetErrorString(e));
     return GDN_OK;
+}
+
+int gdn_prefill_chunked_static(const gdn_dims *dims, const gdn_layer_params *params, const void *qkv,
+                               const void *z, const void *alpha, const void *beta_raw, float *state,
+                               float *conv_state, void *out, int *d_status, void *stream) {
+    g_err.clear();
+    int rc = check_common(dims);
+    if (rc) return rc;
+    std::string why;
+    if ((rc = gdn::prefill_check(*dims, why))) return fail(rc, "%s", why.c_str());
+    const size_t need = gdn::prefill_workspace_bytes(*dims);
+    if (need > GDN_PREFILL_STATIC_SCRATCH_BYTES)
+        return fail(GDN_ERR_WORKSPACE, "prefill needs %zu bytes of scratch; the built-in array holds %zu", need,
+                    (size_t)GDN_PREFILL_STATIC_SCRATCH_BYTES);
+    void *scratch = nullptr;
+    if (need > 0 && (rc = static_scratch(&scratch))) return rc;
+    return gdn_prefill_chunked(dims, params, qkv, z, alpha, beta_raw, state, conv_state, out, scratch,
+                               need > 0 ? (size_t)GDN_PREFILL_STATIC_SCRATCH_BYTES : 0, d_status, stream);
 }
 
 }  // extern "C"

@@ -148,6 +148,32 @@ int gdn_prefill_chunked(const gdn_dims *dims, const gdn_layer_params *params,
                         float *state, float *conv_state, void *out,
                         void *workspace, size_t ws_bytes, int *d_status, void *stream);
 
+/*
+ * gdn_prefill_chunked without a caller workspace: the same computation, with
+ * its scratch taken from a fixed array inside this library.  The method itself
+ * has no such call; it exists for callers that cannot allocate device memory
+ * at the point where they prefill -- a host program that only holds the
+ * buffers it was handed, or a server running under a fixed device-memory
+ * budget whose allocator must not grow -- and so have no workspace to pass.
+ *
+ * Limit: the call needs gdn_prefill_workspace_bytes(dims) bytes of scratch and
+ * the built-in array holds GDN_PREFILL_STATIC_SCRATCH_BYTES (16 MiB, one array
+ * per device, reserved when the call is first used on that device); larger
+ * dims are rejected with GDN_ERR_WORKSPACE before anything is enqueued.  The
+ * scratch needs no initialisation.
+ *
+ * The first call on a device looks the array's device address up (with that
+ * device current) and caches it, so make that first call before any stream
+ * capture on the device.  Calls that overlap on one device -- different
+ * streams, or host threads, with no ordering between them -- share the one
+ * array and race: order them (one stream, or events).  Everything else,
+ * including the error codes, is as for gdn_prefill_chunked.
+ */
+#define GDN_PREFILL_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+int gdn_prefill_chunked_static(const gdn_dims *dims, const gdn_layer_params *params,
+                               const void *qkv, const void *z, const void *alpha, const void *beta_raw,
+                               float *state, float *conv_state, void *out, int *d_status, void *stream);
+
 /* Message for the last non-OK return on this thread ("" if none). */
 const char *gdn_last_error(void);
 
