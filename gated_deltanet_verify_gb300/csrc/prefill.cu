@@ -52,34 +52,32 @@ constexpr int kTmemCols = 512;
 // dynamic shared memory carve-up (bytes)
 constexpr uint32_t kRA = 0;                    // 128 KB: A operand planes; raw chunk inputs at chunk start
 constexpr uint32_t kRB = 128 * 1024;           // 64 KB: B operand planes; T and block temporaries
-constexpr uint32_t kAM = 192 * 1024;           // 16 KB: the A matrix (fp32, 64 x 64)
-constexpr uint32_t kMisc = 208 * 1024;
-constexpr uint32_t kMbar = kMisc;              // 8 B
+constexpr uint32_t kAM = 192 * 1024;           // 16 KB: A (fp32, 64 x 64), stored transposed [s][r]
+constexpr uint32_t kPT = 208 * 1024;           // 16 KB: P (fp32, 64 x 64), stored transposed [s][r]
+constexpr uint32_t kMisc = 224 * 1024;
+constexpr uint32_t kMbar = kMisc;              // 8 B: tensor-core completion
+constexpr uint32_t kRawBar = kMisc + 8;        // 8 B: raw window copies
 constexpr uint32_t kTmemSlot = kMisc + 16;     // 4 B
 constexpr uint32_t kLogG = kMisc + 32;         // 64 floats each
 constexpr uint32_t kBeta = kLogG + 256;
 constexpr uint32_t kGam = kBeta + 256;
 constexpr uint32_t kRinv = kGam + 256;
-constexpr uint32_t kRed = kRinv + 256;         // 4 lane quarters x 64 tokens
+constexpr uint32_t kInvQ = kRinv + 256;        // 1 / ||q_t||, 1 / ||k_t||
+constexpr uint32_t kInvK = kInvQ + 256;
+constexpr uint32_t kRed = kInvK + 256;         // 4 lane quarters x 64 tokens
 constexpr uint32_t kSmemBytes = kRed + 4 * 64 * 4;
-static_assert(kC + 3 <= 67 && 67 * kCh * 4 <= 128 * 1024, "raw chunk staging fits the A region");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+static_assert((kC + 3) * kCh * 4 <= 128 * 1024, "raw chunk window fits the A region");
 
 // TMEM columns of the accumulators
 constexpr uint32_t kColG = 0, kColWT = 64, kColUT = 128, kColOT = 192, kColD2 = 256;
 
-// per-CTA scratch (floats): q^, k^, v of the chunk (64 x 128 each), P (64 x 64)
-constexpr size_t kScrQ = 0, kScrK = 64 * 128, kScrV = 2 * 64 * 128, kScrP = 3 * 64 * 128;
-constexpr size_t kScrFloats = 3 * 64 * 128 + 64 * 64;
+// per-CTA scratch (floats): conv outputs q, k, v of the chunk (64 x 128 each, not normalised)
+constexpr size_t kScrQ = 0, kScrK = 64 * 128, kScrV = 2 * 64 * 128;
+constexpr size_t kScrFloats = 3 * 64 * 128;
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
-__device__ __forceinline__ float4 load4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
-__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
-    const uint2 u = *reinterpret_cast<const uint2 *>(p);
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-    return make_float4(a.x, a.y, b.x, b.y);
-}
 template <typename Act> __device__ __forceinline__ Act from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
@@ -178,6 +176,18 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], %1;\n\t}\n" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+// global -> own shared memory, completion counted in bytes on an mbarrier
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 template <typename Act>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -189,20 +199,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
     const bool qk_writer = (h % a.r) == 0;
     const Act *qkv = static_cast<const Act *>(a.qkv);
     float *scr = a.scratch + ((size_t)s * Hv + h) * kScrFloats;
-    float *qs = scr + kScrQ, *ks = scr + kScrK, *vs = scr + kScrV, *ps = scr + kScrP;
-    float *raw = reinterpret_cast<float *>(sm + kRA);                 // [67][384] raw window of the chunk
-    float *AM = reinterpret_cast<float *>(sm + kAM);
-    float *Tm = reinterpret_cast<float *>(sm + kRB + 32 * 1024);      // T (fp32, 64 x 64)
+    float *qs = scr + kScrQ, *ks = scr + kScrK, *vs = scr + kScrV;
+    const Act *rawA = reinterpret_cast<const Act *>(sm + kRA);        // [67][384] raw window of the chunk
+    float *hist = reinterpret_cast<float *>(sm + kRB);                // [3][384] conv state (first chunk only)
+    float *AMt = reinterpret_cast<float *>(sm + kAM);
+    float *Pt = reinterpret_cast<float *>(sm + kPT);
+    float *Tm = reinterpret_cast<float *>(sm + kRB + 32 * 1024);      // T (fp32, 64 x 64, row-major)
     float *Xb = reinterpret_cast<float *>(sm + kRB + 48 * 1024);      // block-inversion temporaries
     float *logG = reinterpret_cast<float *>(sm + kLogG);
     float *betas = reinterpret_cast<float *>(sm + kBeta);
     float *gam = reinterpret_cast<float *>(sm + kGam);
     float *rinv = reinterpret_cast<float *>(sm + kRinv);
+    float *invq = reinterpret_cast<float *>(sm + kInvQ);
+    float *invk = reinterpret_cast<float *>(sm + kInvK);
     float *red = reinterpret_cast<float *>(sm + kRed);
     unsigned char *RA = sm + kRA, *RB = sm + kRB;
     const uint32_t sRA = smem_u32(RA), sRB = smem_u32(RB);
-    const uint32_t mbar = smem_u32(sm + kMbar);
-    uint32_t phase = 0;
+    const uint32_t mbar = smem_u32(sm + kMbar), rawbar = smem_u32(sm + kRawBar);
+    uint32_t phase = 0, raw_phase = 0;
     bool timed_out = false;
 
     // global conv channel of local channel ch (q 0..127, k 128..255, v 256..383)
@@ -221,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
     }
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(mbar));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(rawbar));
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     fence_before_sync();
@@ -255,32 +270,65 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
         fence_after_sync();
     };
 
+    // raw window rows t0-3 .. t0+63 of chunk cc (those inside the prompt) -> smem, by warp 0
+    auto issue_raw = [&](int cc) {
+        const int tt0 = cc * kC;
+        const int row_lo = cc == 0 ? 3 : 0;                 // rows before the prompt come from the conv state
+        const int row_hi = min(kC + 3, L - tt0 + 3);
+        const uint32_t seg = kD * sizeof(Act);
+        if (lane == 0) mbar_arrive_expect_tx(rawbar, (uint32_t)(row_hi - row_lo) * 3u * seg);
+        __syncwarp();
+        for (int row = row_lo + lane; row < row_hi; row += 32) {
+            const Act *src = qkv + ((size_t)s * L + (tt0 - 3 + row)) * C;
+            const uint32_t dst = smem_u32(sm + kRA) + (uint32_t)(row * kCh) * (uint32_t)sizeof(Act);
+            bulk_g2s(dst, src + kh * kD, seg, rawbar);
+            bulk_g2s(dst + seg, src + Hk * kD + kh * kD, seg, rawbar);
+            bulk_g2s(dst + 2 * seg, src + 2 * Hk * kD + h * kD, seg, rawbar);
+        }
+    };
+    auto wait_raw = [&]() {
+        bool ok = timed_out;
+        for (int it = 0; it < kSpinLimit && !ok; ++it) ok = mbar_try(rawbar, raw_phase & 1u);
+        if (!ok) timed_out = true;
+        raw_phase ^= 1u;
+    };
+    // gate inputs of chunk cc (threads tid < 64, one token each)
+    float g_alpha = 0.f, g_beta = 0.f;
+    auto load_gates = [&](int cc) {
+        const int t = cc * kC + tid;
+        if (tid < kC && t < L) {
+            const size_t idx = ((size_t)s * L + t) * Hv + h;
+            g_alpha = to_f32(static_cast<const Act *>(a.alpha)[idx]);
+            g_beta = to_f32(static_cast<const Act *>(a.beta_raw)[idx]);
+        }
+    };
+
+    if (wid == 0) issue_raw(0);
+    load_gates(0);
+    // the three window rows before the prompt: the conv state (fp32)
+    for (int it = tid; it < 3 * (kCh / 4); it += kThreads) {
+        const int row = it / (kCh / 4), ch = 4 * (it % (kCh / 4));
+        *reinterpret_cast<float4 *>(hist + row * kCh + ch) =
+            *reinterpret_cast<const float4 *>(a.conv_state + ((size_t)s * 3 + row) * C + gch(ch));
+    }
+
     const int n_chunks = (L + kC - 1) / kC;
     for (int c = 0; c < n_chunks; ++c) {
         const int t0 = c * kC, n = min(kC, L - t0);
 
-        // ---------------- (a) raw window rows t0-3 .. t0+63 -> smem (fp32), gates
-        for (int it = tid; it < (kC + 3) * (kCh / 4); it += kThreads) {
-            const int row = it / (kCh / 4), ch = 4 * (it % (kCh / 4));
-            const int t = t0 - 3 + row;
-            const int g = gch(ch);
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < 0) v = load4(a.conv_state + ((size_t)s * 3 + (3 + t)) * C + g);   // before the prompt
-            else if (t < L) v = load4(qkv + ((size_t)s * L + t) * C + g);
-            *reinterpret_cast<float4 *>(raw + row * kCh + ch) = v;
-        }
-        if (tid < kC) {                    // gates; padded tokens: no decay, no write
+        // ---------------- (a) gates; the raw window (issued during the previous chunk) arrives
+        if (tid < kC) {                    // padded tokens: no decay, no write
             float lg = 0.f, b = 0.f;
             if (tid < n) {
-                const size_t idx = ((size_t)s * L + t0 + tid) * Hv + h;
-                const float x = to_f32(static_cast<const Act *>(a.alpha)[idx]) + __ldg(a.dt_bias + h);
+                const float x = g_alpha + __ldg(a.dt_bias + h);
                 const float sp = x > 20.0f ? x : log1pf(expf(x));
                 lg = -expf(__ldg(a.A_log + h)) * sp;
-                b = 1.0f / (1.0f + expf(-to_f32(static_cast<const Act *>(a.beta_raw)[idx])));
+                b = 1.0f / (1.0f + expf(-g_beta));
             }
             logG[tid] = lg;
             betas[tid] = b;
         }
+        wait_raw();
         __syncthreads();
         if (c == 0) {
             // every CTA of the cluster has read the old conv state (q/k channels are shared)
@@ -294,44 +342,65 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
                 gam[t] = expf(acc);
             }
         }
-        // conv + SiLU: thread per channel, sliding window over the 64 tokens; into scratch
-        for (int ch = tid; ch < kCh; ch += kThreads) {
+        // conv + SiLU: item = (channel, 16-token segment), sliding window; into scratch
+#pragma unroll 1
+        for (int k = 0; k < 6; ++k) {
+            const int it = tid + k * kThreads;
+            const int ch = it % kCh, tb = 16 * (it / kCh);
             const int g = gch(ch);
             const float w0 = __ldg(a.conv_w + g), w1 = __ldg(a.conv_w + C + g), w2 = __ldg(a.conv_w + 2 * C + g),
                         w3 = __ldg(a.conv_w + 3 * C + g);
-            float x0 = raw[ch], x1 = raw[kCh + ch], x2 = raw[2 * kCh + ch];
+            auto xin = [&](int row) -> float {    // window row (token t0 - 3 + row)
+                return (c == 0 && row < 3) ? hist[row * kCh + ch] : to_f32(rawA[row * kCh + ch]);
+            };
+            float x0 = xin(tb), x1 = xin(tb + 1), x2 = xin(tb + 2);
             float *dst = ch < kD ? qs + ch : (ch < 2 * kD ? ks + (ch - kD) : vs + (ch - 2 * kD));
-            for (int t = 0; t < kC; ++t) {
-                const float x3 = raw[(t + 3) * kCh + ch];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int t = tb + j;
+                const float x3 = xin(t + 3);
                 const float y = silu(fmaf(w3, x3, fmaf(w2, x2, fmaf(w1, x1, w0 * x0))));
                 dst[t * kD] = t < n ? y : 0.f;
                 x0 = x1; x1 = x2; x2 = x3;
             }
         }
         __syncthreads();
-        // L2 norms of q and k rows (a zero padded row stays zero)
-        for (int t = wid; t < kC; t += kThreads / 32) {
+        // inverse L2 norms of the q and k rows (warp per token; a zero padded row stays zero)
+        {
+            float4 v[16];
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                float *row = (part ? ks : qs) + t * kD + 4 * lane;
-                float4 v = *reinterpret_cast<float4 *>(row);
-                float ss = v.x * v.x;
-                ss = fmaf(v.y, v.y, ss); ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+            for (int k = 0; k < 8; ++k) {
+                const int t = wid + 8 * k;
+                v[2 * k] = *reinterpret_cast<const float4 *>(qs + t * kD + 4 * lane);
+                v[2 * k + 1] = *reinterpret_cast<const float4 *>(ks + t * kD + 4 * lane);
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                float ss = v[k].x * v[k].x;
+                ss = fmaf(v[k].y, v[k].y, ss); ss = fmaf(v[k].z, v[k].z, ss); ss = fmaf(v[k].w, v[k].w, ss);
 #pragma unroll
                 for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-                const float inv = 1.0f / sqrtf(ss + a.l2_eps);
-                v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
-                *reinterpret_cast<float4 *>(row) = v;
+                if (lane == 0) ((k & 1) ? invk : invq)[wid + 8 * (k >> 1)] = 1.0f / sqrtf(ss + a.l2_eps);
             }
         }
         __syncthreads();
 
         // ---------------- (b) G = [K; Q] K^T
-        for (int it = tid; it < 128 * 32; it += kThreads) {
-            int m, k4;
-            item_rc(it, 128, m, k4);
-            const float *src = (m < kC ? ks + m * kD : qs + (m - kC) * kD) + 4 * k4;
-            put4(RA, RA + 64 * 1024, m, k4, 128, *reinterpret_cast<const float4 *>(src));
+        {
+            float4 v[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                int m, k4;
+                item_rc(tid + k * kThreads, 128, m, k4);
+                v[k] = *reinterpret_cast<const float4 *>((m < kC ? ks + m * kD : qs + (m - kC) * kD) + 4 * k4);
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                int m, k4;
+                item_rc(tid + k * kThreads, 128, m, k4);
+                const float sc = m < kC ? invk[m] : invq[m - kC];
+                put4(RA, RA + 64 * 1024, m, k4, 128, make_float4(v[k].x * sc, v[k].y * sc, v[k].z * sc, v[k].w * sc));
+            }
         }
         publish();
         if (tid == 0) mma3(tmem + kColG, sRA, sRA + 64 * 1024, sRA, sRA + 64 * 1024, 128, 64, false);
@@ -342,29 +411,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
             tmem_ld16(tmem + tq + kColG + 32 * half + 16, g32 + 16);
             if (tl < kC) {                 // A[r][s] = beta_r Gamma_r / Gamma_s k_r.k_s for s < r
                 const int r = tl;
+                const float br = betas[r], lr = logG[r];
+#pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     const int sc = 32 * half + q;
-                    AM[r * kC + sc] = sc < r ? betas[r] * expf(logG[r] - logG[sc]) * g32[q] : 0.f;
+                    AMt[sc * kC + r] = sc < r ? br * expf(lr - logG[sc]) * g32[q] : 0.f;
                 }
             } else {                       // P[r][s] = q_r.k_s Gamma_r / Gamma_s for s <= r
                 const int r = tl - kC;
+                const float lr = logG[r];
+#pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     const int sc = 32 * half + q;
-                    ps[r * kC + sc] = sc <= r ? expf(logG[r] - logG[sc]) * g32[q] : 0.f;
+                    Pt[sc * kC + r] = sc <= r ? expf(lr - logG[sc]) * g32[q] : 0.f;
                 }
             }
         }
         __syncthreads();
 
         // ---------------- (c) T = (I + A)^-1, 16 x 16 blocks
-        // diagonal blocks: forward substitution, one column per thread
+        // diagonal blocks: forward substitution, one column per thread, in registers
         if (tid < kC) {
             const int b = tid >> 4, col = tid & 15, o = 16 * b;
+            float tc[16];
+#pragma unroll
             for (int r = 0; r < 16; ++r) {
                 float acc = r == col ? 1.f : 0.f;
-                for (int m = col; m < r; ++m) acc = fmaf(-AM[(o + r) * kC + o + m], Tm[(o + m) * kC + o + col], acc);
-                Tm[(o + r) * kC + o + col] = acc;
+#pragma unroll
+                for (int m = 0; m < r; ++m) acc = fmaf(-AMt[(o + m) * kC + o + r], tc[m], acc);
+                tc[r] = acc;
             }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) Tm[(o + r) * kC + o + col] = tc[r];
             for (int r = 0; r < 16; ++r)          // the strictly upper blocks of this block column are zero
                 for (int bb = 0; bb < b; ++bb) Tm[(16 * bb + r) * kC + o + col] = 0.f;
         }
@@ -376,37 +454,55 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
                 const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15, i = j + dist;
                 float x = 0.f;
                 for (int kb = j; kb < i; ++kb)
+#pragma unroll
                     for (int m = 0; m < 16; ++m)
-                        x = fmaf(AM[(16 * i + rr) * kC + 16 * kb + m], Tm[(16 * kb + m) * kC + 16 * j + cc], x);
+                        x = fmaf(AMt[(16 * kb + m) * kC + 16 * i + rr], Tm[(16 * kb + m) * kC + 16 * j + cc], x);
                 Xb[e] = x;
             }
             __syncthreads();
             for (int e = tid; e < nb * 256; e += kThreads) {
                 const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15, i = j + dist;
                 float t = 0.f;
+#pragma unroll
                 for (int m = 0; m < 16; ++m) t = fmaf(Tm[(16 * i + rr) * kC + 16 * i + m], Xb[(j << 8) + m * 16 + cc], t);
                 Tm[(16 * i + rr) * kC + 16 * j + cc] = -t;
             }
             __syncthreads();
         }
         // B = T (64 x 64) in RB[0, 32K); A1 = (diag(beta Gamma) K)^T, A2 = (diag(beta) V)^T in RA
-        for (int it = tid; it < 64 * 16; it += kThreads) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
             int r, k4;
-            item_rc(it, 64, r, k4);
+            item_rc(tid + k * kThreads, 64, r, k4);
             put4(RB, RB + 16 * 1024, r, k4, 64, *reinterpret_cast<const float4 *>(Tm + r * kC + 4 * k4));
         }
-        for (int it = tid; it < 128 * 16; it += kThreads) {
-            int i, k4;
-            item_rc(it, 64, i, k4);
-            float kv[4], vv[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int sr = 4 * k4 + e;
-                kv[e] = betas[sr] * gam[sr] * ks[sr * kD + i];
-                vv[e] = betas[sr] * vs[sr * kD + i];
+        for (int b = 0; b < 2; ++b) {
+            float kv[4][4], vv[4][4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                int i, k4;
+                item_rc(tid + (4 * b + k) * kThreads, 64, i, k4);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    kv[k][e] = ks[(4 * k4 + e) * kD + i];
+                    vv[k][e] = vs[(4 * k4 + e) * kD + i];
+                }
             }
-            put4(RA, RA + 32 * 1024, i, k4, 64, make_float4(kv[0], kv[1], kv[2], kv[3]));
-            put4(RA + 64 * 1024, RA + 96 * 1024, i, k4, 64, make_float4(vv[0], vv[1], vv[2], vv[3]));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                int i, k4;
+                item_rc(tid + (4 * b + k) * kThreads, 64, i, k4);
+                float ka[4], va[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int sr = 4 * k4 + e;
+                    ka[e] = betas[sr] * gam[sr] * invk[sr] * kv[k][e];
+                    va[e] = betas[sr] * vv[k][e];
+                }
+                put4(RA, RA + 32 * 1024, i, k4, 64, make_float4(ka[0], ka[1], ka[2], ka[3]));
+                put4(RA + 64 * 1024, RA + 96 * 1024, i, k4, 64, make_float4(va[0], va[1], va[2], va[3]));
+            }
         }
         publish();
         if (tid == 0) {
@@ -421,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
             float w32[32];
             tmem_ld16(tmem + tq + kColWT + 32 * half, w32);
             tmem_ld16(tmem + tq + kColWT + 32 * half + 16, w32 + 16);
+#pragma unroll
             for (int q = 0; q < 32; ++q) put1(RB, RB + 32 * 1024, 32 * half + q, tl, 128, -w32[q]);
             // A = S0^T (128 x 128) from the registers
 #pragma unroll
@@ -433,13 +530,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
         commit_wait();
 
         // ---------------- (e) O^T = S0^T (diag(Gamma) Q)^T
-        for (int it = tid; it < 64 * 32; it += kThreads) {
-            int r, k4;
-            item_rc(it, 128, r, k4);
-            float4 v = *reinterpret_cast<const float4 *>(qs + r * kD + 4 * k4);
-            const float gr = gam[r];
-            v.x *= gr; v.y *= gr; v.z *= gr; v.w *= gr;
-            put4(RB, RB + 32 * 1024, r, k4, 128, v);
+        {
+            float4 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                int r, k4;
+                item_rc(tid + k * kThreads, 128, r, k4);
+                v[k] = *reinterpret_cast<const float4 *>(qs + r * kD + 4 * k4);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                int r, k4;
+                item_rc(tid + k * kThreads, 128, r, k4);
+                const float gr = gam[r] * invq[r];
+                put4(RB, RB + 32 * 1024, r, k4, 128, make_float4(v[k].x * gr, v[k].y * gr, v[k].z * gr, v[k].w * gr));
+            }
         }
         publish();
         if (tid == 0) mma3(tmem + kColOT, sRA, sRA + 64 * 1024, sRB, sRB + 32 * 1024, 128, 64, false);
@@ -455,56 +560,95 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
                 put4(RA, RA + 32 * 1024, tl, 8 * half + q, 64,
                      make_float4(u32[4 * q], u32[4 * q + 1], u32[4 * q + 2], u32[4 * q + 3]));
         }
-        for (int it = tid; it < 64 * 16; it += kThreads) {
-            int r, k4;
-            item_rc(it, 64, r, k4);
-            put4(RB, RB + 16 * 1024, r, k4, 64, *reinterpret_cast<const float4 *>(ps + r * kC + 4 * k4));
-        }
-        for (int it = tid; it < 128 * 16; it += kThreads) {
-            int i, k4;
-            item_rc(it, 64, i, k4);
-            float kv[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int sr = 4 * k4 + e;
-                kv[e] = expf(logG[kC - 1] - logG[sr]) * ks[sr * kD + i];
+        for (int k = 0; k < 4; ++k) {
+            int r, k4;
+            item_rc(tid + k * kThreads, 64, r, k4);
+            float p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) p[e] = Pt[(4 * k4 + e) * kC + r];
+            put4(RB, RB + 16 * 1024, r, k4, 64, make_float4(p[0], p[1], p[2], p[3]));
+        }
+        {
+            float kv[8][4];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                int i, k4;
+                item_rc(tid + k * kThreads, 64, i, k4);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) kv[k][e] = ks[(4 * k4 + e) * kD + i];
             }
-            put4(RA + 64 * 1024, RA + 96 * 1024, i, k4, 64, make_float4(kv[0], kv[1], kv[2], kv[3]));
+            const float lc = logG[kC - 1];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                int i, k4;
+                item_rc(tid + k * kThreads, 64, i, k4);
+                float ka[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int sr = 4 * k4 + e;
+                    ka[e] = expf(lc - logG[sr]) * invk[sr] * kv[k][e];
+                }
+                put4(RA + 64 * 1024, RA + 96 * 1024, i, k4, 64, make_float4(ka[0], ka[1], ka[2], ka[3]));
+            }
         }
         publish();
         if (tid == 0) {
             mma3(tmem + kColOT, sRA, sRA + 32 * 1024, sRB, sRB + 16 * 1024, 64, 64, true);
             mma3(tmem + kColD2, sRA, sRA + 32 * 1024, sRA + 64 * 1024, sRA + 96 * 1024, 64, 128, false);
         }
+        // the gate inputs of the epilogue, fetched while the tensor core works
+        Act *out = static_cast<Act *>(a.out);
+        const Act *z = static_cast<const Act *>(a.z);
+        float zg[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+            const int t = 32 * half + q;
+            zg[q] = t < n ? to_f32(z[((size_t)s * L + t0 + t) * Hv * kD + (size_t)h * kD + tl]) : 0.f;
+        }
         commit_wait();
+        // the operand regions are free: fetch the next chunk's window and gate inputs now
+        if (c + 1 < n_chunks) {
+            if (wid == 0) issue_raw(c + 1);
+            load_gates(c + 1);
+        }
 
         // ---------------- (g) outputs (gated RMSNorm) and the state update
         {
             float o32[32];
             tmem_ld16(tmem + tq + kColOT + 32 * half, o32);
             tmem_ld16(tmem + tq + kColOT + 32 * half + 16, o32 + 16);
+            // per-token sums of squares over this warp's 32 columns: reduce-scatter, lane l ends with token l
+            float v[32];
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
                 o32[q] *= a.q_scale;
-                float sq = o32[q] * o32[q];
-#pragma unroll
-                for (int m = 16; m >= 1; m >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, m);
-                if (lane == 0) red[(wid & 3) * 64 + 32 * half + q] = sq;     // lane quarter x token
+                v[q] = o32[q] * o32[q];
             }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+                const bool upper = (lane & off) != 0;
+#pragma unroll
+                for (int i = 0; i < off; ++i) {
+                    const float send = upper ? v[i] : v[i + off];
+                    const float keep = upper ? v[i + off] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            red[(wid & 3) * 64 + 32 * half + lane] = v[0];                  // lane quarter x token
             __syncthreads();
             if (tid < kC) {
                 const float tot = (red[tid] + red[64 + tid]) + (red[128 + tid] + red[192 + tid]);
                 rinv[tid] = 1.0f / sqrtf(tot / float(kD) + a.rms_eps);
             }
             __syncthreads();
-            Act *out = static_cast<Act *>(a.out);
-            const Act *z = static_cast<const Act *>(a.z);
             const float nw = __ldg(a.norm_w + tl);
+#pragma unroll
             for (int q = 0; q < 32; ++q) {
                 const int t = 32 * half + q;
                 if (t < n) {
                     const size_t o_idx = ((size_t)s * L + t0 + t) * Hv * kD + (size_t)h * kD + tl;
-                    out[o_idx] = from_f32<Act>(o32[q] * rinv[t] * nw * silu(to_f32(z[o_idx])));
+                    out[o_idx] = from_f32<Act>(o32[q] * rinv[t] * nw * silu(zg[q]));
                 }
             }
             // S^T <- Gamma_C S^T + D2
