@@ -40,6 +40,7 @@ import numpy as np  # noqa: E402
 from workloads.synth import WORKLOADS, make_inputs, randint  # noqa: E402
 
 METRIC = "GDN verify tokens/sec at 1 GB300; achieved HBM GB/s vs roofline"
+FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -69,6 +70,26 @@ def rollback_bytes(s, trims) -> int:
 
 def prefill_bytes(s) -> int:
     return verify_bytes(s, capture=False)
+
+
+# dense products of one (slot, value head, 64-token chunk) in the chunkwise form,
+# 2 flops per multiply-add: G = [K;Q]K^T, W and U~ (T times two 64x128
+# operands), U -= W S, O = (Gamma Q) S, O += P U, S += (Gamma_C/Gamma K)^T U
+PREFILL_FLOPS_PER_CHUNK = 2 * (128 * 64 * 128 + 2 * 128 * 64 * 64 + 128 * 64 * 128 + 128 * 64 * 128
+                               + 128 * 64 * 64 + 128 * 128 * 64)
+TF32_PER_BF16 = 1.1 / 2.25      # nominal dense tf32 / bf16 tensor rate of the part
+
+
+def prefill_flops(s) -> int:
+    return s.n_slots * s.n_v_heads * (-(-s.n_tokens // s.chunk)) * PREFILL_FLOPS_PER_CHUNK
+
+
+def tf32_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]) * TF32_PER_BF16, "measured"
+    return FALLBACK_BF16_TFLOPS * TF32_PER_BF16, "fallback"
 
 
 def peaks():
@@ -263,27 +284,33 @@ class VerifyWorkload:
                    for li in range(self.layers))
 
     def e2e(self, steps, device):
-        """Public-API loop with host buffers: H2D activations + trims, verify, rollback, D2H out."""
+        """Public-API loop with host buffers: per layer H2D of the activations and
+        trims, verify, rollback, D2H of out; one host sync per step."""
         torch = self.torch
         from workloads.device import act_host
         s = self.shape
-        inp = self.host_inputs[0]
-        host = {"qkv": act_host(inp.qkv, s).pin_memory(), "z": act_host(inp.z, s).pin_memory(),
-                "alpha": act_host(inp.alpha, s).pin_memory(), "beta_raw": act_host(inp.beta_raw, s).pin_memory(),
-                "trim": torch.from_numpy(self.trims[0, 0].astype(np.int32)).pin_memory()}
-        out_host = torch.empty(self.sets[0][0]["out"].shape, dtype=self.sets[0][0]["out"].dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_host.numel() * out_host.element_size()
+        hosts, outs = [], []
+        for li in range(self.layers):
+            inp = self.host_inputs[li if self.layers > 1 else 0]
+            hosts.append({"qkv": act_host(inp.qkv, s).pin_memory(), "z": act_host(inp.z, s).pin_memory(),
+                          "alpha": act_host(inp.alpha, s).pin_memory(),
+                          "beta_raw": act_host(inp.beta_raw, s).pin_memory(),
+                          "trim": torch.from_numpy(self.trims[0, li].astype(np.int32)).pin_memory()})
+            outs.append(torch.empty(self.sets[0][li]["out"].shape, dtype=self.sets[0][li]["out"].dtype).pin_memory())
+        h2d = sum(t.numel() * t.element_size() for h in hosts for t in h.values())
+        d2h = sum(o.numel() * o.element_size() for o in outs)
         stream = torch.cuda.current_stream()
         sp = stream.cuda_stream
 
         def one(k):
-            x = self.sets[k % self.n_sets][0]
-            for key, t in host.items():
-                x[key].copy_(t, non_blocking=True)
-            self.verify(k % self.n_sets, 0, sp)
-            self.rollback(k % self.n_sets, 0, sp)
-            out_host.copy_(x["out"], non_blocking=True)
+            kk = k % self.n_sets
+            for li in range(self.layers):
+                x = self.sets[kk][li]
+                for key, t in hosts[li].items():
+                    x[key].copy_(t, non_blocking=True)
+                self.verify(kk, li, sp)
+                self.rollback(kk, li, sp)
+                outs[li].copy_(x["out"], non_blocking=True)
             stream.synchronize()
 
         for k in range(10):
@@ -292,7 +319,7 @@ class VerifyWorkload:
         for k in range(steps):
             one(k)
         dt = time.perf_counter() - t0
-        return dt, h2d * self.layers, d2h * self.layers
+        return dt, h2d, d2h
 
 
 class PrefillWorkload:
@@ -333,6 +360,36 @@ class PrefillWorkload:
 
     def step_bytes(self, k):
         return prefill_bytes(self.shape)
+
+    def e2e(self, steps, device):
+        """Public-API loop with host buffers: H2D of the prompt's activations,
+        prefill, D2H of out; one host sync per step."""
+        torch = self.torch
+        from workloads.device import act_host
+        s = self.shape
+        inp = self.host_inputs[0]
+        host = {"qkv": act_host(inp.qkv, s).pin_memory(), "z": act_host(inp.z, s).pin_memory(),
+                "alpha": act_host(inp.alpha, s).pin_memory(), "beta_raw": act_host(inp.beta_raw, s).pin_memory()}
+        out_host = torch.empty(self.sets[0][0]["out"].shape, dtype=self.sets[0][0]["out"].dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+        stream = torch.cuda.current_stream()
+        sp = stream.cuda_stream
+
+        def one(k):
+            x = self.sets[k % self.n_sets][0]
+            for key, t in host.items():
+                x[key].copy_(t, non_blocking=True)
+            self.prefill(k % self.n_sets, 0, sp)
+            out_host.copy_(x["out"], non_blocking=True)
+            stream.synchronize()
+
+        for k in range(3):
+            one(k)
+        t0 = time.perf_counter()
+        for k in range(steps):
+            one(k)
+        return time.perf_counter() - t0, h2d, d2h
 
 
 def capture_graph(torch, fn_list):
@@ -495,11 +552,25 @@ def run_cuda(args):
         "gpu_launches": wl.kernels_per_step * args.steps,
         "clocks": clocks.summary(t_wall0 - 0.5, t_wall1 + 0.5),
     }
+    if args.workload == "prefill":
+        # the chunkwise products at the tf32 tensor rate take longer than the
+        # algorithmic bytes at the copy rate: the prefill is tensor-bound
+        flops = prefill_flops(shape)
+        tpk, tkind = tf32_peak()
+        t_ach = flops / kdur[dom] / 1e12
+        res["roofline"] = {
+            "bound": "tensor", "achieved": t_ach, "peak": tpk, "unit": "TFLOP/s", "frac": t_ach / tpk,
+            "traffic": traffic, "kernel": dom, "flops_per_launch": flops, "bytes_per_launch": dom_bytes,
+            "launch_us": kdur[dom] * 1e6, "hbm_gbs": achieved, "hbm_frac": achieved / hbm,
+            "peak_source": (f"{tkind} bf16_tflops x nominal tf32/bf16 ratio 1.1/2.25"
+                            + (" (MEASURED_PEAKS.json)" if tkind == "measured" else " (recipe fallback)")),
+            "note": "operands run as 3xTF32 (three tf32 products per fp32 product); flops counted once"}
     if bad:
         res["device_status_errors"] = bad
-    if args.workload != "prefill" and not args.no_e2e:
-        e_steps = max(20, min(args.steps, 500))
+    if not args.no_e2e:
+        e_steps = max(20, min(args.steps, 500)) if args.workload != "prefill" else max(5, min(args.steps, 50))
         edt, h2d, d2h = wl.e2e(e_steps, device)
+        edt = max_over_ranks(edt, device)
         res["e2e"] = {"value": wl.tokens_per_step * e_steps * world / edt, "unit": "tokens/s",
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
                       "timing": "wall clock, host sync per step"}
