@@ -2,6 +2,7 @@
 // Not part of the public interface (that is include/gdn_verify.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -37,6 +38,7 @@ struct RollbackArgs {
 
 // Everything one chunkwise prefill launch needs (d_k = d_v = 128, W = 4).
 struct PrefillArgs {
+    CUtensorMap qkv_map;              // qkv as a 2-D tensor [B*L rows][C channels], box 128 x 67
     int B, Hk, Hv, L, C, r;           // L: prompt tokens per slot; C: conv channels; r = Hv / Hk
     float rms_eps, l2_eps, q_scale;
     const float *conv_w, *A_log, *dt_bias, *norm_w;

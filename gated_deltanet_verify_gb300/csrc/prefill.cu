@@ -37,6 +37,8 @@
 #include "internal.cuh"
 
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <mutex>
 #include <string>
 
 namespace gdn {
@@ -67,7 +69,11 @@ constexpr uint32_t kInvK = kInvQ + 256;
 constexpr uint32_t kRed = kInvK + 256;         // 4 lane quarters x 64 tokens
 constexpr uint32_t kSmemBytes = kRed + 4 * 64 * 4;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-static_assert((kC + 3) * kCh * 4 <= 128 * 1024, "raw chunk window fits the A region");
+constexpr int kWin = kC + 3;                   // window rows of a chunk (3 rows of history)
+static_assert(kWin * kCh * 4 <= 128 * 1024, "raw chunk window fits the A region");
+// RB during the conv phase: the conv state rows (first chunk) and the per-warp sums of squares
+constexpr uint32_t kHistOff = 0;               // 3 x 384 floats
+constexpr uint32_t kSsqOff = 8 * 1024;         // 8 channel blocks (q, k) x 64 tokens
 
 // TMEM columns of the accumulators
 constexpr uint32_t kColG = 0, kColWT = 64, kColUT = 128, kColOT = 192, kColD2 = 256;
@@ -181,15 +187,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  "r"(bytes)
                  : "memory");
 }
-// global -> own shared memory, completion counted in bytes on an mbarrier
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
+// 2-D tile of a tensor map -> own shared memory, completion counted in bytes on an mbarrier
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
 }
 
 template <typename Act>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int tl = tid & 127, half = tid >> 7;          // TMEM lane of this thread, column half
@@ -200,8 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
     const Act *qkv = static_cast<const Act *>(a.qkv);
     float *scr = a.scratch + ((size_t)s * Hv + h) * kScrFloats;
     float *qs = scr + kScrQ, *ks = scr + kScrK, *vs = scr + kScrV;
-    const Act *rawA = reinterpret_cast<const Act *>(sm + kRA);        // [67][384] raw window of the chunk
-    float *hist = reinterpret_cast<float *>(sm + kRB);                // [3][384] conv state (first chunk only)
+    const Act *rawA = reinterpret_cast<const Act *>(sm + kRA);        // [q|k|v][67][128] raw window of the chunk
+    float *hist = reinterpret_cast<float *>(sm + kRB + kHistOff);     // [3][384] conv state (first chunk only)
+    float *ssq = reinterpret_cast<float *>(sm + kRB + kSsqOff);       // [8][64] partial sums of squares
     float *AMt = reinterpret_cast<float *>(sm + kAM);
     float *Pt = reinterpret_cast<float *>(sm + kPT);
     float *Tm = reinterpret_cast<float *>(sm + kRB + 32 * 1024);      // T (fp32, 64 x 64, row-major)
@@ -270,21 +279,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
         fence_after_sync();
     };
 
-    // raw window rows t0-3 .. t0+63 of chunk cc (those inside the prompt) -> smem, by warp 0
+    // raw window rows t0-3 .. t0+63 of chunk cc: three 128-channel tiles (q, k, v of this head) of the
+    // qkv tensor map, one thread.  Rows outside the tensor read as zero; rows of a neighbouring slot
+    // and rows past the prompt are never used (the history rows of the first chunk come from the
+    // conv state, outputs of padded tokens are discarded).
     auto issue_raw = [&](int cc) {
-        const int tt0 = cc * kC;
-        const int row_lo = cc == 0 ? 3 : 0;                 // rows before the prompt come from the conv state
-        const int row_hi = min(kC + 3, L - tt0 + 3);
-        const uint32_t seg = kD * sizeof(Act);
-        if (lane == 0) mbar_arrive_expect_tx(rawbar, (uint32_t)(row_hi - row_lo) * 3u * seg);
-        __syncwarp();
-        for (int row = row_lo + lane; row < row_hi; row += 32) {
-            const Act *src = qkv + ((size_t)s * L + (tt0 - 3 + row)) * C;
-            const uint32_t dst = smem_u32(sm + kRA) + (uint32_t)(row * kCh) * (uint32_t)sizeof(Act);
-            bulk_g2s(dst, src + kh * kD, seg, rawbar);
-            bulk_g2s(dst + seg, src + Hk * kD + kh * kD, seg, rawbar);
-            bulk_g2s(dst + 2 * seg, src + 2 * Hk * kD + h * kD, seg, rawbar);
-        }
+        constexpr uint32_t kTile = kWin * kD * sizeof(Act);
+        const int y = s * L + cc * kC - 3;
+        const uint32_t dst = smem_u32(sm + kRA);
+        mbar_arrive_expect_tx(rawbar, 3u * kTile);
+        tma_load_2d(dst, &a.qkv_map, kh * kD, y, rawbar);
+        tma_load_2d(dst + kTile, &a.qkv_map, Hk * kD + kh * kD, y, rawbar);
+        tma_load_2d(dst + 2 * kTile, &a.qkv_map, 2 * Hk * kD + h * kD, y, rawbar);
     };
     auto wait_raw = [&]() {
         bool ok = timed_out;
@@ -303,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
         }
     };
 
-    if (wid == 0) issue_raw(0);
+    if (tid == 0) issue_raw(0);
     load_gates(0);
     // the three window rows before the prompt: the conv state (fp32)
     for (int it = tid; it < 3 * (kCh / 4); it += kThreads) {
@@ -342,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
                 gam[t] = expf(acc);
             }
         }
-        // conv + SiLU: item = (channel, 16-token segment), sliding window; into scratch
+        // conv + SiLU: item = (channel, 16-token segment), sliding window; into scratch.  For q and k the
+        // warp also sums y^2 over its 32 channels per token (reduce-scatter, fixed order).
 #pragma unroll 1
         for (int k = 0; k < 6; ++k) {
             const int it = tid + k * kThreads;
@@ -350,38 +357,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
             const int g = gch(ch);
             const float w0 = __ldg(a.conv_w + g), w1 = __ldg(a.conv_w + C + g), w2 = __ldg(a.conv_w + 2 * C + g),
                         w3 = __ldg(a.conv_w + 3 * C + g);
+            const Act *src = rawA + (ch >> 7) * (kWin * kD) + (ch & (kD - 1));
             auto xin = [&](int row) -> float {    // window row (token t0 - 3 + row)
-                return (c == 0 && row < 3) ? hist[row * kCh + ch] : to_f32(rawA[row * kCh + ch]);
+                return (c == 0 && row < 3) ? hist[row * kCh + ch] : to_f32(src[row * kD]);
             };
             float x0 = xin(tb), x1 = xin(tb + 1), x2 = xin(tb + 2);
             float *dst = ch < kD ? qs + ch : (ch < 2 * kD ? ks + (ch - kD) : vs + (ch - 2 * kD));
+            float y2[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int t = tb + j;
                 const float x3 = xin(t + 3);
-                const float y = silu(fmaf(w3, x3, fmaf(w2, x2, fmaf(w1, x1, w0 * x0))));
-                dst[t * kD] = t < n ? y : 0.f;
+                float y = silu(fmaf(w3, x3, fmaf(w2, x2, fmaf(w1, x1, w0 * x0))));
+                y = t < n ? y : 0.f;
+                dst[t * kD] = y;
+                y2[j] = y * y;
                 x0 = x1; x1 = x2; x2 = x3;
+            }
+            if (ch < 2 * kD) {                    // warp-uniform: a warp's 32 channels share q|k|v
+#pragma unroll
+                for (int j = 0; j < 16; ++j) y2[j] += __shfl_xor_sync(0xffffffffu, y2[j], 16);
+#pragma unroll
+                for (int off = 8; off >= 1; off >>= 1) {
+                    const bool upper = (lane & off) != 0;
+#pragma unroll
+                    for (int i = 0; i < off; ++i) {
+                        const float send = upper ? y2[i] : y2[i + off];
+                        const float keep = upper ? y2[i + off] : y2[i];
+                        y2[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    }
+                }
+                if (lane < 16) ssq[(ch >> 5) * kC + tb + lane] = y2[0];   // token tb + lane, channel block ch/32
             }
         }
         __syncthreads();
-        // inverse L2 norms of the q and k rows (warp per token; a zero padded row stays zero)
-        {
-            float4 v[16];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int t = wid + 8 * k;
-                v[2 * k] = *reinterpret_cast<const float4 *>(qs + t * kD + 4 * lane);
-                v[2 * k + 1] = *reinterpret_cast<const float4 *>(ks + t * kD + 4 * lane);
-            }
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                float ss = v[k].x * v[k].x;
-                ss = fmaf(v[k].y, v[k].y, ss); ss = fmaf(v[k].z, v[k].z, ss); ss = fmaf(v[k].w, v[k].w, ss);
-#pragma unroll
-                for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-                if (lane == 0) ((k & 1) ? invk : invq)[wid + 8 * (k >> 1)] = 1.0f / sqrtf(ss + a.l2_eps);
-            }
+        // inverse L2 norms of the q and k rows (a zero padded row stays zero)
+        if (tid < 2 * kC) {
+            const int t = tid & (kC - 1), part = tid >> 6;
+            const float *p = ssq + part * 4 * kC + t;
+            const float sum = (p[0] + p[kC]) + (p[2 * kC] + p[3 * kC]);
+            (part ? invk : invq)[t] = 1.0f / sqrtf(sum + a.l2_eps);
         }
         __syncthreads();
 
@@ -609,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillArgs 
         commit_wait();
         // the operand regions are free: fetch the next chunk's window and gate inputs now
         if (c + 1 < n_chunks) {
-            if (wid == 0) issue_raw(c + 1);
+            if (tid == 0) issue_raw(c + 1);
             load_gates(c + 1);
         }
 
@@ -702,6 +717,10 @@ int prefill_check(const gdn_dims &d, std::string &why) {
         why = "prefill: n_slots must be <= 65535";
         return GDN_ERR_SHAPE;
     }
+    if ((long long)d.n_slots * d.n_tokens >= (1LL << 31)) {
+        why = "prefill: n_slots * n_tokens must be below 2^31";
+        return GDN_ERR_SHAPE;
+    }
     if (d.n_v_heads / d.n_qk_heads > 8) {
         why = "prefill: at most 8 value heads per key head (one thread-block cluster)";
         return GDN_ERR_SHAPE;
@@ -733,6 +752,21 @@ static cudaError_t launch_prefill_args(const PrefillArgs &a, gdn_dtype act, cuda
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
 cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const void *qkv, const void *z,
                            const void *alpha, const void *beta_raw, float *state, float *conv_state,
                            void *out, void *workspace, int *d_status, cudaStream_t stream) {
@@ -745,6 +779,18 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
     a.state = state; a.conv_state = conv_state; a.out = out;
     a.scratch = static_cast<float *>(workspace);
     a.d_status = d_status;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const bool bf = d.act_dtype == GDN_BF16;
+    const cuuint64_t dims[2] = {(cuuint64_t)a.C, (cuuint64_t)a.B * (cuuint64_t)a.L};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.C * (bf ? 2u : 4u)};
+    const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kWin};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(&a.qkv_map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                              const_cast<void *>(qkv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     return launch_prefill_args(a, d.act_dtype, stream);
 }
 
