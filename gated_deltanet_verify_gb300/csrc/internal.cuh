@@ -39,6 +39,7 @@ struct RollbackArgs {
 // Everything one chunkwise prefill launch needs (d_k = d_v = 128, W = 4).
 struct PrefillArgs {
     CUtensorMap qkv_map;              // qkv as a 2-D tensor [B*L rows][C channels], box 128 x 67
+    CUtensorMap z_map;                // z as a 2-D tensor [B*L rows][H_v*d_v], box 128 x 64
     int B, Hk, Hv, L, C, r;           // L: prompt tokens per slot; C: conv channels; r = Hv / Hk
     float rms_eps, l2_eps, q_scale;
     const float *conv_w, *A_log, *dt_bias, *norm_w;

@@ -59,6 +59,7 @@ constexpr uint32_t kPT = 208 * 1024;           // 16 KB: P (fp32, 64 x 64), stor
 constexpr uint32_t kMisc = 224 * 1024;
 constexpr uint32_t kMbar = kMisc;              // 8 B: tensor-core completion
 constexpr uint32_t kRawBar = kMisc + 8;        // 8 B: raw window copies
+constexpr uint32_t kZBar = kMisc + 24;         // 8 B: gate (z) tile copy
 constexpr uint32_t kTmemSlot = kMisc + 16;     // 4 B
 constexpr uint32_t kLogG = kMisc + 32;         // 64 floats each
 constexpr uint32_t kBeta = kLogG + 256;
@@ -75,12 +76,13 @@ static_assert(kWin * kCh * 4 <= 128 * 1024, "raw chunk window fits the A region"
 constexpr uint32_t kHistOff = 0;               // 3 x 384 floats
 constexpr uint32_t kSsqOff = 8 * 1024;         // 8 channel blocks (q, k) x 64 tokens
 
-// TMEM columns of the accumulators
-constexpr uint32_t kColG = 0, kColWT = 64, kColUT = 128, kColOT = 192, kColD2 = 256;
+// TMEM columns: accumulators (G, later W^T, shares columns 0-63), and the chunk's conv outputs q and k
+// (lane = channel, column = token; not normalised)
+constexpr uint32_t kColG = 0, kColWT = 0, kColUT = 64, kColOT = 128, kColQ = 192, kColK = 256, kColD2 = 320;
+static_assert(kColD2 + 128 <= kTmemCols, "TMEM columns");
 
-// per-CTA scratch (floats): conv outputs q, k, v of the chunk (64 x 128 each, not normalised)
-constexpr size_t kScrQ = 0, kScrK = 64 * 128, kScrV = 2 * 64 * 128;
-constexpr size_t kScrFloats = 3 * 64 * 128;
+// per-CTA scratch (floats): the chunk's conv outputs v, transposed (128 channels x 64 tokens)
+constexpr size_t kScrFloats = 128 * 64;
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -109,12 +111,33 @@ __device__ __forceinline__ void put4(unsigned char *hi, unsigned char *lo, int r
     *reinterpret_cast<float4 *>(hi + off) = h;
     *reinterpret_cast<float4 *>(lo + off) = l;
 }
-__device__ __forceinline__ void put1(unsigned char *hi, unsigned char *lo, int r, int k, int K, float v) {
-    const float h = tf32_hi(v);
-    const uint32_t off = plane_off(r, k >> 2, K) + ((k & 3) << 2);
-    *reinterpret_cast<float *>(hi + off) = h;
-    *reinterpret_cast<float *>(lo + off) = v - h;
+// Lanes 4a .. 4a+3 of a warp hold v[e] = X[row0 + e][4a + (lane & 3)], e = 0..3 (a column each);
+// on return lane 4a + c holds X[row0 + c][4a .. 4a+3] (a row each): a 4 x 4 transpose inside each
+// lane quad, two butterfly stages of two shuffles.
+__device__ __forceinline__ float4 quad_transpose(float v0, float v1, float v2, float v3) {
+    const bool b1 = (threadIdx.x & 1) != 0, b2 = (threadIdx.x & 2) != 0;
+    float t0 = __shfl_xor_sync(0xffffffffu, b1 ? v0 : v1, 1);
+    float t1 = __shfl_xor_sync(0xffffffffu, b1 ? v2 : v3, 1);
+    if (b1) { v0 = t0; v2 = t1; } else { v1 = t0; v3 = t1; }
+    t0 = __shfl_xor_sync(0xffffffffu, b2 ? v0 : v2, 2);
+    t1 = __shfl_xor_sync(0xffffffffu, b2 ? v1 : v3, 2);
+    if (b2) { v0 = t0; v1 = t1; } else { v2 = t0; v3 = t1; }
+    return make_float4(v0, v1, v2, v3);
 }
+// Column tl of 32 rows (row0 .. row0+31, values x[0..31]) of a K = 128 operand -> its planes, 16 bytes
+// at a time.  Odd lane quads take the row blocks in the order b ^ 1, so the two quads of an 8-lane store
+// phase fill all eight 16-byte rows of a core matrix (no bank conflict).
+__device__ __forceinline__ void put_col32(unsigned char *hi, unsigned char *lo, int row0, int tl, const float *x) {
+    const bool odd = (threadIdx.x & 4) != 0;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const int bo = b ^ 1;
+        const float4 w = quad_transpose(odd ? x[4 * bo] : x[4 * b], odd ? x[4 * bo + 1] : x[4 * b + 1],
+                                        odd ? x[4 * bo + 2] : x[4 * b + 2], odd ? x[4 * bo + 3] : x[4 * b + 3]);
+        put4(hi, lo, row0 + 4 * (odd ? bo : b) + (threadIdx.x & 3), tl >> 2, 128, w);
+    }
+}
+
 // item -> (row, 16-byte group) so that consecutive items fill consecutive 16-byte slots
 __device__ __forceinline__ void item_rc(int it, int K, int &r, int &k4) {
     const int cm = it >> 3, groups = K >> 2;
@@ -172,6 +195,21 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 16 fp32 columns into this thread's TMEM lane (completion: tmem_wait_st)
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+            taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+        "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+        "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -206,8 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int kh = h / a.r;
     const bool qk_writer = (h % a.r) == 0;
     const Act *qkv = static_cast<const Act *>(a.qkv);
-    float *scr = a.scratch + ((size_t)s * Hv + h) * kScrFloats;
-    float *qs = scr + kScrQ, *ks = scr + kScrK, *vs = scr + kScrV;
+    float *vT = a.scratch + ((size_t)s * Hv + h) * kScrFloats;      // [128 channels][64 tokens]
     const Act *rawA = reinterpret_cast<const Act *>(sm + kRA);        // [q|k|v][67][128] raw window of the chunk
     float *hist = reinterpret_cast<float *>(sm + kRB + kHistOff);     // [3][384] conv state (first chunk only)
     float *ssq = reinterpret_cast<float *>(sm + kRB + kSsqOff);       // [8][64] partial sums of squares
@@ -224,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     float *red = reinterpret_cast<float *>(sm + kRed);
     unsigned char *RA = sm + kRA, *RB = sm + kRB;
     const uint32_t sRA = smem_u32(RA), sRB = smem_u32(RB);
-    const uint32_t mbar = smem_u32(sm + kMbar), rawbar = smem_u32(sm + kRawBar);
-    uint32_t phase = 0, raw_phase = 0;
+    const uint32_t mbar = smem_u32(sm + kMbar), rawbar = smem_u32(sm + kRawBar), zbar = smem_u32(sm + kZBar);
+    uint32_t phase = 0, raw_phase = 0, z_phase = 0;
     bool timed_out = false;
 
     // global conv channel of local channel ch (q 0..127, k 128..255, v 256..383)
@@ -245,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(mbar));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(rawbar));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(zbar));
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     fence_before_sync();
@@ -297,6 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (int it = 0; it < kSpinLimit && !ok; ++it) ok = mbar_try(rawbar, raw_phase & 1u);
         if (!ok) timed_out = true;
         raw_phase ^= 1u;
+    };
+    auto wait_z = [&]() {
+        bool ok = timed_out;
+        for (int it = 0; it < kSpinLimit && !ok; ++it) ok = mbar_try(zbar, z_phase & 1u);
+        if (!ok) timed_out = true;
+        z_phase ^= 1u;
     };
     // gate inputs of chunk cc (threads tid < 64, one token each)
     float g_alpha = 0.f, g_beta = 0.f;
@@ -362,19 +406,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 return (c == 0 && row < 3) ? hist[row * kCh + ch] : to_f32(src[row * kD]);
             };
             float x0 = xin(tb), x1 = xin(tb + 1), x2 = xin(tb + 2);
-            float *dst = ch < kD ? qs + ch : (ch < 2 * kD ? ks + (ch - kD) : vs + (ch - 2 * kD));
-            float y2[16];
+            float yv[16], y2[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int t = tb + j;
                 const float x3 = xin(t + 3);
-                float y = silu(fmaf(w3, x3, fmaf(w2, x2, fmaf(w1, x1, w0 * x0))));
-                y = t < n ? y : 0.f;
-                dst[t * kD] = y;
-                y2[j] = y * y;
+                const float y = silu(fmaf(w3, x3, fmaf(w2, x2, fmaf(w1, x1, w0 * x0))));
+                yv[j] = t < n ? y : 0.f;
+                y2[j] = yv[j] * yv[j];
                 x0 = x1; x1 = x2; x2 = x3;
             }
-            if (ch < 2 * kD) {                    // warp-uniform: a warp's 32 channels share q|k|v
+            // q, k -> TMEM (lane = channel; the warp's lane quarter is (ch % 128) / 32 = warp % 4);
+            // v -> the scratch, transposed.  Warp-uniform: a warp's 32 channels share q|k|v.
+            if (ch < 2 * kD) {
+                tmem_st16(tmem + tq + (ch < kD ? kColQ : kColK) + tb, yv);
+            } else {
+                float4 *dv = reinterpret_cast<float4 *>(vT + (ch - 2 * kD) * kC + tb);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    dv[q4] = make_float4(yv[4 * q4], yv[4 * q4 + 1], yv[4 * q4 + 2], yv[4 * q4 + 3]);
+            }
+            if (ch < 2 * kD) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) y2[j] += __shfl_xor_sync(0xffffffffu, y2[j], 16);
 #pragma unroll
@@ -390,7 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 if (lane < 16) ssq[(ch >> 5) * kC + tb + lane] = y2[0];   // token tb + lane, channel block ch/32
             }
         }
+        tmem_wait_st();
+        fence_before_sync();
         __syncthreads();
+        fence_after_sync();
         // inverse L2 norms of the q and k rows (a zero padded row stays zero)
         if (tid < 2 * kC) {
             const int t = tid & (kC - 1), part = tid >> 6;
@@ -402,20 +457,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
         // ---------------- (b) G = [K; Q] K^T
         {
-            float4 v[16];
+            // this thread holds channel i = tl of 32 tokens: the rows of [K^; Q^] get column i
+            float x32[32];
+            tmem_ld16(tmem + tq + kColK + 32 * half, x32);
+            tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                int m, k4;
-                item_rc(tid + k * kThreads, 128, m, k4);
-                v[k] = *reinterpret_cast<const float4 *>((m < kC ? ks + m * kD : qs + (m - kC) * kD) + 4 * k4);
-            }
+            for (int q = 0; q < 32; ++q) x32[q] *= invk[32 * half + q];
+            put_col32(RA, RA + 64 * 1024, 32 * half, tl, x32);
+            tmem_ld16(tmem + tq + kColQ + 32 * half, x32);
+            tmem_ld16(tmem + tq + kColQ + 32 * half + 16, x32 + 16);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                int m, k4;
-                item_rc(tid + k * kThreads, 128, m, k4);
-                const float sc = m < kC ? invk[m] : invq[m - kC];
-                put4(RA, RA + 64 * 1024, m, k4, 128, make_float4(v[k].x * sc, v[k].y * sc, v[k].z * sc, v[k].w * sc));
-            }
+            for (int q = 0; q < 32; ++q) x32[q] *= invq[32 * half + q];
+            put_col32(RA, RA + 64 * 1024, kC + 32 * half, tl, x32);
         }
         publish();
         if (tid == 0) mma3(tmem + kColG, sRA, sRA + 64 * 1024, sRA, sRA + 64 * 1024, 128, 64, false);
@@ -491,32 +544,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             item_rc(tid + k * kThreads, 64, r, k4);
             put4(RB, RB + 16 * 1024, r, k4, 64, *reinterpret_cast<const float4 *>(Tm + r * kC + 4 * k4));
         }
+        {
+            // row i = tl of (diag(beta Gamma) K^)^T and (diag(beta) V)^T, tokens 32 half .. 32 half + 31
+            float x32[32];
+            tmem_ld16(tmem + tq + kColK + 32 * half, x32);
+            tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
+            const float4 *vrow = reinterpret_cast<const float4 *>(vT + tl * kC + 32 * half);
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            float kv[4][4], vv[4][4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                int i, k4;
-                item_rc(tid + (4 * b + k) * kThreads, 64, i, k4);
+            for (int q4 = 0; q4 < 8; ++q4) {
+                float ka[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    kv[k][e] = ks[(4 * k4 + e) * kD + i];
-                    vv[k][e] = vs[(4 * k4 + e) * kD + i];
+                    const int sr = 32 * half + 4 * q4 + e;
+                    ka[e] = betas[sr] * gam[sr] * invk[sr] * x32[4 * q4 + e];
                 }
+                put4(RA, RA + 32 * 1024, tl, 8 * half + q4, 64, make_float4(ka[0], ka[1], ka[2], ka[3]));
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                int i, k4;
-                item_rc(tid + (4 * b + k) * kThreads, 64, i, k4);
-                float ka[4], va[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int sr = 4 * k4 + e;
-                    ka[e] = betas[sr] * gam[sr] * invk[sr] * kv[k][e];
-                    va[e] = betas[sr] * vv[k][e];
-                }
-                put4(RA, RA + 32 * 1024, i, k4, 64, make_float4(ka[0], ka[1], ka[2], ka[3]));
-                put4(RA + 64 * 1024, RA + 96 * 1024, i, k4, 64, make_float4(va[0], va[1], va[2], va[3]));
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 v = vrow[q4];
+                const int sr = 32 * half + 4 * q4;
+                put4(RA + 64 * 1024, RA + 96 * 1024, tl, 8 * half + q4, 64,
+                     make_float4(betas[sr] * v.x, betas[sr + 1] * v.y, betas[sr + 2] * v.z, betas[sr + 3] * v.w));
+            }
+        }
+        // the gate (z) tile of this chunk -> the A region, free from here until the next chunk's G
+        if constexpr (sizeof(Act) == 2) {
+            if (tid == 0) {
+                fence_proxy_async();
+                mbar_arrive_expect_tx(zbar, (uint32_t)(kC * kD * sizeof(Act)));
+                tma_load_2d(smem_u32(sm + kAM), &a.z_map, h * kD, s * L + t0, zbar);
             }
         }
         publish();
@@ -533,7 +590,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tmem_ld16(tmem + tq + kColWT + 32 * half, w32);
             tmem_ld16(tmem + tq + kColWT + 32 * half + 16, w32 + 16);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) put1(RB, RB + 32 * 1024, 32 * half + q, tl, 128, -w32[q]);
+            for (int q = 0; q < 32; ++q) w32[q] = -w32[q];
+            put_col32(RB, RB + 32 * 1024, 32 * half, tl, w32);
             // A = S0^T (128 x 128) from the registers
 #pragma unroll
             for (int q = 0; q < 16; ++q)
@@ -546,20 +604,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
         // ---------------- (e) O^T = S0^T (diag(Gamma) Q)^T
         {
-            float4 v[8];
+            float x32[32];
+            tmem_ld16(tmem + tq + kColQ + 32 * half, x32);
+            tmem_ld16(tmem + tq + kColQ + 32 * half + 16, x32 + 16);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                int r, k4;
-                item_rc(tid + k * kThreads, 128, r, k4);
-                v[k] = *reinterpret_cast<const float4 *>(qs + r * kD + 4 * k4);
-            }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                int r, k4;
-                item_rc(tid + k * kThreads, 128, r, k4);
-                const float gr = gam[r] * invq[r];
-                put4(RB, RB + 32 * 1024, r, k4, 128, make_float4(v[k].x * gr, v[k].y * gr, v[k].z * gr, v[k].w * gr));
-            }
+            for (int q = 0; q < 32; ++q) x32[q] *= gam[32 * half + q] * invq[32 * half + q];
+            put_col32(RB, RB + 32 * 1024, 32 * half, tl, x32);
         }
         publish();
         if (tid == 0) mma3(tmem + kColOT, sRA, sRA + 64 * 1024, sRB, sRB + 32 * 1024, 128, 64, false);
@@ -585,26 +635,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             put4(RB, RB + 16 * 1024, r, k4, 64, make_float4(p[0], p[1], p[2], p[3]));
         }
         {
-            float kv[8][4];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                int i, k4;
-                item_rc(tid + k * kThreads, 64, i, k4);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) kv[k][e] = ks[(4 * k4 + e) * kD + i];
-            }
+            // row i = tl of diag(Gamma_C / Gamma) K^, as (K^ ...)^T with tokens along K
+            float x32[32];
+            tmem_ld16(tmem + tq + kColK + 32 * half, x32);
+            tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
             const float lc = logG[kC - 1];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                int i, k4;
-                item_rc(tid + k * kThreads, 64, i, k4);
+            for (int q4 = 0; q4 < 8; ++q4) {
                 float ka[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int sr = 4 * k4 + e;
-                    ka[e] = expf(lc - logG[sr]) * invk[sr] * kv[k][e];
+                    const int sr = 32 * half + 4 * q4 + e;
+                    ka[e] = expf(lc - logG[sr]) * invk[sr] * x32[4 * q4 + e];
                 }
-                put4(RA + 64 * 1024, RA + 96 * 1024, i, k4, 64, make_float4(ka[0], ka[1], ka[2], ka[3]));
+                put4(RA + 64 * 1024, RA + 96 * 1024, tl, 8 * half + q4, 64, make_float4(ka[0], ka[1], ka[2], ka[3]));
             }
         }
         publish();
@@ -616,10 +660,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         Act *out = static_cast<Act *>(a.out);
         const Act *z = static_cast<const Act *>(a.z);
         float zg[32];
+        if constexpr (sizeof(Act) == 2) {
+            wait_z();
+            const Act *zs = reinterpret_cast<const Act *>(sm + kAM);       // [64 tokens][128]
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-            const int t = 32 * half + q;
-            zg[q] = t < n ? to_f32(z[((size_t)s * L + t0 + t) * Hv * kD + (size_t)h * kD + tl]) : 0.f;
+            for (int q = 0; q < 32; ++q) zg[q] = to_f32(zs[(32 * half + q) * kD + tl]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const int t = 32 * half + q;
+                zg[q] = t < n ? to_f32(z[((size_t)s * L + t0 + t) * Hv * kD + (size_t)h * kD + tl]) : 0.f;
+            }
         }
         commit_wait();
         // the operand regions are free: fetch the next chunk's window and gate inputs now
@@ -791,6 +842,14 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
                               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const cuuint64_t zdims[2] = {(cuuint64_t)a.Hv * kD, (cuuint64_t)a.B * (cuuint64_t)a.L};
+    const cuuint64_t zstrides[1] = {(cuuint64_t)a.Hv * kD * (bf ? 2u : 4u)};
+    const cuuint32_t zbox[2] = {(cuuint32_t)kD, (cuuint32_t)kC};
+    const CUresult rz = encode(&a.z_map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                               const_cast<void *>(z), zdims, zstrides, zbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rz != CUDA_SUCCESS) return cudaErrorInvalidValue;
     return launch_prefill_args(a, d.act_dtype, stream);
 }
 
