@@ -347,7 +347,8 @@ class PrefillWorkload:
             x["params"] = gdn.layer_params(x["conv_w"], x["A_log"], x["dt_bias"], x["norm_w"])
             self.sets.append([x])
         self.tokens_per_step = s.n_slots * s.n_tokens
-        self.kernels_per_step = 1
+        # the chunkwise kernel (one cooperative launch per group of (slot, head) pairs) + the conv-state kernel
+        self.kernels_per_step = 2 if s.n_slots * s.n_v_heads * 3 <= 152 else None
 
     def prefill(self, k, li, stream):
         x = self.sets[k][0]
@@ -549,7 +550,8 @@ def run_cuda(args):
         "kernels_us": {k: v * 1e6 for k, v in kdur.items()},
         "step_bytes": wl.step_bytes(0),
         "step_gbs": wl.step_bytes(0) * args.steps / dt / 1e9,
-        "gpu_launches": wl.kernels_per_step * args.steps,
+        "gpu_launches": (wl.kernels_per_step if wl.kernels_per_step is not None
+                         else 1 + -(-shape.n_slots * shape.n_v_heads * 3 // 152)) * args.steps,
         "clocks": clocks.summary(t_wall0 - 0.5, t_wall1 + 0.5),
     }
     if args.workload == "prefill":

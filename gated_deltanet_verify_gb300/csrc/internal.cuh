@@ -41,12 +41,15 @@ struct PrefillArgs {
     CUtensorMap qkv_map;              // qkv as a 2-D tensor [B*L rows][C channels], box 128 x 67
     CUtensorMap z_map;                // z as a 2-D tensor [B*L rows][H_v*d_v], box 128 x 64
     int B, Hk, Hv, L, C, r;           // L: prompt tokens per slot; C: conv channels; r = Hv / Hk
+    int pair0;                        // first (slot, value head) pair of this launch (slot * Hv + head)
     float rms_eps, l2_eps, q_scale;
     const float *conv_w, *A_log, *dt_bias, *norm_w;
     const void *qkv, *z, *alpha, *beta_raw;
     float *state, *conv_state;
     void *out;
-    float *scratch;                   // per-(slot, value head) scratch, prefill_workspace_bytes in total
+    float *scratch;                   // the caller's workspace (ring flags first), prefill_workspace_bytes
+    size_t ring_offset;               // bytes from the workspace start to the ring slots
+    float *scratch_vt;                // per-(slot, value head, preparation CTA) v^T scratch
     int *d_status;
 };
 

@@ -18,22 +18,27 @@
 // per-token RMSNorm rescales small outputs, so an operand rounding of 2^-11
 // becomes an error of 10-60 % in the outputs; with the split it is ~1e-5.
 //
-// Layout of the work: one CTA per (value head, slot), 256 threads, the fp32
-// state held in registers (thread (j, half) owns S[i][j] for 64 values of i),
-// chunks processed in order.  The products use transposed forms so that the
-// MMA M dimension is always 128 (d_k or d_v):
-//   G   = [K; Q] K^T                               (N 64, K 128) -> A and masked P
-//   W^T = (diag(beta Gamma) K)^T T^T,  U~^T = (diag(beta) V)^T T^T   (N 64, K 64)
-//   U^T = U~^T - S0^T W^T                          (N 64, K 128)
-//   O^T = S0^T (diag(Gamma) Q)^T + U^T P^T         (N 64)
-//   D2  = U^T (diag(Gamma_C / Gamma) K)            (N 128, K 64);  S^T <- Gamma_C S^T + D2
-// Operands are written into shared memory in the canonical K-major,
-// no-swizzle layout (core matrix = 8 rows x 16 bytes); accumulators are read
-// back with tcgen05.ld.  The conv outputs of a chunk and the masked P matrix
-// pass through a per-CTA scratch area of the caller's workspace (it stays in
-// L2).  T = (I + A)^-1 is formed on the CUDA cores by 16 x 16 block inversion.
-// A thread-block cluster spans the value heads of one key head, so the q/k
-// conv channels they all read are rewritten only after a cluster barrier.
+// Work split.  Everything but U, O and S depends only on the chunk itself, so
+// three CTAs serve one (slot, value head):
+//   * two preparation CTAs take alternate chunks: raw window (TMA), gates,
+//     conv + SiLU, L2 norms, G = [K; Q] K^T, A and the masked, decayed P,
+//     T = (I + A)^-1 (16 x 16 blocks), W^T and U~^T; they publish the chunk's
+//     ready-split operands (-W, Gamma Q, P, Gamma_C/Gamma K planes and U~) to
+//     a ring of four slots in the caller's workspace (bulk stores, L2-resident)
+//     and release a per-slot flag;
+//   * the state CTA holds the fp32 state in registers and, chunk by chunk,
+//     acquires a slot, pulls it in with bulk copies and runs only the
+//     state-dependent products and the epilogue:
+//       X^T = S0^T (-W)^T, U^T = U~^T + X^T          (N 64, K 128)
+//       O^T = S0^T (Gamma Q)^T + U^T P^T             (N 64)
+//       D2  = U^T (diag(Gamma_C / Gamma) K)          (N 128, K 64);  S^T <- Gamma_C S^T + D2
+//     then the gated RMSNorm.  It frees the slot once its bulk copies landed.
+// The launch is cooperative (every CTA resident at once), so the flag waits
+// between the three CTAs cannot starve; (slot, head) pairs beyond what fits
+// at once go to further launches.  Every wait is bounded and reports
+// GDN_ERR_TIMEOUT instead of hanging.  The ring flags are zeroed by a
+// stream-ordered memset before each launch.  The conv state (shared by the
+// value heads of a key head) is advanced by a second, small kernel.
 #include "internal.cuh"
 
 #include <cuda_bf16.h>
@@ -48,19 +53,22 @@ constexpr int kC = 64;                 // chunk length
 constexpr int kD = 128;                // d_k = d_v
 constexpr int kCh = 3 * kD;            // conv channels of one value head: q | k | v
 constexpr int kThreads = 256;
-constexpr int kSpinLimit = 1 << 20;
+constexpr int kSpinLimit = 1 << 20;    // try_wait rounds before an mbarrier wait gives up
+constexpr int kFlagSpin = 1 << 21;     // polls (with back-off) before a ring-flag wait gives up
 constexpr int kTmemCols = 512;
+constexpr int kRing = 4;               // ring slots per (slot, value head)
 
 // dynamic shared memory carve-up (bytes)
 constexpr uint32_t kRA = 0;                    // 128 KB: A operand planes; raw chunk inputs at chunk start
 constexpr uint32_t kRB = 128 * 1024;           // 64 KB: B operand planes; T and block temporaries
-constexpr uint32_t kAM = 192 * 1024;           // 16 KB: A (fp32, 64 x 64), stored transposed [s][r]
+constexpr uint32_t kAM = 192 * 1024;           // 16 KB: A (fp32, 64 x 64, transposed [s][r]); the z tile
 constexpr uint32_t kPT = 208 * 1024;           // 16 KB: P (fp32, 64 x 64), stored transposed [s][r]
 constexpr uint32_t kMisc = 224 * 1024;
 constexpr uint32_t kMbar = kMisc;              // 8 B: tensor-core completion
-constexpr uint32_t kRawBar = kMisc + 8;        // 8 B: raw window copies
-constexpr uint32_t kZBar = kMisc + 24;         // 8 B: gate (z) tile copy
+constexpr uint32_t kRawBar = kMisc + 8;        // 8 B: raw window copies (preparation) / slot copies (state)
 constexpr uint32_t kTmemSlot = kMisc + 16;     // 4 B
+constexpr uint32_t kFlagOk = kMisc + 20;       // 4 B: result of a ring-flag wait, broadcast to the CTA
+constexpr uint32_t kZBar = kMisc + 24;         // 8 B: gate (z) tile copy
 constexpr uint32_t kLogG = kMisc + 32;         // 64 floats each
 constexpr uint32_t kBeta = kLogG + 256;
 constexpr uint32_t kGam = kBeta + 256;
@@ -76,13 +84,22 @@ static_assert(kWin * kCh * 4 <= 128 * 1024, "raw chunk window fits the A region"
 constexpr uint32_t kHistOff = 0;               // 3 x 384 floats
 constexpr uint32_t kSsqOff = 8 * 1024;         // 8 channel blocks (q, k) x 64 tokens
 
-// TMEM columns: accumulators (G, later W^T, shares columns 0-63), and the chunk's conv outputs q and k
-// (lane = channel, column = token; not normalised)
+// TMEM columns.  Preparation: G (later W^T), U~^T, and the chunk's conv outputs q and k (lane =
+// channel, column = token; not normalised).  State: X^T (later U^T), O^T, D2.
 constexpr uint32_t kColG = 0, kColWT = 0, kColUT = 64, kColOT = 128, kColQ = 192, kColK = 256, kColD2 = 320;
 static_assert(kColD2 + 128 <= kTmemCols, "TMEM columns");
 
-// per-CTA scratch (floats): the chunk's conv outputs v, transposed (128 channels x 64 tokens)
-constexpr size_t kScrFloats = 128 * 64;
+// One ring slot: the chunk's operands in the exact shared-memory layout the state CTA uses.
+constexpr uint32_t kSlotNegW = 0;              // -W planes (64 x 128, hi + lo), 64 KB
+constexpr uint32_t kSlotGQ = 64 * 1024;        // Gamma Q planes (64 x 128), 64 KB
+constexpr uint32_t kSlotP = 128 * 1024;        // P planes (64 x 64), 32 KB
+constexpr uint32_t kSlotKd = 160 * 1024;       // (Gamma_C / Gamma) K planes, as (128 x 64), 64 KB
+constexpr uint32_t kSlotU = 224 * 1024;        // U~^T fp32 [128][64], 32 KB
+constexpr size_t kSlotBytes = 256 * 1024;
+// per (slot, value head): ring flags and the chunk decays (ints: full[4], empty[4], Gamma_C[4] bits)
+constexpr size_t kFlagWords = 16;
+// per (slot, value head): the two preparation CTAs' v^T scratch (128 channels x 64 tokens each)
+constexpr size_t kVtFloats = 128 * 64;
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -234,17 +251,105 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// own shared memory -> global, bulk async (completion: bulk_commit / bulk_wait*)
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+// global -> own shared memory, completion counted in bytes on an mbarrier
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;\n" ::: "memory"); }
+__device__ __forceinline__ void st_release(int *p, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// one thread polls *p until it reaches target (bounded, with back-off)
+__device__ __forceinline__ bool poll_flag(const int *p, int target) {
+    for (int it = 0; it < kFlagSpin; ++it) {
+        if (ld_acquire(p) >= target) return true;
+        __nanosleep(64);
+    }
+    return false;
+}
+
+// Per-CTA views of the ring and flags of one (slot, value head).
+struct Ring {
+    int *full, *empty;        // [kRing] chunk index + 1 of the last chunk published / consumed per slot
+    float *gamma_c;           // [kRing] Gamma_C of the chunk in each slot
+    unsigned char *slots;     // [kRing][kSlotBytes]
+};
+
+__device__ __forceinline__ Ring ring_of(const PrefillArgs &a, int s, int h) {
+    unsigned char *ws = reinterpret_cast<unsigned char *>(a.scratch);
+    const size_t pair = (size_t)s * a.Hv + h;
+    int *flags = reinterpret_cast<int *>(ws) + pair * kFlagWords;
+    Ring r;
+    r.full = flags;
+    r.empty = flags + kRing;
+    r.gamma_c = reinterpret_cast<float *>(flags + 2 * kRing);
+    r.slots = ws + a.ring_offset + pair * (kRing * kSlotBytes);
+    return r;
+}
+
+// Shared context of one CTA.
+struct Ctx {
+    unsigned char *sm;
+    int tid, lane, wid, tl, half;
+    uint32_t tmem, tq, mbar, phase;
+    bool timed_out;
+
+    __device__ __forceinline__ void commit_wait() {
+        if (tid == 0) mma_commit(mbar);
+        bool ok = timed_out;           // after one timeout the rest of the launch only drains
+        for (int it = 0; it < kSpinLimit && !ok; ++it) ok = mbar_try(mbar, phase & 1u);
+        if (!ok) timed_out = true;
+        phase ^= 1u;
+        fence_after_sync();
+    }
+    __device__ __forceinline__ void publish() {      // generic smem writes -> visible to the tensor core
+        fence_proxy_async();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    }
+    __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t &ph) {
+        bool ok = timed_out;
+        for (int it = 0; it < kSpinLimit && !ok; ++it) ok = mbar_try(bar, ph & 1u);
+        if (!ok) timed_out = true;
+        ph ^= 1u;
+        return ok;
+    }
+    // thread 0 polls a ring flag; the result reaches every thread of the CTA
+    __device__ __forceinline__ void wait_flag(const int *p, int target) {
+        volatile int *okp = reinterpret_cast<volatile int *>(sm + kFlagOk);
+        if (tid == 0) *okp = (timed_out || poll_flag(p, target)) ? 1 : 0;
+        __syncthreads();
+        if (*okp == 0) timed_out = true;
+        __syncthreads();
+    }
+};
+
+// ---------------------------------------------------------------------------
+// preparation CTA: chunks c = par, par + 2, ...
+// ---------------------------------------------------------------------------
 template <typename Act>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
-    extern __shared__ __align__(1024) unsigned char sm[];
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int tl = tid & 127, half = tid >> 7;          // TMEM lane of this thread, column half
-    const int h = blockIdx.x, s = blockIdx.y;
+__device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int h, int par) {
+    unsigned char *sm = x.sm;
+    const int tid = x.tid, lane = x.lane, tl = x.tl, half = x.half;
     const int Hk = a.Hk, Hv = a.Hv, L = a.L, C = a.C;
     const int kh = h / a.r;
-    const bool qk_writer = (h % a.r) == 0;
-    const Act *qkv = static_cast<const Act *>(a.qkv);
-    float *vT = a.scratch + ((size_t)s * Hv + h) * kScrFloats;      // [128 channels][64 tokens]
+    const uint32_t tmem = x.tmem, tq = x.tq;
     const Act *rawA = reinterpret_cast<const Act *>(sm + kRA);        // [q|k|v][67][128] raw window of the chunk
     float *hist = reinterpret_cast<float *>(sm + kRB + kHistOff);     // [3][384] conv state (first chunk only)
     float *ssq = reinterpret_cast<float *>(sm + kRB + kSsqOff);       // [8][64] partial sums of squares
@@ -255,15 +360,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     float *logG = reinterpret_cast<float *>(sm + kLogG);
     float *betas = reinterpret_cast<float *>(sm + kBeta);
     float *gam = reinterpret_cast<float *>(sm + kGam);
-    float *rinv = reinterpret_cast<float *>(sm + kRinv);
     float *invq = reinterpret_cast<float *>(sm + kInvQ);
     float *invk = reinterpret_cast<float *>(sm + kInvK);
-    float *red = reinterpret_cast<float *>(sm + kRed);
     unsigned char *RA = sm + kRA, *RB = sm + kRB;
     const uint32_t sRA = smem_u32(RA), sRB = smem_u32(RB);
-    const uint32_t mbar = smem_u32(sm + kMbar), rawbar = smem_u32(sm + kRawBar), zbar = smem_u32(sm + kZBar);
-    uint32_t phase = 0, raw_phase = 0, z_phase = 0;
-    bool timed_out = false;
+    const uint32_t rawbar = smem_u32(sm + kRawBar);
+    uint32_t raw_phase = 0;
+    float *vT = a.scratch_vt + (((size_t)s * Hv + h) * 2 + par) * kVtFloats;   // [128 channels][64 tokens]
+    const Ring ring = ring_of(a, s, h);
 
     // global conv channel of local channel ch (q 0..127, k 128..255, v 256..383)
     auto gch = [&](int ch) -> int {
@@ -271,52 +375,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (ch < 2 * kD) return Hk * kD + kh * kD + (ch - kD);
         return 2 * Hk * kD + h * kD + (ch - 2 * kD);
     };
-
-    // ---- set-up: TMEM, mbarrier, state rows into registers
-    if (wid == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
-                         smem_u32(sm + kTmemSlot)),
-                     "r"(kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
-    }
-    if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(mbar));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(rawbar));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(zbar));
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + kTmemSlot);
-    const uint32_t tq = (uint32_t)(32 * (wid & 3)) << 16;         // this warp's TMEM lane quarter
-
-    // thread (j = tl, half) keeps S^T[j][64 half .. 64 half + 63] = S[i][j]
-    float St[64];
-    {
-        const float *src = a.state + (((size_t)s * Hv + h) * kD + tl) * kD + 64 * half;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            const float4 v = *reinterpret_cast<const float4 *>(src + 4 * q);
-            St[4 * q] = v.x; St[4 * q + 1] = v.y; St[4 * q + 2] = v.z; St[4 * q + 3] = v.w;
-        }
-    }
-
-    auto commit_wait = [&]() {
-        if (tid == 0) mma_commit(mbar);
-        bool ok = timed_out;           // after one timeout the rest of the launch only drains
-        for (int it = 0; it < kSpinLimit && !ok; ++it) ok = mbar_try(mbar, phase & 1u);
-        if (!ok) timed_out = true;
-        phase ^= 1u;
-        fence_after_sync();
-    };
-    auto publish = [&]() {              // generic-proxy smem writes -> visible to the tensor core
-        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
-    };
-
     // raw window rows t0-3 .. t0+63 of chunk cc: three 128-channel tiles (q, k, v of this head) of the
     // qkv tensor map, one thread.  Rows outside the tensor read as zero; rows of a neighbouring slot
     // and rows past the prompt are never used (the history rows of the first chunk come from the
@@ -330,18 +388,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         tma_load_2d(dst + kTile, &a.qkv_map, Hk * kD + kh * kD, y, rawbar);
         tma_load_2d(dst + 2 * kTile, &a.qkv_map, 2 * Hk * kD + h * kD, y, rawbar);
     };
-    auto wait_raw = [&]() {
-        bool ok = timed_out;
-        for (int it = 0; it < kSpinLimit && !ok; ++it) ok = mbar_try(rawbar, raw_phase & 1u);
-        if (!ok) timed_out = true;
-        raw_phase ^= 1u;
-    };
-    auto wait_z = [&]() {
-        bool ok = timed_out;
-        for (int it = 0; it < kSpinLimit && !ok; ++it) ok = mbar_try(zbar, z_phase & 1u);
-        if (!ok) timed_out = true;
-        z_phase ^= 1u;
-    };
     // gate inputs of chunk cc (threads tid < 64, one token each)
     float g_alpha = 0.f, g_beta = 0.f;
     auto load_gates = [&](int cc) {
@@ -353,37 +399,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
     };
 
-    if (tid == 0) issue_raw(0);
-    load_gates(0);
-    // the three window rows before the prompt: the conv state (fp32)
-    for (int it = tid; it < 3 * (kCh / 4); it += kThreads) {
-        const int row = it / (kCh / 4), ch = 4 * (it % (kCh / 4));
-        *reinterpret_cast<float4 *>(hist + row * kCh + ch) =
-            *reinterpret_cast<const float4 *>(a.conv_state + ((size_t)s * 3 + row) * C + gch(ch));
+    const int n_chunks = (L + kC - 1) / kC;
+    if (par >= n_chunks) return;
+    if (tid == 0) issue_raw(par);
+    load_gates(par);
+    if (par == 0) {
+        // the three window rows before the prompt: the conv state (fp32)
+        for (int it = tid; it < 3 * (kCh / 4); it += kThreads) {
+            const int row = it / (kCh / 4), ch = 4 * (it % (kCh / 4));
+            *reinterpret_cast<float4 *>(hist + row * kCh + ch) =
+                *reinterpret_cast<const float4 *>(a.conv_state + ((size_t)s * 3 + row) * C + gch(ch));
+        }
     }
 
-    const int n_chunks = (L + kC - 1) / kC;
-    for (int c = 0; c < n_chunks; ++c) {
+    for (int c = par; c < n_chunks; c += 2) {
         const int t0 = c * kC, n = min(kC, L - t0);
+        const int slot = c % kRing;
+        unsigned char *dst_slot = ring.slots + (size_t)slot * kSlotBytes;
 
-        // ---------------- (a) gates; the raw window (issued during the previous chunk) arrives
+        // ---------------- (a) gates; the raw window arrives
         if (tid < kC) {                    // padded tokens: no decay, no write
             float lg = 0.f, b = 0.f;
             if (tid < n) {
-                const float x = g_alpha + __ldg(a.dt_bias + h);
-                const float sp = x > 20.0f ? x : log1pf(expf(x));
+                const float xx = g_alpha + __ldg(a.dt_bias + h);
+                const float sp = xx > 20.0f ? xx : log1pf(expf(xx));
                 lg = -expf(__ldg(a.A_log + h)) * sp;
                 b = 1.0f / (1.0f + expf(-g_beta));
             }
             logG[tid] = lg;
             betas[tid] = b;
         }
-        wait_raw();
+        x.wait_bar(rawbar, raw_phase);
         __syncthreads();
-        if (c == 0) {
-            // every CTA of the cluster has read the old conv state (q/k channels are shared)
-            asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
-        }
         if (tid == 0) {                    // Gamma = exp(cumsum(log g)) inside the chunk
             float acc = 0.f;
             for (int t = 0; t < kC; ++t) {
@@ -392,8 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 gam[t] = expf(acc);
             }
         }
-        // conv + SiLU: item = (channel, 16-token segment), sliding window; into scratch.  For q and k the
-        // warp also sums y^2 over its 32 channels per token (reduce-scatter, fixed order).
+        // conv + SiLU: item = (channel, 16-token segment), sliding window.  q and k go to TMEM (lane =
+        // channel: the warp's lane quarter is (ch % 128) / 32 = warp % 4), v to the scratch, transposed.
+        // For q and k the warp also sums y^2 over its 32 channels per token (reduce-scatter, fixed order).
 #pragma unroll 1
         for (int k = 0; k < 6; ++k) {
             const int it = tid + k * kThreads;
@@ -416,17 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 y2[j] = yv[j] * yv[j];
                 x0 = x1; x1 = x2; x2 = x3;
             }
-            // q, k -> TMEM (lane = channel; the warp's lane quarter is (ch % 128) / 32 = warp % 4);
-            // v -> the scratch, transposed.  Warp-uniform: a warp's 32 channels share q|k|v.
-            if (ch < 2 * kD) {
+            if (ch < 2 * kD) {                    // warp-uniform: a warp's 32 channels share q|k|v
                 tmem_st16(tmem + tq + (ch < kD ? kColQ : kColK) + tb, yv);
-            } else {
-                float4 *dv = reinterpret_cast<float4 *>(vT + (ch - 2 * kD) * kC + tb);
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    dv[q4] = make_float4(yv[4 * q4], yv[4 * q4 + 1], yv[4 * q4 + 2], yv[4 * q4 + 3]);
-            }
-            if (ch < 2 * kD) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) y2[j] += __shfl_xor_sync(0xffffffffu, y2[j], 16);
 #pragma unroll
@@ -440,6 +479,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     }
                 }
                 if (lane < 16) ssq[(ch >> 5) * kC + tb + lane] = y2[0];   // token tb + lane, channel block ch/32
+            } else {
+                float4 *dv = reinterpret_cast<float4 *>(vT + (ch - 2 * kD) * kC + tb);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    dv[q4] = make_float4(yv[4 * q4], yv[4 * q4 + 1], yv[4 * q4 + 2], yv[4 * q4 + 3]);
             }
         }
         tmem_wait_st();
@@ -470,9 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             for (int q = 0; q < 32; ++q) x32[q] *= invq[32 * half + q];
             put_col32(RA, RA + 64 * 1024, kC + 32 * half, tl, x32);
         }
-        publish();
+        x.publish();
         if (tid == 0) mma3(tmem + kColG, sRA, sRA + 64 * 1024, sRA, sRA + 64 * 1024, 128, 64, false);
-        commit_wait();
+        x.commit_wait();
         {
             float g32[32];
             tmem_ld16(tmem + tq + kColG + 32 * half, g32);
@@ -520,24 +564,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const int nb = 4 - dist;               // blocks (j + dist, j), j < nb
             for (int e = tid; e < nb * 256; e += kThreads) {
                 const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15, i = j + dist;
-                float x = 0.f;
+                float acc = 0.f;
                 for (int kb = j; kb < i; ++kb)
 #pragma unroll
                     for (int m = 0; m < 16; ++m)
-                        x = fmaf(AMt[(16 * kb + m) * kC + 16 * i + rr], Tm[(16 * kb + m) * kC + 16 * j + cc], x);
-                Xb[e] = x;
+                        acc = fmaf(AMt[(16 * kb + m) * kC + 16 * i + rr], Tm[(16 * kb + m) * kC + 16 * j + cc], acc);
+                Xb[e] = acc;
             }
             __syncthreads();
             for (int e = tid; e < nb * 256; e += kThreads) {
                 const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15, i = j + dist;
-                float t = 0.f;
+                float acc = 0.f;
 #pragma unroll
-                for (int m = 0; m < 16; ++m) t = fmaf(Tm[(16 * i + rr) * kC + 16 * i + m], Xb[(j << 8) + m * 16 + cc], t);
-                Tm[(16 * i + rr) * kC + 16 * j + cc] = -t;
+                for (int m = 0; m < 16; ++m) acc = fmaf(Tm[(16 * i + rr) * kC + 16 * i + m], Xb[(j << 8) + m * 16 + cc], acc);
+                Tm[(16 * i + rr) * kC + 16 * j + cc] = -acc;
             }
             __syncthreads();
         }
-        // B = T (64 x 64) in RB[0, 32K); A1 = (diag(beta Gamma) K)^T, A2 = (diag(beta) V)^T in RA
+        // B = T (64 x 64) in RB[0, 32K); A1 = (diag(beta Gamma) K^)^T, A2 = (diag(beta) V)^T in RA
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             int r, k4;
@@ -545,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             put4(RB, RB + 16 * 1024, r, k4, 64, *reinterpret_cast<const float4 *>(Tm + r * kC + 4 * k4));
         }
         {
-            // row i = tl of (diag(beta Gamma) K^)^T and (diag(beta) V)^T, tokens 32 half .. 32 half + 31
+            // row i = tl, tokens 32 half .. 32 half + 31
             float x32[32];
             tmem_ld16(tmem + tq + kColK + 32 * half, x32);
             tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
@@ -568,63 +612,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                      make_float4(betas[sr] * v.x, betas[sr + 1] * v.y, betas[sr + 2] * v.z, betas[sr + 3] * v.w));
             }
         }
-        // the gate (z) tile of this chunk -> the A region, free from here until the next chunk's G
-        if constexpr (sizeof(Act) == 2) {
-            if (tid == 0) {
-                fence_proxy_async();
-                mbar_arrive_expect_tx(zbar, (uint32_t)(kC * kD * sizeof(Act)));
-                tma_load_2d(smem_u32(sm + kAM), &a.z_map, h * kD, s * L + t0, zbar);
-            }
-        }
-        publish();
+        x.publish();
         if (tid == 0) {
             mma3(tmem + kColWT, sRA, sRA + 32 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
             mma3(tmem + kColUT, sRA + 64 * 1024, sRA + 96 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
         }
-        commit_wait();
+        x.commit_wait();
 
-        // ---------------- (d) U^T = U~^T - S0^T W^T
+        // ---------------- (p) publish the chunk to its ring slot
+        if (c >= kRing) x.wait_flag(ring.empty + slot, c - kRing + 1);   // the state CTA took chunk c - kRing
         {
-            // B = -W (64 x 128): this thread holds W[r][i = tl] for its 32 values of r
-            float w32[32];
-            tmem_ld16(tmem + tq + kColWT + 32 * half, w32);
-            tmem_ld16(tmem + tq + kColWT + 32 * half + 16, w32 + 16);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) w32[q] = -w32[q];
-            put_col32(RB, RB + 32 * 1024, 32 * half, tl, w32);
-            // A = S0^T (128 x 128) from the registers
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-                put4(RA, RA + 64 * 1024, tl, 16 * half + q, 128,
-                     make_float4(St[4 * q], St[4 * q + 1], St[4 * q + 2], St[4 * q + 3]));
-        }
-        publish();
-        if (tid == 0) mma3(tmem + kColUT, sRA, sRA + 64 * 1024, sRB, sRB + 32 * 1024, 128, 64, true);
-        commit_wait();
-
-        // ---------------- (e) O^T = S0^T (diag(Gamma) Q)^T
-        {
+            // -W planes -> RB (64 x 128): this thread holds W[r][i = tl] for its 32 values of r
             float x32[32];
+            tmem_ld16(tmem + tq + kColWT + 32 * half, x32);
+            tmem_ld16(tmem + tq + kColWT + 32 * half + 16, x32 + 16);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) x32[q] = -x32[q];
+            put_col32(RB, RB + 32 * 1024, 32 * half, tl, x32);
+            // Gamma Q^ planes -> RA[0, 64K) (64 x 128)
             tmem_ld16(tmem + tq + kColQ + 32 * half, x32);
             tmem_ld16(tmem + tq + kColQ + 32 * half + 16, x32 + 16);
 #pragma unroll
             for (int q = 0; q < 32; ++q) x32[q] *= gam[32 * half + q] * invq[32 * half + q];
-            put_col32(RB, RB + 32 * 1024, 32 * half, tl, x32);
-        }
-        publish();
-        if (tid == 0) mma3(tmem + kColOT, sRA, sRA + 64 * 1024, sRB, sRB + 32 * 1024, 128, 64, false);
-        commit_wait();
-
-        // ---------------- (f) O^T += U^T P^T;  D2 = U^T (diag(Gamma_C / Gamma) K)
-        {
-            float u32[32];
-            tmem_ld16(tmem + tq + kColUT + 32 * half, u32);
-            tmem_ld16(tmem + tq + kColUT + 32 * half + 16, u32 + 16);
+            put_col32(RA, RA + 32 * 1024, 32 * half, tl, x32);
+            // U~^T fp32 [j = tl][r] -> RA[64K, 96K)
+            tmem_ld16(tmem + tq + kColUT + 32 * half, x32);
+            tmem_ld16(tmem + tq + kColUT + 32 * half + 16, x32 + 16);
+            float4 *urow = reinterpret_cast<float4 *>(RA + 64 * 1024 + (tl * kC + 32 * half) * 4);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                put4(RA, RA + 32 * 1024, tl, 8 * half + q, 64,
-                     make_float4(u32[4 * q], u32[4 * q + 1], u32[4 * q + 2], u32[4 * q + 3]));
+            for (int q4 = 0; q4 < 8; ++q4)
+                urow[q4] = make_float4(x32[4 * q4], x32[4 * q4 + 1], x32[4 * q4 + 2], x32[4 * q4 + 3]);
         }
+        // P planes -> RA[96K, 128K) (64 x 64)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             int r, k4;
@@ -632,10 +651,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             float p[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) p[e] = Pt[(4 * k4 + e) * kC + r];
-            put4(RB, RB + 16 * 1024, r, k4, 64, make_float4(p[0], p[1], p[2], p[3]));
+            put4(RA + 96 * 1024, RA + 112 * 1024, r, k4, 64, make_float4(p[0], p[1], p[2], p[3]));
         }
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_s2g(dst_slot + kSlotNegW, sRB, 64 * 1024);
+            bulk_s2g(dst_slot + kSlotGQ, sRA, 64 * 1024);
+            bulk_s2g(dst_slot + kSlotU, sRA + 64 * 1024, 32 * 1024);
+            bulk_s2g(dst_slot + kSlotP, sRA + 96 * 1024, 32 * 1024);
+            bulk_commit();
+            bulk_wait_read_all();                 // RB may be overwritten now
+        }
+        __syncthreads();
         {
-            // row i = tl of diag(Gamma_C / Gamma) K^, as (K^ ...)^T with tokens along K
+            // (Gamma_C / Gamma) K^ planes -> RB, as (128 x 64): row i = tl, tokens along K
             float x32[32];
             tmem_ld16(tmem + tq + kColK + 32 * half, x32);
             tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
@@ -648,20 +678,135 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     const int sr = 32 * half + 4 * q4 + e;
                     ka[e] = expf(lc - logG[sr]) * invk[sr] * x32[4 * q4 + e];
                 }
-                put4(RA + 64 * 1024, RA + 96 * 1024, tl, 8 * half + q4, 64, make_float4(ka[0], ka[1], ka[2], ka[3]));
+                put4(RB, RB + 32 * 1024, tl, 8 * half + q4, 64, make_float4(ka[0], ka[1], ka[2], ka[3]));
             }
         }
-        publish();
+        fence_proxy_async();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (tid == 0) {
+            bulk_s2g(dst_slot + kSlotKd, sRB, 64 * 1024);
+            bulk_commit();
+            bulk_wait_all();                      // every byte of the slot is in global memory
+            ring.gamma_c[slot] = gam[kC - 1];
+            fence_proxy_async_global();
+            __threadfence();
+            st_release(ring.full + slot, c + 1);
+            if (c + 2 < n_chunks) issue_raw(c + 2);
+        }
+        if (c + 2 < n_chunks) load_gates(c + 2);
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// state CTA: every chunk in order
+// ---------------------------------------------------------------------------
+template <typename Act>
+__device__ __forceinline__ void advance_state(const PrefillArgs &a, Ctx &x, int s, int h) {
+    unsigned char *sm = x.sm;
+    const int tid = x.tid, lane = x.lane, wid = x.wid, tl = x.tl, half = x.half;
+    const int Hv = a.Hv, L = a.L;
+    const uint32_t tmem = x.tmem, tq = x.tq;
+    float *rinv = reinterpret_cast<float *>(sm + kRinv);
+    float *red = reinterpret_cast<float *>(sm + kRed);
+    unsigned char *RA = sm + kRA;
+    const uint32_t sRA = smem_u32(RA), sRB = smem_u32(sm + kRB);
+    const uint32_t ldbar = smem_u32(sm + kRawBar), zbar = smem_u32(sm + kZBar);
+    uint32_t ld_phase = 0, z_phase = 0;
+    const Ring ring = ring_of(a, s, h);
+    Act *out = static_cast<Act *>(a.out);
+    const Act *z = static_cast<const Act *>(a.z);
+
+    // thread (j = tl, half) keeps S^T[j][64 half .. 64 half + 63] = S[i][j]
+    float St[64];
+    {
+        const float *src = a.state + (((size_t)s * Hv + h) * kD + tl) * kD + 64 * half;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const float4 v = *reinterpret_cast<const float4 *>(src + 4 * q);
+            St[4 * q] = v.x; St[4 * q + 1] = v.y; St[4 * q + 2] = v.z; St[4 * q + 3] = v.w;
+        }
+    }
+
+    const int n_chunks = (L + kC - 1) / kC;
+    for (int c = 0; c < n_chunks; ++c) {
+        const int t0 = c * kC, n = min(kC, L - t0);
+        const int slot = c % kRing;
+        const unsigned char *src_slot = ring.slots + (size_t)slot * kSlotBytes;
+
+        if constexpr (sizeof(Act) == 2) {       // the gate (z) tile of this chunk -> AMt region
+            if (tid == 0) {
+                mbar_arrive_expect_tx(zbar, (uint32_t)(kC * kD * sizeof(Act)));
+                tma_load_2d(smem_u32(sm + kAM), &a.z_map, h * kD, s * L + t0, zbar);
+            }
+        }
+        x.wait_flag(ring.full + slot, c + 1);
+        if (tid == 0) {
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(ldbar, 64 * 1024);
+            bulk_g2s(sRB, src_slot + kSlotNegW, 64 * 1024, ldbar);
+        }
+        // U~^T row j = tl, tokens 32 half .. 32 half + 31; Gamma_C
+        float u32[32];
+        {
+            const float4 *urow = reinterpret_cast<const float4 *>(src_slot + kSlotU + (tl * kC + 32 * half) * 4);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 v = urow[q4];
+                u32[4 * q4] = v.x; u32[4 * q4 + 1] = v.y; u32[4 * q4 + 2] = v.z; u32[4 * q4 + 3] = v.w;
+            }
+        }
+        const float gc = ring.gamma_c[slot];
+        // A = S0^T (128 x 128) from the registers
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            put4(RA, RA + 64 * 1024, tl, 16 * half + q, 128,
+                 make_float4(St[4 * q], St[4 * q + 1], St[4 * q + 2], St[4 * q + 3]));
+        x.wait_bar(ldbar, ld_phase);
+        x.publish();
+        // X^T = S0^T (-W)^T
+        if (tid == 0) mma3(tmem + kColUT, sRA, sRA + 64 * 1024, sRB, sRB + 32 * 1024, 128, 64, false);
+        x.commit_wait();
+        if (tid == 0) {
+            mbar_arrive_expect_tx(ldbar, 64 * 1024);
+            bulk_g2s(sRB, src_slot + kSlotGQ, 64 * 1024, ldbar);
+        }
+        {
+            // U^T = U~^T + X^T
+            float x32[32];
+            tmem_ld16(tmem + tq + kColUT + 32 * half, x32);
+            tmem_ld16(tmem + tq + kColUT + 32 * half + 16, x32 + 16);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) u32[q] += x32[q];
+        }
+        x.wait_bar(ldbar, ld_phase);
+        x.publish();
+        // O^T = S0^T (Gamma Q)^T
+        if (tid == 0) mma3(tmem + kColOT, sRA, sRA + 64 * 1024, sRB, sRB + 32 * 1024, 128, 64, false);
+        x.commit_wait();
+        if (tid == 0) {
+            mbar_arrive_expect_tx(ldbar, 96 * 1024);
+            bulk_g2s(sRB, src_slot + kSlotP, 32 * 1024, ldbar);
+            bulk_g2s(sRA + 64 * 1024, src_slot + kSlotKd, 64 * 1024, ldbar);
+        }
+        // A = U^T (128 x 64) planes -> RA[0, 64K)
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            put4(RA, RA + 32 * 1024, tl, 8 * half + q, 64,
+                 make_float4(u32[4 * q], u32[4 * q + 1], u32[4 * q + 2], u32[4 * q + 3]));
+        x.wait_bar(ldbar, ld_phase);
+        if (tid == 0) st_release(ring.empty + slot, c + 1);     // the slot's bytes are all in shared memory
+        x.publish();
+        // O^T += U^T P^T;  D2 = U^T (diag(Gamma_C / Gamma) K)
         if (tid == 0) {
             mma3(tmem + kColOT, sRA, sRA + 32 * 1024, sRB, sRB + 16 * 1024, 64, 64, true);
             mma3(tmem + kColD2, sRA, sRA + 32 * 1024, sRA + 64 * 1024, sRA + 96 * 1024, 64, 128, false);
         }
-        // the gate inputs of the epilogue, fetched while the tensor core works
-        Act *out = static_cast<Act *>(a.out);
-        const Act *z = static_cast<const Act *>(a.z);
         float zg[32];
         if constexpr (sizeof(Act) == 2) {
-            wait_z();
+            x.wait_bar(zbar, z_phase);
             const Act *zs = reinterpret_cast<const Act *>(sm + kAM);       // [64 tokens][128]
 #pragma unroll
             for (int q = 0; q < 32; ++q) zg[q] = to_f32(zs[(32 * half + q) * kD + tl]);
@@ -672,14 +817,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 zg[q] = t < n ? to_f32(z[((size_t)s * L + t0 + t) * Hv * kD + (size_t)h * kD + tl]) : 0.f;
             }
         }
-        commit_wait();
-        // the operand regions are free: fetch the next chunk's window and gate inputs now
-        if (c + 1 < n_chunks) {
-            if (tid == 0) issue_raw(c + 1);
-            load_gates(c + 1);
-        }
+        x.commit_wait();
 
-        // ---------------- (g) outputs (gated RMSNorm) and the state update
+        // ---------------- outputs (gated RMSNorm) and the state update
         {
             float o32[32];
             tmem_ld16(tmem + tq + kColOT + 32 * half, o32);
@@ -718,7 +858,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 }
             }
             // S^T <- Gamma_C S^T + D2
-            const float gc = gam[kC - 1];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 float d16[16];
@@ -727,34 +866,75 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 for (int e = 0; e < 16; ++e) St[16 * q4 + e] = fmaf(gc, St[16 * q4 + e], d16[e]);
             }
         }
+        fence_before_sync();
         __syncthreads();
+        fence_after_sync();
     }
 
-    // ---- final state, conv state, TMEM release
-    {
-        float *dst = a.state + (((size_t)s * Hv + h) * kD + tl) * kD + 64 * half;
+    float *dst = a.state + (((size_t)s * Hv + h) * kD + tl) * kD + 64 * half;
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-            *reinterpret_cast<float4 *>(dst + 4 * q) =
-                make_float4(St[4 * q], St[4 * q + 1], St[4 * q + 2], St[4 * q + 3]);
+    for (int q = 0; q < 16; ++q)
+        *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(St[4 * q], St[4 * q + 1], St[4 * q + 2], St[4 * q + 3]);
+}
+
+// grid (3 x pairs): for pair p0 + blockIdx.x / 3, CTA 0 and 1 prepare (even / odd chunks), CTA 2 carries
+// the state
+template <typename Act>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
+    extern __shared__ __align__(1024) unsigned char sm[];
+    Ctx x;
+    x.sm = sm;
+    x.tid = threadIdx.x; x.lane = x.tid & 31; x.wid = x.tid >> 5;
+    x.tl = x.tid & 127; x.half = x.tid >> 7;           // TMEM lane of this thread, column half
+    x.phase = 0;
+    x.timed_out = false;
+    const int role = blockIdx.x % 3, pair = a.pair0 + blockIdx.x / 3;
+    const int s = pair / a.Hv, h = pair % a.Hv;
+
+    if (x.wid == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                         smem_u32(sm + kTmemSlot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
-    // the new conv state is the last 3 window rows; rows before the prompt are old conv-state rows
-    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-    for (int ch = tid; ch < kCh; ch += kThreads) {
-        if (ch < 2 * kD && !qk_writer) continue;
-        const int g = gch(ch);
-        float *cs = a.conv_state + (size_t)s * 3 * C + g;
-        float nv[3];
-        for (int rr = 0; rr < 3; ++rr) {
-            const int t = L - 3 + rr;
-            nv[rr] = t >= 0 ? to_f32(qkv[((size_t)s * L + t) * C + g]) : cs[(size_t)(3 + t) * C];
-        }
-        for (int rr = 0; rr < 3; ++rr) cs[(size_t)rr * C] = nv[rr];
+    x.mbar = smem_u32(sm + kMbar);
+    if (x.tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(x.mbar));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(sm + kRawBar)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(sm + kZBar)));
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
-    if (timed_out && tid == 0 && a.d_status) atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TIMEOUT));
     fence_before_sync();
     __syncthreads();
-    if (wid == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
+    fence_after_sync();
+    x.tmem = *reinterpret_cast<volatile uint32_t *>(sm + kTmemSlot);
+    x.tq = (uint32_t)(32 * (x.wid & 3)) << 16;        // this warp's TMEM lane quarter
+
+    if (role < 2) prepare<Act>(a, x, s, h, role);
+    else advance_state<Act>(a, x, s, h);
+
+    if (x.timed_out && x.tid == 0 && a.d_status) atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TIMEOUT));
+    fence_before_sync();
+    __syncthreads();
+    if (x.wid == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(x.tmem), "r"(kTmemCols));
+}
+
+// conv state after the prompt: the last three raw inputs (rows before the prompt shift in from the
+// old conv state when L < 3).  One thread per (slot, channel), in place.
+template <typename Act>
+__global__ void __launch_bounds__(256) prefill_conv_state_kernel(const Act *qkv, float *conv_state, int L, int C) {
+    const int g = blockIdx.x * blockDim.x + threadIdx.x, s = blockIdx.y;
+    if (g >= C) return;
+    float *cs = conv_state + (size_t)s * 3 * C + g;
+    float nv[3];
+#pragma unroll
+    for (int rr = 0; rr < 3; ++rr) {
+        const int t = L - 3 + rr;
+        nv[rr] = t >= 0 ? to_f32(qkv[((size_t)s * L + t) * C + g]) : cs[(size_t)(3 + t) * C];
+    }
+#pragma unroll
+    for (int rr = 0; rr < 3; ++rr) cs[(size_t)rr * C] = nv[rr];
 }
 
 }  // namespace
@@ -772,39 +952,25 @@ int prefill_check(const gdn_dims &d, std::string &why) {
         why = "prefill: n_slots * n_tokens must be below 2^31";
         return GDN_ERR_SHAPE;
     }
-    if (d.n_v_heads / d.n_qk_heads > 8) {
-        why = "prefill: at most 8 value heads per key head (one thread-block cluster)";
+    if (3LL * d.n_slots * d.n_v_heads > 2147483647LL) {
+        why = "prefill: too many (slot, value head) pairs";
         return GDN_ERR_SHAPE;
     }
     return GDN_OK;
 }
 
-size_t prefill_workspace_bytes(const gdn_dims &d) {
-    return (size_t)d.n_slots * d.n_v_heads * kScrFloats * sizeof(float);
+static size_t ring_offset_bytes(const gdn_dims &d) {
+    const size_t flags = (size_t)d.n_slots * d.n_v_heads * kFlagWords * sizeof(int);
+    return (flags + 255) & ~(size_t)255;
 }
 
-static cudaError_t launch_prefill_args(const PrefillArgs &a, gdn_dtype act, cudaStream_t stream) {
-    const bool bf = act == GDN_BF16;
-    void (*kern)(PrefillArgs) = bf ? prefill_kernel<__nv_bfloat16> : prefill_kernel<float>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.Hv, a.B, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = a.r;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+size_t prefill_workspace_bytes(const gdn_dims &d) {
+    const size_t pairs = (size_t)d.n_slots * d.n_v_heads;
+    return ring_offset_bytes(d) + pairs * kRing * kSlotBytes + pairs * 2 * kVtFloats * sizeof(float);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     std::call_once(once, [] {
@@ -829,28 +995,67 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
     a.qkv = qkv; a.z = z; a.alpha = alpha; a.beta_raw = beta_raw;
     a.state = state; a.conv_state = conv_state; a.out = out;
     a.scratch = static_cast<float *>(workspace);
+    a.ring_offset = ring_offset_bytes(d);
+    a.scratch_vt = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + a.ring_offset +
+                                             (size_t)d.n_slots * d.n_v_heads * kRing * kSlotBytes);
     a.d_status = d_status;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const bool bf = d.act_dtype == GDN_BF16;
-    const cuuint64_t dims[2] = {(cuuint64_t)a.C, (cuuint64_t)a.B * (cuuint64_t)a.L};
-    const cuuint64_t strides[1] = {(cuuint64_t)a.C * (bf ? 2u : 4u)};
-    const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kWin};
+    const CUtensorMapDataType dt = bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const cuuint32_t esz = bf ? 2u : 4u;
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = encode(&a.qkv_map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                              const_cast<void *>(qkv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const cuuint64_t dims[2] = {(cuuint64_t)a.C, (cuuint64_t)a.B * (cuuint64_t)a.L};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.C * esz};
+    const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kWin};
+    if (encode(&a.qkv_map, dt, 2, const_cast<void *>(qkv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     const cuuint64_t zdims[2] = {(cuuint64_t)a.Hv * kD, (cuuint64_t)a.B * (cuuint64_t)a.L};
-    const cuuint64_t zstrides[1] = {(cuuint64_t)a.Hv * kD * (bf ? 2u : 4u)};
+    const cuuint64_t zstrides[1] = {(cuuint64_t)a.Hv * kD * esz};
     const cuuint32_t zbox[2] = {(cuuint32_t)kD, (cuuint32_t)kC};
-    const CUresult rz = encode(&a.z_map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                               const_cast<void *>(z), zdims, zstrides, zbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (rz != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    return launch_prefill_args(a, d.act_dtype, stream);
+    if (encode(&a.z_map, dt, 2, const_cast<void *>(z), zdims, zstrides, zbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
+    void (*kern)(PrefillArgs) = bf ? prefill_kernel<__nv_bfloat16> : prefill_kernel<float>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmemBytes)) != cudaSuccess)
+        return e;
+    const int pairs_per_launch = (sms * per_sm) / 3;
+    if (pairs_per_launch < 1) return cudaErrorCooperativeLaunchTooLarge;
+    // fresh ring flags (and slot decays) for every (slot, head)
+    if ((e = cudaMemsetAsync(workspace, 0, a.ring_offset, stream)) != cudaSuccess) return e;
+    const int pairs = a.B * a.Hv;
+    for (int p0 = 0; p0 < pairs; p0 += pairs_per_launch) {
+        a.pair0 = p0;
+        const int np = pairs - p0 < pairs_per_launch ? pairs - p0 : pairs_per_launch;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(3 * np, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, kern, a)) != cudaSuccess) return e;
+    }
+    const dim3 cgrid((a.C + 255) / 256, a.B);
+    if (bf)
+        prefill_conv_state_kernel<__nv_bfloat16><<<cgrid, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(qkv), conv_state, a.L, a.C);
+    else
+        prefill_conv_state_kernel<float><<<cgrid, 256, 0, stream>>>(static_cast<const float *>(qkv), conv_state,
+                                                                     a.L, a.C);
+    return cudaGetLastError();
 }
 
 }  // namespace gdn
