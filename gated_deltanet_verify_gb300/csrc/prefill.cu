@@ -251,14 +251,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// own shared memory -> global, bulk async (completion: bulk_commit / bulk_wait*)
-__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 // global -> own shared memory, completion counted in bytes on an mbarrier
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
@@ -346,7 +338,7 @@ struct Ctx {
 template <typename Act>
 __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int h, int par) {
     unsigned char *sm = x.sm;
-    const int tid = x.tid, lane = x.lane, tl = x.tl, half = x.half;
+    const int tid = x.tid, lane = x.lane, wid = x.wid, tl = x.tl, half = x.half;
     const int Hk = a.Hk, Hv = a.Hv, L = a.L, C = a.C;
     const int kh = h / a.r;
     const uint32_t tmem = x.tmem, tq = x.tq;
@@ -399,6 +391,25 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
         }
     };
 
+    // A published chunk is released one phase later (after the next chunk's conv), so the stores
+    // drain while that work runs: every thread fences its own stores, the CTA synchronises, thread 0
+    // releases the flag.  pend_* are uniform across the CTA.
+    int pend_slot = -1, pend_c = 0;
+    float pend_gamma = 0.f;
+    auto release_pending = [&]() {            // after a __syncthreads that followed fence_pending()
+        if (pend_slot >= 0) {
+            if (tid == 0) {
+                ring.gamma_c[pend_slot] = pend_gamma;
+                __threadfence();
+                st_release(ring.full + pend_slot, pend_c + 1);
+            }
+            pend_slot = -1;
+        }
+    };
+    auto fence_pending = [&]() {
+        if (pend_slot >= 0) __threadfence();
+    };
+
     const int n_chunks = (L + kC - 1) / kC;
     if (par >= n_chunks) return;
     if (tid == 0) issue_raw(par);
@@ -431,13 +442,19 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
         }
         x.wait_bar(rawbar, raw_phase);
         __syncthreads();
-        if (tid == 0) {                    // Gamma = exp(cumsum(log g)) inside the chunk
-            float acc = 0.f;
-            for (int t = 0; t < kC; ++t) {
-                acc += logG[t];
-                logG[t] = acc;
-                gam[t] = expf(acc);
+        if (wid == 0) {                    // Gamma = exp(cumsum(log g)) inside the chunk: lane l owns 2l, 2l+1
+            const float l0 = logG[2 * lane], l1 = logG[2 * lane + 1];
+            float incl = l0 + l1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
             }
+            const float c0 = incl - l1;
+            logG[2 * lane] = c0;
+            logG[2 * lane + 1] = incl;
+            gam[2 * lane] = expf(c0);
+            gam[2 * lane + 1] = expf(incl);
         }
         // conv + SiLU: item = (channel, 16-token segment), sliding window.  q and k go to TMEM (lane =
         // channel: the warp's lane quarter is (ch % 128) / 32 = warp % 4), v to the scratch, transposed.
@@ -450,15 +467,18 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
             const float w0 = __ldg(a.conv_w + g), w1 = __ldg(a.conv_w + C + g), w2 = __ldg(a.conv_w + 2 * C + g),
                         w3 = __ldg(a.conv_w + 3 * C + g);
             const Act *src = rawA + (ch >> 7) * (kWin * kD) + (ch & (kD - 1));
-            auto xin = [&](int row) -> float {    // window row (token t0 - 3 + row)
-                return (c == 0 && row < 3) ? hist[row * kCh + ch] : to_f32(src[row * kD]);
-            };
-            float x0 = xin(tb), x1 = xin(tb + 1), x2 = xin(tb + 2);
+            // window row r holds token t0 - 3 + r; rows 0-2 of the first chunk come from the conv state
+            float x0, x1, x2;
+            if (c == 0 && tb == 0) {
+                x0 = hist[ch]; x1 = hist[kCh + ch]; x2 = hist[2 * kCh + ch];
+            } else {
+                x0 = to_f32(src[tb * kD]); x1 = to_f32(src[(tb + 1) * kD]); x2 = to_f32(src[(tb + 2) * kD]);
+            }
             float yv[16], y2[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int t = tb + j;
-                const float x3 = xin(t + 3);
+                const float x3 = to_f32(src[(t + 3) * kD]);
                 const float y = silu(fmaf(w3, x3, fmaf(w2, x2, fmaf(w1, x1, w0 * x0))));
                 yv[j] = t < n ? y : 0.f;
                 y2[j] = yv[j] * yv[j];
@@ -487,9 +507,11 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
             }
         }
         tmem_wait_st();
+        fence_pending();
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
+        release_pending();
         // inverse L2 norms of the q and k rows (a zero padded row stays zero)
         if (tid < 2 * kC) {
             const int t = tid & (kC - 1), part = tid >> 6;
@@ -527,7 +549,7 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     const int sc = 32 * half + q;
-                    AMt[sc * kC + r] = sc < r ? br * expf(lr - logG[sc]) * g32[q] : 0.f;
+                    AMt[sc * kC + r] = sc < r ? br * __expf(lr - logG[sc]) * g32[q] : 0.f;
                 }
             } else {                       // P[r][s] = q_r.k_s Gamma_r / Gamma_s for s <= r
                 const int r = tl - kC;
@@ -535,16 +557,49 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     const int sc = 32 * half + q;
-                    Pt[sc * kC + r] = sc <= r ? expf(lr - logG[sc]) * g32[q] : 0.f;
+                    Pt[sc * kC + r] = sc <= r ? __expf(lr - logG[sc]) * g32[q] : 0.f;
                 }
             }
         }
         __syncthreads();
 
+        // this thread's row of v^T for the A2 operand below, fetched before the inversion
+        float4 vpre[8];
+        {
+            const float4 *vrow = reinterpret_cast<const float4 *>(vT + tl * kC + 32 * half);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) vpre[q4] = vrow[q4];
+        }
+
+        // A1 = (diag(beta Gamma) K^)^T, A2 = (diag(beta) V)^T -> RA: warp (quarter, half) builds rows
+        // 32 quarter .. +31 of tokens 32 half .. +31
+        auto build_a12 = [&]() {
+            float x32[32];
+            tmem_ld16(tmem + tq + kColK + 32 * half, x32);
+            tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                float ka[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int sr = 32 * half + 4 * q4 + e;
+                    ka[e] = betas[sr] * gam[sr] * invk[sr] * x32[4 * q4 + e];
+                }
+                put4(RA, RA + 32 * 1024, tl, 8 * half + q4, 64, make_float4(ka[0], ka[1], ka[2], ka[3]));
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 v = vpre[q4];
+                const int sr = 32 * half + 4 * q4;
+                put4(RA + 64 * 1024, RA + 96 * 1024, tl, 8 * half + q4, 64,
+                     make_float4(betas[sr] * v.x, betas[sr + 1] * v.y, betas[sr + 2] * v.z, betas[sr + 3] * v.w));
+            }
+        };
         // ---------------- (c) T = (I + A)^-1, 16 x 16 blocks
-        // diagonal blocks: forward substitution, one column per thread, in registers
-        if (tid < kC) {
-            const int b = tid >> 4, col = tid & 15, o = 16 * b;
+        // diagonal blocks: forward substitution, one column per thread, in registers, by warps 6-7 while
+        // warps 0-5 build their rows of the A1 / A2 operands (RA is free since G completed)
+        if (wid >= 6) {
+            const int b = (tid - 192) >> 4, col = tid & 15, o = 16 * b;
             float tc[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
@@ -557,6 +612,8 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
             for (int r = 0; r < 16; ++r) Tm[(o + r) * kC + o + col] = tc[r];
             for (int r = 0; r < 16; ++r)          // the strictly upper blocks of this block column are zero
                 for (int bb = 0; bb < b; ++bb) Tm[(16 * bb + r) * kC + o + col] = 0.f;
+        } else {
+            build_a12();
         }
         __syncthreads();
         // off-diagonal blocks by distance: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
@@ -581,37 +638,14 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
             }
             __syncthreads();
         }
-        // B = T (64 x 64) in RB[0, 32K); A1 = (diag(beta Gamma) K^)^T, A2 = (diag(beta) V)^T in RA
+        // B = T (64 x 64) in RB[0, 32K); warps 6-7 build their rows of A1 / A2 now
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             int r, k4;
             item_rc(tid + k * kThreads, 64, r, k4);
             put4(RB, RB + 16 * 1024, r, k4, 64, *reinterpret_cast<const float4 *>(Tm + r * kC + 4 * k4));
         }
-        {
-            // row i = tl, tokens 32 half .. 32 half + 31
-            float x32[32];
-            tmem_ld16(tmem + tq + kColK + 32 * half, x32);
-            tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
-            const float4 *vrow = reinterpret_cast<const float4 *>(vT + tl * kC + 32 * half);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                float ka[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int sr = 32 * half + 4 * q4 + e;
-                    ka[e] = betas[sr] * gam[sr] * invk[sr] * x32[4 * q4 + e];
-                }
-                put4(RA, RA + 32 * 1024, tl, 8 * half + q4, 64, make_float4(ka[0], ka[1], ka[2], ka[3]));
-            }
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 v = vrow[q4];
-                const int sr = 32 * half + 4 * q4;
-                put4(RA + 64 * 1024, RA + 96 * 1024, tl, 8 * half + q4, 64,
-                     make_float4(betas[sr] * v.x, betas[sr + 1] * v.y, betas[sr + 2] * v.z, betas[sr + 3] * v.w));
-            }
-        }
+        if (wid >= 6) build_a12();
         x.publish();
         if (tid == 0) {
             mma3(tmem + kColWT, sRA, sRA + 32 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
@@ -619,54 +653,37 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
         }
         x.commit_wait();
 
-        // ---------------- (p) publish the chunk to its ring slot
+        // the A region is free: fetch the next chunk's window and gate inputs now
+        if (c + 2 < n_chunks) {
+            if (tid == 0) issue_raw(c + 2);
+            load_gates(c + 2);
+        }
+
+        // ---------------- (p) publish the chunk to its ring slot: every operand goes from registers
+        // straight to the slot (16-byte stores into L2), in the layout the state CTA copies in
         if (c >= kRing) x.wait_flag(ring.empty + slot, c - kRing + 1);   // the state CTA took chunk c - kRing
         {
-            // -W planes -> RB (64 x 128): this thread holds W[r][i = tl] for its 32 values of r
+            // -W planes (64 x 128): this thread holds W[r][i = tl] for its 32 values of r
             float x32[32];
             tmem_ld16(tmem + tq + kColWT + 32 * half, x32);
             tmem_ld16(tmem + tq + kColWT + 32 * half + 16, x32 + 16);
 #pragma unroll
             for (int q = 0; q < 32; ++q) x32[q] = -x32[q];
-            put_col32(RB, RB + 32 * 1024, 32 * half, tl, x32);
-            // Gamma Q^ planes -> RA[0, 64K) (64 x 128)
+            put_col32(dst_slot + kSlotNegW, dst_slot + kSlotNegW + 32 * 1024, 32 * half, tl, x32);
+            // Gamma Q^ planes (64 x 128)
             tmem_ld16(tmem + tq + kColQ + 32 * half, x32);
             tmem_ld16(tmem + tq + kColQ + 32 * half + 16, x32 + 16);
 #pragma unroll
             for (int q = 0; q < 32; ++q) x32[q] *= gam[32 * half + q] * invq[32 * half + q];
-            put_col32(RA, RA + 32 * 1024, 32 * half, tl, x32);
-            // U~^T fp32 [j = tl][r] -> RA[64K, 96K)
+            put_col32(dst_slot + kSlotGQ, dst_slot + kSlotGQ + 32 * 1024, 32 * half, tl, x32);
+            // U~^T fp32 [j = tl][r]
             tmem_ld16(tmem + tq + kColUT + 32 * half, x32);
             tmem_ld16(tmem + tq + kColUT + 32 * half + 16, x32 + 16);
-            float4 *urow = reinterpret_cast<float4 *>(RA + 64 * 1024 + (tl * kC + 32 * half) * 4);
+            float4 *urow = reinterpret_cast<float4 *>(dst_slot + kSlotU + (tl * kC + 32 * half) * 4);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4)
                 urow[q4] = make_float4(x32[4 * q4], x32[4 * q4 + 1], x32[4 * q4 + 2], x32[4 * q4 + 3]);
-        }
-        // P planes -> RA[96K, 128K) (64 x 64)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            int r, k4;
-            item_rc(tid + k * kThreads, 64, r, k4);
-            float p[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) p[e] = Pt[(4 * k4 + e) * kC + r];
-            put4(RA + 96 * 1024, RA + 112 * 1024, r, k4, 64, make_float4(p[0], p[1], p[2], p[3]));
-        }
-        fence_proxy_async();
-        __syncthreads();
-        if (tid == 0) {
-            bulk_s2g(dst_slot + kSlotNegW, sRB, 64 * 1024);
-            bulk_s2g(dst_slot + kSlotGQ, sRA, 64 * 1024);
-            bulk_s2g(dst_slot + kSlotU, sRA + 64 * 1024, 32 * 1024);
-            bulk_s2g(dst_slot + kSlotP, sRA + 96 * 1024, 32 * 1024);
-            bulk_commit();
-            bulk_wait_read_all();                 // RB may be overwritten now
-        }
-        __syncthreads();
-        {
-            // (Gamma_C / Gamma) K^ planes -> RB, as (128 x 64): row i = tl, tokens along K
-            float x32[32];
+            // (Gamma_C / Gamma) K^ planes, as (128 x 64): row i = tl, tokens along K
             tmem_ld16(tmem + tq + kColK + 32 * half, x32);
             tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
             const float lc = logG[kC - 1];
@@ -676,28 +693,30 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int sr = 32 * half + 4 * q4 + e;
-                    ka[e] = expf(lc - logG[sr]) * invk[sr] * x32[4 * q4 + e];
+                    ka[e] = __expf(lc - logG[sr]) * invk[sr] * x32[4 * q4 + e];
                 }
-                put4(RB, RB + 32 * 1024, tl, 8 * half + q4, 64, make_float4(ka[0], ka[1], ka[2], ka[3]));
+                put4(dst_slot + kSlotKd, dst_slot + kSlotKd + 32 * 1024, tl, 8 * half + q4, 64,
+                     make_float4(ka[0], ka[1], ka[2], ka[3]));
             }
         }
-        fence_proxy_async();
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
-        if (tid == 0) {
-            bulk_s2g(dst_slot + kSlotKd, sRB, 64 * 1024);
-            bulk_commit();
-            bulk_wait_all();                      // every byte of the slot is in global memory
-            ring.gamma_c[slot] = gam[kC - 1];
-            fence_proxy_async_global();
-            __threadfence();
-            st_release(ring.full + slot, c + 1);
-            if (c + 2 < n_chunks) issue_raw(c + 2);
+        // P planes (64 x 64)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            int r, k4;
+            item_rc(tid + k * kThreads, 64, r, k4);
+            float p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) p[e] = Pt[(4 * k4 + e) * kC + r];
+            put4(dst_slot + kSlotP, dst_slot + kSlotP + 16 * 1024, r, k4, 64, make_float4(p[0], p[1], p[2], p[3]));
         }
-        if (c + 2 < n_chunks) load_gates(c + 2);
+        pend_slot = slot;                         // released after the next chunk's conv (or at the end)
+        pend_c = c;
+        pend_gamma = gam[kC - 1];
         __syncthreads();
     }
+    fence_pending();
+    __syncthreads();
+    release_pending();
 }
 
 // ---------------------------------------------------------------------------
