@@ -20,8 +20,8 @@ def _built():
     torch.cuda.set_device(0)
 
 
-def run_prefill(shape, x, status=None):
-    d = dims_of(shape)
+def run_prefill(shape, x, status=None, q_scale=1.0):
+    d = dims_of(shape, q_scale=q_scale)
     ws_bytes = gdn.gdn_prefill_workspace_bytes(d)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda") if ws_bytes else None
     out = torch.empty((shape.n_slots, shape.n_tokens, shape.n_v_heads * shape.d_v), dtype=act_torch_dtype(shape),
@@ -42,8 +42,11 @@ CASES = {
     "L300_ragged": _shape(),
     "L64_one_chunk": _shape(n_tokens=64),
     "L1": _shape(n_tokens=1),
+    "L2_conv_tail": _shape(n_tokens=2),
     "L129_two_slots": _shape(n_tokens=129, n_slots=2),
     "L200_f32": _shape(n_tokens=200, act="f32"),
+    "L520_r1": _shape(n_tokens=520, n_qk_heads=3, n_v_heads=3, seed=42),
+    "L190_r8": _shape(n_tokens=190, n_qk_heads=1, n_v_heads=8, seed=43),
 }
 
 
@@ -69,3 +72,31 @@ def test_prefill_full_size_sampled_heads():
         sl = slice(h * shape.d_v, (h + 1) * shape.d_v)
         assert_act_close(gpu["out"][:, :, sl], ref["out"][:, :, sl], shape.act, f"out h{h}")
     assert np.array_equal(gpu["conv_state"], ref["conv_state"])
+
+
+def test_prefill_q_scale():
+    shape = _shape(n_tokens=150, seed=44)
+    inp = make_inputs(shape)
+    qs = 1.0 / np.sqrt(128.0)
+    gpu = run_prefill(shape, upload(inp), q_scale=qs)
+    ref = oracle.verify(shape, inp.as_f64(), capture=False, n_threads=8, q_scale=qs)
+    assert_f32_close(gpu["state"], ref["state"], "state")
+    assert_act_close(gpu["out"], ref["out"], shape.act, "out")
+
+
+def test_prefill_more_pairs_than_one_launch():
+    # 2 slots x 48 value heads = 96 (slot, head) pairs: more than one cooperative launch holds on the
+    # GPU (three CTAs per pair), so the call spans several launches
+    shape = Shape("prefill_pairs", n_slots=2, n_qk_heads=16, n_v_heads=48, d_k=128, d_v=128, n_tokens=130,
+                  act="bf16", seed=45)
+    inp = make_inputs(shape)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpu = run_prefill(shape, upload(inp), status=status)
+    heads = [0, 23, 47]
+    ref = oracle.verify(shape, inp.as_f64(), capture=False, head_mask=heads, n_threads=8)
+    for h in heads:
+        assert_f32_close(gpu["state"][:, h], ref["state"][:, h], f"state h{h}")
+        sl = slice(h * shape.d_v, (h + 1) * shape.d_v)
+        assert_act_close(gpu["out"][:, :, sl], ref["out"][:, :, sl], shape.act, f"out h{h}")
+    assert np.array_equal(gpu["conv_state"], ref["conv_state"])
+    assert int(status.item()) == gdn.GDN_OK
