@@ -43,6 +43,7 @@
 
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
+#include <cstdlib>
 #include <mutex>
 #include <string>
 
@@ -54,7 +55,7 @@ constexpr int kD = 128;                // d_k = d_v
 constexpr int kCh = 3 * kD;            // conv channels of one value head: q | k | v
 constexpr int kThreads = 256;
 constexpr int kSpinLimit = 1 << 20;    // try_wait rounds before an mbarrier wait gives up
-constexpr int kFlagSpin = 1 << 21;     // polls (with back-off) before a ring-flag wait gives up
+constexpr int kFlagSpin = 1 << 21;     // polls (with back-off, about a second) before a ring-flag wait gives up
 constexpr int kTmemCols = 512;
 constexpr int kRing = 4;               // ring slots per (slot, value head)
 
@@ -709,7 +710,7 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
             for (int e = 0; e < 4; ++e) p[e] = Pt[(4 * k4 + e) * kC + r];
             put4(dst_slot + kSlotP, dst_slot + kSlotP + 16 * 1024, r, k4, 64, make_float4(p[0], p[1], p[2], p[3]));
         }
-        pend_slot = slot;                         // released after the next chunk's conv (or at the end)
+        pend_slot = c == a.drop_chunk ? -1 : slot;   // released after the next chunk's conv (or at the end)
         pend_c = c;
         pend_gamma = gam[kC - 1];
         __syncthreads();
@@ -1018,6 +1019,11 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
     a.scratch_vt = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + a.ring_offset +
                                              (size_t)d.n_slots * d.n_v_heads * kRing * kSlotBytes);
     a.d_status = d_status;
+    // Fault injection for tests, on the host: GDN_FAULT_DROP_CHUNK=<c> makes the preparation CTAs never
+    // publish chunk c, so the state CTA's bounded wait runs out and the call reports GDN_ERR_TIMEOUT
+    // through d_status (the outputs are then undefined; nothing faults or hangs).
+    const char *drop = getenv("GDN_FAULT_DROP_CHUNK");
+    a.drop_chunk = drop ? atoi(drop) : -1;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const bool bf = d.act_dtype == GDN_BF16;

@@ -100,3 +100,22 @@ def test_prefill_more_pairs_than_one_launch():
         assert_act_close(gpu["out"][:, :, sl], ref["out"][:, :, sl], shape.act, f"out h{h}")
     assert np.array_equal(gpu["conv_state"], ref["conv_state"])
     assert int(status.item()) == gdn.GDN_OK
+
+
+def test_prefill_lost_chunk_reports_timeout(monkeypatch):
+    # fault injected on the host: chunk 2 is never published to the state CTA, whose bounded wait
+    # (about a second) then gives up and writes GDN_ERR_TIMEOUT to the status word; the device stays
+    # usable and the next clean call matches the oracle
+    shape = _shape(n_tokens=300, seed=46)
+    inp = make_inputs(shape)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    monkeypatch.setenv("GDN_FAULT_DROP_CHUNK", "2")
+    run_prefill(shape, upload(inp), status=status)
+    assert int(status.item()) == gdn.GDN_ERR_TIMEOUT
+    monkeypatch.delenv("GDN_FAULT_DROP_CHUNK")
+    status.zero_()
+    gpu = run_prefill(shape, upload(inp), status=status)
+    assert int(status.item()) == gdn.GDN_OK
+    ref = oracle.verify(shape, inp.as_f64(), capture=False, n_threads=8)
+    assert_f32_close(gpu["state"], ref["state"], "state after recovery")
+    assert_act_close(gpu["out"], ref["out"], shape.act, "out after recovery")
