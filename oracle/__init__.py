@@ -66,6 +66,9 @@ def configure(L: ctypes.CDLL) -> ctypes.CDLL:
     L.gdno_prefill_chunked.argtypes = ([ctypes.POINTER(_Dims), ctypes.c_int] + [_D] * 11 +
                                               [ctypes.c_void_p, ctypes.c_int])
     L.gdno_rollback.argtypes = [ctypes.POINTER(_Dims), ctypes.c_void_p] + [_D] * 4 + [ctypes.c_void_p]
+    L.gdno_verify_tree.argtypes = ([ctypes.POINTER(_Dims), ctypes.c_void_p] + [_D] * 13 +
+                                   [ctypes.c_void_p, ctypes.c_int])
+    L.gdno_rollback_tree.argtypes = [ctypes.POINTER(_Dims), ctypes.c_void_p] + [_D] * 4 + [ctypes.c_void_p]
     return L
 
 
@@ -201,6 +204,50 @@ def rollback(shape, trim, state, conv_state, cap_state, cap_conv, n_tokens: Opti
     status = np.zeros(shape.n_slots, dtype=np.int32)
     lib().gdno_rollback(ctypes.byref(d), tr.ctypes.data_as(ctypes.c_void_p), _p(st), _p(cs),
                         _p(_f64(cap_state)), _p(_f64(cap_conv)), status.ctypes.data_as(ctypes.c_void_p))
+    return st, cs, status
+
+
+def verify_tree(shape, x: Dict[str, np.ndarray], parent, head_mask=None, n_threads: int = 1,
+                q_scale: float = 1.0, rms_eps: float = 1e-6, l2_eps: float = 1e-6) -> Dict[str, np.ndarray]:
+    """Tree (DDTree) verify of shape.n_tokens tokens per slot; parent is [B][T] int
+    (parent[s][t] in [-1, t-1]).  state / conv_state are not changed; returns
+    out, cap_state [B][T][H_v][d_v][d_k] and cap_conv [B][T][W-1][C]."""
+    s = shape
+    T = s.n_tokens
+    d = dims(s, T, rms_eps, l2_eps, q_scale)
+    B, C, Hv, dk, dv, W = s.n_slots, s.conv_channels, s.n_v_heads, s.d_k, s.d_v, s.conv_width
+    par = np.ascontiguousarray(parent, dtype=np.int32)
+    assert par.shape == (B, T)
+    assert x["state"].shape == (B, Hv, dv, dk) and x["conv_state"].shape == (B, W - 1, C)
+    out = np.zeros((B, T, Hv * dv))
+    cap_state = np.zeros((B, T, Hv, dv, dk))
+    cap_conv = np.zeros((B, T, W - 1, C))
+    m, mp = _mask(head_mask, Hv)
+    rc = lib().gdno_verify_tree(ctypes.byref(d), par.ctypes.data_as(ctypes.c_void_p), _p(_f64(x["conv_w"])),
+                                _p(_f64(x["A_log"])), _p(_f64(x["dt_bias"])), _p(_f64(x["norm_w"])),
+                                _p(_f64(x["qkv"][:, :T])), _p(_f64(x["z"][:, :T])), _p(_f64(x["alpha"][:, :T])),
+                                _p(_f64(x["beta_raw"][:, :T])), _p(_f64(x["state"])), _p(_f64(x["conv_state"])),
+                                _p(cap_state), _p(cap_conv), _p(out), mp, int(n_threads))
+    if rc == -2:
+        raise ValueError("parent is not a tree in token order")
+    assert rc == 0
+    return {"out": out, "cap_state": cap_state, "cap_conv": cap_conv}
+
+
+def rollback_tree(shape, accept, state, conv_state, cap_state, cap_conv):
+    """Returns (state, conv_state, slot_status) after moving copies to the accepted nodes."""
+    s = shape
+    T = s.n_tokens
+    d = dims(s, T)
+    B, C = s.n_slots, s.conv_channels
+    assert np.shape(cap_state) == (B, T, s.n_v_heads, s.d_v, s.d_k)
+    assert np.shape(cap_conv) == (B, T, s.conv_width - 1, C)
+    st, cs = _f64(state).copy(), _f64(conv_state).copy()
+    acc = np.ascontiguousarray(accept, dtype=np.int32)
+    assert acc.shape == (B,)
+    status = np.zeros(B, dtype=np.int32)
+    lib().gdno_rollback_tree(ctypes.byref(d), acc.ctypes.data_as(ctypes.c_void_p), _p(st), _p(cs),
+                             _p(_f64(cap_state)), _p(_f64(cap_conv)), status.ctypes.data_as(ctypes.c_void_p))
     return st, cs, status
 
 

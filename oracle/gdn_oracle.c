@@ -157,6 +157,7 @@ typedef struct {
     const unsigned char *head_mask;
     int chunk;                 /* 0 = sequential form */
     int tid, n_threads;
+    const int *parent;         /* tree verify: [B][T] parent of each token, else NULL */
 } job_t;
 
 /* q^, k^, v of token t for (slot s, value head h) from the post-SiLU stream.
@@ -305,6 +306,37 @@ static void run_head_chunked(const job_t *J, int s, int h)
     free(O); free(Snew);
 }
 
+/* Tree verify for (slot s, value head h): token t starts from the state after
+ * its parent (the state before the batch when the parent is -1), so along any
+ * path from the root the recurrence is the chain recurrence over that path. */
+static void run_head_tree(const job_t *J, int s, int h)
+{
+    const gdno_dims *d = J->d;
+    const int dk = d->d_k, dv = d->d_v, T = d->n_tokens, Hv = d->n_v_heads;
+    double *S = (double *)malloc(sizeof(double) * dk * dv);
+    double qn[dk], kn[dk], o[dv];
+    for (int t = 0; t < T; ++t) {
+        const int p = J->parent[(size_t)s * T + t];
+        if (p < 0) load_state(d, J->state, s, h, S);
+        else {
+            /* cap_state[s][p] has the layout of one slot of `state` */
+            const double *src = J->cap_state + (((size_t)s * T + p) * Hv + h) * dv * dk;
+            for (int j = 0; j < dv; ++j)
+                for (int i = 0; i < dk; ++i) S[(size_t)i * dv + j] = src[(size_t)j * dk + i];
+        }
+        const double *v;
+        token_qkv(J, s, h, t, qn, kn, &v);
+        const size_t st = (size_t)s * T + t;
+        double g, beta;
+        gdno_gates(J->A_log[h], J->dt_bias[h], J->alpha[st * Hv + h], J->beta_raw[st * Hv + h], &g, &beta);
+        gdno_delta_step(dk, dv, S, kn, v, qn, g, beta, d->q_scale, o);
+        store_state(d, J->cap_state + (st * Hv + h) * dv * dk, S);
+        gdno_rmsnorm_gate(dv, o, J->z + st * Hv * dv + (size_t)h * dv, J->norm_w, d->rms_eps,
+                          J->out + st * Hv * dv + (size_t)h * dv);
+    }
+    free(S);
+}
+
 static void *worker(void *arg)
 {
     const job_t *J = (const job_t *)arg;
@@ -312,7 +344,8 @@ static void *worker(void *arg)
     for (int it = J->tid; it < n_items; it += J->n_threads) {
         const int s = it / Hv, h = it % Hv;
         if (J->head_mask && !J->head_mask[h]) continue;
-        if (J->chunk > 0) run_head_chunked(J, s, h);
+        if (J->parent) run_head_tree(J, s, h);
+        else if (J->chunk > 0) run_head_chunked(J, s, h);
         else run_head_sequential(J, s, h);
     }
     return NULL;
@@ -353,7 +386,7 @@ int gdno_verify(const gdno_dims *d, const double *conv_w, const double *A_log,
     double *y_all = (double *)malloc(sizeof(double) * (size_t)d->n_slots * d->n_tokens * C + 1);
     conv_all_slots(d, conv_w, qkv, conv_state, cap_conv, y_all);
     job_t J = {d, conv_w, A_log, dt_bias, norm_w, z, alpha, beta_raw, y_all,
-               state, cap_state, out, head_mask, 0, 0, 1};
+               state, cap_state, out, head_mask, 0, 0, 1, NULL};
     run_items(&J, n_threads);
     free(y_all);
     return 0;
@@ -370,7 +403,7 @@ int gdno_prefill_chunked(const gdno_dims *d, int chunk, const double *conv_w,
     double *y_all = (double *)malloc(sizeof(double) * (size_t)d->n_slots * d->n_tokens * C + 1);
     conv_all_slots(d, conv_w, qkv, conv_state, NULL, y_all);
     job_t J = {d, conv_w, A_log, dt_bias, norm_w, z, alpha, beta_raw, y_all,
-               state, NULL, out, head_mask, chunk, 0, 1};
+               state, NULL, out, head_mask, chunk, 0, 1, NULL};
     run_items(&J, n_threads);
     free(y_all);
     return 0;
@@ -398,6 +431,80 @@ int gdno_rollback(const gdno_dims *d, const int *trim, double *state, double *co
                cap_state + ((size_t)s * T + accepted_idx) * per_state, sizeof(double) * per_state);
         memcpy(conv_state + (size_t)s * (W - 1) * C,
                cap_conv + ((size_t)s * (W - 1 + T) + commit_n) * C, sizeof(double) * (W - 1) * C);
+    }
+    return refused;
+}
+
+/* ---------------------------------------------------------------------- */
+/* tree (DDTree) verify                                                   */
+/* ---------------------------------------------------------------------- */
+
+/* The raw input row of node n for slot s: a token of the batch for n >= 0,
+ * else the old conv state, most recent row first (n = -1 is row W-2). */
+static const double *node_input(const gdno_dims *d, const double *qkv, const double *conv_state, int s, int n)
+{
+    const int W = d->conv_width, T = d->n_tokens;
+    const size_t C = n_channels(d);
+    if (n >= 0) return qkv + ((size_t)s * T + n) * C;
+    return conv_state + ((size_t)s * (W - 1) + (W - 1) + n) * C;
+}
+
+int gdno_verify_tree(const gdno_dims *d, const int *parent, const double *conv_w, const double *A_log,
+                     const double *dt_bias, const double *norm_w,
+                     const double *qkv, const double *z, const double *alpha, const double *beta_raw,
+                     const double *state, const double *conv_state, double *cap_state, double *cap_conv,
+                     double *out, const unsigned char *head_mask, int n_threads)
+{
+    if (!dims_ok(d) || !parent || !cap_state || !cap_conv) return -1;
+    const int W = d->conv_width, T = d->n_tokens;
+    const size_t C = n_channels(d);
+    for (int s = 0; s < d->n_slots; ++s)
+        for (int t = 0; t < T; ++t) {
+            const int p = parent[(size_t)s * T + t];
+            if (p < -1 || p >= t) return -2;            /* not a tree in token order */
+        }
+    double *y_all = (double *)malloc(sizeof(double) * (size_t)d->n_slots * T * C + 1);
+    double *win = (double *)malloc(sizeof(double) * (size_t)W * C + 1);
+    for (int s = 0; s < d->n_slots; ++s)
+        for (int t = 0; t < T; ++t) {
+            /* window of t: its W-1 nearest ancestors (oldest first), then t; past the
+             * root the ancestors continue into the old conv state */
+            int anc = t;
+            for (int j = W - 1; j >= 0; --j) {
+                memcpy(win + (size_t)j * C, node_input(d, qkv, conv_state, s, anc), sizeof(double) * C);
+                anc = anc >= 0 ? parent[(size_t)s * T + anc] : anc - 1;
+            }
+            gdno_conv_silu(W, 1, (int)C, conv_w, win, y_all + ((size_t)s * T + t) * C);
+            memcpy(cap_conv + ((size_t)s * T + t) * (W - 1) * C, win + C, sizeof(double) * (W - 1) * C);
+        }
+    free(win);
+    job_t J = {d, conv_w, A_log, dt_bias, norm_w, z, alpha, beta_raw, y_all,
+               (double *)state, cap_state, out, head_mask, 0, 0, 1, parent};
+    run_items(&J, n_threads);
+    free(y_all);
+    return 0;
+}
+
+int gdno_rollback_tree(const gdno_dims *d, const int *accept, double *state, double *conv_state,
+                       const double *cap_state, const double *cap_conv, int *slot_status)
+{
+    if (!dims_ok(d)) return -1;
+    const int T = d->n_tokens, W = d->conv_width;
+    const size_t C = n_channels(d);
+    const size_t per_state = (size_t)d->n_v_heads * d->d_v * d->d_k;
+    int refused = 0;
+    for (int s = 0; s < d->n_slots; ++s) {
+        slot_status[s] = 0;
+        if (accept[s] == -1) continue;                  /* nothing accepted: keep the state before the batch */
+        if (accept[s] < -1 || accept[s] >= T) {
+            slot_status[s] = 1;
+            ++refused;
+            continue;
+        }
+        memcpy(state + (size_t)s * per_state, cap_state + ((size_t)s * T + accept[s]) * per_state,
+               sizeof(double) * per_state);
+        memcpy(conv_state + (size_t)s * (W - 1) * C, cap_conv + ((size_t)s * T + accept[s]) * (W - 1) * C,
+               sizeof(double) * (W - 1) * C);
     }
     return refused;
 }

@@ -111,6 +111,27 @@ int gdno_prefill_chunked(const gdno_dims *d, int chunk, const double *conv_w,
                          const double *beta_raw, double *state, double *conv_state,
                          double *out, const unsigned char *head_mask, int n_threads);
 
+/* Tree (DDTree) verify.  parent[s][t] in [-1, t-1] is the parent of token t
+ * (-1: the state before the batch).  Token t runs from its parent's state, and
+ * its conv window is the raw input of its W-1 nearest ancestors and itself,
+ * the ancestors continuing into the old conv state rows past the root.
+ * state / conv_state are read only.  cap_state[s][t] = state after t;
+ * cap_conv[s][t] = the conv state after t (W-1 rows: its W-2 nearest ancestors
+ * and t, oldest first).  Returns 0, -1 on bad dims / missing captures, -2 when
+ * parent is not a tree in token order. */
+int gdno_verify_tree(const gdno_dims *d, const int *parent, const double *conv_w, const double *A_log,
+                     const double *dt_bias, const double *norm_w,
+                     const double *qkv, const double *z, const double *alpha, const double *beta_raw,
+                     const double *state, const double *conv_state, double *cap_state, double *cap_conv,
+                     double *out, const unsigned char *head_mask, int n_threads);
+
+/* Rollback after a tree verify: accept[s] = the accepted node (-1 = none, the
+ * slot keeps its state); state and conv state are copied from its captures.
+ * slot_status[s] = 1 for an index out of range (slot untouched).  Returns the
+ * number of refused slots. */
+int gdno_rollback_tree(const gdno_dims *d, const int *accept, double *state, double *conv_state,
+                       const double *cap_state, const double *cap_conv, int *slot_status);
+
 #ifdef __cplusplus
 }
 #endif

@@ -45,6 +45,12 @@ MUTATIONS = [
      "if (J->cap_state)\n            store_state(d, J->cap_state + (st * Hv + h) * dv * dk, S);\n        gdno_delta_step(dk, dv, S, kn, v, qn, g, beta, d->q_scale, o);"),
     ("chunk_decay_ratio_inverted", "intra += qk * exp(logG[r] - logG[m]) * U[(size_t)m * dv + j];",
      "intra += qk * exp(logG[m] - logG[r]) * U[(size_t)m * dv + j];"),
+    ("tree_ignores_parent_state", "if (p < 0) load_state(d, J->state, s, h, S);",
+     "if (p < 0 || p >= 0) load_state(d, J->state, s, h, S);"),
+    ("tree_window_stops_at_root", "anc = anc >= 0 ? parent[(size_t)s * T + anc] : anc - 1;",
+     "anc = anc >= 0 ? parent[(size_t)s * T + anc] : -1;"),
+    ("tree_window_follows_token_order", "anc = anc >= 0 ? parent[(size_t)s * T + anc] : anc - 1;",
+     "anc = anc - 1;"),
 ]
 
 

@@ -396,3 +396,99 @@ def test_chunked_form_long_sequence_realistic_dims():
     chk = oracle.prefill_chunked(s, x, 64)
     assert np.abs(chk["state"] - seq["state"]).max() <= 1e-10 * np.abs(seq["state"]).max()
     assert np.abs(chk["out"] - seq["out"]).max() <= 1e-10 * np.abs(seq["out"]).max()
+
+
+# ---------------------------------------------------------------------------
+# tree (DDTree) verify: token t runs from its parent's state; pinned to the
+# chain verify (itself pinned above) through root-to-node paths
+# ---------------------------------------------------------------------------
+
+from workloads.synth import make_parents, tree_accept  # noqa: E402
+
+
+def _path(par, t):
+    """Nodes on the path root -> t (token indices, in order)."""
+    p = []
+    while t >= 0:
+        p.append(t)
+        t = par[t]
+    return p[::-1]
+
+
+def _tokens(x, s, nodes):
+    """The chain-verify inputs of slot s whose tokens are `nodes`, in that order."""
+    y = dict(x)
+    for k in ("qkv", "z", "alpha", "beta_raw"):
+        y[k] = x[k][s:s + 1, nodes]
+    y["state"] = x["state"][s:s + 1]
+    y["conv_state"] = x["conv_state"][s:s + 1]
+    return y
+
+
+def test_tree_with_chain_parents_is_the_chain_verify():
+    s = small_shape(n_slots=2, n_tokens=6)
+    x = make_inputs(s).as_f64()
+    par = make_parents(s, "chain")
+    tr = oracle.verify_tree(s, x, par)
+    ch = oracle.verify(s, x, capture=True)
+    np.testing.assert_array_equal(tr["cap_state"], ch["cap_state"])
+    np.testing.assert_array_equal(tr["out"], ch["out"])
+    for t in range(s.n_tokens):            # conv state after t = window rows t+1 .. t+3
+        np.testing.assert_array_equal(tr["cap_conv"][:, t], ch["cap_conv"][:, t + 1:t + 4])
+
+
+@pytest.mark.parametrize("kind", ["random", "star", "spine"])
+def test_tree_node_equals_chain_verify_of_its_root_path(kind):
+    # every node's capture, conv state and output equal a chain verify run over the tokens
+    # on its path from the root: parent state, ancestor conv window and the continuation of
+    # the window into the old conv state past the root all enter this check
+    s = small_shape(n_slots=2, n_tokens=9, seed=7)
+    x = make_inputs(s).as_f64()
+    par = make_parents(s, kind, seed=8)
+    tr = oracle.verify_tree(s, x, par)
+    for b in range(s.n_slots):
+        for t in range(s.n_tokens):
+            nodes = _path(par[b], t)
+            one = s.with_(n_slots=1, n_tokens=len(nodes))
+            ref = oracle.verify(one, _tokens(x, b, nodes), capture=False)
+            np.testing.assert_allclose(tr["cap_state"][b, t], ref["state"][0], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(tr["cap_conv"][b, t], ref["conv_state"][0], rtol=0, atol=0)
+            np.testing.assert_allclose(tr["out"][b, t], ref["out"][0, -1], rtol=1e-12, atol=1e-12)
+
+
+def test_tree_leaves_state_and_conv_state_alone():
+    s = small_shape(n_slots=1, n_tokens=5)
+    x = make_inputs(s).as_f64()
+    st0, cs0 = x["state"].copy(), x["conv_state"].copy()
+    oracle.verify_tree(s, x, make_parents(s, "random", seed=3))
+    np.testing.assert_array_equal(x["state"], st0)
+    np.testing.assert_array_equal(x["conv_state"], cs0)
+
+
+def test_tree_rejects_parents_out_of_token_order():
+    s = small_shape(n_slots=1, n_tokens=4)
+    x = make_inputs(s).as_f64()
+    for bad in ([-1, 1, 0, 1], [-1, 0, -2, 1], [0, 0, 1, 2]):
+        with pytest.raises(ValueError):
+            oracle.verify_tree(s, x, np.array([bad], dtype=np.int32))
+
+
+def test_tree_rollback_moves_to_the_accepted_node():
+    s = small_shape(n_slots=4, n_tokens=6, seed=9)
+    x = make_inputs(s).as_f64()
+    par = make_parents(s, "random", seed=10)
+    tr = oracle.verify_tree(s, x, par)
+    accept = np.array([-1, 0, 5, 6], dtype=np.int32)            # none, first, last, out of range
+    st, cs, status = oracle.rollback_tree(s, accept, x["state"], x["conv_state"], tr["cap_state"], tr["cap_conv"])
+    np.testing.assert_array_equal(status, [0, 0, 0, 1])
+    np.testing.assert_array_equal(st[0], x["state"][0])
+    np.testing.assert_array_equal(cs[0], x["conv_state"][0])
+    np.testing.assert_array_equal(st[1], tr["cap_state"][1, 0])
+    np.testing.assert_array_equal(cs[2], tr["cap_conv"][2, 5])
+    np.testing.assert_array_equal(st[3], x["state"][3])          # refused: untouched
+    # the accepted node's state is the chain verify of its root path
+    nodes = _path(par[2], 5)
+    ref = oracle.verify(s.with_(n_slots=1, n_tokens=len(nodes)), _tokens(x, 2, nodes), capture=False)
+    np.testing.assert_allclose(st[2], ref["state"][0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(cs[2], ref["conv_state"][0])
+    assert tree_accept(s, par).shape == (s.n_slots,)

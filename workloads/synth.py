@@ -167,7 +167,7 @@ WORKLOADS: Dict[str, Shape] = {
 
 # stream tags (one independent stream per tensor and layer)
 _TAGS = {"qkv": 1, "z": 2, "alpha": 3, "beta_raw": 4, "A_log": 5, "dt_bias": 6,
-         "conv_w": 7, "norm_w": 8, "state": 9, "conv_state": 10, "trim": 11}
+         "conv_w": 7, "norm_w": 8, "state": 9, "conv_state": 10, "trim": 11, "parent": 13, "accept": 14}
 
 
 def _tag(name: str, layer: int) -> int:
@@ -243,3 +243,46 @@ def make_inputs(shape: Shape, layer: int = 0, seed: Optional[int] = None) -> Inp
         conv_state=normal_f32(seed, _tag("conv_state", layer), B * (W - 1) * C).reshape(B, W - 1, C),
         trim=randint(seed, _tag("trim", layer), B, T),
     )
+
+
+def make_parents(shape: Shape, kind: str = "random", seed: Optional[int] = None, layer: int = 0) -> np.ndarray:
+    """Draft-tree parents for a tree verify, [B][T] int32, parent[s][t] in [-1, t-1]
+    (-1: the committed state before the batch).
+
+    kind: "chain" (t-1: the linear verify), "star" (every token hangs off the
+    root), "random" (each parent uniform over -1 .. t-1), "spine" (a DDTree-like
+    shape: a main chain through every other token, each remaining token a
+    one-token branch off the chain node before it).
+    """
+    s = shape
+    seed = s.seed if seed is None else seed
+    B, T = s.n_slots, s.n_tokens
+    t = np.arange(T)
+    if kind == "chain":
+        par = np.tile(t - 1, (B, 1))
+    elif kind == "star":
+        par = np.full((B, T), -1)
+    elif kind == "random":
+        u = uniform01(seed, _tag("parent", layer), B * T).reshape(B, T) - 2.0 ** -53
+        par = np.floor(u * (t + 1)).astype(np.int64) - 1          # uniform over -1 .. t-1
+        par = np.minimum(par, t - 1)
+    elif kind == "spine":
+        par = np.empty((B, T), dtype=np.int64)
+        for b in range(B):
+            last = -1
+            for i in range(T):
+                if i % 2 == 0:                 # chain node
+                    par[b, i] = last
+                    last = i
+                else:                          # branch off the previous chain node
+                    par[b, i] = i - 1
+    else:
+        raise ValueError(kind)
+    return par.astype(np.int32)
+
+
+def tree_accept(shape: Shape, parents: np.ndarray, seed: Optional[int] = None, layer: int = 0) -> np.ndarray:
+    """An accepted node per slot, uniform over -1 .. T-1 (-1: nothing accepted)."""
+    s = shape
+    seed = s.seed if seed is None else seed
+    return (randint(seed, _tag("accept", layer), s.n_slots, s.n_tokens + 1) - 1).astype(np.int32)
