@@ -26,14 +26,16 @@ GDN_ERR_NO_CAPTURE = 6
 GDN_ERR_LAUNCH = 7
 GDN_ERR_TIMEOUT = 8
 GDN_ERR_WORKSPACE = 9
+GDN_ERR_TREE = 10
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_ALIGN", 4: "GDN_ERR_DTYPE",
                 5: "GDN_ERR_TRIM_RANGE", 6: "GDN_ERR_NO_CAPTURE", 7: "GDN_ERR_LAUNCH", 8: "GDN_ERR_TIMEOUT",
-                9: "GDN_ERR_WORKSPACE"}
+                9: "GDN_ERR_WORKSPACE", 10: "GDN_ERR_TREE"}
 
 GDN_F32 = 0
 GDN_BF16 = 1
 
-EXPORTED_SYMBOLS = ("gdn_verify_forward", "gdn_rollback", "gdn_prefill_workspace_bytes",
+EXPORTED_SYMBOLS = ("gdn_verify_forward", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_tree",
+                    "gdn_prefill_workspace_bytes",
                     "gdn_prefill_chunked", "gdn_prefill_chunked_static", "gdn_last_error", "gdn_version")
 
 # size of the library's built-in prefill scratch (GDN_PREFILL_STATIC_SCRATCH_BYTES)
@@ -81,6 +83,10 @@ def lib() -> ctypes.CDLL:
         L.gdn_verify_forward.restype = ip
         L.gdn_rollback.argtypes = [ctypes.POINTER(Dims)] + [vp] * 7
         L.gdn_rollback.restype = ip
+        L.gdn_verify_tree.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 12
+        L.gdn_verify_tree.restype = ip
+        L.gdn_rollback_tree.argtypes = [ctypes.POINTER(Dims)] + [vp] * 7
+        L.gdn_rollback_tree.restype = ip
         L.gdn_prefill_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
         L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
         L.gdn_prefill_chunked.argtypes = ([ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 8 +
@@ -140,6 +146,19 @@ def gdn_rollback(dims: Dims, d_trim, state, conv_state, cap_state, cap_conv, d_s
                  stream=None) -> None:
     _check(lib().gdn_rollback(ctypes.byref(dims), _ptr(d_trim), _ptr(state), _ptr(conv_state),
                               _ptr(cap_state), _ptr(cap_conv), _ptr(d_status), _stream(stream)))
+
+
+def gdn_verify_tree(dims: Dims, params: LayerParams, qkv, z, alpha, beta_raw, d_parent, state, conv_state,
+                    cap_state, cap_conv, out, d_status=None, stream=None) -> None:
+    _check(lib().gdn_verify_tree(ctypes.byref(dims), ctypes.byref(params), _ptr(qkv), _ptr(z), _ptr(alpha),
+                                 _ptr(beta_raw), _ptr(d_parent), _ptr(state), _ptr(conv_state), _ptr(cap_state),
+                                 _ptr(cap_conv), _ptr(out), _ptr(d_status), _stream(stream)))
+
+
+def gdn_rollback_tree(dims: Dims, d_accept, state, conv_state, cap_state, cap_conv, d_status=None,
+                      stream=None) -> None:
+    _check(lib().gdn_rollback_tree(ctypes.byref(dims), _ptr(d_accept), _ptr(state), _ptr(conv_state),
+                                   _ptr(cap_state), _ptr(cap_conv), _ptr(d_status), _stream(stream)))
 
 
 def gdn_prefill_workspace_bytes(dims: Dims) -> int:

@@ -10,7 +10,7 @@
 #include <string>
 
 namespace gdn {
-size_t verify_smem_bytes(int T, int dk, int dv, int P, int act_bytes);
+size_t verify_smem_bytes(int T, int dk, int dv, int P, int act_bytes, bool tree);
 }  // namespace gdn
 
 namespace {
@@ -131,8 +131,8 @@ const char *gdn_last_error(void) { return g_err.c_str(); }
 
 const char *gdn_version(void) { return "gdn-verify 0.1.0 (sm_103a)"; }
 
-int gdn_verify_forward(const gdn_dims *dims, const gdn_layer_params *params, const void *qkv,
-                       const void *z, const void *alpha, const void *beta_raw, float *state,
+static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, const void *qkv, const void *z,
+                       const void *alpha, const void *beta_raw, const int32_t *d_parent, float *state,
                        float *conv_state, float *cap_state, float *cap_conv, void *out, int *d_status,
                        void *stream) {
     g_err.clear();
@@ -155,7 +155,7 @@ int gdn_verify_forward(const gdn_dims *dims, const gdn_layer_params *params, con
     const int P = gdn::verify_parts_per_head(d.n_slots, d.n_v_heads, r, d.d_v, info.sms);
     if (P == 0) return fail(GDN_ERR_SHAPE, "H_v/H_k = %d is too large for one thread-block cluster", r);
     const int act_bytes = d.act_dtype == GDN_BF16 ? 2 : 4;
-    const size_t smem = gdn::verify_smem_bytes(d.n_tokens, d.d_k, d.d_v, P, act_bytes);
+    const size_t smem = gdn::verify_smem_bytes(d.n_tokens, d.d_k, d.d_v, P, act_bytes, d_parent != nullptr);
     if (info.smem_optin > 0 && smem > size_t(info.smem_optin))
         return fail(GDN_ERR_SHAPE, "verify needs %zu bytes of shared memory per CTA (max %d)", smem,
                     info.smem_optin);
@@ -168,13 +168,34 @@ int gdn_verify_forward(const gdn_dims *dims, const gdn_layer_params *params, con
     a.qkv = qkv; a.z = z; a.alpha = alpha; a.beta_raw = beta_raw;
     a.state = state; a.conv_state = conv_state; a.cap_state = cap_state; a.cap_conv = cap_conv; a.out = out;
     a.d_status = d_status;
+    a.parent = d_parent;
     cudaError_t e = gdn::launch_verify(a, d.act_dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "verify launch failed: %s", cudaGetErrorString(e));
     return GDN_OK;
 }
 
-int gdn_rollback(const gdn_dims *dims, const int32_t *d_trim, float *state, float *conv_state,
-                 const float *cap_state, const float *cap_conv, int *d_status, void *stream) {
+int gdn_verify_forward(const gdn_dims *dims, const gdn_layer_params *params, const void *qkv,
+                       const void *z, const void *alpha, const void *beta_raw, float *state,
+                       float *conv_state, float *cap_state, float *cap_conv, void *out, int *d_status,
+                       void *stream) {
+    return verify_impl(dims, params, qkv, z, alpha, beta_raw, nullptr, state, conv_state, cap_state, cap_conv, out,
+                       d_status, stream);
+}
+
+int gdn_verify_tree(const gdn_dims *dims, const gdn_layer_params *params, const void *qkv, const void *z,
+                    const void *alpha, const void *beta_raw, const int32_t *d_parent, const float *state,
+                    const float *conv_state, float *cap_state, float *cap_conv, void *out, int *d_status,
+                    void *stream) {
+    g_err.clear();
+    if (!d_parent) return fail(GDN_ERR_ARG, "parent ids are NULL");
+    if (!cap_state || !cap_conv) return fail(GDN_ERR_NO_CAPTURE, "a tree verify needs cap_state and cap_conv");
+    // state and conv_state are only read (the kernel takes them through the shared argument block)
+    return verify_impl(dims, params, qkv, z, alpha, beta_raw, d_parent, const_cast<float *>(state),
+                       const_cast<float *>(conv_state), cap_state, cap_conv, out, d_status, stream);
+}
+
+static int rollback_impl(const gdn_dims *dims, const int32_t *d_trim, float *state, float *conv_state,
+                         const float *cap_state, const float *cap_conv, int *d_status, void *stream, int tree) {
     g_err.clear();
     int rc = check_common(dims);
     if (rc) return rc;
@@ -193,9 +214,20 @@ int gdn_rollback(const gdn_dims *dims, const int32_t *d_trim, float *state, floa
     a.conv_elems = (long long)a.W1 * a.C;
     a.trim = d_trim; a.state = state; a.conv_state = conv_state; a.cap_state = cap_state; a.cap_conv = cap_conv;
     a.d_status = d_status;
+    a.tree = tree;
     cudaError_t e = gdn::launch_rollback(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "rollback launch failed: %s", cudaGetErrorString(e));
     return GDN_OK;
+}
+
+int gdn_rollback(const gdn_dims *dims, const int32_t *d_trim, float *state, float *conv_state,
+                 const float *cap_state, const float *cap_conv, int *d_status, void *stream) {
+    return rollback_impl(dims, d_trim, state, conv_state, cap_state, cap_conv, d_status, stream, 0);
+}
+
+int gdn_rollback_tree(const gdn_dims *dims, const int32_t *d_accept, float *state, float *conv_state,
+                      const float *cap_state, const float *cap_conv, int *d_status, void *stream) {
+    return rollback_impl(dims, d_accept, state, conv_state, cap_state, cap_conv, d_status, stream, 1);
 }
 
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims) {

@@ -23,6 +23,7 @@ struct VerifyArgs {
     float *state, *conv_state, *cap_state, *cap_conv;
     void *out;
     int *d_status;                    // device status word (may be NULL)
+    const int32_t *parent;            // tree verify: [B][T] parent of each token (NULL: the chain)
 };
 
 struct RollbackArgs {
@@ -30,10 +31,11 @@ struct RollbackArgs {
     long long state_elems;        // floats per slot state (H_v * d_v * d_k)
     long long conv_elems;         // floats per slot conv state (W1 * C)
     long long C;
-    const int32_t *trim;
+    const int32_t *trim;              // per slot: trim (chain) or the accepted node (tree)
     float *state, *conv_state;
     const float *cap_state, *cap_conv;
     int *d_status;
+    int tree;                         // 1: cap_conv holds per-node conv states [B][T][W-1][C]
 };
 
 // Everything one chunkwise prefill launch needs (d_k = d_v = 128, W = 4).

@@ -5,10 +5,13 @@
 // state comes from capture element accepted_idx and the conv state from
 // window rows [commit_n .. commit_n + kernel - 2], commit_n = accepted_idx + 1.
 //
+// After a tree verify the slot moves to its accepted node instead: state and
+// conv state come from that node's captures (-1: nothing accepted, no-op).
+//
 // A pure copy, so HBM-bound: grid (blocks_per_slot, B); every block reads the
-// slot's trim from device memory (the call can live in a CUDA graph), and
-// copies its share of the 16-byte vectors with several loads in flight per
-// thread.  A slot with an invalid trim is left untouched and reported through
+// slot's trim (or node) from device memory (the call can live in a CUDA graph),
+// and copies its share of the 16-byte vectors with several loads in flight per
+// thread.  A slot with an invalid index is left untouched and reported through
 // the status word.
 #include "internal.cuh"
 
@@ -32,19 +35,27 @@ __global__ void __launch_bounds__(kThreads) rollback_kernel(const RollbackArgs a
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int s = blockIdx.y;
-    const int trim = __ldg(a.trim + s);
-    if (trim == 0) return;                                   // nothing to discard
-    if (trim < 0 || trim >= a.T) {                           // more than was verified
+    const int idx = __ldg(a.trim + s);
+    int accepted_idx;
+    if (a.tree) {
+        if (idx == -1) return;                               // nothing accepted: the state stays
+        accepted_idx = idx;
+    } else {
+        if (idx == 0) return;                                // nothing to discard
+        accepted_idx = a.T - 1 - idx;
+    }
+    if (accepted_idx < 0 || accepted_idx >= a.T) {          // more than was verified
         if (blockIdx.x == 0 && threadIdx.x == 0 && a.d_status)
             atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TRIM_RANGE));
         return;
     }
-    const int accepted_idx = a.T - 1 - trim;
     const long long n4_state = a.state_elems / 4, n4_conv = a.conv_elems / 4;
     const float4 *src_s = reinterpret_cast<const float4 *>(a.cap_state + (size_t(s) * a.T + accepted_idx) * a.state_elems);
     float4 *dst_s = reinterpret_cast<float4 *>(a.state + size_t(s) * a.state_elems);
+    // chain: window rows accepted_idx + 1 .. + W-1; tree: the node's own conv state
     const float4 *src_c = reinterpret_cast<const float4 *>(
-        a.cap_conv + (size_t(s) * (a.W1 + a.T) + accepted_idx + 1) * a.C);
+        a.tree ? a.cap_conv + (size_t(s) * a.T + accepted_idx) * a.W1 * a.C
+               : a.cap_conv + (size_t(s) * (a.W1 + a.T) + accepted_idx + 1) * a.C);
     float4 *dst_c = reinterpret_cast<float4 *>(a.conv_state + size_t(s) * a.conv_elems);
 
     const long long total = n4_state + n4_conv;

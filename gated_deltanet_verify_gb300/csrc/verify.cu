@@ -165,8 +165,9 @@ __device__ __forceinline__ void grid_launch_dependents() {
 // Shared-memory carve-up; identical on host and device.
 struct Smem {
     int NCH;
-    size_t xs, zs, cw, cs, nw, ys, os, gs, bs, kqs, rinv, allp, redbar, total;
-    __host__ __device__ Smem(int T, int dk, int rows, int warps, int P, int act_bytes) : NCH(2 * dk + rows) {
+    size_t xs, zs, cw, cs, nw, ys, os, gs, bs, kqs, rinv, allp, redbar, arow, total;
+    __host__ __device__ Smem(int T, int dk, int rows, int warps, int P, int act_bytes, bool tree)
+        : NCH(2 * dk + rows) {
         size_t off = 0;
         auto take = [&](size_t bytes) {
             size_t o = off;
@@ -186,11 +187,12 @@ struct Smem {
         rinv = take(size_t(T) * 4);
         allp = take(size_t(T) * P * warps * 4);     // per-warp sums of o^2 of the whole head
         redbar = take(8);                           // all RMSNorm partials of the head arrived
+        arow = take(tree ? size_t(T) * 5 * 4 : 0);  // tree: parent and the window row of each conv tap
         total = off;
     }
 };
 
-template <int DK, typename Act>
+template <int DK, typename Act, bool TREE>
 __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs a) {
     static_assert(DK == 32 || DK == 64 || DK == 128, "d_k must be 32, 64 or 128");
     constexpr int LR = DK >= 64 ? 16 : 8;          // lanes per row group
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     const int j0 = p * ROWS;                                   // first value row of this CTA
     const bool qk_writer = (h % a.r == 0) && (p == 0);        // writes the shared q/k conv channels
 
-    const Smem L(T, DK, ROWS, WARPS, P, sizeof(Act));
+    const Smem L(T, DK, ROWS, WARPS, P, sizeof(Act), TREE);
     Act *xs = reinterpret_cast<Act *>(smem_raw + L.xs);
     Act *zs = reinterpret_cast<Act *>(smem_raw + L.zs);
     float *cw = reinterpret_cast<float *>(smem_raw + L.cw);
@@ -227,6 +229,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     float *rinv = reinterpret_cast<float *>(smem_raw + L.rinv);
     float *allp = reinterpret_cast<float *>(smem_raw + L.allp);
     const uint32_t redbar = smem_u32(smem_raw + L.redbar);
+    int *tpar = reinterpret_cast<int *>(smem_raw + L.arow);     // tree: [T] parents, then [T][4] window rows
+    int *trow = tpar + T;
     const int NCH = L.NCH;
 
     // local channel c -> global conv channel
@@ -316,12 +320,37 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         const float sp = x > 20.0f ? x : log1pf(expf(x));               // softplus
         gs[t] = expf(-expf(__ldg(a.A_log + h)) * sp);
         bs[t] = 1.0f / (1.0f + expf(-br));
+        if constexpr (TREE) {
+            int pt = __ldg(a.parent + size_t(s) * T + t);
+            if (pt < -1 || pt >= t) {                   // not a tree in token order: reported, root used
+                if (a.d_status) atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TREE));
+                pt = -1;
+            }
+            tpar[t] = pt;
+        }
     }
     cp_async_wait_all();
     __syncthreads();
     // cluster phase 1: this CTA has read the old conv state (the copies above have
     // landed) and initialised its mbarrier (published by fence.mbarrier_init)
     cluster_arrive_relaxed();
+    if constexpr (TREE) {
+        // window row of each conv tap: tap 3 is the token, taps 2, 1, 0 its nearest ancestors; past the
+        // root the ancestors continue into the old conv state (node -1 = row 2, -2 = row 1, -3 = row 0)
+        for (int t = tid; t < T; t += nthr) {
+            int n = t;
+            for (int j = 3; j >= 0; --j) {
+                trow[t * 4 + j] = 3 + n;
+                n = n >= 0 ? tpar[n] : n - 1;
+            }
+        }
+        __syncthreads();
+    }
+    // window row of conv tap j for token t
+    auto tap_row = [&](int t, int j) -> int {
+        if constexpr (TREE) return trow[t * 4 + j];
+        else return t + j;
+    };
 
     // ------------------------------------ conv + SiLU, q/k L2 norm, k.q per token
     {
@@ -342,7 +371,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
                 if (valid) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const float4 w4 = load4(cw + j * NCH + ch), x4 = win4(t + j, ch);
+                        const float4 w4 = load4(cw + j * NCH + ch), x4 = win4(tap_row(t, j), ch);
                         if (j == 0) acc = make_float4(w4.x * x4.x, w4.y * x4.y, w4.z * x4.z, w4.w * x4.w);
                         else acc = make_float4(fmaf(w4.x, x4.x, acc.x), fmaf(w4.y, x4.y, acc.y),
                                                fmaf(w4.z, x4.z, acc.z), fmaf(w4.w, x4.w, acc.w));
@@ -385,7 +414,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         float4 acc;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float4 w4 = load4(cw + j * NCH + c), x4 = win4(t + j, c);
+            const float4 w4 = load4(cw + j * NCH + c), x4 = win4(tap_row(t, j), c);
             if (j == 0) acc = make_float4(w4.x * x4.x, w4.y * x4.y, w4.z * x4.z, w4.w * x4.w);
             else acc = make_float4(fmaf(w4.x, x4.x, acc.x), fmaf(w4.y, x4.y, acc.y), fmaf(w4.z, x4.z, acc.z),
                                    fmaf(w4.w, x4.w, acc.w));
@@ -402,6 +431,22 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         const float q_scale = a.q_scale;
 
         for (int t = 0; t < T; ++t) {
+            if constexpr (TREE) {
+                // the token runs from its parent's state: already in registers when the parent is t-1,
+                // else this thread's own rows of the parent's capture (or of the state before the batch)
+                const int pt = tpar[t];
+                if (pt != t - 1) {
+                    const float *src = pt < 0 ? a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b
+                                              : cap_row + (size_t(s) * T + pt) * cap_token_stride;
+#pragma unroll
+                    for (int rho = 0; rho < RPG; ++rho)
+#pragma unroll
+                        for (int m = 0; m < NCL; ++m) {
+                            const float4 v = ld_na4(src + size_t(rho) * DK + 4 * LR * m);
+                            S[rho][m][0] = v.x; S[rho][m][1] = v.y; S[rho][m][2] = v.z; S[rho][m][3] = v.w;
+                        }
+                }
+            }
             const float *yt = ys + size_t(t) * NCH;
             const float g = gs[t], beta = bs[t], kq = kqs[t];
             float kk[NCL][4], qq[NCL][4];
@@ -467,8 +512,17 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         }
         // the next kernel in the stream may start launching (it waits for this grid's completion itself)
         grid_launch_dependents();
-        // conv window capture: concat(old conv state, new tokens) of the channels this CTA owns
-        if (a.cap_conv) {
+        if constexpr (TREE) {
+            // conv state after each node: the window rows of its taps 1, 2, 3, channels this CTA owns
+            const int c_first = qk_writer ? 0 : 2 * DK;
+            const int n4 = (NCH - c_first) / 4;
+            float *base = a.cap_conv + size_t(s) * T * 3 * C;
+            for (int i = tid; i < T * 3 * n4; i += nthr) {
+                const int t = i / (3 * n4), rr = (i / n4) % 3, c = c_first + 4 * (i % n4);
+                store4(base + (size_t(t) * 3 + rr) * C + gchan(c), win4(trow[t * 4 + 1 + rr], c));
+            }
+        } else if (a.cap_conv) {
+            // conv window capture: concat(old conv state, new tokens) of the channels this CTA owns
             const int c_first = qk_writer ? 0 : 2 * DK;
             const int n4 = (NCH - c_first) / 4;
             float *base = a.cap_conv + size_t(s) * (3 + T) * C;
@@ -494,7 +548,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
                 st_async_f32(map_cluster(allp_local + off, rank), acc, map_cluster(redbar, rank));
             }
         }
-        {
+        if constexpr (!TREE) {             // a tree verify leaves the state to the rollback
             float *dst = a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b;
 #pragma unroll
             for (int rho = 0; rho < RPG; ++rho)
@@ -529,7 +583,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
             store4(out + (size_t(s) * a.Ts + t) * size_t(Hv) * DV + size_t(h) * DV + j0 + c, y);
         }
     }
-    {
+    if constexpr (!TREE) {
         // conv state <- window rows T .. T+2 (after cluster phase 1: every reader is done)
         const int c_first = qk_writer ? 0 : 2 * DK;
         const int n4 = (NCH - c_first) / 4;
@@ -541,12 +595,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     }
 }
 
-template <int DK, typename Act>
+template <int DK, typename Act, bool TREE>
 cudaError_t launch_t(const VerifyArgs &a, cudaStream_t stream) {
     const int rows = a.dv / a.P;
     const int warps = rows / kRowsPerWarp;
-    const Smem L(a.T, DK, rows, warps, a.P, sizeof(Act));
-    auto kern = verify_kernel<DK, Act>;
+    const Smem L(a.T, DK, rows, warps, a.P, sizeof(Act), TREE);
+    auto kern = verify_kernel<DK, Act, TREE>;
     // Function attributes are set once per device (and raised when a launch needs more).
     static int smem_set[kMaxDevices] = {};
     static bool nonportable_set[kMaxDevices] = {};
@@ -584,19 +638,24 @@ cudaError_t launch_t(const VerifyArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
-size_t verify_smem_bytes(int T, int dk, int dv, int P, int act_bytes) {
+size_t verify_smem_bytes(int T, int dk, int dv, int P, int act_bytes, bool tree) {
     const int rows = dv / P;
-    return Smem(T, dk, rows, rows / kRowsPerWarp, P, act_bytes).total;
+    return Smem(T, dk, rows, rows / kRowsPerWarp, P, act_bytes, tree).total;
+}
+
+template <bool TREE>
+static cudaError_t launch_mode(const VerifyArgs &a, bool bf, cudaStream_t stream) {
+    switch (a.dk) {
+        case 128: return bf ? launch_t<128, __nv_bfloat16, TREE>(a, stream) : launch_t<128, float, TREE>(a, stream);
+        case 64: return bf ? launch_t<64, __nv_bfloat16, TREE>(a, stream) : launch_t<64, float, TREE>(a, stream);
+        case 32: return bf ? launch_t<32, __nv_bfloat16, TREE>(a, stream) : launch_t<32, float, TREE>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_verify(const VerifyArgs &a, gdn_dtype act, cudaStream_t stream) {
     const bool bf = act == GDN_BF16;
-    switch (a.dk) {
-        case 128: return bf ? launch_t<128, __nv_bfloat16>(a, stream) : launch_t<128, float>(a, stream);
-        case 64: return bf ? launch_t<64, __nv_bfloat16>(a, stream) : launch_t<64, float>(a, stream);
-        case 32: return bf ? launch_t<32, __nv_bfloat16>(a, stream) : launch_t<32, float>(a, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    return a.parent ? launch_mode<true>(a, bf, stream) : launch_mode<false>(a, bf, stream);
 }
 
 }  // namespace gdn

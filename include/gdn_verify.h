@@ -72,7 +72,8 @@ typedef enum {
     GDN_ERR_NO_CAPTURE = 6,  /* rollback asked without capture buffers */
     GDN_ERR_LAUNCH = 7,      /* the CUDA launch itself failed (message in gdn_last_error) */
     GDN_ERR_TIMEOUT = 8,     /* (device) a bounded wait gave up */
-    GDN_ERR_WORKSPACE = 9    /* workspace missing or smaller than the query returned */
+    GDN_ERR_WORKSPACE = 9,   /* workspace missing or smaller than the query returned */
+    GDN_ERR_TREE = 10        /* (device) a parent id is outside [-1, t-1]; that token ran from the root */
 } gdn_status;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
@@ -129,6 +130,39 @@ int gdn_verify_forward(const gdn_dims *dims, const gdn_layer_params *params,
  */
 int gdn_rollback(const gdn_dims *dims, const int32_t *d_trim, float *state, float *conv_state,
                  const float *cap_state, const float *cap_conv, int *d_status, void *stream);
+
+/*
+ * Tree (DDTree) verify: the T = dims->n_tokens tokens of each slot form a
+ * draft tree in token order (internal.h, Target forward graph:
+ * QwenGraphInputs::parent_ids, "tree mode when non-null"; the capture is sized
+ * for the tree: create_target_cache, max_verify_tokens).  d_parent is a DEVICE
+ * int32[B][T]; parent t' of token t is in [-1, t-1], -1 meaning the state
+ * before the batch.  Token t runs from its parent's state, and its conv window
+ * is the raw input of t and of its three nearest ancestors, continuing into
+ * the old conv-state rows past the root; along any root-to-node path this is
+ * the chain verify of that path's tokens.  state and conv_state are only read
+ * (a tree has no single "after all tokens" state): gdn_rollback_tree moves a
+ * slot to its accepted node.  cap_state [B][T][H_v][d_v][d_k] receives the
+ * state after every node; cap_conv [B][T][W-1][C] the conv state after every
+ * node (its two nearest ancestors' raw inputs and its own, oldest first); both
+ * are required (GDN_ERR_NO_CAPTURE).  out as gdn_verify_forward.  A parent id
+ * out of range writes GDN_ERR_TREE to *d_status and that token runs from the
+ * root.  Same shapes as gdn_verify_forward.
+ */
+int gdn_verify_tree(const gdn_dims *dims, const gdn_layer_params *params,
+                    const void *qkv, const void *z, const void *alpha, const void *beta_raw,
+                    const int32_t *d_parent, const float *state, const float *conv_state,
+                    float *cap_state, float *cap_conv, void *out, int *d_status, void *stream);
+
+/*
+ * Rollback after a tree verify: d_accept is a DEVICE int32[B], the accepted
+ * node of each slot (-1: nothing accepted, no-op).  state[s] = cap_state[s][a]
+ * and conv_state[s] = cap_conv[s][a] (the gdn_verify_tree layouts); an index
+ * outside [-1, T-1] leaves the slot untouched and writes GDN_ERR_TRIM_RANGE to
+ * *d_status.  Same launch and error behaviour as gdn_rollback.
+ */
+int gdn_rollback_tree(const gdn_dims *dims, const int32_t *d_accept, float *state, float *conv_state,
+                      const float *cap_state, const float *cap_conv, int *d_status, void *stream);
 
 /* Bytes of device workspace gdn_prefill_chunked needs for these dims (0 on bad dims). */
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims);
