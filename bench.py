@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
-from workloads.synth import WORKLOADS, make_inputs, randint  # noqa: E402
+from workloads.synth import make_parents, WORKLOADS, make_inputs, randint  # noqa: E402
 
 METRIC = "GDN verify tokens/sec at 1 GB300; achieved HBM GB/s vs roofline"
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -60,6 +60,21 @@ def verify_bytes(s, capture=True) -> int:
     n += 2 * B * T * Hv * a                               # alpha, beta_raw
     n += 2 * B * (W - 1) * C * 4                          # conv state read + write
     n += W * C * 4 + 2 * Hv * 4 + dv * 4                  # parameters
+    return n
+
+
+def tree_verify_bytes(s) -> int:
+    """Compulsory bytes of a tree verify: the state read once, a captured state and a
+    per-node conv state (3 rows) for every node, activations, the old conv state,
+    parent ids and parameters.  Parent states re-read from the capture (L2) are not
+    counted, and a tree verify writes neither the state nor the conv state."""
+    a = 2 if s.act == "bf16" else 4
+    B, T, C, Hv, dk, dv, W = s.n_slots, s.n_tokens, s.conv_channels, s.n_v_heads, s.d_k, s.d_v, s.conv_width
+    st = B * Hv * dv * dk * 4
+    n = st + T * st + B * T * (W - 1) * C * 4
+    n += B * T * C * a + B * T * Hv * dv * a * 2 + 2 * B * T * Hv * a
+    n += B * (W - 1) * C * 4 + B * T * 4
+    n += W * C * 4 + 2 * Hv * 4 + dv * 4
     return n
 
 
@@ -238,7 +253,8 @@ class VerifyWorkload:
         self.gdn, self.torch = gdn, torch
         self.shape = s = shape
         self.layers = s.n_layers
-        per_set = verify_bytes(s) * self.layers
+        self.tree = s.name.startswith("tree")          # draft-tree verify + rollback to the accepted node
+        per_set = (tree_verify_bytes(s) if self.tree else verify_bytes(s)) * self.layers
         self.n_sets = 1 if per_set > 3 * l2_bytes else int(min(64, -(-3 * l2_bytes // per_set) + 1))
         self.dims = gdn.make_dims(s.n_slots, s.n_qk_heads, s.n_v_heads, s.d_k, s.d_v, s.n_tokens,
                                   gdn.GDN_BF16 if s.act == "bf16" else gdn.GDN_F32)
@@ -250,13 +266,20 @@ class VerifyWorkload:
             self.host_inputs.append(inp)
         trims = randint(s.seed, 12, self.n_sets * self.layers * s.n_slots, s.n_tokens).reshape(
             self.n_sets, self.layers, s.n_slots)
+        if self.tree:                                # accepted node per slot, -1 .. T-1
+            trims = trims.astype(np.int64) - 1
         self.trims = trims
+        self.parents = make_parents(s, "spine")
         for k in range(self.n_sets):
             layers = []
             for li in range(self.layers):
                 x = to_device(self.host_inputs[li if self.layers > 1 else 0], device)
                 x["trim"] = torch.from_numpy(trims[k, li].astype(np.int32)).to(device)
                 x.update(empty_outputs(s, device))
+                if self.tree:
+                    x["parent"] = torch.from_numpy(self.parents).to(device)
+                    x["cap_conv"] = torch.empty((s.n_slots, s.n_tokens, s.conv_width - 1, s.conv_channels),
+                                                dtype=torch.float32, device=device)
                 x["status"] = torch.zeros(1, dtype=torch.int32, device=device)
                 x["params"] = gdn.layer_params(x["conv_w"], x["A_log"], x["dt_bias"], x["norm_w"])
                 layers.append(x)
@@ -266,13 +289,18 @@ class VerifyWorkload:
 
     def verify(self, k, li, stream):
         x = self.sets[k][li]
+        if self.tree:
+            self.gdn.gdn_verify_tree(self.dims, x["params"], x["qkv"], x["z"], x["alpha"], x["beta_raw"],
+                                     x["parent"], x["state"], x["conv_state"], x["cap_state"], x["cap_conv"],
+                                     x["out"], x["status"], stream)
+            return
         self.gdn.gdn_verify_forward(self.dims, x["params"], x["qkv"], x["z"], x["alpha"], x["beta_raw"], x["state"],
                                     x["conv_state"], x["cap_state"], x["cap_conv"], x["out"], x["status"], stream)
 
     def rollback(self, k, li, stream):
         x = self.sets[k][li]
-        self.gdn.gdn_rollback(self.dims, x["trim"], x["state"], x["conv_state"], x["cap_state"], x["cap_conv"],
-                              x["status"], stream)
+        fn = self.gdn.gdn_rollback_tree if self.tree else self.gdn.gdn_rollback
+        fn(self.dims, x["trim"], x["state"], x["conv_state"], x["cap_state"], x["cap_conv"], x["status"], stream)
 
     def step(self, k, stream):
         for li in range(self.layers):
@@ -280,8 +308,9 @@ class VerifyWorkload:
             self.rollback(k, li, stream)
 
     def step_bytes(self, k):
-        return sum(verify_bytes(self.shape) + rollback_bytes(self.shape, self.trims[k, li])
-                   for li in range(self.layers))
+        vb = tree_verify_bytes(self.shape) if self.tree else verify_bytes(self.shape)
+        moved = (self.trims[k] >= 0) if self.tree else self.trims[k]     # slots whose rollback copies
+        return sum(vb + rollback_bytes(self.shape, moved[li]) for li in range(self.layers))
 
     def e2e(self, steps, device):
         """Public-API loop with host buffers: per layer H2D of the activations and
@@ -296,6 +325,8 @@ class VerifyWorkload:
                           "alpha": act_host(inp.alpha, s).pin_memory(),
                           "beta_raw": act_host(inp.beta_raw, s).pin_memory(),
                           "trim": torch.from_numpy(self.trims[0, li].astype(np.int32)).pin_memory()})
+            if self.tree:
+                hosts[-1]["parent"] = torch.from_numpy(self.parents).pin_memory()
             outs.append(torch.empty(self.sets[0][li]["out"].shape, dtype=self.sets[0][li]["out"].dtype).pin_memory())
         h2d = sum(t.numel() * t.element_size() for h in hosts for t in h.values())
         d2h = sum(o.numel() * o.element_size() for o in outs)
@@ -522,7 +553,8 @@ def run_cuda(args):
     if args.workload == "prefill":
         dom, dom_bytes, dom_src = "prefill", prefill_bytes(shape), ["prefill.cu", "internal.cuh"]
     else:
-        dom, dom_bytes, dom_src = "verify", verify_bytes(shape), ["verify.cu", "internal.cuh"]
+        dom, dom_bytes, dom_src = "verify", (tree_verify_bytes(shape) if getattr(wl, "tree", False)
+                                             else verify_bytes(shape)), ["verify.cu", "internal.cuh"]
     achieved = dom_bytes / kdur[dom] / 1e9
     sha = kernel_source_sha(dom_src)
     traffic = recorded_traffic(dom, sha, args.workload)
@@ -593,6 +625,11 @@ def _oracle_pass(shape, x, heads, n_threads, trims):
     import oracle
     if shape.name == "prefill":
         oracle.verify(shape, x, capture=False, head_mask=heads, n_threads=n_threads)
+        return
+    if shape.name.startswith("tree"):
+        r = oracle.verify_tree(shape, x, make_parents(shape, "spine"), head_mask=heads, n_threads=n_threads)
+        oracle.rollback_tree(shape, np.asarray(trims, dtype=np.int32) - 1, x["state"], x["conv_state"],
+                             r["cap_state"], r["cap_conv"])
         return
     r = oracle.verify(shape, x, head_mask=heads, n_threads=n_threads)
     oracle.rollback(shape, trims, r["state"], r["conv_state"], r["cap_state"], r["cap_conv"])

@@ -163,6 +163,8 @@ WORKLOADS: Dict[str, Shape] = {
     "stack_verify": Shape("stack_verify", 8, 16, 48, 128, 128, 16, "bf16", n_layers=48, seed=3),
     # chunked prefill, 8192 tokens in chunks of 64
     "prefill": Shape("prefill", 1, 16, 48, 128, 128, 8192, "bf16", seed=4, chunk=64),
+    # tree (DDTree) verify of a 16-node draft tree, one slot of the layer shape
+    "tree_verify": Shape("tree_verify", 1, 16, 48, 128, 128, 16, "bf16", seed=5),
 }
 
 # stream tags (one independent stream per tensor and layer)
