@@ -20,12 +20,15 @@
 //
 // Work split.  Everything but U, O and S depends only on the chunk itself, so
 // three CTAs serve one (slot, value head):
-//   * two preparation CTAs take alternate chunks: raw window (TMA), gates,
-//     conv + SiLU, L2 norms, G = [K; Q] K^T, A and the masked, decayed P,
-//     T = (I + A)^-1 (16 x 16 blocks), W^T and U~^T; they publish the chunk's
-//     ready-split operands (-W, Gamma Q, P, Gamma_C/Gamma K planes and U~) to
-//     a ring of four slots in the caller's workspace (bulk stores, L2-resident)
-//     and release a per-slot flag;
+//   * preparation CTAs (NP per key head) claim (chunk, key head) work items
+//     in chunk order from a counter; per item the q/k work is done once for
+//     the r value heads that share the key head (raw window by TMA,
+//     conv + SiLU into TMEM, L2 norms, G = [K; Q] K^T kept in TMEM), then per
+//     value head its gates, v conv, A and the masked, decayed P, T = (I + A)^-1
+//     (16 x 16 blocks), W^T and U~^T; they publish the ready-split operands
+//     (-W, Gamma Q, P, Gamma_C/Gamma K planes and U~) to that head's ring of
+//     eight slots in the caller's workspace (L2-resident) and release a
+//     per-slot flag;
 //   * the state CTA holds the fp32 state in registers and, chunk by chunk,
 //     acquires a slot, pulls it in with bulk copies and runs only the
 //     state-dependent products and the epilogue:
@@ -57,7 +60,8 @@ constexpr int kThreads = 256;
 constexpr int kSpinLimit = 1 << 20;    // try_wait rounds before an mbarrier wait gives up
 constexpr int kFlagSpin = 1 << 21;     // polls (with back-off, about a second) before a ring-flag wait gives up
 constexpr int kTmemCols = 512;
-constexpr int kRing = 4;               // ring slots per (slot, value head)
+constexpr int kRing = 8;               // ring slots per (slot, value head)
+constexpr int kMaxPrep = 8;            // preparation CTAs per key head, at most
 
 // dynamic shared memory carve-up (bytes)
 constexpr uint32_t kRA = 0;                    // 128 KB: A operand planes; raw chunk inputs at chunk start
@@ -70,7 +74,8 @@ constexpr uint32_t kRawBar = kMisc + 8;        // 8 B: raw window copies (prepar
 constexpr uint32_t kTmemSlot = kMisc + 16;     // 4 B
 constexpr uint32_t kFlagOk = kMisc + 20;       // 4 B: result of a ring-flag wait, broadcast to the CTA
 constexpr uint32_t kZBar = kMisc + 24;         // 8 B: gate (z) tile copy
-constexpr uint32_t kLogG = kMisc + 32;         // 64 floats each
+constexpr uint32_t kItem = kMisc + 32;         // 4 B: work item claimed by a preparation CTA, broadcast
+constexpr uint32_t kLogG = kMisc + 48;         // 64 floats each
 constexpr uint32_t kBeta = kLogG + 256;
 constexpr uint32_t kGam = kBeta + 256;
 constexpr uint32_t kRinv = kGam + 256;
@@ -85,21 +90,24 @@ static_assert(kWin * kCh * 4 <= 128 * 1024, "raw chunk window fits the A region"
 constexpr uint32_t kHistOff = 0;               // 3 x 384 floats
 constexpr uint32_t kSsqOff = 8 * 1024;         // 8 channel blocks (q, k) x 64 tokens
 
-// TMEM columns.  Preparation: G (later W^T), U~^T, and the chunk's conv outputs q and k (lane =
-// channel, column = token; not normalised).  State: X^T (later U^T), O^T, D2.
-constexpr uint32_t kColG = 0, kColWT = 0, kColUT = 64, kColOT = 128, kColQ = 192, kColK = 256, kColD2 = 320;
-static_assert(kColD2 + 128 <= kTmemCols, "TMEM columns");
+// TMEM columns of a preparation CTA: G (kept for all value heads of the group), U~^T, W^T and the
+// chunk's conv outputs q and k (lane = channel, column = token; not normalised).
+constexpr uint32_t kColG = 0, kColUT = 64, kColWT = 128, kColQ = 192, kColK = 256;
+static_assert(kColK + 64 <= kTmemCols, "TMEM columns");
+// State CTA: X^T (then U^T hi) | O^T | U^T lo | S^T hi (then D2) | S^T lo
+constexpr uint32_t kSX = 64, kSO = 128, kSUlo = 192, kSShi = 256, kSSlo = 384;
+static_assert(kSSlo + 128 <= kTmemCols, "TMEM columns of the state CTA");
 
 // One ring slot: the chunk's operands in the exact shared-memory layout the state CTA uses.
-constexpr uint32_t kSlotNegW = 0;              // -W planes (64 x 128, hi + lo), 64 KB
-constexpr uint32_t kSlotGQ = 64 * 1024;        // Gamma Q planes (64 x 128), 64 KB
+constexpr uint32_t kSlotB = 0;                 // [-W; Gamma Q] planes: one 128 x 128 operand, hi 64 KB + lo 64 KB
 constexpr uint32_t kSlotP = 128 * 1024;        // P planes (64 x 64), 32 KB
 constexpr uint32_t kSlotKd = 160 * 1024;       // (Gamma_C / Gamma) K planes, as (128 x 64), 64 KB
 constexpr uint32_t kSlotU = 224 * 1024;        // U~^T fp32 [128][64], 32 KB
 constexpr size_t kSlotBytes = 256 * 1024;
-// per (slot, value head): ring flags and the chunk decays (ints: full[4], empty[4], Gamma_C[4] bits)
-constexpr size_t kFlagWords = 16;
-// per (slot, value head): the two preparation CTAs' v^T scratch (128 channels x 64 tokens each)
+// per (slot, value head): ring flags and the chunk decays (ints: full[8], empty[8], Gamma_C[8] bits)
+constexpr size_t kFlagWords = 32;
+static_assert(kFlagWords >= 3 * kRing, "flag words");
+// per (slot, key head, preparation CTA): v^T scratch (128 channels x 64 tokens)
 constexpr size_t kVtFloats = 128 * 64;
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
@@ -191,6 +199,23 @@ __device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo, u
         mma_tf32(d, ah, bh, id, (ks > 0 || accumulate) ? 1u : 0u);
         mma_tf32(d, ah, bl, id, 1u);
         mma_tf32(d, al, bh, id, 1u);
+    }
+}
+// D (128 x N) (+)= A (128 x K, tf32 columns of TMEM: lane = row) . B (N x K, smem)^T, 3xTF32
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d),
+                 "r"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma3_ts(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo, int K,
+                                        int N, bool accumulate) {
+    const uint32_t id = idesc_tf32(N);
+    for (int ks = 0; ks < K / 8; ++ks) {
+        const uint32_t o = (uint32_t)ks * 256u;
+        const uint64_t bh = make_desc(b_hi + o, K), bl = make_desc(b_lo + o, K);
+        mma_tf32_ts(d, a_hi + 8 * ks, bh, id, (ks > 0 || accumulate) ? 1u : 0u);
+        mma_tf32_ts(d, a_hi + 8 * ks, bl, id, 1u);
+        mma_tf32_ts(d, a_lo + 8 * ks, bh, id, 1u);
     }
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -334,17 +359,18 @@ struct Ctx {
 };
 
 // ---------------------------------------------------------------------------
-// preparation CTA: chunks c = par, par + 2, ...
+// preparation CTA: claims (chunk, slot, key head) items; for each, the q/k work
+// (conv, norms, G) once, then A, T, W, U~, P for each of the r value heads of
+// the group, each published to that head's ring
 // ---------------------------------------------------------------------------
 template <typename Act>
-__device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int h, int par) {
+__device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) {
     unsigned char *sm = x.sm;
     const int tid = x.tid, lane = x.lane, wid = x.wid, tl = x.tl, half = x.half;
-    const int Hk = a.Hk, Hv = a.Hv, L = a.L, C = a.C;
-    const int kh = h / a.r;
+    const int Hk = a.Hk, Hv = a.Hv, L = a.L, C = a.C, R = a.r;
     const uint32_t tmem = x.tmem, tq = x.tq;
-    const Act *rawA = reinterpret_cast<const Act *>(sm + kRA);        // [q|k|v][67][128] raw window of the chunk
-    float *hist = reinterpret_cast<float *>(sm + kRB + kHistOff);     // [3][384] conv state (first chunk only)
+    const Act *rawA = reinterpret_cast<const Act *>(sm + kRA);        // q|k tiles, later one v tile: [67][128]
+    float *hist = reinterpret_cast<float *>(sm + kRB + kHistOff);     // [3][256] q|k, later [3][128] v history
     float *ssq = reinterpret_cast<float *>(sm + kRB + kSsqOff);       // [8][64] partial sums of squares
     float *AMt = reinterpret_cast<float *>(sm + kAM);
     float *Pt = reinterpret_cast<float *>(sm + kPT);
@@ -359,31 +385,25 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
     const uint32_t sRA = smem_u32(RA), sRB = smem_u32(RB);
     const uint32_t rawbar = smem_u32(sm + kRawBar);
     uint32_t raw_phase = 0;
-    float *vT = a.scratch_vt + (((size_t)s * Hv + h) * 2 + par) * kVtFloats;   // [128 channels][64 tokens]
-    const Ring ring = ring_of(a, s, h);
+    float *vT = a.scratch_vt + (size_t)pidx * kVtFloats;      // [128 channels][64 tokens]
+    constexpr uint32_t kTile = kWin * kD * sizeof(Act);
 
-    // global conv channel of local channel ch (q 0..127, k 128..255, v 256..383)
-    auto gch = [&](int ch) -> int {
-        if (ch < kD) return kh * kD + ch;
-        if (ch < 2 * kD) return Hk * kD + kh * kD + (ch - kD);
-        return 2 * Hk * kD + h * kD + (ch - 2 * kD);
-    };
-    // raw window rows t0-3 .. t0+63 of chunk cc: three 128-channel tiles (q, k, v of this head) of the
-    // qkv tensor map, one thread.  Rows outside the tensor read as zero; rows of a neighbouring slot
-    // and rows past the prompt are never used (the history rows of the first chunk come from the
-    // conv state, outputs of padded tokens are discarded).
-    auto issue_raw = [&](int cc) {
-        constexpr uint32_t kTile = kWin * kD * sizeof(Act);
+    // raw window rows t0-3 .. t0+63 of chunk cc: 128-channel tiles of the qkv tensor map, one thread.
+    // Rows outside the tensor read as zero; rows of a neighbouring slot and rows past the prompt are never
+    // used (the history rows of the first chunk come from the conv state, padded tokens are discarded).
+    auto issue_qk = [&](int cc, int s, int kh) {
         const int y = s * L + cc * kC - 3;
-        const uint32_t dst = smem_u32(sm + kRA);
-        mbar_arrive_expect_tx(rawbar, 3u * kTile);
-        tma_load_2d(dst, &a.qkv_map, kh * kD, y, rawbar);
-        tma_load_2d(dst + kTile, &a.qkv_map, Hk * kD + kh * kD, y, rawbar);
-        tma_load_2d(dst + 2 * kTile, &a.qkv_map, 2 * Hk * kD + h * kD, y, rawbar);
+        mbar_arrive_expect_tx(rawbar, 2u * kTile);
+        tma_load_2d(sRA, &a.qkv_map, kh * kD, y, rawbar);
+        tma_load_2d(sRA + kTile, &a.qkv_map, Hk * kD + kh * kD, y, rawbar);
     };
-    // gate inputs of chunk cc (threads tid < 64, one token each)
+    auto issue_v = [&](int cc, int s, int h) {
+        mbar_arrive_expect_tx(rawbar, kTile);
+        tma_load_2d(sRA, &a.qkv_map, 2 * Hk * kD + h * kD, s * L + cc * kC - 3, rawbar);
+    };
+    // gate inputs of (chunk cc, value head h) (threads tid < 64, one token each)
     float g_alpha = 0.f, g_beta = 0.f;
-    auto load_gates = [&](int cc) {
+    auto load_gates = [&](int cc, int s, int h) {
         const int t = cc * kC + tid;
         if (tid < kC && t < L) {
             const size_t idx = ((size_t)s * L + t) * Hv + h;
@@ -391,121 +411,116 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
             g_beta = to_f32(static_cast<const Act *>(a.beta_raw)[idx]);
         }
     };
+    // sliding-window conv + SiLU of 16 tokens of one channel; rows 0-2 of the first chunk from `hist`
+    auto conv16 = [&](const Act *src, const float *hrow, int hstride, int g, int tb, int c, int n, float *yv) {
+        const float w0 = __ldg(a.conv_w + g), w1 = __ldg(a.conv_w + C + g), w2 = __ldg(a.conv_w + 2 * C + g),
+                    w3 = __ldg(a.conv_w + 3 * C + g);
+        float x0, x1, x2;
+        if (c == 0 && tb == 0) {
+            x0 = hrow[0]; x1 = hrow[hstride]; x2 = hrow[2 * hstride];
+        } else {
+            x0 = to_f32(src[tb * kD]); x1 = to_f32(src[(tb + 1) * kD]); x2 = to_f32(src[(tb + 2) * kD]);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int t = tb + j;
+            const float x3 = to_f32(src[(t + 3) * kD]);
+            const float y = silu(fmaf(w3, x3, fmaf(w2, x2, fmaf(w1, x1, w0 * x0))));
+            yv[j] = t < n ? y : 0.f;
+            x0 = x1; x1 = x2; x2 = x3;
+        }
+    };
 
-    // A published chunk is released one phase later (after the next chunk's conv), so the stores
-    // drain while that work runs: every thread fences its own stores, the CTA synchronises, thread 0
-    // releases the flag.  pend_* are uniform across the CTA.
-    int pend_slot = -1, pend_c = 0;
+    // A published (chunk, head) is released one phase later, so its stores drain while the next
+    // phase runs: every thread fences its own stores, the CTA synchronises, thread 0 releases the
+    // flag.  pend_* are uniform across the CTA.
+    int pend_slot = -1, pend_c = 0, pend_h = 0, pend_s = 0;
     float pend_gamma = 0.f;
+    auto fence_pending = [&]() {
+        if (pend_slot >= 0) __threadfence();
+    };
     auto release_pending = [&]() {            // after a __syncthreads that followed fence_pending()
         if (pend_slot >= 0) {
             if (tid == 0) {
-                ring.gamma_c[pend_slot] = pend_gamma;
+                const Ring rg = ring_of(a, pend_s, pend_h);
+                rg.gamma_c[pend_slot] = pend_gamma;
                 __threadfence();
-                st_release(ring.full + pend_slot, pend_c + 1);
+                st_release(rg.full + pend_slot, pend_c + 1);
             }
             pend_slot = -1;
         }
     };
-    auto fence_pending = [&]() {
-        if (pend_slot >= 0) __threadfence();
-    };
 
+    // Work items (chunk, slot, key head) in chunk order, claimed from a counter: a slower SM simply
+    // takes fewer.  Every wait of an item refers to a smaller chunk, whose item was claimed earlier.
     const int n_chunks = (L + kC - 1) / kC;
-    if (par >= n_chunks) return;
-    if (tid == 0) issue_raw(par);
-    load_gates(par);
-    if (par == 0) {
-        // the three window rows before the prompt: the conv state (fp32)
-        for (int it = tid; it < 3 * (kCh / 4); it += kThreads) {
-            const int row = it / (kCh / 4), ch = 4 * (it % (kCh / 4));
-            *reinterpret_cast<float4 *>(hist + row * kCh + ch) =
-                *reinterpret_cast<const float4 *>(a.conv_state + ((size_t)s * 3 + row) * C + gch(ch));
-        }
+    const int n_items = n_chunks * a.ns * Hk;
+    auto claim = [&]() -> int {
+        volatile int *ip = reinterpret_cast<volatile int *>(sm + kItem);
+        if (tid == 0) *ip = atomicAdd(a.counter, 1);
+        __syncthreads();
+        const int v = *ip;
+        __syncthreads();
+        return v;
+    };
+    auto decode = [&](int item, int &c, int &s, int &kh) {
+        c = item / (a.ns * Hk);
+        const int r2 = item % (a.ns * Hk);
+        s = a.slot0 + r2 / Hk;
+        kh = r2 % Hk;
+    };
+    int item = claim();
+    if (item >= n_items) return;
+    {
+        int c0, s0, kh0;
+        decode(item, c0, s0, kh0);
+        if (tid == 0) issue_qk(c0, s0, kh0);
+        load_gates(c0, s0, kh0 * R);
     }
 
-    for (int c = par; c < n_chunks; c += 2) {
+    while (item < n_items) {
+        const int next = claim();
+        int c, s, kh;
+        decode(item, c, s, kh);
         const int t0 = c * kC, n = min(kC, L - t0);
         const int slot = c % kRing;
-        unsigned char *dst_slot = ring.slots + (size_t)slot * kSlotBytes;
 
-        // ---------------- (a) gates; the raw window arrives
-        if (tid < kC) {                    // padded tokens: no decay, no write
-            float lg = 0.f, b = 0.f;
-            if (tid < n) {
-                const float xx = g_alpha + __ldg(a.dt_bias + h);
-                const float sp = xx > 20.0f ? xx : log1pf(expf(xx));
-                lg = -expf(__ldg(a.A_log + h)) * sp;
-                b = 1.0f / (1.0f + expf(-g_beta));
+        // ---------------- (a) q, k of the key head: conv + SiLU -> TMEM, L2 norms, G = [K; Q] K^T
+        if (c == 0) {
+            for (int it = tid; it < 3 * (2 * kD / 4); it += kThreads) {   // conv state rows of q, k (fp32)
+                const int row = it / (2 * kD / 4), ch = 4 * (it % (2 * kD / 4));
+                const int g = ch < kD ? kh * kD + ch : Hk * kD + kh * kD + (ch - kD);
+                *reinterpret_cast<float4 *>(hist + row * 2 * kD + ch) =
+                    *reinterpret_cast<const float4 *>(a.conv_state + ((size_t)s * 3 + row) * C + g);
             }
-            logG[tid] = lg;
-            betas[tid] = b;
         }
         x.wait_bar(rawbar, raw_phase);
         __syncthreads();
-        if (wid == 0) {                    // Gamma = exp(cumsum(log g)) inside the chunk: lane l owns 2l, 2l+1
-            const float l0 = logG[2 * lane], l1 = logG[2 * lane + 1];
-            float incl = l0 + l1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += y;
-            }
-            const float c0 = incl - l1;
-            logG[2 * lane] = c0;
-            logG[2 * lane + 1] = incl;
-            gam[2 * lane] = expf(c0);
-            gam[2 * lane + 1] = expf(incl);
-        }
-        // conv + SiLU: item = (channel, 16-token segment), sliding window.  q and k go to TMEM (lane =
-        // channel: the warp's lane quarter is (ch % 128) / 32 = warp % 4), v to the scratch, transposed.
-        // For q and k the warp also sums y^2 over its 32 channels per token (reduce-scatter, fixed order).
+        // item = (channel, 16-token segment); the warp's TMEM lane quarter is (ch % 128) / 32 = warp % 4;
+        // the warp also sums y^2 over its 32 channels per token (reduce-scatter, fixed order)
 #pragma unroll 1
-        for (int k = 0; k < 6; ++k) {
+        for (int k = 0; k < 4; ++k) {
             const int it = tid + k * kThreads;
-            const int ch = it % kCh, tb = 16 * (it / kCh);
-            const int g = gch(ch);
-            const float w0 = __ldg(a.conv_w + g), w1 = __ldg(a.conv_w + C + g), w2 = __ldg(a.conv_w + 2 * C + g),
-                        w3 = __ldg(a.conv_w + 3 * C + g);
-            const Act *src = rawA + (ch >> 7) * (kWin * kD) + (ch & (kD - 1));
-            // window row r holds token t0 - 3 + r; rows 0-2 of the first chunk come from the conv state
-            float x0, x1, x2;
-            if (c == 0 && tb == 0) {
-                x0 = hist[ch]; x1 = hist[kCh + ch]; x2 = hist[2 * kCh + ch];
-            } else {
-                x0 = to_f32(src[tb * kD]); x1 = to_f32(src[(tb + 1) * kD]); x2 = to_f32(src[(tb + 2) * kD]);
-            }
+            const int ch = it % (2 * kD), tb = 16 * (it / (2 * kD));
+            const int g = ch < kD ? kh * kD + ch : Hk * kD + kh * kD + (ch - kD);
             float yv[16], y2[16];
+            conv16(rawA + (ch >> 7) * (kWin * kD) + (ch & (kD - 1)), hist + ch, 2 * kD, g, tb, c, n, yv);
+            tmem_st16(tmem + tq + (ch < kD ? kColQ : kColK) + tb, yv);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int t = tb + j;
-                const float x3 = to_f32(src[(t + 3) * kD]);
-                const float y = silu(fmaf(w3, x3, fmaf(w2, x2, fmaf(w1, x1, w0 * x0))));
-                yv[j] = t < n ? y : 0.f;
-                y2[j] = yv[j] * yv[j];
-                x0 = x1; x1 = x2; x2 = x3;
-            }
-            if (ch < 2 * kD) {                    // warp-uniform: a warp's 32 channels share q|k|v
-                tmem_st16(tmem + tq + (ch < kD ? kColQ : kColK) + tb, yv);
+            for (int j = 0; j < 16; ++j) y2[j] = yv[j] * yv[j];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) y2[j] += __shfl_xor_sync(0xffffffffu, y2[j], 16);
+            for (int j = 0; j < 16; ++j) y2[j] += __shfl_xor_sync(0xffffffffu, y2[j], 16);
 #pragma unroll
-                for (int off = 8; off >= 1; off >>= 1) {
-                    const bool upper = (lane & off) != 0;
+            for (int off = 8; off >= 1; off >>= 1) {
+                const bool upper = (lane & off) != 0;
 #pragma unroll
-                    for (int i = 0; i < off; ++i) {
-                        const float send = upper ? y2[i] : y2[i + off];
-                        const float keep = upper ? y2[i + off] : y2[i];
-                        y2[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                    }
+                for (int i = 0; i < off; ++i) {
+                    const float send = upper ? y2[i] : y2[i + off];
+                    const float keep = upper ? y2[i + off] : y2[i];
+                    y2[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
                 }
-                if (lane < 16) ssq[(ch >> 5) * kC + tb + lane] = y2[0];   // token tb + lane, channel block ch/32
-            } else {
-                float4 *dv = reinterpret_cast<float4 *>(vT + (ch - 2 * kD) * kC + tb);
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    dv[q4] = make_float4(yv[4 * q4], yv[4 * q4 + 1], yv[4 * q4 + 2], yv[4 * q4 + 3]);
             }
+            if (lane < 16) ssq[(ch >> 5) * kC + tb + lane] = y2[0];   // token tb + lane, channel block ch/32
         }
         tmem_wait_st();
         fence_pending();
@@ -521,8 +536,6 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
             (part ? invk : invq)[t] = 1.0f / sqrtf(sum + a.l2_eps);
         }
         __syncthreads();
-
-        // ---------------- (b) G = [K; Q] K^T
         {
             // this thread holds channel i = tl of 32 tokens: the rows of [K^; Q^] get column i
             float x32[32];
@@ -539,181 +552,248 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int s, int
         }
         x.publish();
         if (tid == 0) mma3(tmem + kColG, sRA, sRA + 64 * 1024, sRA, sRA + 64 * 1024, 128, 64, false);
-        x.commit_wait();
-        {
-            float g32[32];
-            tmem_ld16(tmem + tq + kColG + 32 * half, g32);
-            tmem_ld16(tmem + tq + kColG + 32 * half + 16, g32 + 16);
-            if (tl < kC) {                 // A[r][s] = beta_r Gamma_r / Gamma_s k_r.k_s for s < r
-                const int r = tl;
-                const float br = betas[r], lr = logG[r];
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int sc = 32 * half + q;
-                    AMt[sc * kC + r] = sc < r ? br * __expf(lr - logG[sc]) * g32[q] : 0.f;
-                }
-            } else {                       // P[r][s] = q_r.k_s Gamma_r / Gamma_s for s <= r
-                const int r = tl - kC;
-                const float lr = logG[r];
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int sc = 32 * half + q;
-                    Pt[sc * kC + r] = sc <= r ? __expf(lr - logG[sc]) * g32[q] : 0.f;
-                }
-            }
-        }
-        __syncthreads();
+        x.commit_wait();                                    // G stays in TMEM for every value head
+        if (tid == 0) issue_v(c, s, kh * R);
 
-        // this thread's row of v^T for the A2 operand below, fetched before the inversion
-        float4 vpre[8];
-        {
-            const float4 *vrow = reinterpret_cast<const float4 *>(vT + tl * kC + 32 * half);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) vpre[q4] = vrow[q4];
-        }
+        for (int hi = 0; hi < R; ++hi) {
+            const int h = kh * R + hi;
+            const Ring ring = ring_of(a, s, h);
+            unsigned char *dst_slot = ring.slots + (size_t)slot * kSlotBytes;
 
-        // A1 = (diag(beta Gamma) K^)^T, A2 = (diag(beta) V)^T -> RA: warp (quarter, half) builds rows
-        // 32 quarter .. +31 of tokens 32 half .. +31
-        auto build_a12 = [&]() {
-            float x32[32];
-            tmem_ld16(tmem + tq + kColK + 32 * half, x32);
-            tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                float ka[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int sr = 32 * half + 4 * q4 + e;
-                    ka[e] = betas[sr] * gam[sr] * invk[sr] * x32[4 * q4 + e];
+            // ---------------- (b) gates of the head; v conv -> v^T scratch
+            if (tid < kC) {                    // padded tokens: no decay, no write
+                float lg = 0.f, b = 0.f;
+                if (tid < n) {
+                    const float xx = g_alpha + __ldg(a.dt_bias + h);
+                    const float sp = xx > 20.0f ? xx : log1pf(expf(xx));
+                    lg = -expf(__ldg(a.A_log + h)) * sp;
+                    b = 1.0f / (1.0f + expf(-g_beta));
                 }
-                put4(RA, RA + 32 * 1024, tl, 8 * half + q4, 64, make_float4(ka[0], ka[1], ka[2], ka[3]));
+                logG[tid] = lg;
+                betas[tid] = b;
             }
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 v = vpre[q4];
-                const int sr = 32 * half + 4 * q4;
-                put4(RA + 64 * 1024, RA + 96 * 1024, tl, 8 * half + q4, 64,
-                     make_float4(betas[sr] * v.x, betas[sr + 1] * v.y, betas[sr + 2] * v.z, betas[sr + 3] * v.w));
+            if (c == 0) {
+                for (int it = tid; it < 3 * (kD / 4); it += kThreads) {   // conv state rows of v (fp32)
+                    const int row = it / (kD / 4), ch = 4 * (it % (kD / 4));
+                    *reinterpret_cast<float4 *>(hist + row * kD + ch) = *reinterpret_cast<const float4 *>(
+                        a.conv_state + ((size_t)s * 3 + row) * C + 2 * Hk * kD + h * kD + ch);
+                }
             }
-        };
-        // ---------------- (c) T = (I + A)^-1, 16 x 16 blocks
-        // diagonal blocks: forward substitution, one column per thread, in registers, by warps 6-7 while
-        // warps 0-5 build their rows of the A1 / A2 operands (RA is free since G completed)
-        if (wid >= 6) {
-            const int b = (tid - 192) >> 4, col = tid & 15, o = 16 * b;
-            float tc[16];
+            x.wait_bar(rawbar, raw_phase);
+            __syncthreads();
+            if (wid == 0) {                    // Gamma = exp(cumsum(log g)): lane l owns tokens 2l, 2l+1
+                const float l0 = logG[2 * lane], l1 = logG[2 * lane + 1];
+                float incl = l0 + l1;
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = r == col ? 1.f : 0.f;
-#pragma unroll
-                for (int m = 0; m < r; ++m) acc = fmaf(-AMt[(o + m) * kC + o + r], tc[m], acc);
-                tc[r] = acc;
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += y;
+                }
+                const float c0 = incl - l1;
+                logG[2 * lane] = c0;
+                logG[2 * lane + 1] = incl;
+                gam[2 * lane] = expf(c0);
+                gam[2 * lane + 1] = expf(incl);
             }
+#pragma unroll 1
+            for (int k = 0; k < 2; ++k) {
+                const int it = tid + k * kThreads;
+                const int ch = it % kD, tb = 16 * (it / kD);
+                float yv[16];
+                conv16(rawA + ch, hist + ch, kD, 2 * Hk * kD + h * kD + ch, tb, c, n, yv);
+                float4 *dv = reinterpret_cast<float4 *>(vT + ch * kC + tb);
 #pragma unroll
-            for (int r = 0; r < 16; ++r) Tm[(o + r) * kC + o + col] = tc[r];
-            for (int r = 0; r < 16; ++r)          // the strictly upper blocks of this block column are zero
-                for (int bb = 0; bb < b; ++bb) Tm[(16 * bb + r) * kC + o + col] = 0.f;
-        } else {
-            build_a12();
-        }
-        __syncthreads();
-        // off-diagonal blocks by distance: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
-        for (int dist = 1; dist < 4; ++dist) {
-            const int nb = 4 - dist;               // blocks (j + dist, j), j < nb
-            for (int e = tid; e < nb * 256; e += kThreads) {
-                const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15, i = j + dist;
-                float acc = 0.f;
-                for (int kb = j; kb < i; ++kb)
+                for (int q4 = 0; q4 < 4; ++q4)
+                    dv[q4] = make_float4(yv[4 * q4], yv[4 * q4 + 1], yv[4 * q4 + 2], yv[4 * q4 + 3]);
+            }
+            fence_pending();
+            __syncthreads();
+            release_pending();
+
+            // ---------------- (c) A and the masked, decayed P from G
+            {
+                float g32[32];
+                tmem_ld16(tmem + tq + kColG + 32 * half, g32);
+                tmem_ld16(tmem + tq + kColG + 32 * half + 16, g32 + 16);
+                if (tl < kC) {                 // A[r][s] = beta_r Gamma_r / Gamma_s k_r.k_s for s < r
+                    const int r = tl;
+                    const float br = betas[r], lr = logG[r];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const int sc = 32 * half + q;
+                        AMt[sc * kC + r] = sc < r ? br * __expf(lr - logG[sc]) * g32[q] : 0.f;
+                    }
+                } else {                       // P[r][s] = q_r.k_s Gamma_r / Gamma_s for s <= r
+                    const int r = tl - kC;
+                    const float lr = logG[r];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const int sc = 32 * half + q;
+                        Pt[sc * kC + r] = sc <= r ? __expf(lr - logG[sc]) * g32[q] : 0.f;
+                    }
+                }
+            }
+            __syncthreads();
+
+            // this thread's row of v^T for the A2 operand below, fetched before the inversion
+            float4 vpre[8];
+            {
+                const float4 *vrow = reinterpret_cast<const float4 *>(vT + tl * kC + 32 * half);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) vpre[q4] = vrow[q4];
+            }
+            // A1 = (diag(beta Gamma) K^)^T, A2 = (diag(beta) V)^T -> RA: warp (quarter, half) builds rows
+            // 32 quarter .. +31 of tokens 32 half .. +31
+            auto build_a12 = [&]() {
+                float x32[32];
+                tmem_ld16(tmem + tq + kColK + 32 * half, x32);
+                tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    float ka[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int sr = 32 * half + 4 * q4 + e;
+                        ka[e] = betas[sr] * gam[sr] * invk[sr] * x32[4 * q4 + e];
+                    }
+                    put4(RA, RA + 32 * 1024, tl, 8 * half + q4, 64, make_float4(ka[0], ka[1], ka[2], ka[3]));
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 v = vpre[q4];
+                    const int sr = 32 * half + 4 * q4;
+                    put4(RA + 64 * 1024, RA + 96 * 1024, tl, 8 * half + q4, 64,
+                         make_float4(betas[sr] * v.x, betas[sr + 1] * v.y, betas[sr + 2] * v.z, betas[sr + 3] * v.w));
+                }
+            };
+            // ---------------- (d) T = (I + A)^-1, 16 x 16 blocks
+            // diagonal blocks: forward substitution, one column per thread, in registers, by warps 6-7
+            // while warps 0-5 build their rows of the A1 / A2 operands (RA: the v tile is consumed)
+            if (wid >= 6) {
+                const int b = (tid - 192) >> 4, col = tid & 15, o = 16 * b;
+                float tc[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    float acc = r == col ? 1.f : 0.f;
+#pragma unroll
+                    for (int m = 0; m < r; ++m) acc = fmaf(-AMt[(o + m) * kC + o + r], tc[m], acc);
+                    tc[r] = acc;
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Tm[(o + r) * kC + o + col] = tc[r];
+                for (int r = 0; r < 16; ++r)          // the strictly upper blocks of this block column are zero
+                    for (int bb = 0; bb < b; ++bb) Tm[(16 * bb + r) * kC + o + col] = 0.f;
+            } else {
+                build_a12();
+            }
+            __syncthreads();
+            // off-diagonal blocks by distance: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
+            for (int dist = 1; dist < 4; ++dist) {
+                const int nb = 4 - dist;               // blocks (j + dist, j), j < nb
+                for (int e = tid; e < nb * 256; e += kThreads) {
+                    const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15, i = j + dist;
+                    float acc = 0.f;
+                    for (int kb = j; kb < i; ++kb)
+#pragma unroll
+                        for (int m = 0; m < 16; ++m)
+                            acc = fmaf(AMt[(16 * kb + m) * kC + 16 * i + rr], Tm[(16 * kb + m) * kC + 16 * j + cc], acc);
+                    Xb[e] = acc;
+                }
+                __syncthreads();
+                for (int e = tid; e < nb * 256; e += kThreads) {
+                    const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15, i = j + dist;
+                    float acc = 0.f;
 #pragma unroll
                     for (int m = 0; m < 16; ++m)
-                        acc = fmaf(AMt[(16 * kb + m) * kC + 16 * i + rr], Tm[(16 * kb + m) * kC + 16 * j + cc], acc);
-                Xb[e] = acc;
-            }
-            __syncthreads();
-            for (int e = tid; e < nb * 256; e += kThreads) {
-                const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15, i = j + dist;
-                float acc = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) acc = fmaf(Tm[(16 * i + rr) * kC + 16 * i + m], Xb[(j << 8) + m * 16 + cc], acc);
-                Tm[(16 * i + rr) * kC + 16 * j + cc] = -acc;
-            }
-            __syncthreads();
-        }
-        // B = T (64 x 64) in RB[0, 32K); warps 6-7 build their rows of A1 / A2 now
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            int r, k4;
-            item_rc(tid + k * kThreads, 64, r, k4);
-            put4(RB, RB + 16 * 1024, r, k4, 64, *reinterpret_cast<const float4 *>(Tm + r * kC + 4 * k4));
-        }
-        if (wid >= 6) build_a12();
-        x.publish();
-        if (tid == 0) {
-            mma3(tmem + kColWT, sRA, sRA + 32 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
-            mma3(tmem + kColUT, sRA + 64 * 1024, sRA + 96 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
-        }
-        x.commit_wait();
-
-        // the A region is free: fetch the next chunk's window and gate inputs now
-        if (c + 2 < n_chunks) {
-            if (tid == 0) issue_raw(c + 2);
-            load_gates(c + 2);
-        }
-
-        // ---------------- (p) publish the chunk to its ring slot: every operand goes from registers
-        // straight to the slot (16-byte stores into L2), in the layout the state CTA copies in
-        if (c >= kRing) x.wait_flag(ring.empty + slot, c - kRing + 1);   // the state CTA took chunk c - kRing
-        {
-            // -W planes (64 x 128): this thread holds W[r][i = tl] for its 32 values of r
-            float x32[32];
-            tmem_ld16(tmem + tq + kColWT + 32 * half, x32);
-            tmem_ld16(tmem + tq + kColWT + 32 * half + 16, x32 + 16);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) x32[q] = -x32[q];
-            put_col32(dst_slot + kSlotNegW, dst_slot + kSlotNegW + 32 * 1024, 32 * half, tl, x32);
-            // Gamma Q^ planes (64 x 128)
-            tmem_ld16(tmem + tq + kColQ + 32 * half, x32);
-            tmem_ld16(tmem + tq + kColQ + 32 * half + 16, x32 + 16);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) x32[q] *= gam[32 * half + q] * invq[32 * half + q];
-            put_col32(dst_slot + kSlotGQ, dst_slot + kSlotGQ + 32 * 1024, 32 * half, tl, x32);
-            // U~^T fp32 [j = tl][r]
-            tmem_ld16(tmem + tq + kColUT + 32 * half, x32);
-            tmem_ld16(tmem + tq + kColUT + 32 * half + 16, x32 + 16);
-            float4 *urow = reinterpret_cast<float4 *>(dst_slot + kSlotU + (tl * kC + 32 * half) * 4);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-                urow[q4] = make_float4(x32[4 * q4], x32[4 * q4 + 1], x32[4 * q4 + 2], x32[4 * q4 + 3]);
-            // (Gamma_C / Gamma) K^ planes, as (128 x 64): row i = tl, tokens along K
-            tmem_ld16(tmem + tq + kColK + 32 * half, x32);
-            tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
-            const float lc = logG[kC - 1];
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                float ka[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int sr = 32 * half + 4 * q4 + e;
-                    ka[e] = __expf(lc - logG[sr]) * invk[sr] * x32[4 * q4 + e];
+                        acc = fmaf(Tm[(16 * i + rr) * kC + 16 * i + m], Xb[(j << 8) + m * 16 + cc], acc);
+                    Tm[(16 * i + rr) * kC + 16 * j + cc] = -acc;
                 }
-                put4(dst_slot + kSlotKd, dst_slot + kSlotKd + 32 * 1024, tl, 8 * half + q4, 64,
-                     make_float4(ka[0], ka[1], ka[2], ka[3]));
+                __syncthreads();
             }
-        }
-        // P planes (64 x 64)
+            // B = T (64 x 64) in RB[0, 32K); warps 6-7 build their rows of A1 / A2 now
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            int r, k4;
-            item_rc(tid + k * kThreads, 64, r, k4);
-            float p[4];
+            for (int k = 0; k < 4; ++k) {
+                int r, k4;
+                item_rc(tid + k * kThreads, 64, r, k4);
+                put4(RB, RB + 16 * 1024, r, k4, 64, *reinterpret_cast<const float4 *>(Tm + r * kC + 4 * k4));
+            }
+            if (wid >= 6) build_a12();
+            x.publish();
+            if (tid == 0) {
+                mma3(tmem + kColWT, sRA, sRA + 32 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
+                mma3(tmem + kColUT, sRA + 64 * 1024, sRA + 96 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
+            }
+            x.commit_wait();
+
+            // the A region is free: fetch the next tile (next head's v, or the next chunk's q, k) and gates
+            if (hi + 1 < R) {
+                if (tid == 0) issue_v(c, s, h + 1);
+                load_gates(c, s, h + 1);
+            } else if (next < n_items) {
+                int c2, s2, kh2;
+                decode(next, c2, s2, kh2);
+                if (tid == 0) issue_qk(c2, s2, kh2);
+                load_gates(c2, s2, kh2 * R);
+            }
+
+            // ---------------- (e) publish (chunk, head) to the head's ring: every operand goes from
+            // registers straight to the slot (16-byte stores into L2), in the layout the state CTA copies in
+            if (c >= kRing) x.wait_flag(ring.empty + slot, c - kRing + 1);   // the state CTA took c - kRing
+            {
+                // -W planes, rows 0-63 of the B operand: this thread holds W[r][i = tl] for its 32 values of r
+                float x32[32];
+                tmem_ld16(tmem + tq + kColWT + 32 * half, x32);
+                tmem_ld16(tmem + tq + kColWT + 32 * half + 16, x32 + 16);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) p[e] = Pt[(4 * k4 + e) * kC + r];
-            put4(dst_slot + kSlotP, dst_slot + kSlotP + 16 * 1024, r, k4, 64, make_float4(p[0], p[1], p[2], p[3]));
+                for (int q = 0; q < 32; ++q) x32[q] = -x32[q];
+                put_col32(dst_slot + kSlotB, dst_slot + kSlotB + 64 * 1024, 32 * half, tl, x32);
+                // Gamma Q^ planes, rows 64-127 of the B operand
+                tmem_ld16(tmem + tq + kColQ + 32 * half, x32);
+                tmem_ld16(tmem + tq + kColQ + 32 * half + 16, x32 + 16);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) x32[q] *= gam[32 * half + q] * invq[32 * half + q];
+                put_col32(dst_slot + kSlotB, dst_slot + kSlotB + 64 * 1024, kC + 32 * half, tl, x32);
+                // U~^T fp32 [j = tl][r]
+                tmem_ld16(tmem + tq + kColUT + 32 * half, x32);
+                tmem_ld16(tmem + tq + kColUT + 32 * half + 16, x32 + 16);
+                float4 *urow = reinterpret_cast<float4 *>(dst_slot + kSlotU + (tl * kC + 32 * half) * 4);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                    urow[q4] = make_float4(x32[4 * q4], x32[4 * q4 + 1], x32[4 * q4 + 2], x32[4 * q4 + 3]);
+                // (Gamma_C / Gamma) K^ planes, as (128 x 64): row i = tl, tokens along K
+                tmem_ld16(tmem + tq + kColK + 32 * half, x32);
+                tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
+                const float lc = logG[kC - 1];
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    float ka[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int sr = 32 * half + 4 * q4 + e;
+                        ka[e] = __expf(lc - logG[sr]) * invk[sr] * x32[4 * q4 + e];
+                    }
+                    put4(dst_slot + kSlotKd, dst_slot + kSlotKd + 32 * 1024, tl, 8 * half + q4, 64,
+                         make_float4(ka[0], ka[1], ka[2], ka[3]));
+                }
+            }
+            // P planes (64 x 64)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                int r, k4;
+                item_rc(tid + k * kThreads, 64, r, k4);
+                float p[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) p[e] = Pt[(4 * k4 + e) * kC + r];
+                put4(dst_slot + kSlotP, dst_slot + kSlotP + 16 * 1024, r, k4, 64, make_float4(p[0], p[1], p[2], p[3]));
+            }
+            pend_slot = c == a.drop_chunk ? -1 : slot;   // released one phase later (or at the end)
+            pend_c = c;
+            pend_h = h;
+            pend_s = s;
+            pend_gamma = gam[kC - 1];
+            __syncthreads();
         }
-        pend_slot = c == a.drop_chunk ? -1 : slot;   // released after the next chunk's conv (or at the end)
-        pend_c = c;
-        pend_gamma = gam[kC - 1];
-        __syncthreads();
+        item = next;
     }
     fence_pending();
     __syncthreads();
@@ -765,8 +845,9 @@ __device__ __forceinline__ void advance_state(const PrefillArgs &a, Ctx &x, int 
         x.wait_flag(ring.full + slot, c + 1);
         if (tid == 0) {
             fence_proxy_async_global();
-            mbar_arrive_expect_tx(ldbar, 64 * 1024);
-            bulk_g2s(sRB, src_slot + kSlotNegW, 64 * 1024, ldbar);
+            mbar_arrive_expect_tx(ldbar, 160 * 1024);
+            bulk_g2s(sRA, src_slot + kSlotB, 128 * 1024, ldbar);          // [-W; Gamma Q] hi | lo
+            bulk_g2s(sRB, src_slot + kSlotP, 32 * 1024, ldbar);           // P hi | lo
         }
         // U~^T row j = tl, tokens 32 half .. 32 half + 31; Gamma_C
         float u32[32];
@@ -779,50 +860,55 @@ __device__ __forceinline__ void advance_state(const PrefillArgs &a, Ctx &x, int 
             }
         }
         const float gc = ring.gamma_c[slot];
-        // A = S0^T (128 x 128) from the registers
+        // A = S0^T into TMEM as tf32 hi / lo columns (this thread: row j = tl, columns 64 half .. +63)
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-            put4(RA, RA + 64 * 1024, tl, 16 * half + q, 128,
-                 make_float4(St[4 * q], St[4 * q + 1], St[4 * q + 2], St[4 * q + 3]));
+        for (int q4 = 0; q4 < 4; ++q4) {
+            float hi16[16], lo16[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                hi16[e] = tf32_hi(St[16 * q4 + e]);
+                lo16[e] = St[16 * q4 + e] - hi16[e];
+            }
+            tmem_st16(tmem + tq + kSShi + 64 * half + 16 * q4, hi16);
+            tmem_st16(tmem + tq + kSSlo + 64 * half + 16 * q4, lo16);
+        }
+        tmem_wait_st();
         x.wait_bar(ldbar, ld_phase);
         x.publish();
-        // X^T = S0^T (-W)^T
-        if (tid == 0) mma3(tmem + kColUT, sRA, sRA + 64 * 1024, sRB, sRB + 32 * 1024, 128, 64, false);
+        // [X^T | O^T] = S0^T [-W; Gamma Q]^T  (N 128: X^T in the first 64 columns, O^T in the next 64)
+        if (tid == 0) mma3_ts(tmem + kSX, tmem + kSShi, tmem + kSSlo, sRA, sRA + 64 * 1024, 128, 128, false);
         x.commit_wait();
         if (tid == 0) {
             mbar_arrive_expect_tx(ldbar, 64 * 1024);
-            bulk_g2s(sRB, src_slot + kSlotGQ, 64 * 1024, ldbar);
+            bulk_g2s(sRA, src_slot + kSlotKd, 64 * 1024, ldbar);          // (Gamma_C/Gamma) K hi | lo
         }
         {
-            // U^T = U~^T + X^T
+            // U^T = U~^T + X^T, into TMEM as tf32 hi (over X^T) / lo columns
             float x32[32];
-            tmem_ld16(tmem + tq + kColUT + 32 * half, x32);
-            tmem_ld16(tmem + tq + kColUT + 32 * half + 16, x32 + 16);
+            tmem_ld16(tmem + tq + kSX + 32 * half, x32);
+            tmem_ld16(tmem + tq + kSX + 32 * half + 16, x32 + 16);
 #pragma unroll
             for (int q = 0; q < 32; ++q) u32[q] += x32[q];
-        }
-        x.wait_bar(ldbar, ld_phase);
-        x.publish();
-        // O^T = S0^T (Gamma Q)^T
-        if (tid == 0) mma3(tmem + kColOT, sRA, sRA + 64 * 1024, sRB, sRB + 32 * 1024, 128, 64, false);
-        x.commit_wait();
-        if (tid == 0) {
-            mbar_arrive_expect_tx(ldbar, 96 * 1024);
-            bulk_g2s(sRB, src_slot + kSlotP, 32 * 1024, ldbar);
-            bulk_g2s(sRA + 64 * 1024, src_slot + kSlotKd, 64 * 1024, ldbar);
-        }
-        // A = U^T (128 x 64) planes -> RA[0, 64K)
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-            put4(RA, RA + 32 * 1024, tl, 8 * half + q, 64,
-                 make_float4(u32[4 * q], u32[4 * q + 1], u32[4 * q + 2], u32[4 * q + 3]));
+            for (int q2 = 0; q2 < 2; ++q2) {
+                float hi16[16], lo16[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    hi16[e] = tf32_hi(u32[16 * q2 + e]);
+                    lo16[e] = u32[16 * q2 + e] - hi16[e];
+                }
+                tmem_st16(tmem + tq + kSX + 32 * half + 16 * q2, hi16);
+                tmem_st16(tmem + tq + kSUlo + 32 * half + 16 * q2, lo16);
+            }
+            tmem_wait_st();
+        }
         x.wait_bar(ldbar, ld_phase);
-        if (tid == 0) st_release(ring.empty + slot, c + 1);     // the slot's bytes are all in shared memory
+        if (tid == 0) st_release(ring.empty + slot, c + 1);     // the slot's bytes are all on chip
         x.publish();
         // O^T += U^T P^T;  D2 = U^T (diag(Gamma_C / Gamma) K)
         if (tid == 0) {
-            mma3(tmem + kColOT, sRA, sRA + 32 * 1024, sRB, sRB + 16 * 1024, 64, 64, true);
-            mma3(tmem + kColD2, sRA, sRA + 32 * 1024, sRA + 64 * 1024, sRA + 96 * 1024, 64, 128, false);
+            mma3_ts(tmem + kSO, tmem + kSX, tmem + kSUlo, sRB, sRB + 16 * 1024, 64, 64, true);
+            mma3_ts(tmem + kSShi, tmem + kSX, tmem + kSUlo, sRA, sRA + 32 * 1024, 64, 128, false);
         }
         float zg[32];
         if constexpr (sizeof(Act) == 2) {
@@ -842,8 +928,8 @@ __device__ __forceinline__ void advance_state(const PrefillArgs &a, Ctx &x, int 
         // ---------------- outputs (gated RMSNorm) and the state update
         {
             float o32[32];
-            tmem_ld16(tmem + tq + kColOT + 32 * half, o32);
-            tmem_ld16(tmem + tq + kColOT + 32 * half + 16, o32 + 16);
+            tmem_ld16(tmem + tq + kSO + 32 * half, o32);
+            tmem_ld16(tmem + tq + kSO + 32 * half + 16, o32 + 16);
             // per-token sums of squares over this warp's 32 columns: reduce-scatter, lane l ends with token l
             float v[32];
 #pragma unroll
@@ -881,7 +967,7 @@ __device__ __forceinline__ void advance_state(const PrefillArgs &a, Ctx &x, int 
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 float d16[16];
-                tmem_ld16(tmem + tq + kColD2 + 64 * half + 16 * q4, d16);
+                tmem_ld16(tmem + tq + kSShi + 64 * half + 16 * q4, d16);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) St[16 * q4 + e] = fmaf(gc, St[16 * q4 + e], d16[e]);
             }
@@ -897,8 +983,7 @@ __device__ __forceinline__ void advance_state(const PrefillArgs &a, Ctx &x, int 
         *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(St[4 * q], St[4 * q + 1], St[4 * q + 2], St[4 * q + 3]);
 }
 
-// grid (3 x pairs): for pair p0 + blockIdx.x / 3, CTA 0 and 1 prepare (even / odd chunks), CTA 2 carries
-// the state
+// grid: ns x H_k x NP preparation CTAs (claiming work items), then ns x H_v state CTAs
 template <typename Act>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -908,8 +993,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     x.tl = x.tid & 127; x.half = x.tid >> 7;           // TMEM lane of this thread, column half
     x.phase = 0;
     x.timed_out = false;
-    const int role = blockIdx.x % 3, pair = a.pair0 + blockIdx.x / 3;
-    const int s = pair / a.Hv, h = pair % a.Hv;
+    const int n_prep = a.ns * a.Hk * a.np;
+    const bool prep = (int)blockIdx.x < n_prep;
+    const int sidx = (int)blockIdx.x - n_prep;
 
     if (x.wid == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
@@ -930,8 +1016,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     x.tmem = *reinterpret_cast<volatile uint32_t *>(sm + kTmemSlot);
     x.tq = (uint32_t)(32 * (x.wid & 3)) << 16;        // this warp's TMEM lane quarter
 
-    if (role < 2) prepare<Act>(a, x, s, h, role);
-    else advance_state<Act>(a, x, s, h);
+    if (prep) prepare<Act>(a, x, blockIdx.x);
+    else advance_state<Act>(a, x, a.slot0 + sidx / a.Hv, sidx % a.Hv);
 
     if (x.timed_out && x.tid == 0 && a.d_status) atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TIMEOUT));
     fence_before_sync();
@@ -972,21 +1058,26 @@ int prefill_check(const gdn_dims &d, std::string &why) {
         why = "prefill: n_slots * n_tokens must be below 2^31";
         return GDN_ERR_SHAPE;
     }
-    if (3LL * d.n_slots * d.n_v_heads > 2147483647LL) {
-        why = "prefill: too many (slot, value head) pairs";
+    if (d.n_v_heads + d.n_qk_heads > 150) {
+        why = "prefill: a slot's CTAs (H_v state + at least H_k preparation) must fit on the device at once";
         return GDN_ERR_SHAPE;
     }
     return GDN_OK;
 }
 
+// workspace: ring flags of every (slot, value head), then one work counter per launch
+static size_t counters_offset_bytes(const gdn_dims &d) {
+    return (size_t)d.n_slots * d.n_v_heads * kFlagWords * sizeof(int);
+}
 static size_t ring_offset_bytes(const gdn_dims &d) {
-    const size_t flags = (size_t)d.n_slots * d.n_v_heads * kFlagWords * sizeof(int);
-    return (flags + 255) & ~(size_t)255;
+    const size_t head = counters_offset_bytes(d) + (size_t)d.n_slots * sizeof(int);
+    return (head + 255) & ~(size_t)255;
 }
 
 size_t prefill_workspace_bytes(const gdn_dims &d) {
     const size_t pairs = (size_t)d.n_slots * d.n_v_heads;
-    return ring_offset_bytes(d) + pairs * kRing * kSlotBytes + pairs * 2 * kVtFloats * sizeof(float);
+    return ring_offset_bytes(d) + pairs * kRing * kSlotBytes +
+           (size_t)d.n_slots * d.n_qk_heads * kMaxPrep * kVtFloats * sizeof(float);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once
@@ -1018,6 +1109,7 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
     a.ring_offset = ring_offset_bytes(d);
     a.scratch_vt = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + a.ring_offset +
                                              (size_t)d.n_slots * d.n_v_heads * kRing * kSlotBytes);
+    a.np = 1;
     a.d_status = d_status;
     // Fault injection for tests, on the host: GDN_FAULT_DROP_CHUNK=<c> makes the preparation CTAs never
     // publish chunk c, so the state CTA's bounded wait runs out and the call reports GDN_ERR_TIMEOUT
@@ -1053,16 +1145,25 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmemBytes)) != cudaSuccess)
         return e;
-    const int pairs_per_launch = (sms * per_sm) / 3;
-    if (pairs_per_launch < 1) return cudaErrorCooperativeLaunchTooLarge;
-    // fresh ring flags (and slot decays) for every (slot, head)
+    // every CTA of a launch must be resident at once: per slot H_k x NP preparation CTAs + H_v state CTAs
+    // (NP sizes the pool of preparation CTAs; they share all the slot's work items)
+    const int max_ctas = sms * per_sm;
+    int np = (max_ctas - a.Hv) / a.Hk;
+    if (np > kMaxPrep) np = kMaxPrep;
+    if (np < 1) return cudaErrorCooperativeLaunchTooLarge;
+    a.np = np;
+    const int per_slot = a.Hk * np + a.Hv;
+    const int slots_per_launch = max_ctas / per_slot;
+    // fresh ring flags (and slot decays) for every (slot, head), fresh work counters
     if ((e = cudaMemsetAsync(workspace, 0, a.ring_offset, stream)) != cudaSuccess) return e;
-    const int pairs = a.B * a.Hv;
-    for (int p0 = 0; p0 < pairs; p0 += pairs_per_launch) {
-        a.pair0 = p0;
-        const int np = pairs - p0 < pairs_per_launch ? pairs - p0 : pairs_per_launch;
+    int *counters = reinterpret_cast<int *>(static_cast<unsigned char *>(workspace) + counters_offset_bytes(d));
+    for (int s0 = 0, li = 0; s0 < a.B; s0 += slots_per_launch, ++li) {
+        a.slot0 = s0;
+        const int ns = a.B - s0 < slots_per_launch ? a.B - s0 : slots_per_launch;
+        a.ns = ns;
+        a.counter = counters + li;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(3 * np, 1, 1);
+        cfg.gridDim = dim3(ns * per_slot, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = kSmemBytes;
         cfg.stream = stream;

@@ -173,13 +173,13 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims *dims);
  * gdn_verify_forward with T = L, no capture (a prefill-only cache skips the
  * rollback tensors: internal.h, create_target_cache, prefill_only).  Updates
  * state and conv_state in place.  workspace: caller-owned device scratch of
- * at least gdn_prefill_workspace_bytes(dims) bytes, 256-byte aligned (about
- * 1.06 MiB per (slot, value head) pair: a ring of operand slots between the
- * CTAs of a pair, their flags and a v scratch); its contents need no
- * initialisation and are garbage afterwards.  The call enqueues, on `stream`,
- * a memset of the ring flags, one cooperative launch per group of (slot,
- * value head) pairs that fits on the device at once, and a small kernel that
- * advances conv_state; calls sharing a workspace must be ordered.  Supported:
+ * at least gdn_prefill_workspace_bytes(dims) bytes, 256-byte aligned (2 MiB
+ * per (slot, value head): a ring of operand slots with its flags; 256 KiB per
+ * (slot, key head): v scratch); its contents need no initialisation and are
+ * garbage afterwards.  The call enqueues, on `stream`, a memset of the ring
+ * flags, one cooperative launch per group of slots that fits on the device
+ * at once, and a small kernel that advances conv_state; calls sharing a
+ * workspace must be ordered.  Supported:
  * d_k == d_v == 128, W == 4, act_dtype bf16 or f32.
  */
 int gdn_prefill_chunked(const gdn_dims *dims, const gdn_layer_params *params,

@@ -14,7 +14,7 @@ from workloads.synth import Shape, make_inputs
 
 pytestmark = pytest.mark.gpu
 
-SHAPE = Shape("prefill_static", n_slots=2, n_qk_heads=2, n_v_heads=6, d_k=128, d_v=128, n_tokens=200,
+SHAPE = Shape("prefill_static", n_slots=1, n_qk_heads=2, n_v_heads=6, d_k=128, d_v=128, n_tokens=200,
               act="bf16", seed=47)
 
 
@@ -52,6 +52,7 @@ def _static(shape, inp, status):
 
 
 def test_static_scratch_prefill_matches_workspace_prefill_on_two_calls():
+    assert gdn.gdn_prefill_workspace_bytes(dims_of(SHAPE)) <= gdn.PREFILL_STATIC_SCRATCH_BYTES
     inp = make_inputs(SHAPE)
     ref = _with_workspace(SHAPE, inp)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
