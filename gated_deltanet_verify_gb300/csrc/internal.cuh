@@ -44,7 +44,7 @@ struct PrefillArgs {
     CUtensorMap z_map;                // z as a 2-D tensor [B*L rows][H_v*d_v], box 128 x 64
     int B, Hk, Hv, L, C, r;           // L: prompt tokens per slot; C: conv channels; r = Hv / Hk
     int slot0, ns;                    // slots of this launch: slot0 .. slot0 + ns - 1
-    int np;                           // preparation CTAs per key head
+    int n_prep;                       // preparation CTAs of this launch
     int *counter;                     // work counter of this launch (zeroed before the launch)
     int drop_chunk;                   // fault injection: this chunk is never published (-1: none)
     float rms_eps, l2_eps, q_scale;

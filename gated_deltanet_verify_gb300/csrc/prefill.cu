@@ -20,7 +20,7 @@
 //
 // Work split.  Everything but U, O and S depends only on the chunk itself, so
 // three CTAs serve one (slot, value head):
-//   * preparation CTAs (NP per key head) claim (chunk, key head) work items
+//   * preparation CTAs (every SM the state CTAs leave) claim (chunk, key head) work items
 //     in chunk order from a counter; per item the q/k work is done once for
 //     the r value heads that share the key head (raw window by TMA,
 //     conv + SiLU into TMEM, L2 norms, G = [K; Q] K^T kept in TMEM), then per
@@ -983,7 +983,7 @@ __device__ __forceinline__ void advance_state(const PrefillArgs &a, Ctx &x, int 
         *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(St[4 * q], St[4 * q + 1], St[4 * q + 2], St[4 * q + 3]);
 }
 
-// grid: ns x H_k x NP preparation CTAs (claiming work items), then ns x H_v state CTAs
+// grid: n_prep preparation CTAs (claiming work items), then ns x H_v state CTAs
 template <typename Act>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -993,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     x.tl = x.tid & 127; x.half = x.tid >> 7;           // TMEM lane of this thread, column half
     x.phase = 0;
     x.timed_out = false;
-    const int n_prep = a.ns * a.Hk * a.np;
+    const int n_prep = a.n_prep;
     const bool prep = (int)blockIdx.x < n_prep;
     const int sidx = (int)blockIdx.x - n_prep;
 
@@ -1109,7 +1109,7 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
     a.ring_offset = ring_offset_bytes(d);
     a.scratch_vt = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + a.ring_offset +
                                              (size_t)d.n_slots * d.n_v_heads * kRing * kSlotBytes);
-    a.np = 1;
+    a.n_prep = 1;
     a.d_status = d_status;
     // Fault injection for tests, on the host: GDN_FAULT_DROP_CHUNK=<c> makes the preparation CTAs never
     // publish chunk c, so the state CTA's bounded wait runs out and the call reports GDN_ERR_TIMEOUT
@@ -1145,15 +1145,12 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmemBytes)) != cudaSuccess)
         return e;
-    // every CTA of a launch must be resident at once: per slot H_k x NP preparation CTAs + H_v state CTAs
-    // (NP sizes the pool of preparation CTAs; they share all the slot's work items)
+    // every CTA of a launch must be resident at once: H_v state CTAs per slot, and the remaining
+    // SMs as a pool of preparation CTAs that share all the launch's work items
     const int max_ctas = sms * per_sm;
-    int np = (max_ctas - a.Hv) / a.Hk;
-    if (np > kMaxPrep) np = kMaxPrep;
-    if (np < 1) return cudaErrorCooperativeLaunchTooLarge;
-    a.np = np;
-    const int per_slot = a.Hk * np + a.Hv;
-    const int slots_per_launch = max_ctas / per_slot;
+    if (a.Hv + 1 > max_ctas) return cudaErrorCooperativeLaunchTooLarge;
+    int slots_per_launch = max_ctas / (a.Hv + 2 * a.Hk);
+    if (slots_per_launch < 1) slots_per_launch = 1;
     // fresh ring flags (and slot decays) for every (slot, head), fresh work counters
     if ((e = cudaMemsetAsync(workspace, 0, a.ring_offset, stream)) != cudaSuccess) return e;
     int *counters = reinterpret_cast<int *>(static_cast<unsigned char *>(workspace) + counters_offset_bytes(d));
@@ -1162,8 +1159,11 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
         const int ns = a.B - s0 < slots_per_launch ? a.B - s0 : slots_per_launch;
         a.ns = ns;
         a.counter = counters + li;
+        int n_prep = max_ctas - ns * a.Hv;
+        if (n_prep > ns * a.Hk * kMaxPrep) n_prep = ns * a.Hk * kMaxPrep;       // v^T scratch areas
+        a.n_prep = n_prep;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(ns * per_slot, 1, 1);
+        cfg.gridDim = dim3(n_prep + ns * a.Hv, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = kSmemBytes;
         cfg.stream = stream;
