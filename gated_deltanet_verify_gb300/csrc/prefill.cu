@@ -60,7 +60,7 @@ constexpr int kThreads = 256;
 constexpr int kSpinLimit = 1 << 20;    // try_wait rounds before an mbarrier wait gives up
 constexpr int kFlagSpin = 1 << 21;     // polls (with back-off, about a second) before a ring-flag wait gives up
 constexpr int kTmemCols = 512;
-constexpr int kRing = 8;               // ring slots per (slot, value head)
+constexpr int kRing = 4;               // ring slots per (slot, value head)
 constexpr int kMaxPrep = 8;            // preparation CTAs per key head, at most
 
 // dynamic shared memory carve-up (bytes)
@@ -104,7 +104,7 @@ constexpr uint32_t kSlotP = 128 * 1024;        // P planes (64 x 64), 32 KB
 constexpr uint32_t kSlotKd = 160 * 1024;       // (Gamma_C / Gamma) K planes, as (128 x 64), 64 KB
 constexpr uint32_t kSlotU = 224 * 1024;        // U~^T fp32 [128][64], 32 KB
 constexpr size_t kSlotBytes = 256 * 1024;
-// per (slot, value head): ring flags and the chunk decays (ints: full[8], empty[8], Gamma_C[8] bits)
+// per (slot, value head): ring flags and the chunk decays (ints: full[4], empty[4], Gamma_C[4] bits)
 constexpr size_t kFlagWords = 32;
 static_assert(kFlagWords >= 3 * kRing, "flag words");
 // per (slot, key head, preparation CTA): v^T scratch (128 channels x 64 tokens)
@@ -431,9 +431,9 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) 
         }
     };
 
-    // A published (chunk, head) is released one phase later, so its stores drain while the next
-    // phase runs: every thread fences its own stores, the CTA synchronises, thread 0 releases the
-    // flag.  pend_* are uniform across the CTA.
+    // A published (chunk, head) is released once the next head's W/U~ products are done, so its stores
+    // drain while that work runs: every thread fences its own stores, the CTA synchronises, thread 0
+    // releases the flag.  pend_* are uniform across the CTA.
     int pend_slot = -1, pend_c = 0, pend_h = 0, pend_s = 0;
     float pend_gamma = 0.f;
     auto fence_pending = [&]() {
@@ -523,11 +523,9 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) 
             if (lane < 16) ssq[(ch >> 5) * kC + tb + lane] = y2[0];   // token tb + lane, channel block ch/32
         }
         tmem_wait_st();
-        fence_pending();
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
-        release_pending();
         // inverse L2 norms of the q and k rows (a zero padded row stays zero)
         if (tid < 2 * kC) {
             const int t = tid & (kC - 1), part = tid >> 6;
@@ -606,9 +604,14 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) 
                 for (int q4 = 0; q4 < 4; ++q4)
                     dv[q4] = make_float4(yv[4 * q4], yv[4 * q4 + 1], yv[4 * q4 + 2], yv[4 * q4 + 3]);
             }
-            fence_pending();
             __syncthreads();
-            release_pending();
+            // this thread's row of v^T for the A2 operand below, fetched ahead of the readout
+            float4 vpre[8];
+            {
+                const float4 *vrow = reinterpret_cast<const float4 *>(vT + tl * kC + 32 * half);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) vpre[q4] = vrow[q4];
+            }
 
             // ---------------- (c) A and the masked, decayed P from G
             {
@@ -634,14 +637,6 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) 
                 }
             }
             __syncthreads();
-
-            // this thread's row of v^T for the A2 operand below, fetched before the inversion
-            float4 vpre[8];
-            {
-                const float4 *vrow = reinterpret_cast<const float4 *>(vT + tl * kC + 32 * half);
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) vpre[q4] = vrow[q4];
-            }
             // A1 = (diag(beta Gamma) K^)^T, A2 = (diag(beta) V)^T -> RA: warp (quarter, half) builds rows
             // 32 quarter .. +31 of tokens 32 half .. +31
             auto build_a12 = [&]() {
@@ -723,7 +718,10 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) 
                 mma3(tmem + kColWT, sRA, sRA + 32 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
                 mma3(tmem + kColUT, sRA + 64 * 1024, sRA + 96 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
             }
+            fence_pending();                   // the previous head's stores were issued a whole phase ago
             x.commit_wait();
+            __syncthreads();
+            release_pending();
 
             // the A region is free: fetch the next tile (next head's v, or the next chunk's q, k) and gates
             if (hi + 1 < R) {

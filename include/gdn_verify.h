@@ -173,7 +173,7 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims *dims);
  * gdn_verify_forward with T = L, no capture (a prefill-only cache skips the
  * rollback tensors: internal.h, create_target_cache, prefill_only).  Updates
  * state and conv_state in place.  workspace: caller-owned device scratch of
- * at least gdn_prefill_workspace_bytes(dims) bytes, 256-byte aligned (2 MiB
+ * at least gdn_prefill_workspace_bytes(dims) bytes, 256-byte aligned (1 MiB
  * per (slot, value head): a ring of operand slots with its flags; 256 KiB per
  * (slot, key head): v scratch); its contents need no initialisation and are
  * garbage afterwards.  The call enqueues, on `stream`, a memset of the ring
