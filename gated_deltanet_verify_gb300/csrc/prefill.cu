@@ -431,9 +431,9 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) 
         }
     };
 
-    // A published (chunk, head) is released once the next head's W/U~ products are done, so its stores
-    // drain while that work runs: every thread fences its own stores, the CTA synchronises, thread 0
-    // releases the flag.  pend_* are uniform across the CTA.
+    // A published (chunk, head) is released one phase later (after the next head's v conv, or the next
+    // item's q/k conv), so its stores drain while that runs: every thread fences its own stores, the CTA
+    // synchronises, thread 0 releases the flag.  pend_* are uniform across the CTA.
     int pend_slot = -1, pend_c = 0, pend_h = 0, pend_s = 0;
     float pend_gamma = 0.f;
     auto fence_pending = [&]() {
@@ -523,9 +523,11 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) 
             if (lane < 16) ssq[(ch >> 5) * kC + tb + lane] = y2[0];   // token tb + lane, channel block ch/32
         }
         tmem_wait_st();
+        fence_pending();
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
+        release_pending();
         // inverse L2 norms of the q and k rows (a zero padded row stays zero)
         if (tid < 2 * kC) {
             const int t = tid & (kC - 1), part = tid >> 6;
@@ -604,7 +606,9 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) 
                 for (int q4 = 0; q4 < 4; ++q4)
                     dv[q4] = make_float4(yv[4 * q4], yv[4 * q4 + 1], yv[4 * q4 + 2], yv[4 * q4 + 3]);
             }
+            fence_pending();
             __syncthreads();
+            release_pending();
             // this thread's row of v^T for the A2 operand below, fetched ahead of the readout
             float4 vpre[8];
             {
@@ -718,10 +722,7 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) 
                 mma3(tmem + kColWT, sRA, sRA + 32 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
                 mma3(tmem + kColUT, sRA + 64 * 1024, sRA + 96 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
             }
-            fence_pending();                   // the previous head's stores were issued a whole phase ago
             x.commit_wait();
-            __syncthreads();
-            release_pending();
 
             // the A region is free: fetch the next tile (next head's v, or the next chunk's q, k) and gates
             if (hi + 1 < R) {
