@@ -78,6 +78,42 @@ def tree_verify_bytes(s) -> int:
     return n
 
 
+def lazy_verify_bytes(s) -> int:
+    """Compulsory bytes of an outputs-only verify: the state and conv state read once,
+    activations in and out, parameters; nothing else is written."""
+    st = s.n_slots * s.n_v_heads * s.d_v * s.d_k * 4
+    return verify_bytes(s, capture=False) - st - s.n_slots * (s.conv_width - 1) * s.conv_channels * 4
+
+
+def lazy_step_bytes(s, trims) -> int:
+    """Compulsory bytes of a lazy verify with a pending batch: the outputs-only verify
+    plus, per slot, the committed state and conv state written and the pending
+    batch's accepted tokens (qkv, alpha, beta_raw) read."""
+    a = 2 if s.act == "bf16" else 4
+    st = s.n_v_heads * s.d_v * s.d_k * 4
+    n = lazy_verify_bytes(s) + 4 * s.n_slots
+    for tr in np.asarray(trims).reshape(-1):
+        keep = s.n_tokens - int(tr)
+        n += st + (s.conv_width - 1) * s.conv_channels * 4 + keep * (s.conv_channels + 2 * s.n_v_heads) * a
+    return n
+
+
+def commit_bytes(s, trims) -> int:
+    """Compulsory bytes of the lazy commit: per slot with a valid trim, the state read and
+    written, the conv state read and written, and the accepted tokens' qkv, alpha and
+    beta_raw read again; the parameters once."""
+    a = 2 if s.act == "bf16" else 4
+    st = s.n_v_heads * s.d_v * s.d_k * 4
+    n = 0
+    for tr in np.asarray(trims).reshape(-1):
+        if 0 <= tr < s.n_tokens:
+            keep = s.n_tokens - int(tr)
+            n += 2 * st + 2 * (s.conv_width - 1) * s.conv_channels * 4
+            n += keep * (s.conv_channels + 2 * s.n_v_heads) * a
+    n += 4 * s.n_slots + s.conv_width * s.conv_channels * 4 + 2 * s.n_v_heads * 4
+    return n
+
+
 def rollback_bytes(s, trims) -> int:
     per_slot = 2 * (s.n_v_heads * s.d_v * s.d_k * 4 + (s.conv_width - 1) * s.conv_channels * 4)
     return int(np.count_nonzero(np.asarray(trims))) * per_slot + 4 * s.n_slots
@@ -254,7 +290,11 @@ class VerifyWorkload:
         self.shape = s = shape
         self.layers = s.n_layers
         self.tree = s.name.startswith("tree")          # draft-tree verify + rollback to the accepted node
-        per_set = (tree_verify_bytes(s) if self.tree else verify_bytes(s)) * self.layers
+        # lazy capture: one launch per step commits the pending batch (this buffer set's previous
+        # one, with its trims) and verifies the new one, outputs only
+        self.lazy = s.name.startswith("lazy")
+        per_set = (tree_verify_bytes(s) if self.tree else
+                   lazy_step_bytes(s, [0] * s.n_slots) if self.lazy else verify_bytes(s)) * self.layers
         self.n_sets = 1 if per_set > 3 * l2_bytes else int(min(64, -(-3 * l2_bytes // per_set) + 1))
         self.dims = gdn.make_dims(s.n_slots, s.n_qk_heads, s.n_v_heads, s.d_k, s.d_v, s.n_tokens,
                                   gdn.GDN_BF16 if s.act == "bf16" else gdn.GDN_F32)
@@ -275,7 +315,7 @@ class VerifyWorkload:
             for li in range(self.layers):
                 x = to_device(self.host_inputs[li if self.layers > 1 else 0], device)
                 x["trim"] = torch.from_numpy(trims[k, li].astype(np.int32)).to(device)
-                x.update(empty_outputs(s, device))
+                x.update(empty_outputs(s, device, capture=not self.lazy))
                 if self.tree:
                     x["parent"] = torch.from_numpy(self.parents).to(device)
                     x["cap_conv"] = torch.empty((s.n_slots, s.n_tokens, s.conv_width - 1, s.conv_channels),
@@ -285,7 +325,7 @@ class VerifyWorkload:
                 layers.append(x)
             self.sets.append(layers)
         self.tokens_per_step = s.n_slots * s.n_tokens
-        self.kernels_per_step = 2 * self.layers
+        self.kernels_per_step = (1 if self.lazy else 2) * self.layers
 
     def verify(self, k, li, stream):
         x = self.sets[k][li]
@@ -294,11 +334,19 @@ class VerifyWorkload:
                                      x["parent"], x["state"], x["conv_state"], x["cap_state"], x["cap_conv"],
                                      x["out"], x["status"], stream)
             return
+        if self.lazy:
+            self.gdn.gdn_verify_lazy(self.dims, x["params"], x["qkv"], x["z"], x["alpha"], x["beta_raw"],
+                                     x["state"], x["conv_state"], x["out"], x["status"], stream,
+                                     prev_trim=x["trim"], prev_qkv=x["qkv"], prev_alpha=x["alpha"],
+                                     prev_beta_raw=x["beta_raw"])
+            return
         self.gdn.gdn_verify_forward(self.dims, x["params"], x["qkv"], x["z"], x["alpha"], x["beta_raw"], x["state"],
                                     x["conv_state"], x["cap_state"], x["cap_conv"], x["out"], x["status"], stream)
 
     def rollback(self, k, li, stream):
         x = self.sets[k][li]
+        if self.lazy:                   # the commit rides in the next verify
+            return
         fn = self.gdn.gdn_rollback_tree if self.tree else self.gdn.gdn_rollback
         fn(self.dims, x["trim"], x["state"], x["conv_state"], x["cap_state"], x["cap_conv"], x["status"], stream)
 
@@ -308,6 +356,8 @@ class VerifyWorkload:
             self.rollback(k, li, stream)
 
     def step_bytes(self, k):
+        if self.lazy:
+            return sum(lazy_step_bytes(self.shape, self.trims[k][li]) for li in range(self.layers))
         vb = tree_verify_bytes(self.shape) if self.tree else verify_bytes(self.shape)
         moved = (self.trims[k] >= 0) if self.tree else self.trims[k]     # slots whose rollback copies
         return sum(vb + rollback_bytes(self.shape, moved[li]) for li in range(self.layers))
@@ -542,6 +592,8 @@ def run_cuda(args):
     n_launch = max(1, min(64, 8 * wl.n_sets * wl.layers))
     if args.workload == "prefill":
         kdur = {"prefill": kernel_duration(torch, wl, "prefill", 2)}
+    elif wl.lazy:
+        kdur = {"lazy_verify": kernel_duration(torch, wl, "verify", n_launch)}
     else:
         kdur = {"verify": kernel_duration(torch, wl, "verify", n_launch),
                 "rollback": kernel_duration(torch, wl, "rollback", n_launch)}
@@ -552,6 +604,11 @@ def run_cuda(args):
     hbm, peak_kind = peaks()
     if args.workload == "prefill":
         dom, dom_bytes, dom_src = "prefill", prefill_bytes(shape), ["prefill.cu", "internal.cuh"]
+    elif wl.lazy:
+        # the timed launches cycle over every buffer set's pending trims: their mean bytes
+        dom = "lazy_verify"
+        dom_bytes = float(np.mean([lazy_step_bytes(shape, t) for t in wl.trims.reshape(-1, shape.n_slots)]))
+        dom_src = ["verify.cu", "internal.cuh"]
     else:
         dom, dom_bytes, dom_src = "verify", (tree_verify_bytes(shape) if getattr(wl, "tree", False)
                                              else verify_bytes(shape)), ["verify.cu", "internal.cuh"]
@@ -568,7 +625,10 @@ def run_cuda(args):
                          f"{shape.n_qk_heads} QK / {shape.n_v_heads} V heads, d_k=d_v={shape.d_k}, "
                          f"{shape.n_tokens} tokens"),
             "act_dtype": shape.act, "state_dtype": "f32",
-            "step": "verify+rollback" if args.workload != "prefill" else "chunked prefill",
+            "step": ("chunked prefill" if args.workload == "prefill" else
+                     "lazy verify: commit of the pending batch (accepted-prefix re-run) + outputs of the new one"
+                     if wl.lazy else
+                     "verify+rollback"),
             "l2": (f"rotating {wl.n_sets} buffer sets, {wl.n_sets * wl.step_bytes(0) / 1e6:.0f} MB "
                    f"touched per rotation (> 3x L2 {l2 / 2**20:.0f} MiB)"),
             "timing": f"CUDA events around CUDA-graph replays of {graph_len} steps",
@@ -625,6 +685,10 @@ def _oracle_pass(shape, x, heads, n_threads, trims):
     import oracle
     if shape.name == "prefill":
         oracle.verify(shape, x, capture=False, head_mask=heads, n_threads=n_threads)
+        return
+    if shape.name.startswith("lazy"):
+        oracle.verify(shape, x, capture=False, head_mask=heads, n_threads=n_threads)
+        oracle.commit_lazy(shape, x, trims, head_mask=heads, n_threads=n_threads)
         return
     if shape.name.startswith("tree"):
         r = oracle.verify_tree(shape, x, make_parents(shape, "spine"), head_mask=heads, n_threads=n_threads)

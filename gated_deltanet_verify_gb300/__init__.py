@@ -35,7 +35,7 @@ GDN_F32 = 0
 GDN_BF16 = 1
 
 EXPORTED_SYMBOLS = ("gdn_verify_forward", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_tree",
-                    "gdn_prefill_workspace_bytes",
+                    "gdn_verify_lazy", "gdn_commit_lazy", "gdn_prefill_workspace_bytes",
                     "gdn_prefill_chunked", "gdn_prefill_chunked_static", "gdn_last_error", "gdn_version")
 
 # size of the library's built-in prefill scratch (GDN_PREFILL_STATIC_SCRATCH_BYTES)
@@ -87,6 +87,10 @@ def lib() -> ctypes.CDLL:
         L.gdn_verify_tree.restype = ip
         L.gdn_rollback_tree.argtypes = [ctypes.POINTER(Dims)] + [vp] * 7
         L.gdn_rollback_tree.restype = ip
+        L.gdn_verify_lazy.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 13
+        L.gdn_verify_lazy.restype = ip
+        L.gdn_commit_lazy.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 8
+        L.gdn_commit_lazy.restype = ip
         L.gdn_prefill_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
         L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
         L.gdn_prefill_chunked.argtypes = ([ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 8 +
@@ -159,6 +163,24 @@ def gdn_rollback_tree(dims: Dims, d_accept, state, conv_state, cap_state, cap_co
                       stream=None) -> None:
     _check(lib().gdn_rollback_tree(ctypes.byref(dims), _ptr(d_accept), _ptr(state), _ptr(conv_state),
                                    _ptr(cap_state), _ptr(cap_conv), _ptr(d_status), _stream(stream)))
+
+
+def gdn_verify_lazy(dims: Dims, params: LayerParams, qkv, z, alpha, beta_raw, state, conv_state, out,
+                    d_status=None, stream=None, prev_trim=None, prev_qkv=None, prev_alpha=None,
+                    prev_beta_raw=None) -> None:
+    """Outputs-only verify; with prev_trim (device int32[B]) it first commits the
+    pending batch (prev_qkv, prev_alpha, prev_beta_raw) into state / conv_state."""
+    _check(lib().gdn_verify_lazy(ctypes.byref(dims), ctypes.byref(params), _ptr(prev_trim), _ptr(prev_qkv),
+                                 _ptr(prev_alpha), _ptr(prev_beta_raw), _ptr(qkv), _ptr(z), _ptr(alpha),
+                                 _ptr(beta_raw), _ptr(state), _ptr(conv_state), _ptr(out), _ptr(d_status),
+                                 _stream(stream)))
+
+
+def gdn_commit_lazy(dims: Dims, params: LayerParams, d_trim, qkv, alpha, beta_raw, state, conv_state,
+                    d_status=None, stream=None) -> None:
+    _check(lib().gdn_commit_lazy(ctypes.byref(dims), ctypes.byref(params), _ptr(d_trim), _ptr(qkv),
+                                 _ptr(alpha), _ptr(beta_raw), _ptr(state), _ptr(conv_state), _ptr(d_status),
+                                 _stream(stream)))
 
 
 def gdn_prefill_workspace_bytes(dims: Dims) -> int:

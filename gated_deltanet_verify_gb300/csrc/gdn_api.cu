@@ -134,7 +134,9 @@ const char *gdn_version(void) { return "gdn-verify 0.1.0 (sm_103a)"; }
 static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, const void *qkv, const void *z,
                        const void *alpha, const void *beta_raw, const int32_t *d_parent, float *state,
                        float *conv_state, float *cap_state, float *cap_conv, void *out, int *d_status,
-                       void *stream) {
+                       void *stream, int mode = gdn::kChain, const int32_t *d_trim = nullptr,
+                       const void *qkv_prev = nullptr, const void *alpha_prev = nullptr,
+                       const void *beta_prev = nullptr) {
     g_err.clear();
     int rc = check_common(dims);
     if (rc) return rc;
@@ -145,9 +147,14 @@ static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, con
     if (d.d_v % 8 || d.d_v > 256) return fail(GDN_ERR_SHAPE, "d_v must be a multiple of 8 up to 256 (got %d)", d.d_v);
     if (d.n_tokens > 64) return fail(GDN_ERR_SHAPE, "n_tokens must be <= 64 for verify (got %d)", d.n_tokens);
     if (d.n_slots > 65535) return fail(GDN_ERR_SHAPE, "n_slots must be <= 65535");
-    if (!qkv || !z || !alpha || !beta_raw || !state || !conv_state || !out)
+    const bool commit = mode == gdn::kCommit;
+    const bool pending = mode == gdn::kLazy && d_trim != nullptr;
+    if (!qkv || (!z && !commit) || !alpha || !beta_raw || !state || !conv_state || (!out && !commit))
         return fail(GDN_ERR_ARG, "a required buffer pointer is NULL");
-    const void *ptrs[] = {qkv, z, alpha, beta_raw, state, conv_state, cap_state, cap_conv, out};
+    if (pending && (!qkv_prev || !alpha_prev || !beta_prev))
+        return fail(GDN_ERR_ARG, "a pending batch needs its qkv, alpha and beta_raw");
+    const void *ptrs[] = {qkv, z, alpha, beta_raw, state, conv_state, cap_state, cap_conv, out, qkv_prev,
+                          alpha_prev, beta_prev};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return fail(GDN_ERR_ALIGN, "buffer %p is not 16-byte aligned", p);
     const int r = d.n_v_heads / d.n_qk_heads;
@@ -155,20 +162,25 @@ static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, con
     const int P = gdn::verify_parts_per_head(d.n_slots, d.n_v_heads, r, d.d_v, info.sms);
     if (P == 0) return fail(GDN_ERR_SHAPE, "H_v/H_k = %d is too large for one thread-block cluster", r);
     const int act_bytes = d.act_dtype == GDN_BF16 ? 2 : 4;
-    const size_t smem = gdn::verify_smem_bytes(d.n_tokens, d.d_k, d.d_v, P, act_bytes, d_parent != nullptr);
+    // a lazy verify with a pending batch runs up to 2T tokens through shared memory
+    const int Tm = pending ? 2 * d.n_tokens : d.n_tokens;
+    const size_t smem = gdn::verify_smem_bytes(Tm, d.d_k, d.d_v, P, act_bytes, mode == gdn::kTree);
     if (info.smem_optin > 0 && smem > size_t(info.smem_optin))
         return fail(GDN_ERR_SHAPE, "verify needs %zu bytes of shared memory per CTA (max %d)", smem,
                     info.smem_optin);
 
     gdn::VerifyArgs a{};
     a.B = d.n_slots; a.Hk = d.n_qk_heads; a.Hv = d.n_v_heads; a.dk = d.d_k; a.dv = d.d_v;
-    a.T = d.n_tokens; a.Ts = d.n_tokens; a.C = int(conv_channels(&d)); a.r = r; a.P = P;
+    a.T = d.n_tokens; a.Ts = d.n_tokens; a.Tm = Tm; a.C = int(conv_channels(&d)); a.r = r; a.P = P;
     a.rms_eps = d.rms_eps; a.l2_eps = d.l2_eps; a.q_scale = d.q_scale;
     a.conv_w = params->conv_w; a.A_log = params->A_log; a.dt_bias = params->dt_bias; a.norm_w = params->norm_w;
     a.qkv = qkv; a.z = z; a.alpha = alpha; a.beta_raw = beta_raw;
     a.state = state; a.conv_state = conv_state; a.cap_state = cap_state; a.cap_conv = cap_conv; a.out = out;
     a.d_status = d_status;
     a.parent = d_parent;
+    a.trim = d_trim;
+    a.qkv_prev = qkv_prev; a.alpha_prev = alpha_prev; a.beta_prev = beta_prev;
+    a.mode = mode;
     cudaError_t e = gdn::launch_verify(a, d.act_dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "verify launch failed: %s", cudaGetErrorString(e));
     return GDN_OK;
@@ -191,7 +203,24 @@ int gdn_verify_tree(const gdn_dims *dims, const gdn_layer_params *params, const 
     if (!cap_state || !cap_conv) return fail(GDN_ERR_NO_CAPTURE, "a tree verify needs cap_state and cap_conv");
     // state and conv_state are only read (the kernel takes them through the shared argument block)
     return verify_impl(dims, params, qkv, z, alpha, beta_raw, d_parent, const_cast<float *>(state),
-                       const_cast<float *>(conv_state), cap_state, cap_conv, out, d_status, stream);
+                       const_cast<float *>(conv_state), cap_state, cap_conv, out, d_status, stream, gdn::kTree);
+}
+
+int gdn_verify_lazy(const gdn_dims *dims, const gdn_layer_params *params, const int32_t *d_prev_trim,
+                    const void *prev_qkv, const void *prev_alpha, const void *prev_beta_raw, const void *qkv,
+                    const void *z, const void *alpha, const void *beta_raw, float *state, float *conv_state,
+                    void *out, int *d_status, void *stream) {
+    return verify_impl(dims, params, qkv, z, alpha, beta_raw, nullptr, state, conv_state, nullptr, nullptr, out,
+                       d_status, stream, gdn::kLazy, d_prev_trim, prev_qkv, prev_alpha, prev_beta_raw);
+}
+
+int gdn_commit_lazy(const gdn_dims *dims, const gdn_layer_params *params, const int32_t *d_trim,
+                    const void *qkv, const void *alpha, const void *beta_raw, float *state, float *conv_state,
+                    int *d_status, void *stream) {
+    g_err.clear();
+    if (!d_trim) return fail(GDN_ERR_ARG, "trim is NULL");
+    return verify_impl(dims, params, qkv, nullptr, alpha, beta_raw, nullptr, state, conv_state, nullptr, nullptr,
+                       nullptr, d_status, stream, gdn::kCommit, d_trim);
 }
 
 static int rollback_impl(const gdn_dims *dims, const int32_t *d_trim, float *state, float *conv_state,

@@ -12,10 +12,15 @@
 
 namespace gdn {
 
+// Verify kernel modes: the chain, a draft tree, lazy (outputs only) and the
+// lazy commit (re-run of each slot's accepted tokens).
+enum VerifyMode { kChain = 0, kTree = 1, kLazy = 2, kCommit = 3 };
+
 // Everything one verify launch needs, validated on the host.
 struct VerifyArgs {
     int B, Hk, Hv, dk, dv, T, C, r;   // C: conv channels; r = Hv / Hk
     int Ts;                           // tokens per slot in the activation buffers (>= T)
+    int Tm;                           // tokens the shared memory holds (T; 2T for a lazy verify with a pending batch)
     int P;                            // CTAs per value head (each owns d_v / P rows)
     float rms_eps, l2_eps, q_scale;
     const float *conv_w, *A_log, *dt_bias, *norm_w;
@@ -23,7 +28,10 @@ struct VerifyArgs {
     float *state, *conv_state, *cap_state, *cap_conv;
     void *out;
     int *d_status;                    // device status word (may be NULL)
-    const int32_t *parent;            // tree verify: [B][T] parent of each token (NULL: the chain)
+    const int32_t *parent;            // tree verify: [B][T] parent of each token
+    const int32_t *trim;              // lazy commit, or the pending batch of a lazy verify: [B] trims, 0 .. T-1
+    const void *qkv_prev, *alpha_prev, *beta_prev;   // lazy verify: the pending batch (same layouts)
+    int mode;                         // VerifyMode
 };
 
 struct RollbackArgs {

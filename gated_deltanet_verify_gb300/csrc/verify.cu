@@ -43,6 +43,24 @@
 //   * Programmatic dependent launch: the kernel waits on its predecessor only
 //     right before its first global read, so its launch overlaps the tail of
 //     the previous kernel in the stream.
+//
+// Modes (one template instance each)
+//   kChain  the (K+1)-token chain: outputs, optional captures, state and conv
+//           state advanced past all T tokens.
+//   kTree   a draft tree: each token runs from its parent's state; captures
+//           per node, state and conv state left as they were.
+//   kLazy   outputs of the batch only, so the state stays the one before it
+//           (lazy capture).  With a pending batch (prev buffers and trims) the
+//           launch first re-runs that batch's accepted tokens from the stored
+//           state, writes the state and conv state after them, and continues
+//           from there into the new batch: the commit of one step rides in the
+//           verify of the next.
+//   kCommit the lazy counterpart of a rollback: per slot, re-runs the first
+//           T - trim[s] tokens from the state before the batch and writes the
+//           state and conv state after them; no z, no outputs.  Since the
+//           state after token t does not depend on the tokens that follow
+//           it, this is bit-identical to a chain verify with capture followed
+//           by a rollback with the same trims.
 #include "internal.cuh"
 
 #include <cuda_bf16.h>
@@ -189,9 +207,10 @@ struct Smem {
     }
 };
 
-template <int DK, typename Act, bool TREE>
+template <int DK, typename Act, int MODE>
 __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs a) {
     static_assert(DK == 32 || DK == 64 || DK == 128, "d_k must be 32, 64 or 128");
+    constexpr bool TREE = MODE == kTree, LAZY = MODE == kLazy, COMMIT = MODE == kCommit;
     constexpr int LR = DK >= 64 ? 16 : 8;          // lanes per row group
     constexpr int NG = 32 / LR;                    // row groups per warp
     constexpr int RPG = kRowsPerWarp / NG;         // rows per group
@@ -212,7 +231,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     const int j0 = p * ROWS;                                   // first value row of this CTA
     const bool qk_writer = (h % a.r == 0) && (p == 0);        // writes the shared q/k conv channels
 
-    const Smem L(T, DK, ROWS, WARPS, P, sizeof(Act), TREE);
+    const Smem L(LAZY ? a.Tm : T, DK, ROWS, WARPS, P, sizeof(Act), TREE);   // only a lazy launch holds 2T
     Act *xs = reinterpret_cast<Act *>(smem_raw + L.xs);
     Act *zs = reinterpret_cast<Act *>(smem_raw + L.zs);
     float *cw = reinterpret_cast<float *>(smem_raw + L.cw);
@@ -252,6 +271,23 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     }
     // everything below may read what the previous kernel in the stream wrote
     grid_dependency_wait();
+    int TT = T;                                 // tokens run for this slot
+    int n_prev = 0;                             // lazy: the pending batch's accepted tokens, run first
+    if constexpr (COMMIT || LAZY) {
+        if (a.trim) {
+            const int tr = a.trim[s];           // uniform over the cluster: one slot
+            if (tr < 0 || tr >= T) {            // reported; the slot is left untouched
+                if (tid == 0 && blockIdx.x == 0 && a.d_status)
+                    atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TRIM_RANGE));
+                return;
+            }
+            if constexpr (COMMIT) TT = T - tr;
+            else {
+                n_prev = T - tr;
+                TT = n_prev + T;
+            }
+        }
+    }
 
     // ---------------------------------------------------------------- loads
     // (1) this warp's state rows, straight into registers (recurrence lane layout)
@@ -274,12 +310,14 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     {
         constexpr int kPer16 = 16 / sizeof(Act);
         const int vq = DK / kPer16, vv = ROWS / kPer16;     // 16-byte vectors per segment
-        const int per_t = 2 * vq + 2 * vv;                  // q, k, v, z
-        const Act *qkv = static_cast<const Act *>(a.qkv);
+        const int per_t = 2 * vq + vv + (COMMIT ? 0 : vv);  // q, k, v, z (no z in a commit)
         const Act *z = static_cast<const Act *>(a.z);
-        for (int i = tid; i < T * per_t; i += nthr) {
+        for (int i = tid; i < TT * per_t; i += nthr) {
             const int t = i / per_t, w = i % per_t;
-            const size_t rw = size_t(s) * a.Ts + t;
+            // tokens of the pending batch come first (lazy), then the batch itself
+            const bool pend = t < n_prev;
+            const Act *qkv = static_cast<const Act *>(pend ? a.qkv_prev : a.qkv);
+            const size_t rw = size_t(s) * a.Ts + (pend ? t : t - n_prev);
             const Act *src;
             Act *dst;
             if (w < vq) {
@@ -292,8 +330,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
                 src = qkv + rw * C + size_t(2 * Hk) * DK + size_t(h) * DV + j0 + (w - 2 * vq) * kPer16;
                 dst = xs + size_t(t) * NCH + 2 * DK + (w - 2 * vq) * kPer16;
             } else {
+                if (pend) continue;                 // no outputs for the pending tokens
                 src = z + rw * size_t(Hv) * DV + size_t(h) * DV + j0 + (w - 2 * vq - vv) * kPer16;
-                dst = zs + size_t(t) * ROWS + (w - 2 * vq - vv) * kPer16;
+                dst = zs + size_t(t - n_prev) * ROWS + (w - 2 * vq - vv) * kPer16;
             }
             cp_async16(dst, src);
         }
@@ -306,13 +345,15 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
             if (rrow < 4) cp_async16(cw + rrow * NCH + c0, a.conv_w + size_t(rrow) * C + g0);
             else cp_async16(cs + (rrow - 4) * NCH + c0, a.conv_state + (size_t(s) * 3 + (rrow - 4)) * C + g0);
         }
-        for (int i = tid; i < ROWS / 4; i += nthr) cp_async16(nw + i * 4, a.norm_w + j0 + i * 4);
+        if constexpr (!COMMIT)
+            for (int i = tid; i < ROWS / 4; i += nthr) cp_async16(nw + i * 4, a.norm_w + j0 + i * 4);
     }
     // (3) gates for this head, one token per thread
-    for (int t = tid; t < T; t += nthr) {
-        const size_t idx = (size_t(s) * a.Ts + t) * Hv + h;
-        const float al = to_f32(static_cast<const Act *>(a.alpha)[idx]);
-        const float br = to_f32(static_cast<const Act *>(a.beta_raw)[idx]);
+    for (int t = tid; t < TT; t += nthr) {
+        const bool pend = t < n_prev;
+        const size_t idx = (size_t(s) * a.Ts + (pend ? t : t - n_prev)) * Hv + h;
+        const float al = to_f32(static_cast<const Act *>(pend ? a.alpha_prev : a.alpha)[idx]);
+        const float br = to_f32(static_cast<const Act *>(pend ? a.beta_prev : a.beta_raw)[idx]);
         const float x = al + __ldg(a.dt_bias + h);
         const float sp = x > 20.0f ? x : log1pf(expf(x));               // softplus
         gs[t] = expf(-expf(__ldg(a.A_log + h)) * sp);
@@ -353,7 +394,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     {
         constexpr int QC = DK / 16;                 // 16-channel chunks per q (or k) vector
         constexpr int PER_T = 2 * QC;               // q and k items per token (divides 32)
-        const int n_items = T * PER_T;
+        const int n_items = TT * PER_T;
         const int n_round = (n_items + 31) & ~31;   // whole warps, so every lane joins the shuffles
         for (int base = wid * 32; base < n_round; base += nthr) {
             const int i = base + lane;
@@ -406,7 +447,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         }
     }
     // v: four channels of one token per item
-    for (int i = tid; i < T * (ROWS / 4); i += nthr) {
+    for (int i = tid; i < TT * (ROWS / 4); i += nthr) {
         const int t = i / (ROWS / 4), c = 2 * DK + 4 * (i % (ROWS / 4));
         float4 acc;
 #pragma unroll
@@ -427,7 +468,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         const size_t cap_token_stride = size_t(Hv) * DV * DK;
         const float q_scale = a.q_scale;
 
-        for (int t = 0; t < T; ++t) {
+        for (int t = 0; t < TT; ++t) {
             if constexpr (TREE) {
                 // the token runs from its parent's state: already in registers when the parent is t-1,
                 // else this thread's own rows of the parent's capture (or of the state before the batch)
@@ -487,7 +528,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
             const float kd = my_kind ? other : mine;       // (S^T k)_j of row my_rho
             const float qd = my_kind ? mine : other;       // (S^T q)_j of row my_rho
             const float w = beta * (vj - g * kd);           // beta (v - (g S)^T k)
-            if (my_kind == 0 && (b & 1) == 0) os[size_t(t) * ROWS + row0 + my_rho] = q_scale * fmaf(g, qd, kq * w);
+            if (!COMMIT && t >= n_prev && my_kind == 0 && (b & 1) == 0)
+                os[size_t(t - n_prev) * ROWS + row0 + my_rho] = q_scale * fmaf(g, qd, kq * w);
             // S <- g S + k w^T for the group's rows
 #pragma unroll
             for (int rho = 0; rho < RPG; ++rho) {
@@ -496,6 +538,16 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
                 for (int m = 0; m < NCL; ++m)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) S[rho][m][e] = fmaf(kk[m][e], wr, g * S[rho][m][e]);
+            }
+            if (LAZY && t + 1 == n_prev) {
+                // the pending batch is committed: its state becomes the stored one (own rows only)
+                float *dst = a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b;
+#pragma unroll
+                for (int rho = 0; rho < RPG; ++rho)
+#pragma unroll
+                    for (int m = 0; m < NCL; ++m)
+                        store4(dst + size_t(rho) * DK + 4 * LR * m,
+                               make_float4(S[rho][m][0], S[rho][m][1], S[rho][m][2], S[rho][m][3]));
             }
             if (capture) {
                 float *dst = cap_row + (size_t(s) * T + t) * cap_token_stride;
@@ -530,7 +582,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         }
         __syncwarp();
         cluster_wait_acquire();            // phase 1: every peer's mbarrier is initialised
-        {
+        if constexpr (!COMMIT) {
             // this warp's sums of o^2 per token, sent to the allp table of every CTA of this head
             const int first_rank = (h - kh * a.r) * P;
             const uint32_t allp_local = smem_u32(allp);
@@ -545,7 +597,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
                 st_async_f32(map_cluster(allp_local + off, rank), acc, map_cluster(redbar, rank));
             }
         }
-        if constexpr (!TREE) {             // a tree verify leaves the state to the rollback
+        if constexpr (!TREE && !LAZY) {    // a tree or lazy verify leaves the state as it was
             float *dst = a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b;
 #pragma unroll
             for (int rho = 0; rho < RPG; ++rho)
@@ -557,6 +609,17 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     }
 
     // ------------------------------------------------------------- epilogue
+    if constexpr (COMMIT) {
+        // conv state <- window rows TT .. TT+2 (after cluster phase 1: every reader is done)
+        const int c_first = qk_writer ? 0 : 2 * DK;
+        const int n4 = (NCH - c_first) / 4;
+        float *base = a.conv_state + size_t(s) * 3 * C;
+        for (int i = tid; i < 3 * n4; i += nthr) {
+            const int rr = i / n4, c = c_first + 4 * (i % n4);
+            store4(base + size_t(rr) * C + gchan(c), win4(TT + rr, c));
+        }
+        return;
+    }
     if (tid < T) {
         mbar_wait_cluster(redbar, 0, a.d_status);   // every partial of this head has landed
         const int t = tid;
@@ -580,7 +643,17 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
             store4(out + (size_t(s) * a.Ts + t) * size_t(Hv) * DV + size_t(h) * DV + j0 + c, y);
         }
     }
-    if constexpr (!TREE) {
+    if (LAZY && n_prev > 0) {
+        // conv state after the committed tokens: window rows n_prev .. n_prev+2 (after cluster phase 1)
+        const int c_first = qk_writer ? 0 : 2 * DK;
+        const int n4 = (NCH - c_first) / 4;
+        float *base = a.conv_state + size_t(s) * 3 * C;
+        for (int i = tid; i < 3 * n4; i += nthr) {
+            const int rr = i / n4, c = c_first + 4 * (i % n4);
+            store4(base + size_t(rr) * C + gchan(c), win4(n_prev + rr, c));
+        }
+    }
+    if constexpr (MODE == kChain) {
         // conv state <- window rows T .. T+2 (after cluster phase 1: every reader is done)
         const int c_first = qk_writer ? 0 : 2 * DK;
         const int n4 = (NCH - c_first) / 4;
@@ -592,12 +665,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     }
 }
 
-template <int DK, typename Act, bool TREE>
+template <int DK, typename Act, int MODE>
 cudaError_t launch_t(const VerifyArgs &a, cudaStream_t stream) {
     const int rows = a.dv / a.P;
     const int warps = rows / kRowsPerWarp;
-    const Smem L(a.T, DK, rows, warps, a.P, sizeof(Act), TREE);
-    auto kern = verify_kernel<DK, Act, TREE>;
+    const Smem L(a.Tm, DK, rows, warps, a.P, sizeof(Act), MODE == kTree);
+    auto kern = verify_kernel<DK, Act, MODE>;
     // Function attributes are set once per device (and raised when a launch needs more).
     static int smem_set[kMaxDevices] = {};
     static bool nonportable_set[kMaxDevices] = {};
@@ -640,19 +713,25 @@ size_t verify_smem_bytes(int T, int dk, int dv, int P, int act_bytes, bool tree)
     return Smem(T, dk, rows, rows / kRowsPerWarp, P, act_bytes, tree).total;
 }
 
-template <bool TREE>
+template <int MODE>
 static cudaError_t launch_mode(const VerifyArgs &a, bool bf, cudaStream_t stream) {
     switch (a.dk) {
-        case 128: return bf ? launch_t<128, __nv_bfloat16, TREE>(a, stream) : launch_t<128, float, TREE>(a, stream);
-        case 64: return bf ? launch_t<64, __nv_bfloat16, TREE>(a, stream) : launch_t<64, float, TREE>(a, stream);
-        case 32: return bf ? launch_t<32, __nv_bfloat16, TREE>(a, stream) : launch_t<32, float, TREE>(a, stream);
+        case 128: return bf ? launch_t<128, __nv_bfloat16, MODE>(a, stream) : launch_t<128, float, MODE>(a, stream);
+        case 64: return bf ? launch_t<64, __nv_bfloat16, MODE>(a, stream) : launch_t<64, float, MODE>(a, stream);
+        case 32: return bf ? launch_t<32, __nv_bfloat16, MODE>(a, stream) : launch_t<32, float, MODE>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_verify(const VerifyArgs &a, gdn_dtype act, cudaStream_t stream) {
     const bool bf = act == GDN_BF16;
-    return a.parent ? launch_mode<true>(a, bf, stream) : launch_mode<false>(a, bf, stream);
+    switch (a.mode) {
+        case kChain: return launch_mode<kChain>(a, bf, stream);
+        case kTree: return launch_mode<kTree>(a, bf, stream);
+        case kLazy: return launch_mode<kLazy>(a, bf, stream);
+        case kCommit: return launch_mode<kCommit>(a, bf, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace gdn

@@ -164,6 +164,55 @@ int gdn_verify_tree(const gdn_dims *dims, const gdn_layer_params *params,
 int gdn_rollback_tree(const gdn_dims *dims, const int32_t *d_accept, float *state, float *conv_state,
                       const float *cap_state, const float *cap_conv, int *d_status, void *stream);
 
+/*
+ * Lazy capture: the byte-saving alternative to per-position capture.  Instead
+ * of writing the state after every token and copying one back, a lazy verify
+ * writes only its outputs and leaves the batch "pending": state and
+ * conv_state keep the state before it.  Once the acceptance is known, the
+ * pending batch is committed by re-running its accepted tokens from that
+ * state -- inside the next lazy verify (one launch per step), or by
+ * gdn_commit_lazy.  The single-snapshot rollback of the lucebox-hub page
+ * (internal.h, "Target cache" and its snapshot tensors) keeps the same one
+ * state per slot; the re-run rests on the prefix property of the recurrence
+ * (the state after token t depends only on tokens 0..t).
+ *
+ * gdn_verify_lazy: d_prev_trim == NULL: no batch is pending; as
+ * gdn_verify_forward with no capture, except that state and conv_state are
+ * only read.  d_prev_trim != NULL: a DEVICE int32[B], the trims of the pending
+ * batch whose qkv, alpha and beta_raw are prev_qkv / prev_alpha /
+ * prev_beta_raw (same dims and layouts as the new batch; z is not needed).
+ * Per slot the launch first runs the pending batch's tokens 0..T-1-trim from
+ * state / conv_state and writes the state and conv state after them in place
+ * (what gdn_commit_lazy would write), then runs the new batch from there and
+ * writes its outputs; the new batch is then the pending one.  Outputs and
+ * committed states are bit-identical to gdn_verify_forward with capture +
+ * gdn_rollback.  A pending trim outside [0, T-1] leaves the slot untouched
+ * (no outputs either) and writes GDN_ERR_TRIM_RANGE to *d_status.  With a
+ * pending batch the shared memory holds 2T tokens, so T is limited by the
+ * device's shared memory (GDN_ERR_SHAPE).
+ */
+int gdn_verify_lazy(const gdn_dims *dims, const gdn_layer_params *params,
+                    const int32_t *d_prev_trim, const void *prev_qkv, const void *prev_alpha,
+                    const void *prev_beta_raw,
+                    const void *qkv, const void *z, const void *alpha, const void *beta_raw,
+                    float *state, float *conv_state, void *out, int *d_status, void *stream);
+
+/*
+ * gdn_commit_lazy: commits a pending batch on its own (e.g. at the end of a
+ * generation).  d_trim is a DEVICE int32[B] with gdn_rollback's meaning (trim
+ * in 0..T-1; the slot keeps tokens 0..T-1-trim).  For every slot it runs those
+ * T - trim tokens of the batch's qkv, alpha and beta_raw (z and the outputs
+ * are not needed) from state / conv_state -- which must still hold the state
+ * before the batch -- and writes the state and conv state after them in
+ * place.  Bit-identical to gdn_verify_forward with capture followed by
+ * gdn_rollback with the same trims.  A trim outside [0, T-1] leaves the slot
+ * untouched and writes GDN_ERR_TRIM_RANGE to *d_status.  Same shapes and
+ * limits as gdn_verify_forward.
+ */
+int gdn_commit_lazy(const gdn_dims *dims, const gdn_layer_params *params, const int32_t *d_trim,
+                    const void *qkv, const void *alpha, const void *beta_raw,
+                    float *state, float *conv_state, int *d_status, void *stream);
+
 /* Bytes of device workspace gdn_prefill_chunked needs for these dims (0 on bad dims). */
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims);
 

@@ -207,6 +207,35 @@ def rollback(shape, trim, state, conv_state, cap_state, cap_conv, n_tokens: Opti
     return st, cs, status
 
 
+def commit_lazy(shape, x: Dict[str, np.ndarray], trim, head_mask=None, n_threads: int = 1,
+                q_scale: float = 1.0, rms_eps: float = 1e-6, l2_eps: float = 1e-6):
+    """Lazy capture's commit (the byte-saving alternative to per-position capture,
+    after the single-snapshot rollback of the lucebox-hub page internal.h,
+    "Target cache"): the verify kept only the state before the batch, so each
+    slot s re-runs its accepted tokens 0 .. T-1-trim[s] from it.  No arithmetic
+    of its own: the state after a token is defined by the recurrence over the
+    tokens up to it, so this is ``verify`` of one slot over that prefix.  A trim
+    outside [0, T-1] leaves the slot as it was with status 1 (as ``rollback``).
+    Returns (state, conv_state, slot_status)."""
+    s = shape
+    T, B = s.n_tokens, s.n_slots
+    tr = np.asarray(trim).reshape(-1)
+    assert tr.shape == (B,)
+    state, conv_state = _f64(x["state"]).copy(), _f64(x["conv_state"]).copy()
+    status = np.zeros(B, dtype=np.int32)
+    one = s.with_(n_slots=1)
+    per_slot = ("qkv", "z", "alpha", "beta_raw", "state", "conv_state")
+    for b in range(B):
+        if not 0 <= int(tr[b]) < T:
+            status[b] = 1
+            continue
+        xb = {k: (v[b:b + 1] if k in per_slot else v) for k, v in x.items()}
+        r = verify(one, xb, capture=False, n_tokens=T - int(tr[b]), head_mask=head_mask, n_threads=n_threads,
+                   q_scale=q_scale, rms_eps=rms_eps, l2_eps=l2_eps)
+        state[b], conv_state[b] = r["state"][0], r["conv_state"][0]
+    return state, conv_state, status
+
+
 def verify_tree(shape, x: Dict[str, np.ndarray], parent, head_mask=None, n_threads: int = 1,
                 q_scale: float = 1.0, rms_eps: float = 1e-6, l2_eps: float = 1e-6) -> Dict[str, np.ndarray]:
     """Tree (DDTree) verify of shape.n_tokens tokens per slot; parent is [B][T] int

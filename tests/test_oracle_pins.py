@@ -373,6 +373,27 @@ def test_rollback_equals_prefix_rerun(name):
         assert np.allclose(res["out"][:, :T - trim], pre["out"], rtol=1e-12, atol=1e-14)
 
 
+def test_lazy_commit_equals_capture_rollback():
+    """Lazy capture keeps only the pre-batch state and re-runs the accepted prefix; it
+    must land on the state the per-position capture holds for the same trim (the
+    state after token t does not depend on the tokens after it), slot by slot."""
+    s = small_shape(n_slots=5, n_tokens=6)
+    x = make_inputs(s, seed=23).as_f64()
+    res = oracle.verify(s, x)
+    trim = [0, 5, 2, 6, -1]                                    # last two are refused
+    st, cs, status = oracle.commit_lazy(s, x, trim)
+    rst, rcs, rstatus = oracle.rollback(s, trim, res["state"], res["conv_state"], res["cap_state"],
+                                        res["cap_conv"])
+    np.testing.assert_array_equal(status, [0, 0, 0, 1, 1])
+    np.testing.assert_array_equal(status, rstatus)
+    for b in range(3):
+        np.testing.assert_allclose(st[b], rst[b], rtol=1e-12, atol=1e-14)
+        np.testing.assert_array_equal(cs[b], rcs[b])
+    for b in (3, 4):                                           # refused: the pre-batch state
+        np.testing.assert_array_equal(st[b], x["state"][b])
+        np.testing.assert_array_equal(cs[b], x["conv_state"][b])
+
+
 # --------------------------------------------------------------------------
 # chunkwise form vs sequential form (two algorithms)
 # --------------------------------------------------------------------------

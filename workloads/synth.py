@@ -165,6 +165,8 @@ WORKLOADS: Dict[str, Shape] = {
     "prefill": Shape("prefill", 1, 16, 48, 128, 128, 8192, "bf16", seed=4, chunk=64),
     # tree (DDTree) verify of a 16-node draft tree, one slot of the layer shape
     "tree_verify": Shape("tree_verify", 1, 16, 48, 128, 128, 16, "bf16", seed=5),
+    # lazy capture on the layer shape (same inputs): outputs-only verify, then the accepted prefix re-run
+    "lazy_verify": Shape("lazy_verify", 1, 16, 48, 128, 128, 16, "bf16", seed=1),
 }
 
 # stream tags (one independent stream per tensor and layer)
