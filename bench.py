@@ -9,7 +9,13 @@ a 64-layer hybrid target, 1 slot, 16 QK / 48 V heads, d_k = d_v = 128, K+1 =
 16 verify tokens, bf16 activations, fp32 state.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
-                    [--workload layer_verify|multislot_verify|stack_verify|prefill]
+                    [--workload layer_verify|multislot_verify|stack_verify|prefill|tree_verify|
+                                lazy_verify|lazy_multislot_verify|lazy_stack_verify]
+
+The tree_verify workload verifies a draft tree and rolls back to the accepted
+node; the lazy_* workloads run lazy capture on the same inputs as their
+capture counterparts: one launch per step commits the pending batch (re-runs
+its accepted tokens) and writes the new batch's outputs, nothing captured.
 
 Prints one JSON line.  ``value`` = verified tokens/s over all ranks (device
 time, CUDA events, steps replayed from CUDA graphs over rotating buffer sets
@@ -553,7 +559,7 @@ def run_cuda(args):
         return
 
     graph_len = max(1, min(args.graph_len, args.steps))
-    if args.workload in ("stack_verify", "prefill"):
+    if args.workload in ("stack_verify", "lazy_stack_verify", "prefill"):
         graph_len = 1
     g_full, n_full, g_rem = time_graph_steps(torch, wl, args.steps, graph_len)
     g_warm, nw_full, g_wrem = time_graph_steps(torch, wl, args.warmup, graph_len)

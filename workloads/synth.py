@@ -167,6 +167,8 @@ WORKLOADS: Dict[str, Shape] = {
     "tree_verify": Shape("tree_verify", 1, 16, 48, 128, 128, 16, "bf16", seed=5),
     # lazy capture on the layer shape (same inputs): outputs-only verify, then the accepted prefix re-run
     "lazy_verify": Shape("lazy_verify", 1, 16, 48, 128, 128, 16, "bf16", seed=1),
+    "lazy_multislot_verify": Shape("lazy_multislot_verify", 32, 16, 48, 128, 128, 16, "bf16", seed=2),
+    "lazy_stack_verify": Shape("lazy_stack_verify", 8, 16, 48, 128, 128, 16, "bf16", n_layers=48, seed=3),
 }
 
 # stream tags (one independent stream per tensor and layer)
