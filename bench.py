@@ -43,7 +43,7 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
-from workloads.synth import make_parents, WORKLOADS, make_inputs, randint  # noqa: E402
+from workloads.synth import make_parents, make_proj, proj_in_rows, WORKLOADS, make_inputs, randint  # noqa: E402
 
 METRIC = "GDN verify tokens/sec at 1 GB300; achieved HBM GB/s vs roofline"
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -118,6 +118,19 @@ def commit_bytes(s, trims) -> int:
             n += keep * (s.conv_channels + 2 * s.n_v_heads) * a
     n += 4 * s.n_slots + s.conv_width * s.conv_channels * 4 + 2 * s.n_v_heads * 4
     return n
+
+
+def proj_in_bytes(s) -> int:
+    """Compulsory bytes of the fused input projection: x and w_in read, the
+    activation matrix (row stride rounded up to 8 columns) written."""
+    M = s.n_slots * s.n_tokens
+    ld = -(-proj_in_rows(s) // 8) * 8
+    return 2 * (M * s.n_embd + proj_in_rows(s) * s.n_embd + M * ld)
+
+
+def proj_out_bytes(s) -> int:
+    M = s.n_slots * s.n_tokens
+    return 2 * (M * s.value_dim + s.n_embd * s.value_dim + M * s.n_embd)
 
 
 def rollback_bytes(s, trims) -> int:
@@ -299,8 +312,12 @@ class VerifyWorkload:
         # lazy capture: one launch per step commits the pending batch (this buffer set's previous
         # one, with its trims) and verifies the new one, outputs only
         self.lazy = s.name.startswith("lazy")
+        # the layer with its projections: x -> GEMM -> verify (strided activations) -> GEMM -> y
+        self.proj = s.n_embd > 0
         per_set = (tree_verify_bytes(s) if self.tree else
                    lazy_step_bytes(s, [0] * s.n_slots) if self.lazy else verify_bytes(s)) * self.layers
+        if self.proj:
+            per_set += (proj_in_bytes(s) + proj_out_bytes(s)) * self.layers
         self.n_sets = 1 if per_set > 3 * l2_bytes else int(min(64, -(-3 * l2_bytes // per_set) + 1))
         self.dims = gdn.make_dims(s.n_slots, s.n_qk_heads, s.n_v_heads, s.d_k, s.d_v, s.n_tokens,
                                   gdn.GDN_BF16 if s.act == "bf16" else gdn.GDN_F32)
@@ -328,6 +345,21 @@ class VerifyWorkload:
                                                 dtype=torch.float32, device=device)
                 x["status"] = torch.zeros(1, dtype=torch.int32, device=device)
                 x["params"] = gdn.layer_params(x["conv_w"], x["A_log"], x["dt_bias"], x["norm_w"])
+                if self.proj:                   # every buffer set has its own weights, so they rotate too
+                    if not hasattr(self, "host_proj"):
+                        self.host_proj = make_proj(s)
+                    for key, v in self.host_proj.items():
+                        x[key] = torch.from_numpy(v).view(torch.bfloat16).to(device)
+                    x["w"] = gdn.proj_weights(s.n_embd, x["w_in"], x["w_out"])
+                    x["ws_bytes"] = gdn.gdn_layer_workspace_bytes(self.dims, s.n_embd)
+                    x["ws"] = torch.empty(x["ws_bytes"], dtype=torch.uint8, device=device)
+                    x["y"] = torch.empty((s.n_slots, s.n_tokens, s.n_embd), dtype=torch.bfloat16, device=device)
+                    M = s.n_slots * s.n_tokens
+                    act_b = M * gdn.gdn_proj_in_ld(self.dims) * 2
+                    out_off = -(-act_b // 256) * 256
+                    x["lt_off"] = out_off + -(-(M * s.value_dim * 2) // 256) * 256
+                    x["act"] = x["ws"][:act_b]
+                    x["act_out"] = x["ws"][out_off:out_off + M * s.value_dim * 2]
                 layers.append(x)
             self.sets.append(layers)
         self.tokens_per_step = s.n_slots * s.n_tokens
@@ -340,6 +372,11 @@ class VerifyWorkload:
                                      x["parent"], x["state"], x["conv_state"], x["cap_state"], x["cap_conv"],
                                      x["out"], x["status"], stream)
             return
+        if self.proj:
+            self.gdn.gdn_layer_verify(self.dims, x["params"], x["w"], x["x"], x["state"], x["conv_state"],
+                                      x["cap_state"], x["cap_conv"], x["y"], x["ws"], x["ws_bytes"], x["status"],
+                                      stream)
+            return
         if self.lazy:
             self.gdn.gdn_verify_lazy(self.dims, x["params"], x["qkv"], x["z"], x["alpha"], x["beta_raw"],
                                      x["state"], x["conv_state"], x["out"], x["status"], stream,
@@ -348,6 +385,16 @@ class VerifyWorkload:
             return
         self.gdn.gdn_verify_forward(self.dims, x["params"], x["qkv"], x["z"], x["alpha"], x["beta_raw"], x["state"],
                                     x["conv_state"], x["cap_state"], x["cap_conv"], x["out"], x["status"], stream)
+
+    def gemm_in(self, k, li, stream):
+        x = self.sets[k][li]
+        lt = x["ws"][x["lt_off"]:]
+        self.gdn.gdn_project_in(self.dims, x["w"], x["x"], x["act"], lt, lt.numel(), stream)
+
+    def gemm_out(self, k, li, stream):
+        x = self.sets[k][li]
+        lt = x["ws"][x["lt_off"]:]
+        self.gdn.gdn_project_out(self.dims, x["w"], x["act_out"], x["y"], lt, lt.numel(), stream)
 
     def rollback(self, k, li, stream):
         x = self.sets[k][li]
@@ -364,6 +411,10 @@ class VerifyWorkload:
     def step_bytes(self, k):
         if self.lazy:
             return sum(lazy_step_bytes(self.shape, self.trims[k][li]) for li in range(self.layers))
+        if self.proj:
+            s = self.shape
+            return sum(verify_bytes(s) + proj_in_bytes(s) + proj_out_bytes(s) + rollback_bytes(s, self.trims[k][li])
+                       for li in range(self.layers))
         vb = tree_verify_bytes(self.shape) if self.tree else verify_bytes(self.shape)
         moved = (self.trims[k] >= 0) if self.tree else self.trims[k]     # slots whose rollback copies
         return sum(vb + rollback_bytes(self.shape, moved[li]) for li in range(self.layers))
@@ -375,15 +426,20 @@ class VerifyWorkload:
         from workloads.device import act_host
         s = self.shape
         hosts, outs = [], []
+        out_key = "y" if self.proj else "out"
         for li in range(self.layers):
             inp = self.host_inputs[li if self.layers > 1 else 0]
-            hosts.append({"qkv": act_host(inp.qkv, s).pin_memory(), "z": act_host(inp.z, s).pin_memory(),
-                          "alpha": act_host(inp.alpha, s).pin_memory(),
-                          "beta_raw": act_host(inp.beta_raw, s).pin_memory(),
-                          "trim": torch.from_numpy(self.trims[0, li].astype(np.int32)).pin_memory()})
+            if self.proj:                   # the layer's input is the hidden state x
+                hosts.append({"x": act_host(self.host_proj["x"], s).pin_memory()})
+            else:
+                hosts.append({"qkv": act_host(inp.qkv, s).pin_memory(), "z": act_host(inp.z, s).pin_memory(),
+                              "alpha": act_host(inp.alpha, s).pin_memory(),
+                              "beta_raw": act_host(inp.beta_raw, s).pin_memory()})
+            hosts[-1]["trim"] = torch.from_numpy(self.trims[0, li].astype(np.int32)).pin_memory()
             if self.tree:
                 hosts[-1]["parent"] = torch.from_numpy(self.parents).pin_memory()
-            outs.append(torch.empty(self.sets[0][li]["out"].shape, dtype=self.sets[0][li]["out"].dtype).pin_memory())
+            ref = self.sets[0][li][out_key]
+            outs.append(torch.empty(ref.shape, dtype=ref.dtype).pin_memory())
         h2d = sum(t.numel() * t.element_size() for h in hosts for t in h.values())
         d2h = sum(o.numel() * o.element_size() for o in outs)
         stream = torch.cuda.current_stream()
@@ -397,7 +453,7 @@ class VerifyWorkload:
                     x[key].copy_(t, non_blocking=True)
                 self.verify(kk, li, sp)
                 self.rollback(kk, li, sp)
-                outs[li].copy_(x["out"], non_blocking=True)
+                outs[li].copy_(x[out_key], non_blocking=True)
             stream.synchronize()
 
         for k in range(10):
@@ -600,6 +656,14 @@ def run_cuda(args):
         kdur = {"prefill": kernel_duration(torch, wl, "prefill", 2)}
     elif wl.lazy:
         kdur = {"lazy_verify": kernel_duration(torch, wl, "verify", n_launch)}
+    elif wl.proj:
+        # the layer call is GEMM + verify + GEMM; what it takes beyond the two GEMMs timed alone is the
+        # verify plus the launch gaps between the library's kernels and it
+        kdur = {"layer": kernel_duration(torch, wl, "verify", n_launch),
+                "gemm_in": kernel_duration(torch, wl, "gemm_in", n_launch),
+                "gemm_out": kernel_duration(torch, wl, "gemm_out", n_launch),
+                "rollback": kernel_duration(torch, wl, "rollback", n_launch)}
+        kdur["verify_and_launch_gaps"] = max(0.0, kdur["layer"] - kdur["gemm_in"] - kdur["gemm_out"])
     else:
         kdur = {"verify": kernel_duration(torch, wl, "verify", n_launch),
                 "rollback": kernel_duration(torch, wl, "rollback", n_launch)}
@@ -610,6 +674,9 @@ def run_cuda(args):
     hbm, peak_kind = peaks()
     if args.workload == "prefill":
         dom, dom_bytes, dom_src = "prefill", prefill_bytes(shape), ["prefill.cu", "internal.cuh"]
+    elif wl.proj:
+        # dominant: the input projection GEMM (cuBLASLt), streaming the fused weights
+        dom, dom_bytes, dom_src = "gemm_in", proj_in_bytes(shape), ["proj.cu"]
     elif wl.lazy:
         # the timed launches cycle over every buffer set's pending trims: their mean bytes
         dom = "lazy_verify"
@@ -632,6 +699,7 @@ def run_cuda(args):
                          f"{shape.n_tokens} tokens"),
             "act_dtype": shape.act, "state_dtype": "f32",
             "step": ("chunked prefill" if args.workload == "prefill" else
+                     "layer: input projection GEMM + verify + output projection GEMM, then rollback" if wl.proj else
                      "lazy verify: commit of the pending batch (accepted-prefix re-run) + outputs of the new one"
                      if wl.lazy else
                      "verify+rollback"),
@@ -687,8 +755,19 @@ def run_cuda(args):
 # the oracle on the host cores
 # ---------------------------------------------------------------------------
 
+_PROJ_CACHE = {}
+
+
 def _oracle_pass(shape, x, heads, n_threads, trims):
     import oracle
+    if shape.n_embd:
+        if shape.name not in _PROJ_CACHE:
+            from workloads.synth import bf16_bits_to_f64
+            _PROJ_CACHE[shape.name] = {k: bf16_bits_to_f64(v) for k, v in make_proj(shape).items()}
+        p = _PROJ_CACHE[shape.name]
+        r = oracle.layer_verify(shape, x, p["x"], p["w_in"], p["w_out"], head_mask=heads, n_threads=n_threads)
+        oracle.rollback(shape, trims, r["state"], r["conv_state"], r["cap_state"], r["cap_conv"])
+        return
     if shape.name == "prefill":
         oracle.verify(shape, x, capture=False, head_mask=heads, n_threads=n_threads)
         return

@@ -35,7 +35,8 @@ GDN_F32 = 0
 GDN_BF16 = 1
 
 EXPORTED_SYMBOLS = ("gdn_verify_forward", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_tree",
-                    "gdn_verify_lazy", "gdn_commit_lazy", "gdn_prefill_workspace_bytes",
+                    "gdn_verify_lazy", "gdn_commit_lazy", "gdn_proj_in_ld", "gdn_layer_workspace_bytes",
+                    "gdn_project_in", "gdn_project_out", "gdn_layer_verify", "gdn_prefill_workspace_bytes",
                     "gdn_prefill_chunked", "gdn_prefill_chunked_static", "gdn_last_error", "gdn_version")
 
 # size of the library's built-in prefill scratch (GDN_PREFILL_STATIC_SCRATCH_BYTES)
@@ -58,6 +59,10 @@ class Dims(ctypes.Structure):
 class LayerParams(ctypes.Structure):
     _fields_ = [("conv_w", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
                 ("norm_w", ctypes.c_void_p)]
+
+
+class ProjWeights(ctypes.Structure):
+    _fields_ = [("n_embd", ctypes.c_int), ("w_in", ctypes.c_void_p), ("w_out", ctypes.c_void_p)]
 
 
 def make_dims(n_slots: int, n_qk_heads: int, n_v_heads: int, d_k: int, d_v: int, n_tokens: int,
@@ -91,6 +96,16 @@ def lib() -> ctypes.CDLL:
         L.gdn_verify_lazy.restype = ip
         L.gdn_commit_lazy.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 8
         L.gdn_commit_lazy.restype = ip
+        L.gdn_proj_in_ld.argtypes = [ctypes.POINTER(Dims)]
+        L.gdn_proj_in_ld.restype = ctypes.c_longlong
+        L.gdn_layer_workspace_bytes.argtypes = [ctypes.POINTER(Dims), ip]
+        L.gdn_layer_workspace_bytes.restype = ctypes.c_size_t
+        for fn in (L.gdn_project_in, L.gdn_project_out):
+            fn.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(ProjWeights), vp, vp, vp, ctypes.c_size_t, vp]
+            fn.restype = ip
+        L.gdn_layer_verify.argtypes = ([ctypes.POINTER(Dims), ctypes.POINTER(LayerParams),
+                                        ctypes.POINTER(ProjWeights)] + [vp] * 7 + [ctypes.c_size_t, vp, vp])
+        L.gdn_layer_verify.restype = ip
         L.gdn_prefill_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
         L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
         L.gdn_prefill_chunked.argtypes = ([ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 8 +
@@ -181,6 +196,38 @@ def gdn_commit_lazy(dims: Dims, params: LayerParams, d_trim, qkv, alpha, beta_ra
     _check(lib().gdn_commit_lazy(ctypes.byref(dims), ctypes.byref(params), _ptr(d_trim), _ptr(qkv),
                                  _ptr(alpha), _ptr(beta_raw), _ptr(state), _ptr(conv_state), _ptr(d_status),
                                  _stream(stream)))
+
+
+def proj_weights(n_embd: int, w_in, w_out) -> "ProjWeights":
+    """The projection weights of one layer (device tensors or pointers): w_in
+    [C + H_v*d_v + 2*H_v][n_embd] (wqkv, wqkv_gate, ssm_alpha, ssm_beta rows),
+    w_out [n_embd][H_v*d_v]; both bf16."""
+    return ProjWeights(int(n_embd), _ptr(w_in), _ptr(w_out))
+
+
+def gdn_proj_in_ld(dims: Dims) -> int:
+    return int(lib().gdn_proj_in_ld(ctypes.byref(dims)))
+
+
+def gdn_layer_workspace_bytes(dims: Dims, n_embd: int) -> int:
+    return int(lib().gdn_layer_workspace_bytes(ctypes.byref(dims), int(n_embd)))
+
+
+def gdn_project_in(dims: Dims, w: "ProjWeights", x, act, workspace, ws_bytes: int, stream=None) -> None:
+    _check(lib().gdn_project_in(ctypes.byref(dims), ctypes.byref(w), _ptr(x), _ptr(act), _ptr(workspace),
+                                int(ws_bytes), _stream(stream)))
+
+
+def gdn_project_out(dims: Dims, w: "ProjWeights", out, y, workspace, ws_bytes: int, stream=None) -> None:
+    _check(lib().gdn_project_out(ctypes.byref(dims), ctypes.byref(w), _ptr(out), _ptr(y), _ptr(workspace),
+                                 int(ws_bytes), _stream(stream)))
+
+
+def gdn_layer_verify(dims: Dims, params: LayerParams, w: "ProjWeights", x, state, conv_state, cap_state, cap_conv,
+                     y, workspace, ws_bytes: int, d_status=None, stream=None) -> None:
+    _check(lib().gdn_layer_verify(ctypes.byref(dims), ctypes.byref(params), ctypes.byref(w), _ptr(x), _ptr(state),
+                                  _ptr(conv_state), _ptr(cap_state), _ptr(cap_conv), _ptr(y), _ptr(workspace),
+                                  int(ws_bytes), _ptr(d_status), _stream(stream)))
 
 
 def gdn_prefill_workspace_bytes(dims: Dims) -> int:

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdn_verify.so")
 
-SOURCES = ["gdn_api.cu", "verify.cu", "rollback.cu", "prefill.cu"]
+SOURCES = ["gdn_api.cu", "verify.cu", "rollback.cu", "prefill.cu", "proj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]
@@ -31,6 +31,17 @@ def nvcc() -> str:
         if cand and os.path.exists(cand):
             return cand
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libgdn_verify.so")
+
+
+def link_flags(cc: str) -> List[str]:
+    """cuBLASLt (the projection GEMMs), found through an rpath to the toolkit's
+    library directory so the library loads without LD_LIBRARY_PATH."""
+    home = os.path.dirname(os.path.dirname(os.path.realpath(cc)))
+    libdir = next((d for d in (os.path.join(home, "lib64"), os.path.join(home, "lib"))
+                   if os.path.exists(os.path.join(d, "libcublasLt.so"))), None)
+    if libdir is None:
+        raise RuntimeError(f"libcublasLt.so not found under {home}: the CUDA toolkit's cuBLAS is required")
+    return ["-L", libdir, "-lcublasLt", "-Xlinker", "-rpath=" + libdir]
 
 
 def _headers() -> List[str]:
@@ -90,7 +101,7 @@ def build(verbose: bool = False, extra_flags: List[str] = ()) -> str:
         list(ex.map(run, jobs))
     if jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        run([cc, *ARCH, "-shared", "-o", tmp, *objs])
+        run([cc, *ARCH, "-shared", "-o", tmp, *objs, *link_flags(cc)])
         os.replace(tmp, LIB)
     return LIB
 

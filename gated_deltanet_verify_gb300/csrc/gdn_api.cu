@@ -136,7 +136,7 @@ static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, con
                        float *conv_state, float *cap_state, float *cap_conv, void *out, int *d_status,
                        void *stream, int mode = gdn::kChain, const int32_t *d_trim = nullptr,
                        const void *qkv_prev = nullptr, const void *alpha_prev = nullptr,
-                       const void *beta_prev = nullptr) {
+                       const void *beta_prev = nullptr, long long ld_act = 0) {
     g_err.clear();
     int rc = check_common(dims);
     if (rc) return rc;
@@ -172,6 +172,8 @@ static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, con
     gdn::VerifyArgs a{};
     a.B = d.n_slots; a.Hk = d.n_qk_heads; a.Hv = d.n_v_heads; a.dk = d.d_k; a.dv = d.d_v;
     a.T = d.n_tokens; a.Ts = d.n_tokens; a.Tm = Tm; a.C = int(conv_channels(&d)); a.r = r; a.P = P;
+    a.ld_qkv = a.C; a.ld_z = (long long)d.n_v_heads * d.d_v; a.ld_ab = d.n_v_heads;
+    if (ld_act) a.ld_qkv = a.ld_z = a.ld_ab = ld_act;     // column blocks of one activation matrix
     a.rms_eps = d.rms_eps; a.l2_eps = d.l2_eps; a.q_scale = d.q_scale;
     a.conv_w = params->conv_w; a.A_log = params->A_log; a.dt_bias = params->dt_bias; a.norm_w = params->norm_w;
     a.qkv = qkv; a.z = z; a.alpha = alpha; a.beta_raw = beta_raw;
@@ -307,6 +309,106 @@ int gdn_prefill_chunked_static(const gdn_dims *dims, const gdn_layer_params *par
     if (need > 0 && (rc = static_scratch(&scratch))) return rc;
     return gdn_prefill_chunked(dims, params, qkv, z, alpha, beta_raw, state, conv_state, out, scratch,
                                need > 0 ? (size_t)GDN_PREFILL_STATIC_SCRATCH_BYTES : 0, d_status, stream);
+}
+
+// ---- projections around the block and the layer step ----------------------
+
+static long long proj_in_cols(const gdn_dims &d) {
+    return conv_channels(&d) + (long long)d.n_v_heads * d.d_v + 2LL * d.n_v_heads;
+}
+
+static size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+static constexpr size_t kLtWorkspace = size_t(32) << 20;
+
+// checks shared by the projection calls; M = B * T rows
+static int check_proj(const gdn_dims *dims, const gdn_proj_weights *w) {
+    int rc = check_common(dims);
+    if (rc) return rc;
+    if (!w) return fail(GDN_ERR_ARG, "projection weights are NULL");
+    if (dims->act_dtype != GDN_BF16) return fail(GDN_ERR_DTYPE, "the projections run in bf16 (act_dtype GDN_BF16)");
+    if (w->n_embd < 8 || w->n_embd % 8)
+        return fail(GDN_ERR_SHAPE, "n_embd must be a positive multiple of 8 (got %d)", w->n_embd);
+    if (dims->n_v_heads % 8)
+        return fail(GDN_ERR_SHAPE, "the layer step needs n_v_heads to be a multiple of 8 (got %d)", dims->n_v_heads);
+    if (!w->w_in || !w->w_out) return fail(GDN_ERR_ARG, "a projection weight pointer is NULL");
+    if (!aligned16(w->w_in) || !aligned16(w->w_out)) return fail(GDN_ERR_ALIGN, "weights must be 16-byte aligned");
+    const long long M = (long long)dims->n_slots * dims->n_tokens;
+    if (M > (1LL << 30) || proj_in_cols(*dims) > (1LL << 30))
+        return fail(GDN_ERR_SHAPE, "projection sizes out of range");
+    return GDN_OK;
+}
+
+long long gdn_proj_in_ld(const gdn_dims *dims) {
+    if (!dims) return 0;
+    return (proj_in_cols(*dims) + 7) / 8 * 8;
+}
+
+size_t gdn_layer_workspace_bytes(const gdn_dims *dims, int n_embd) {
+    if (!dims || n_embd < 1) return 0;
+    const size_t M = size_t(dims->n_slots) * size_t(dims->n_tokens);
+    return align256(M * size_t(gdn_proj_in_ld(dims)) * 2) + align256(M * size_t(dims->n_v_heads) * dims->d_v * 2) +
+           kLtWorkspace;
+}
+
+int gdn_project_in(const gdn_dims *dims, const gdn_proj_weights *w, const void *x, void *act, void *workspace,
+                   size_t ws_bytes, void *stream) {
+    g_err.clear();
+    int rc = check_proj(dims, w);
+    if (rc) return rc;
+    if (!x || !act) return fail(GDN_ERR_ARG, "x or act is NULL");
+    if (!aligned16(x) || !aligned16(act)) return fail(GDN_ERR_ALIGN, "x and act must be 16-byte aligned");
+    if (!workspace || ws_bytes < kLtWorkspace)
+        return fail(GDN_ERR_WORKSPACE, "the GEMM needs %zu bytes of workspace (got %zu)", kLtWorkspace, ws_bytes);
+    std::string why;
+    const int M = dims->n_slots * dims->n_tokens;
+    if (!gdn::gemm_xwt_bf16(w->w_in, x, act, M, int(proj_in_cols(*dims)), w->n_embd, gdn_proj_in_ld(dims), workspace,
+                            kLtWorkspace, static_cast<cudaStream_t>(stream), why))
+        return fail(GDN_ERR_LAUNCH, "input projection: %s", why.c_str());
+    return GDN_OK;
+}
+
+int gdn_project_out(const gdn_dims *dims, const gdn_proj_weights *w, const void *out, void *y, void *workspace,
+                    size_t ws_bytes, void *stream) {
+    g_err.clear();
+    int rc = check_proj(dims, w);
+    if (rc) return rc;
+    if (!out || !y) return fail(GDN_ERR_ARG, "out or y is NULL");
+    if (!aligned16(out) || !aligned16(y)) return fail(GDN_ERR_ALIGN, "out and y must be 16-byte aligned");
+    if (!workspace || ws_bytes < kLtWorkspace)
+        return fail(GDN_ERR_WORKSPACE, "the GEMM needs %zu bytes of workspace (got %zu)", kLtWorkspace, ws_bytes);
+    std::string why;
+    const int M = dims->n_slots * dims->n_tokens;
+    if (!gdn::gemm_xwt_bf16(w->w_out, out, y, M, w->n_embd, dims->n_v_heads * dims->d_v, w->n_embd, workspace,
+                            kLtWorkspace, static_cast<cudaStream_t>(stream), why))
+        return fail(GDN_ERR_LAUNCH, "output projection: %s", why.c_str());
+    return GDN_OK;
+}
+
+int gdn_layer_verify(const gdn_dims *dims, const gdn_layer_params *params, const gdn_proj_weights *w,
+                     const void *x, float *state, float *conv_state, float *cap_state, float *cap_conv, void *y,
+                     void *workspace, size_t ws_bytes, int *d_status, void *stream) {
+    g_err.clear();
+    int rc = check_proj(dims, w);
+    if (rc) return rc;
+    const size_t need = gdn_layer_workspace_bytes(dims, w->n_embd);
+    if (!workspace || ws_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need, ws_bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(GDN_ERR_ALIGN, "workspace must be 256-byte aligned");
+    const gdn_dims &d = *dims;
+    const size_t M = size_t(d.n_slots) * d.n_tokens;
+    const long long ld = gdn_proj_in_ld(dims);
+    unsigned char *act = static_cast<unsigned char *>(workspace);
+    unsigned char *out = act + align256(M * size_t(ld) * 2);
+    unsigned char *lt = out + align256(M * size_t(d.n_v_heads) * d.d_v * 2);
+    if ((rc = gdn_project_in(dims, w, x, act, lt, kLtWorkspace, stream))) return rc;
+    // the verify reads q|k|v, z, alpha and beta_raw as column blocks of the activation matrix
+    const long long C = conv_channels(dims), V = (long long)d.n_v_heads * d.d_v;
+    unsigned char *z = act + C * 2, *alpha = act + (C + V) * 2, *beta = alpha + size_t(d.n_v_heads) * 2;
+    if ((rc = verify_impl(dims, params, act, z, alpha, beta, nullptr, state, conv_state, cap_state, cap_conv, out,
+                          d_status, stream, gdn::kChain, nullptr, nullptr, nullptr, nullptr, ld)))
+        return rc;
+    return gdn_project_out(dims, w, out, y, lt, kLtWorkspace, stream);
 }
 
 }  // extern "C"

@@ -21,6 +21,8 @@ struct VerifyArgs {
     int B, Hk, Hv, dk, dv, T, C, r;   // C: conv channels; r = Hv / Hk
     int Ts;                           // tokens per slot in the activation buffers (>= T)
     int Tm;                           // tokens the shared memory holds (T; 2T for a lazy verify with a pending batch)
+    long long ld_qkv, ld_z, ld_ab;    // row strides (elements) of qkv, z and alpha / beta_raw (C, H_v*d_v, H_v
+                                      // when separate; one shared stride when they are column blocks of one matrix)
     int P;                            // CTAs per value head (each owns d_v / P rows)
     float rms_eps, l2_eps, q_scale;
     const float *conv_w, *A_log, *dt_bias, *norm_w;
@@ -77,6 +79,11 @@ size_t prefill_workspace_bytes(const gdn_dims &d);
 cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const void *qkv, const void *z,
                            const void *alpha, const void *beta_raw, float *state, float *conv_state,
                            void *out, void *workspace, int *d_status, cudaStream_t stream);
+
+// Row-major C[M][N] (row stride ldc) = X[M][K] @ W[N][K]^T, bf16 in and out,
+// fp32 accumulation (cuBLASLt).  false with the reason in why.
+bool gemm_xwt_bf16(const void *W, const void *X, void *C, int M, int N, int K, long long ldc, void *ws,
+                   size_t ws_bytes, cudaStream_t stream, std::string &why);
 
 // Choice of CTAs per value head for a verify launch (host heuristic).
 int verify_parts_per_head(int B, int Hv, int r, int dv, int sm_count);

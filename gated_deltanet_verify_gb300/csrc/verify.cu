@@ -321,17 +321,17 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
             const Act *src;
             Act *dst;
             if (w < vq) {
-                src = qkv + rw * C + size_t(kh) * DK + w * kPer16;
+                src = qkv + rw * a.ld_qkv + size_t(kh) * DK + w * kPer16;
                 dst = xs + size_t(t) * NCH + w * kPer16;
             } else if (w < 2 * vq) {
-                src = qkv + rw * C + size_t(Hk + kh) * DK + (w - vq) * kPer16;
+                src = qkv + rw * a.ld_qkv + size_t(Hk + kh) * DK + (w - vq) * kPer16;
                 dst = xs + size_t(t) * NCH + DK + (w - vq) * kPer16;
             } else if (w < 2 * vq + vv) {
-                src = qkv + rw * C + size_t(2 * Hk) * DK + size_t(h) * DV + j0 + (w - 2 * vq) * kPer16;
+                src = qkv + rw * a.ld_qkv + size_t(2 * Hk) * DK + size_t(h) * DV + j0 + (w - 2 * vq) * kPer16;
                 dst = xs + size_t(t) * NCH + 2 * DK + (w - 2 * vq) * kPer16;
             } else {
                 if (pend) continue;                 // no outputs for the pending tokens
-                src = z + rw * size_t(Hv) * DV + size_t(h) * DV + j0 + (w - 2 * vq - vv) * kPer16;
+                src = z + rw * a.ld_z + size_t(h) * DV + j0 + (w - 2 * vq - vv) * kPer16;
                 dst = zs + size_t(t - n_prev) * ROWS + (w - 2 * vq - vv) * kPer16;
             }
             cp_async16(dst, src);
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     // (3) gates for this head, one token per thread
     for (int t = tid; t < TT; t += nthr) {
         const bool pend = t < n_prev;
-        const size_t idx = (size_t(s) * a.Ts + (pend ? t : t - n_prev)) * Hv + h;
+        const size_t idx = (size_t(s) * a.Ts + (pend ? t : t - n_prev)) * a.ld_ab + h;
         const float al = to_f32(static_cast<const Act *>(pend ? a.alpha_prev : a.alpha)[idx]);
         const float br = to_f32(static_cast<const Act *>(pend ? a.beta_prev : a.beta_raw)[idx]);
         const float x = al + __ldg(a.dt_bias + h);

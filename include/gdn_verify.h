@@ -213,6 +213,61 @@ int gdn_commit_lazy(const gdn_dims *dims, const gdn_layer_params *params, const 
                     const void *qkv, const void *alpha, const void *beta_raw,
                     float *state, float *conv_state, int *d_status, void *stream);
 
+/*
+ * The projections either side of the block, as plain bf16 GEMMs (fp32
+ * accumulation; cuBLASLt), and the layer step that chains them around the
+ * verify.  They follow the GDN tensors of internal.h, Target weights
+ * (TargetLayer: wqkv, the fused Q/K/V projection; wqkv_gate, the z
+ * projection; ssm_alpha and ssm_beta, the per-token gate inputs; ssm_out, the
+ * output projection), each weight stored as its output rows with n_embd
+ * contiguous (the K-major "TN" layout of the tensor cores):
+ *   w_in  [C + H_v*d_v + 2*H_v][n_embd] bf16: the wqkv rows (C, channels
+ *         [q | k | v] as in qkv), then the wqkv_gate rows (H_v*d_v), then
+ *         ssm_alpha (H_v), then ssm_beta (H_v) -- the four input projections
+ *         fused so that one GEMM streams them all;
+ *   w_out [n_embd][H_v*d_v] bf16 (ssm_out).
+ * x and y are [B][T][n_embd] bf16.  The norm before the block, the residual
+ * add after it and the rest of the model are not part of this library.
+ * Limits: act_dtype GDN_BF16, n_embd a multiple of 8, n_v_heads a multiple of
+ * 8 (GDN_ERR_DTYPE / GDN_ERR_SHAPE).
+ */
+typedef struct {
+    int n_embd;            /* hidden size */
+    const void *w_in;      /* [C + H_v*d_v + 2*H_v][n_embd] bf16 */
+    const void *w_out;     /* [n_embd][H_v*d_v] bf16 */
+} gdn_proj_weights;
+
+/* Row stride (elements) of gdn_project_in's output: C + H_v*d_v + 2*H_v rounded up to 8. */
+long long gdn_proj_in_ld(const gdn_dims *dims);
+
+/* Device workspace of gdn_layer_verify: the activation matrix, the block's
+ * output and 32 MiB of GEMM workspace (0 on bad arguments).  The GEMM-only
+ * calls below need 32 MiB. */
+size_t gdn_layer_workspace_bytes(const gdn_dims *dims, int n_embd);
+
+/* act[B*T][gdn_proj_in_ld] = x @ w_in^T: columns [0, C) are qkv, then z, then
+ * alpha, then beta_raw, per row (bf16).  workspace >= 32 MiB of GEMM scratch. */
+int gdn_project_in(const gdn_dims *dims, const gdn_proj_weights *w, const void *x, void *act,
+                   void *workspace, size_t ws_bytes, void *stream);
+
+/* y[B*T][n_embd] = out @ w_out^T (bf16). */
+int gdn_project_out(const gdn_dims *dims, const gdn_proj_weights *w, const void *out, void *y,
+                    void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * One GDN layer of a verify step: gdn_project_in into the workspace, the
+ * verify of gdn_verify_forward reading qkv, z, alpha and beta_raw as column
+ * blocks of that matrix (state, conv_state and the optional captures as
+ * there), its output into the workspace, then gdn_project_out into y.  Roll
+ * back with gdn_rollback as usual.  workspace: gdn_layer_workspace_bytes,
+ * 256-byte aligned; the activation matrix sits at its start (row stride
+ * gdn_proj_in_ld) and the block's output [B*T][H_v*d_v] right after it (at
+ * the next 256-byte boundary).
+ */
+int gdn_layer_verify(const gdn_dims *dims, const gdn_layer_params *params, const gdn_proj_weights *w,
+                     const void *x, float *state, float *conv_state, float *cap_state, float *cap_conv,
+                     void *y, void *workspace, size_t ws_bytes, int *d_status, void *stream);
+
 /* Bytes of device workspace gdn_prefill_chunked needs for these dims (0 on bad dims). */
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims);
 

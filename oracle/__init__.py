@@ -236,6 +236,52 @@ def commit_lazy(shape, x: Dict[str, np.ndarray], trim, head_mask=None, n_threads
     return state, conv_state, status
 
 
+def project(a, w):
+    """One projection of the block's neighbours (internal.h, Target weights: the
+    TargetLayer GDN projections wqkv, wqkv_gate, ssm_alpha, ssm_beta, ssm_out):
+    a [..., K] times the weight w [N, K] (output rows, K contiguous), in fp64:
+    result[..., n] = sum_k a[..., k] w[n, k]."""
+    a, w = _f64(a), _f64(w)
+    assert a.shape[-1] == w.shape[1]
+    return np.matmul(a, w.T)
+
+
+def split_projected(shape, act):
+    """The input projection's columns, in the order of its weight rows: qkv
+    (C channels [q | k | v]), z (H_v*d_v), alpha (H_v), beta_raw (H_v)."""
+    C, V, H = shape.conv_channels, shape.n_v_heads * shape.d_v, shape.n_v_heads
+    assert act.shape[-1] == C + V + 2 * H
+    return {"qkv": act[..., :C], "z": act[..., C:C + V], "alpha": act[..., C + V:C + V + H],
+            "beta_raw": act[..., C + V + H:]}
+
+
+def round_bf16(a):
+    """Round fp64 values to the nearest bf16 (8 significant bits), ties to even,
+    returned as fp64: with a = m 2^e, 1/2 <= |m| < 1, the result is
+    rint(m 2^8) 2^(e-8) (numpy's rint rounds half to even).  Normal range only
+    (bf16 shares fp32's exponent range; no overflow or subnormals occur here)."""
+    m, e = np.frexp(_f64(a))
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def layer_verify(shape, x: Dict[str, np.ndarray], hidden, w_in, w_out, n_threads: int = 1,
+                 store_bf16: bool = True, **kw):
+    """The block with its projections: act = hidden @ w_in^T, split into qkv, z,
+    alpha, beta_raw; ``verify`` (with capture) on them from x's parameters and
+    states; y = out @ w_out^T.  All arithmetic in fp64; with ``store_bf16`` the
+    two matrices the layer stores between its steps (act and the block's out,
+    held in the activation dtype) are rounded to bf16 there.  Returns verify's
+    dict (out unrounded) plus act (unrounded) and y."""
+    act = project(hidden, w_in)
+    stored = round_bf16(act) if store_bf16 else act
+    xin = dict(x)
+    xin.update({k: np.ascontiguousarray(v) for k, v in split_projected(shape, stored).items()})
+    r = verify(shape, xin, n_threads=n_threads, **kw)
+    r["act"] = act
+    r["y"] = project(round_bf16(r["out"]) if store_bf16 else r["out"], w_out)
+    return r
+
+
 def verify_tree(shape, x: Dict[str, np.ndarray], parent, head_mask=None, n_threads: int = 1,
                 q_scale: float = 1.0, rms_eps: float = 1e-6, l2_eps: float = 1e-6) -> Dict[str, np.ndarray]:
     """Tree (DDTree) verify of shape.n_tokens tokens per slot; parent is [B][T] int

@@ -513,3 +513,55 @@ def test_tree_rollback_moves_to_the_accepted_node():
     np.testing.assert_allclose(st[2], ref["state"][0], rtol=1e-12, atol=1e-12)
     np.testing.assert_array_equal(cs[2], ref["conv_state"][0])
     assert tree_accept(s, par).shape == (s.n_slots,)
+
+
+# --------------------------------------------------------------------------
+# projections around the block
+# --------------------------------------------------------------------------
+
+def test_projection_is_the_row_dot_product_by_brute_force():
+    """project(a, w)[m, n] = sum_k a[m, k] w[n, k]: explicit loops on a tiny
+    non-square case catch a transposed operand."""
+    rng = np.random.default_rng(3)
+    a, w = rng.normal(size=(3, 5)), rng.normal(size=(4, 5))
+    got = oracle.project(a, w)
+    assert got.shape == (3, 4)
+    for m in range(3):
+        for n in range(4):
+            assert abs(got[m, n] - sum(a[m, k] * w[n, k] for k in range(5))) < 1e-12
+
+
+def test_layer_with_identity_projections_is_the_block():
+    """With n_embd = C + H_v d_v + 2 H_v and w_in = I, the hidden input is the
+    activation matrix itself: the layer must equal ``verify`` on its column
+    blocks taken in the order qkv | z | alpha | beta_raw; with w_out = I
+    (n_embd' = H_v d_v) y is the block's output."""
+    s = small_shape(n_tokens=4)
+    x = make_inputs(s, seed=41).as_f64()
+    N = s.conv_channels + s.value_dim + 2 * s.n_v_heads
+    hidden = np.concatenate([x["qkv"], x["z"], x["alpha"], x["beta_raw"]], axis=-1)
+    assert hidden.shape[-1] == N
+    r = oracle.layer_verify(s, x, hidden, np.eye(N), np.eye(s.value_dim), store_bf16=False)
+    ref = oracle.verify(s, x)
+    np.testing.assert_array_equal(r["act"], hidden)
+    for k in ("out", "state", "conv_state", "cap_state"):
+        np.testing.assert_array_equal(r[k], ref[k])
+    np.testing.assert_array_equal(r["y"], ref["out"])
+    # a swapped block order (z before qkv) is a different layer
+    sw = np.concatenate([x["z"], x["qkv"], x["alpha"], x["beta_raw"]], axis=-1)
+    assert not np.allclose(oracle.layer_verify(s, x, sw, np.eye(N), np.eye(s.value_dim), store_bf16=False)["out"],
+                           ref["out"])
+
+
+def test_bf16_rounding_matches_the_bit_rounding_of_the_generator():
+    """round_bf16 (frexp / rint) against the generator's independent f32 -> bf16
+    bit rounding on fp32 values (where rounding fp64 directly and rounding the
+    same fp32 value agree), including exact ties, which go to the even
+    neighbour: 1 + 2^-8 -> 1, 1 + 3 2^-8 -> 1 + 2^-6."""
+    from workloads.synth import bf16_bits_to_f64, to_bf16_bits
+    rng = np.random.default_rng(5)
+    v = np.concatenate([rng.normal(size=20000) * 10.0 ** rng.integers(-6, 6, size=20000),
+                        [1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 2.0 ** -100, 0.0, 3.0]]).astype(np.float32)
+    np.testing.assert_array_equal(oracle.round_bf16(v.astype(np.float64)), bf16_bits_to_f64(to_bf16_bits(v)))
+    assert oracle.round_bf16(np.array([1 + 2 ** -8]))[0] == 1.0
+    assert oracle.round_bf16(np.array([1 + 3 * 2 ** -8]))[0] == 1 + 2 ** -6

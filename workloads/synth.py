@@ -139,6 +139,7 @@ class Shape:
     n_layers: int = 1
     seed: int = 0
     chunk: int = 64     # prefill chunk length (prefill workloads only)
+    n_embd: int = 0     # hidden size of the projections around the block (0: the block alone)
 
     @property
     def conv_channels(self) -> int:
@@ -169,11 +170,14 @@ WORKLOADS: Dict[str, Shape] = {
     "lazy_verify": Shape("lazy_verify", 1, 16, 48, 128, 128, 16, "bf16", seed=1),
     "lazy_multislot_verify": Shape("lazy_multislot_verify", 32, 16, 48, 128, 128, 16, "bf16", seed=2),
     "lazy_stack_verify": Shape("lazy_stack_verify", 8, 16, 48, 128, 128, 16, "bf16", n_layers=48, seed=3),
+    # the layer with its projections (hidden 5120): x -> [qkv | z | alpha | beta] -> verify -> y
+    "proj_verify": Shape("proj_verify", 1, 16, 48, 128, 128, 16, "bf16", seed=1, n_embd=5120),
 }
 
 # stream tags (one independent stream per tensor and layer)
 _TAGS = {"qkv": 1, "z": 2, "alpha": 3, "beta_raw": 4, "A_log": 5, "dt_bias": 6,
-         "conv_w": 7, "norm_w": 8, "state": 9, "conv_state": 10, "trim": 11, "parent": 13, "accept": 14}
+         "conv_w": 7, "norm_w": 8, "state": 9, "conv_state": 10, "trim": 11, "parent": 13, "accept": 14,
+         "x": 15, "w_in": 16, "w_out": 17}
 
 
 def _tag(name: str, layer: int) -> int:
@@ -292,3 +296,25 @@ def tree_accept(shape: Shape, parents: np.ndarray, seed: Optional[int] = None, l
     s = shape
     seed = s.seed if seed is None else seed
     return (randint(seed, _tag("accept", layer), s.n_slots, s.n_tokens + 1) - 1).astype(np.int32)
+
+
+def proj_in_rows(shape: Shape) -> int:
+    """Output rows of the fused input projection: qkv channels, z, alpha, beta_raw."""
+    return shape.conv_channels + shape.value_dim + 2 * shape.n_v_heads
+
+
+def make_proj(shape: Shape, layer: int = 0, seed: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """Hidden input and random projection weights of one layer, as bf16 bit patterns
+    (uint16): x [B, T, n_embd] ~ N(0, 1); w_in [C + H_v*d_v + 2*H_v, n_embd] and
+    w_out [n_embd, H_v*d_v] ~ N(0, 1/fan_in), so the projected activations are
+    ~N(0, 1) like the block's own inputs."""
+    s = shape
+    assert s.n_embd > 0
+    seed = s.seed if seed is None else seed
+    E, V = s.n_embd, s.value_dim
+    return {
+        "x": normal_bf16_bits(seed, _tag("x", layer), s.n_slots * s.n_tokens * E).reshape(s.n_slots, s.n_tokens, E),
+        "w_in": normal_bf16_bits(seed, _tag("w_in", layer), proj_in_rows(s) * E, E ** -0.5).reshape(
+            proj_in_rows(s), E),
+        "w_out": normal_bf16_bits(seed, _tag("w_out", layer), E * V, V ** -0.5).reshape(E, V),
+    }
