@@ -10,10 +10,12 @@ a 64-layer hybrid target, 1 slot, 16 QK / 48 V heads, d_k = d_v = 128, K+1 =
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
                     [--workload layer_verify|multislot_verify|stack_verify|prefill|tree_verify|
-                                lazy_verify|lazy_multislot_verify|lazy_stack_verify]
+                                rolled_verify|rolled_multislot_verify|lazy_verify|lazy_multislot_verify|
+                                lazy_stack_verify|proj_verify]
 
 The tree_verify workload verifies a draft tree and rolls back to the accepted
-node; the lazy_* workloads run lazy capture on the same inputs as their
+node; the rolled_* workloads fold each step's rollback into the next verify
+(one launch per step); the lazy_* workloads run lazy capture on the same inputs as their
 capture counterparts: one launch per step commits the pending batch (re-runs
 its accepted tokens) and writes the new batch's outputs, nothing captured.
 
@@ -314,6 +316,8 @@ class VerifyWorkload:
         self.lazy = s.name.startswith("lazy")
         # the layer with its projections: x -> GEMM -> verify (strided activations) -> GEMM -> y
         self.proj = s.n_embd > 0
+        # the rollback of each step folded into the next verify: one launch per step
+        self.rolled = s.name.startswith("rolled")
         per_set = (tree_verify_bytes(s) if self.tree else
                    lazy_step_bytes(s, [0] * s.n_slots) if self.lazy else verify_bytes(s)) * self.layers
         if self.proj:
@@ -362,8 +366,13 @@ class VerifyWorkload:
                     x["act_out"] = x["ws"][out_off:out_off + M * s.value_dim * 2]
                 layers.append(x)
             self.sets.append(layers)
+        if self.rolled:                 # every set's captures start out valid
+            for layers in self.sets:
+                for li, x in enumerate(layers):
+                    gdn.gdn_verify_forward(self.dims, x["params"], x["qkv"], x["z"], x["alpha"], x["beta_raw"],
+                                           x["state"], x["conv_state"], x["cap_state"], x["cap_conv"], x["out"])
         self.tokens_per_step = s.n_slots * s.n_tokens
-        self.kernels_per_step = (1 if self.lazy else 2) * self.layers
+        self.kernels_per_step = (1 if self.lazy or self.rolled else 2) * self.layers
 
     def verify(self, k, li, stream):
         x = self.sets[k][li]
@@ -376,6 +385,11 @@ class VerifyWorkload:
             self.gdn.gdn_layer_verify(self.dims, x["params"], x["w"], x["x"], x["state"], x["conv_state"],
                                       x["cap_state"], x["cap_conv"], x["y"], x["ws"], x["ws_bytes"], x["status"],
                                       stream)
+            return
+        if self.rolled:
+            self.gdn.gdn_verify_after_rollback(self.dims, x["params"], x["trim"], x["qkv"], x["z"], x["alpha"],
+                                               x["beta_raw"], x["state"], x["conv_state"], x["cap_state"],
+                                               x["cap_conv"], x["out"], x["status"], stream)
             return
         if self.lazy:
             self.gdn.gdn_verify_lazy(self.dims, x["params"], x["qkv"], x["z"], x["alpha"], x["beta_raw"],
@@ -398,7 +412,7 @@ class VerifyWorkload:
 
     def rollback(self, k, li, stream):
         x = self.sets[k][li]
-        if self.lazy:                   # the commit rides in the next verify
+        if self.lazy or self.rolled:    # the commit / rollback rides in the next verify
             return
         fn = self.gdn.gdn_rollback_tree if self.tree else self.gdn.gdn_rollback
         fn(self.dims, x["trim"], x["state"], x["conv_state"], x["cap_state"], x["cap_conv"], x["status"], stream)
@@ -411,6 +425,8 @@ class VerifyWorkload:
     def step_bytes(self, k):
         if self.lazy:
             return sum(lazy_step_bytes(self.shape, self.trims[k][li]) for li in range(self.layers))
+        if self.rolled:                 # the captured state replaces the state as the verify's input
+            return verify_bytes(self.shape) * self.layers
         if self.proj:
             s = self.shape
             return sum(verify_bytes(s) + proj_in_bytes(s) + proj_out_bytes(s) + rollback_bytes(s, self.trims[k][li])
@@ -656,6 +672,8 @@ def run_cuda(args):
         kdur = {"prefill": kernel_duration(torch, wl, "prefill", 2)}
     elif wl.lazy:
         kdur = {"lazy_verify": kernel_duration(torch, wl, "verify", n_launch)}
+    elif wl.rolled:
+        kdur = {"verify": kernel_duration(torch, wl, "verify", n_launch)}
     elif wl.proj:
         # the layer call is GEMM + verify + GEMM; what it takes beyond the two GEMMs timed alone is the
         # verify plus the launch gaps between the library's kernels and it
@@ -700,6 +718,7 @@ def run_cuda(args):
             "act_dtype": shape.act, "state_dtype": "f32",
             "step": ("chunked prefill" if args.workload == "prefill" else
                      "layer: input projection GEMM + verify + output projection GEMM, then rollback" if wl.proj else
+                     "verify with the previous step's rollback folded in (one launch)" if wl.rolled else
                      "lazy verify: commit of the pending batch (accepted-prefix re-run) + outputs of the new one"
                      if wl.lazy else
                      "verify+rollback"),
@@ -770,6 +789,10 @@ def _oracle_pass(shape, x, heads, n_threads, trims):
         return
     if shape.name == "prefill":
         oracle.verify(shape, x, capture=False, head_mask=heads, n_threads=n_threads)
+        return
+    if shape.name.startswith("rolled"):         # the same work as verify + rollback
+        r = oracle.verify(shape, x, head_mask=heads, n_threads=n_threads)
+        oracle.rollback(shape, trims, r["state"], r["conv_state"], r["cap_state"], r["cap_conv"])
         return
     if shape.name.startswith("lazy"):
         oracle.verify(shape, x, capture=False, head_mask=heads, n_threads=n_threads)

@@ -35,7 +35,7 @@ GDN_F32 = 0
 GDN_BF16 = 1
 
 EXPORTED_SYMBOLS = ("gdn_verify_forward", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_tree",
-                    "gdn_verify_lazy", "gdn_commit_lazy", "gdn_proj_in_ld", "gdn_layer_workspace_bytes",
+                    "gdn_verify_after_rollback", "gdn_verify_lazy", "gdn_commit_lazy", "gdn_proj_in_ld", "gdn_layer_workspace_bytes",
                     "gdn_project_in", "gdn_project_out", "gdn_layer_verify", "gdn_prefill_workspace_bytes",
                     "gdn_prefill_chunked", "gdn_prefill_chunked_static", "gdn_last_error", "gdn_version")
 
@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_verify_tree.restype = ip
         L.gdn_rollback_tree.argtypes = [ctypes.POINTER(Dims)] + [vp] * 7
         L.gdn_rollback_tree.restype = ip
+        L.gdn_verify_after_rollback.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 12
+        L.gdn_verify_after_rollback.restype = ip
         L.gdn_verify_lazy.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 13
         L.gdn_verify_lazy.restype = ip
         L.gdn_commit_lazy.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 8
@@ -178,6 +180,16 @@ def gdn_rollback_tree(dims: Dims, d_accept, state, conv_state, cap_state, cap_co
                       stream=None) -> None:
     _check(lib().gdn_rollback_tree(ctypes.byref(dims), _ptr(d_accept), _ptr(state), _ptr(conv_state),
                                    _ptr(cap_state), _ptr(cap_conv), _ptr(d_status), _stream(stream)))
+
+
+def gdn_verify_after_rollback(dims: Dims, params: LayerParams, d_prev_trim, qkv, z, alpha, beta_raw, state,
+                              conv_state, cap_state, cap_conv, out, d_status=None, stream=None) -> None:
+    """Verify starting from what gdn_rollback(d_prev_trim) would leave, read from the
+    previous batch's captures (which this call overwrites)."""
+    _check(lib().gdn_verify_after_rollback(ctypes.byref(dims), ctypes.byref(params), _ptr(d_prev_trim), _ptr(qkv),
+                                           _ptr(z), _ptr(alpha), _ptr(beta_raw), _ptr(state), _ptr(conv_state),
+                                           _ptr(cap_state), _ptr(cap_conv), _ptr(out), _ptr(d_status),
+                                           _stream(stream)))
 
 
 def gdn_verify_lazy(dims: Dims, params: LayerParams, qkv, z, alpha, beta_raw, state, conv_state, out,

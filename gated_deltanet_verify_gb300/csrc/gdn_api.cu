@@ -208,6 +208,18 @@ int gdn_verify_tree(const gdn_dims *dims, const gdn_layer_params *params, const 
                        const_cast<float *>(conv_state), cap_state, cap_conv, out, d_status, stream, gdn::kTree);
 }
 
+int gdn_verify_after_rollback(const gdn_dims *dims, const gdn_layer_params *params, const int32_t *d_prev_trim,
+                              const void *qkv, const void *z, const void *alpha, const void *beta_raw,
+                              float *state, float *conv_state, float *cap_state, float *cap_conv, void *out,
+                              int *d_status, void *stream) {
+    g_err.clear();
+    if (!d_prev_trim) return fail(GDN_ERR_ARG, "trim is NULL");
+    if (!cap_state || !cap_conv)
+        return fail(GDN_ERR_NO_CAPTURE, "the previous batch's captures (cap_state, cap_conv) are needed");
+    return verify_impl(dims, params, qkv, z, alpha, beta_raw, nullptr, state, conv_state, cap_state, cap_conv, out,
+                       d_status, stream, gdn::kRolled, d_prev_trim);
+}
+
 int gdn_verify_lazy(const gdn_dims *dims, const gdn_layer_params *params, const int32_t *d_prev_trim,
                     const void *prev_qkv, const void *prev_alpha, const void *prev_beta_raw, const void *qkv,
                     const void *z, const void *alpha, const void *beta_raw, float *state, float *conv_state,

@@ -12,9 +12,10 @@
 
 namespace gdn {
 
-// Verify kernel modes: the chain, a draft tree, lazy (outputs only) and the
-// lazy commit (re-run of each slot's accepted tokens).
-enum VerifyMode { kChain = 0, kTree = 1, kLazy = 2, kCommit = 3 };
+// Verify kernel modes: the chain, a draft tree, lazy (outputs only), the
+// lazy commit (re-run of each slot's accepted tokens), and the chain started
+// from the previous batch's captures (its rollback folded in).
+enum VerifyMode { kChain = 0, kTree = 1, kLazy = 2, kCommit = 3, kRolled = 4 };
 
 // Everything one verify launch needs, validated on the host.
 struct VerifyArgs {
@@ -31,7 +32,8 @@ struct VerifyArgs {
     void *out;
     int *d_status;                    // device status word (may be NULL)
     const int32_t *parent;            // tree verify: [B][T] parent of each token
-    const int32_t *trim;              // lazy commit, or the pending batch of a lazy verify: [B] trims, 0 .. T-1
+    const int32_t *trim;              // [B] trims, 0 .. T-1: lazy commit, a lazy verify's pending batch, or the
+                                      // previous batch's rollback folded into a verify
     const void *qkv_prev, *alpha_prev, *beta_prev;   // lazy verify: the pending batch (same layouts)
     int mode;                         // VerifyMode
 };

@@ -55,6 +55,11 @@
 //           state, writes the state and conv state after them, and continues
 //           from there into the new batch: the commit of one step rides in the
 //           verify of the next.
+//   kRolled the chain verify started from the state a rollback of the
+//           previous batch would leave: per slot, the captured state
+//           cap[T-1-trim] and the window rows after that token, read from the
+//           previous verify's capture buffers (which this launch then
+//           overwrites with its own captures), so a step is one launch.
 //   kCommit the lazy counterpart of a rollback: per slot, re-runs the first
 //           T - trim[s] tokens from the state before the batch and writes the
 //           state and conv state after them; no z, no outputs.  Since the
@@ -119,6 +124,18 @@ __device__ __forceinline__ float4 ld_na4(const float *p) {
     asm volatile("ld.global.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];\n"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                  : "l"(p));
+    return v;
+}
+
+// Warm L2 with the line holding p.  Nothing comes back to the SM, so this may
+// run before the grid-dependency wait: a line the previous kernel is still
+// writing stays coherent in L2, and the real loads come after the wait.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+__device__ __forceinline__ int ld_relaxed_s32(const int32_t *p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 
@@ -210,7 +227,7 @@ struct Smem {
 template <int DK, typename Act, int MODE>
 __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs a) {
     static_assert(DK == 32 || DK == 64 || DK == 128, "d_k must be 32, 64 or 128");
-    constexpr bool TREE = MODE == kTree, LAZY = MODE == kLazy, COMMIT = MODE == kCommit;
+    constexpr bool TREE = MODE == kTree, LAZY = MODE == kLazy, COMMIT = MODE == kCommit, ROLLED = MODE == kRolled;
     constexpr int LR = DK >= 64 ? 16 : 8;          // lanes per row group
     constexpr int NG = 32 / LR;                    // row groups per warp
     constexpr int RPG = kRowsPerWarp / NG;         // rows per group
@@ -269,11 +286,46 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         // the single arrival; the phase completes once every partial of the head has landed
         mbar_arrive_expect_tx(redbar, uint32_t(T * P * WARPS * 4));
     }
+    {
+        // while the previous kernel finishes: L2 prefetch of this CTA's state rows (for a rolled verify the
+        // captured ones, at a trim read early -- possibly stale, only an address) and of its activation
+        // segments (q, k of the key head, its own v and z rows), one 128-byte line per prefetch
+        constexpr int kLine = 128;
+        const float *st = a.state + ((size_t(s) * Hv + h) * DV + j0) * DK;
+        if constexpr (ROLLED) {
+            int tr = a.trim ? ld_relaxed_s32(a.trim + s) : 0;
+            tr = tr < 0 ? 0 : (tr >= T ? T - 1 : tr);
+            st = a.cap_state + ((size_t(s) * T + (T - 1 - tr)) * Hv + h) * DV * DK + size_t(j0) * DK;
+        }
+        const int st_lines = ROWS * DK * 4 / kLine;
+        for (int i = tid; i < st_lines; i += nthr) prefetch_l2(reinterpret_cast<const char *>(st) + size_t(i) * kLine);
+        constexpr int qk_lines = DK * int(sizeof(Act)) / kLine;          // 0 when a segment is below a line
+        const int seg = qk_lines > 0 ? 2 * qk_lines + 2 : 4;
+        const Act *qkv = static_cast<const Act *>(a.qkv);
+        const Act *zp = static_cast<const Act *>(a.z);
+        for (int i = tid; i < T * seg; i += nthr) {
+            const int t = i / seg, w = i % seg;
+            const size_t rw = size_t(s) * a.Ts + t;
+            const Act *p;
+            if (w < seg - 2) {
+                const int half = qk_lines > 0 ? qk_lines : 1;
+                const int part = w / half, l = w % half;
+                p = qkv + rw * a.ld_qkv + size_t(part ? Hk + kh : kh) * DK + size_t(l) * (kLine / sizeof(Act));
+            } else if (w == seg - 2) {
+                p = qkv + rw * a.ld_qkv + size_t(2 * Hk) * DK + size_t(h) * DV + j0;
+            } else {
+                if (COMMIT) continue;
+                p = zp + rw * a.ld_z + size_t(h) * DV + j0;
+            }
+            prefetch_l2(p);
+        }
+    }
     // everything below may read what the previous kernel in the stream wrote
     grid_dependency_wait();
     int TT = T;                                 // tokens run for this slot
     int n_prev = 0;                             // lazy: the pending batch's accepted tokens, run first
-    if constexpr (COMMIT || LAZY) {
+    int src_tok = 0;                            // rolled: the previous batch's accepted token
+    if constexpr (COMMIT || LAZY || ROLLED) {
         if (a.trim) {
             const int tr = a.trim[s];           // uniform over the cluster: one slot
             if (tr < 0 || tr >= T) {            // reported; the slot is left untouched
@@ -282,6 +334,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
                 return;
             }
             if constexpr (COMMIT) TT = T - tr;
+            else if constexpr (ROLLED) src_tok = T - 1 - tr;
             else {
                 n_prev = T - tr;
                 TT = n_prev + T;
@@ -297,7 +350,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     const int my_rho = (b >> 1) & (RPG - 1);
     float S[RPG][NCL][4];
     {
-        const float *src = a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b;
+        const float *src = ROLLED ? a.cap_state + ((size_t(s) * T + src_tok) * Hv + h) * DV * DK +
+                                        size_t(j0 + row0) * DK + 4 * b
+                                  : a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b;
 #pragma unroll
         for (int rho = 0; rho < RPG; ++rho)
 #pragma unroll
@@ -343,6 +398,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
             const int c0 = w < fq ? w * 4 : (w < 2 * fq ? DK + (w - fq) * 4 : 2 * DK + (w - 2 * fq) * 4);
             const int g0 = gchan(c0);
             if (rrow < 4) cp_async16(cw + rrow * NCH + c0, a.conv_w + size_t(rrow) * C + g0);
+            else if (ROLLED)        // window rows after the accepted token of the previous batch
+                cp_async16(cs + (rrow - 4) * NCH + c0,
+                           a.cap_conv + (size_t(s) * (3 + T) + src_tok + 1 + (rrow - 4)) * C + g0);
             else cp_async16(cs + (rrow - 4) * NCH + c0, a.conv_state + (size_t(s) * 3 + (rrow - 4)) * C + g0);
         }
         if constexpr (!COMMIT)
@@ -570,7 +628,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
                 const int t = i / (3 * n4), rr = (i / n4) % 3, c = c_first + 4 * (i % n4);
                 store4(base + (size_t(t) * 3 + rr) * C + gchan(c), win4(trow[t * 4 + 1 + rr], c));
             }
-        } else if (a.cap_conv) {
+        } else if (a.cap_conv && !ROLLED) {
             // conv window capture: concat(old conv state, new tokens) of the channels this CTA owns
             const int c_first = qk_writer ? 0 : 2 * DK;
             const int n4 = (NCH - c_first) / 4;
@@ -582,6 +640,17 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         }
         __syncwarp();
         cluster_wait_acquire();            // phase 1: every peer's mbarrier is initialised
+        if constexpr (ROLLED) {
+            // the window capture overwrites the rows every CTA of the cluster read its old conv state
+            // from: only after cluster phase 1
+            const int c_first = qk_writer ? 0 : 2 * DK;
+            const int n4 = (NCH - c_first) / 4;
+            float *base = a.cap_conv + size_t(s) * (3 + T) * C;
+            for (int i = tid; i < (3 + T) * n4; i += nthr) {
+                const int rho = i / n4, c = c_first + 4 * (i % n4);
+                store4(base + size_t(rho) * C + gchan(c), win4(rho, c));
+            }
+        }
         if constexpr (!COMMIT) {
             // this warp's sums of o^2 per token, sent to the allp table of every CTA of this head
             const int first_rank = (h - kh * a.r) * P;
@@ -653,7 +722,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
             store4(base + size_t(rr) * C + gchan(c), win4(n_prev + rr, c));
         }
     }
-    if constexpr (MODE == kChain) {
+    if constexpr (MODE == kChain || ROLLED) {
         // conv state <- window rows T .. T+2 (after cluster phase 1: every reader is done)
         const int c_first = qk_writer ? 0 : 2 * DK;
         const int n4 = (NCH - c_first) / 4;
@@ -730,6 +799,7 @@ cudaError_t launch_verify(const VerifyArgs &a, gdn_dtype act, cudaStream_t strea
         case kTree: return launch_mode<kTree>(a, bf, stream);
         case kLazy: return launch_mode<kLazy>(a, bf, stream);
         case kCommit: return launch_mode<kCommit>(a, bf, stream);
+        case kRolled: return launch_mode<kRolled>(a, bf, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -165,6 +165,26 @@ int gdn_rollback_tree(const gdn_dims *dims, const int32_t *d_accept, float *stat
                       const float *cap_state, const float *cap_conv, int *d_status, void *stream);
 
 /*
+ * gdn_verify_after_rollback: a verify step with the previous step's rollback
+ * folded in (one launch per step instead of a verify and a rollback).
+ * cap_state / cap_conv hold the previous gdn_verify_forward (or
+ * gdn_verify_after_rollback) of the same dims, not yet rolled back; d_prev_trim
+ * is a DEVICE int32[B] with gdn_rollback's meaning.  Per slot the batch starts
+ * from exactly what gdn_rollback(d_prev_trim) would leave -- the captured
+ * state cap_state[s][T-1-trim] and the window rows after that token -- and
+ * state / conv_state are not read.  Everything else is gdn_verify_forward:
+ * outputs, the new captures (overwriting the old ones), state and conv_state
+ * after all T tokens, bit-identical to gdn_rollback followed by
+ * gdn_verify_forward.  A trim outside [0, T-1] leaves the slot untouched (no
+ * outputs) and writes GDN_ERR_TRIM_RANGE to *d_status.  Without capture
+ * buffers: GDN_ERR_NO_CAPTURE.
+ */
+int gdn_verify_after_rollback(const gdn_dims *dims, const gdn_layer_params *params, const int32_t *d_prev_trim,
+                              const void *qkv, const void *z, const void *alpha, const void *beta_raw,
+                              float *state, float *conv_state, float *cap_state, float *cap_conv,
+                              void *out, int *d_status, void *stream);
+
+/*
  * Lazy capture: the byte-saving alternative to per-position capture.  Instead
  * of writing the state after every token and copying one back, a lazy verify
  * writes only its outputs and leaves the batch "pending": state and
