@@ -620,7 +620,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         // the next kernel in the stream may start launching (it waits for this grid's completion itself)
         grid_launch_dependents();
         if constexpr (TREE) {
-            // conv state after each node: the window rows of its taps 1, 2, 3, channels this CTA owns
+            // conv state after each node: the window rows of its taps 1, 2, 3, channels this CTA owns (a large
+            // store burst, measured to be better issued before the RMSNorm exchange)
             const int c_first = qk_writer ? 0 : 2 * DK;
             const int n4 = (NCH - c_first) / 4;
             float *base = a.cap_conv + size_t(s) * T * 3 * C;
@@ -628,29 +629,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
                 const int t = i / (3 * n4), rr = (i / n4) % 3, c = c_first + 4 * (i % n4);
                 store4(base + (size_t(t) * 3 + rr) * C + gchan(c), win4(trow[t * 4 + 1 + rr], c));
             }
-        } else if (a.cap_conv && !ROLLED) {
-            // conv window capture: concat(old conv state, new tokens) of the channels this CTA owns
-            const int c_first = qk_writer ? 0 : 2 * DK;
-            const int n4 = (NCH - c_first) / 4;
-            float *base = a.cap_conv + size_t(s) * (3 + T) * C;
-            for (int i = tid; i < (3 + T) * n4; i += nthr) {
-                const int rho = i / n4, c = c_first + 4 * (i % n4);
-                store4(base + size_t(rho) * C + gchan(c), win4(rho, c));
-            }
         }
         __syncwarp();
-        cluster_wait_acquire();            // phase 1: every peer's mbarrier is initialised
-        if constexpr (ROLLED) {
-            // the window capture overwrites the rows every CTA of the cluster read its old conv state
-            // from: only after cluster phase 1
-            const int c_first = qk_writer ? 0 : 2 * DK;
-            const int n4 = (NCH - c_first) / 4;
-            float *base = a.cap_conv + size_t(s) * (3 + T) * C;
-            for (int i = tid; i < (3 + T) * n4; i += nthr) {
-                const int rho = i / n4, c = c_first + 4 * (i % n4);
-                store4(base + size_t(rho) * C + gchan(c), win4(rho, c));
-            }
-        }
+        cluster_wait_acquire();            // phase 1: every peer's mbarrier is initialised, every old conv row read
         if constexpr (!COMMIT) {
             // this warp's sums of o^2 per token, sent to the allp table of every CTA of this head
             const int first_rank = (h - kh * a.r) * P;
@@ -664,6 +645,17 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
                 const uint32_t rank = uint32_t(first_rank + dst_p);
                 const uint32_t off = uint32_t((size_t(t) * P * WARPS + p * WARPS + wid) * 4);
                 st_async_f32(map_cluster(allp_local + off, rank), acc, map_cluster(redbar, rank));
+            }
+        }
+        if constexpr (!TREE) if (a.cap_conv) {
+            // conv window capture: concat(old conv state, new tokens) of the channels this CTA owns (a rolled
+            // verify read its old conv rows from these very rows: after cluster phase 1 like everything here)
+            const int c_first = qk_writer ? 0 : 2 * DK;
+            const int n4 = (NCH - c_first) / 4;
+            float *base = a.cap_conv + size_t(s) * (3 + T) * C;
+            for (int i = tid; i < (3 + T) * n4; i += nthr) {
+                const int rho = i / n4, c = c_first + 4 * (i % n4);
+                store4(base + size_t(rho) * C + gchan(c), win4(rho, c));
             }
         }
         if constexpr (!TREE && !LAZY) {    // a tree or lazy verify leaves the state as it was
