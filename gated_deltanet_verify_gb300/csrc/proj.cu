@@ -55,7 +55,15 @@ const char *lt_name(cublasStatus_t s) {
         }                                                                             \
     } while (0)
 
-bool make_plan(Plan &p, cublasLtHandle_t h, std::string &why) {
+void free_plan(Plan &p) {
+    if (p.d) cublasLtMatrixLayoutDestroy(p.d);
+    if (p.b) cublasLtMatrixLayoutDestroy(p.b);
+    if (p.a) cublasLtMatrixLayoutDestroy(p.a);
+    if (p.op) cublasLtMatmulDescDestroy(p.op);
+    p.op = nullptr; p.a = p.b = p.d = nullptr;
+}
+
+bool make_plan_steps(Plan &p, cublasLtHandle_t h, std::string &why) {
     LT_TRY(cublasLtMatmulDescCreate(&p.op, CUBLAS_COMPUTE_32F, CUDA_R_32F), "matmul descriptor");
     const cublasOperation_t tA = CUBLAS_OP_T, tB = CUBLAS_OP_N;
     LT_TRY(cublasLtMatmulDescSetAttribute(p.op, CUBLASLT_MATMUL_DESC_TRANSA, &tA, sizeof(tA)), "transa");
@@ -79,6 +87,13 @@ bool make_plan(Plan &p, cublasLtHandle_t h, std::string &why) {
     }
     p.algo = res.algo;
     return true;
+}
+
+// a plan whose setup failed half way releases what it created
+bool make_plan(Plan &p, cublasLtHandle_t h, std::string &why) {
+    if (make_plan_steps(p, h, why)) return true;
+    free_plan(p);
+    return false;
 }
 
 }  // namespace
