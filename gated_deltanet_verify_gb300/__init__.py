@@ -27,9 +27,11 @@ GDN_ERR_LAUNCH = 7
 GDN_ERR_TIMEOUT = 8
 GDN_ERR_WORKSPACE = 9
 GDN_ERR_TREE = 10
+GDN_ERR_BOUNDS = 11
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_ALIGN", 4: "GDN_ERR_DTYPE",
                 5: "GDN_ERR_TRIM_RANGE", 6: "GDN_ERR_NO_CAPTURE", 7: "GDN_ERR_LAUNCH", 8: "GDN_ERR_TIMEOUT",
-                9: "GDN_ERR_WORKSPACE", 10: "GDN_ERR_TREE"}
+                9: "GDN_ERR_WORKSPACE", 10: "GDN_ERR_TREE",
+                11: "GDN_ERR_BOUNDS"}
 
 GDN_F32 = 0
 GDN_BF16 = 1

@@ -19,6 +19,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdn_verify.so")
+# the checked variant: every global access of the verify-family and rollback kernels bounds-checked
+CHECKED_BUILD = os.path.join(PKG, "_build_checked")
+CHECKED_LIB = os.path.join(PKG, "libgdn_verify_checked.so")
 
 SOURCES = ["gdn_api.cu", "verify.cu", "rollback.cu", "prefill.cu", "proj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -57,26 +60,32 @@ def _stale(target: str, deps: List[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _machine_marker() -> str:
+def _machine_marker(build_dir: str, lib: str) -> str:
     """Objects from another host architecture (e.g. an x86 build copied to an
     aarch64 machine) are discarded rather than linked."""
-    m = os.path.join(BUILD, "MACHINE")
+    m = os.path.join(build_dir, "MACHINE")
     here = platform.machine()
     prev = open(m).read().strip() if os.path.exists(m) else None
     if prev != here:
-        for f in os.listdir(BUILD):
+        for f in os.listdir(build_dir):
             if f.endswith(".o"):
-                os.remove(os.path.join(BUILD, f))
-        if os.path.exists(LIB):
-            os.remove(LIB)
+                os.remove(os.path.join(build_dir, f))
+        if os.path.exists(lib):
+            os.remove(lib)
         with open(m, "w") as fh:
             fh.write(here + "\n")
     return here
 
 
-def build(verbose: bool = False, extra_flags: List[str] = ()) -> str:
+def build(verbose: bool = False, extra_flags: List[str] = (), checked: bool = False) -> str:
+    """Build libgdn_verify.so, or with ``checked`` the bounds-checked variant
+    libgdn_verify_checked.so (-DGDN_CHECKED=1, its own object directory)."""
+    BUILD = CHECKED_BUILD if checked else globals()["BUILD"]
+    LIB = CHECKED_LIB if checked else globals()["LIB"]
+    if checked:
+        extra_flags = [*extra_flags, "-DGDN_CHECKED=1"]
     os.makedirs(BUILD, exist_ok=True)
-    _machine_marker()
+    _machine_marker(BUILD, LIB)
     cc = nvcc()
     hdrs = _headers()
     jobs = []

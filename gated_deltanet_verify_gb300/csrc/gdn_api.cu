@@ -129,7 +129,7 @@ extern "C" {
 
 const char *gdn_last_error(void) { return g_err.c_str(); }
 
-const char *gdn_version(void) { return "gdn-verify 0.1.0 (sm_103a)"; }
+const char *gdn_version(void) { return GDN_CHECKED ? "gdn-verify 0.1.0 (sm_103a, checked)" : "gdn-verify 0.1.0 (sm_103a)"; }
 
 static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, const void *qkv, const void *z,
                        const void *alpha, const void *beta_raw, const int32_t *d_parent, float *state,
@@ -183,6 +183,24 @@ static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, con
     a.trim = d_trim;
     a.qkv_prev = qkv_prev; a.alpha_prev = alpha_prev; a.beta_prev = beta_prev;
     a.mode = mode;
+    {   // extents in bytes (the bounds checks of a checked build)
+        const size_t ab = size_t(act_bytes), M = size_t(d.n_slots) * d.n_tokens;
+        const size_t st = size_t(d.n_slots) * d.n_v_heads * d.d_v * d.d_k * 4, V = size_t(d.n_v_heads) * d.d_v;
+        a.ext_qkv = ((M - 1) * size_t(a.ld_qkv) + size_t(a.C)) * ab;
+        a.ext_z = ((M - 1) * size_t(a.ld_z) + V) * ab;
+        a.ext_ab = ((M - 1) * size_t(a.ld_ab) + size_t(d.n_v_heads)) * ab;
+        a.ext_state = st;
+        a.ext_conv_state = size_t(d.n_slots) * 3 * size_t(a.C) * 4;
+        a.ext_cap_state = st * size_t(d.n_tokens);
+        a.ext_cap_conv = size_t(d.n_slots) * (mode == gdn::kTree ? 3 * size_t(d.n_tokens) : 3 + size_t(d.n_tokens)) *
+                         size_t(a.C) * 4;
+        a.ext_out = M * V * ab;
+        a.ext_conv_w = 4 * size_t(a.C) * 4;
+        a.ext_head = size_t(d.n_v_heads) * 4;
+        a.ext_norm_w = size_t(d.d_v) * 4;
+        a.ext_parent = M * 4;
+        a.ext_trim = size_t(d.n_slots) * 4;
+    }
     cudaError_t e = gdn::launch_verify(a, d.act_dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "verify launch failed: %s", cudaGetErrorString(e));
     return GDN_OK;
@@ -258,6 +276,10 @@ static int rollback_impl(const gdn_dims *dims, const int32_t *d_trim, float *sta
     a.trim = d_trim; a.state = state; a.conv_state = conv_state; a.cap_state = cap_state; a.cap_conv = cap_conv;
     a.d_status = d_status;
     a.tree = tree;
+    a.ext_state = size_t(a.B) * size_t(a.state_elems) * 4;
+    a.ext_conv_state = size_t(a.B) * size_t(a.conv_elems) * 4;
+    a.ext_cap_state = size_t(a.B) * a.T * size_t(a.state_elems) * 4;
+    a.ext_cap_conv = size_t(a.B) * (tree ? size_t(a.T) * a.W1 : size_t(a.W1 + a.T)) * size_t(a.C) * 4;
     cudaError_t e = gdn::launch_rollback(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "rollback launch failed: %s", cudaGetErrorString(e));
     return GDN_OK;

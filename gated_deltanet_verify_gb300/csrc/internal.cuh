@@ -9,6 +9,7 @@
 #include <string>
 
 #include "gdn_verify.h"
+#include "check.cuh"
 
 namespace gdn {
 
@@ -36,6 +37,9 @@ struct VerifyArgs {
                                       // previous batch's rollback folded into a verify
     const void *qkv_prev, *alpha_prev, *beta_prev;   // lazy verify: the pending batch (same layouts)
     int mode;                         // VerifyMode
+    // buffer extents in bytes, for the bounds checks of a checked build
+    size_t ext_qkv, ext_z, ext_ab, ext_state, ext_conv_state, ext_cap_state, ext_cap_conv, ext_out;
+    size_t ext_conv_w, ext_head, ext_norm_w, ext_parent, ext_trim;
 };
 
 struct RollbackArgs {
@@ -48,6 +52,7 @@ struct RollbackArgs {
     const float *cap_state, *cap_conv;
     int *d_status;
     int tree;                         // 1: cap_conv holds per-node conv states [B][T][W-1][C]
+    size_t ext_state, ext_conv_state, ext_cap_state, ext_cap_conv;   // bytes, for a checked build
 };
 
 // Everything one chunkwise prefill launch needs (d_k = d_v = 128, W = 4).

@@ -35,6 +35,11 @@ __global__ void __launch_bounds__(kThreads) rollback_kernel(const RollbackArgs a
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int s = blockIdx.y;
+    // a checked build tests each global access against its buffer first (compiled away otherwise)
+    auto chk = [&](const void *p, size_t bytes, const void *base, size_t ext) -> bool {
+        return in_bounds(p, bytes, base, ext, a.d_status);
+    };
+    if (!chk(a.trim + s, 4, a.trim, size_t(a.B) * 4)) return;
     const int idx = __ldg(a.trim + s);
     int accepted_idx;
     if (a.tree) {
@@ -64,13 +69,22 @@ __global__ void __launch_bounds__(kThreads) rollback_kernel(const RollbackArgs a
     for (; i + (kUnroll - 1) * stride < n4_state; i += kUnroll * stride) {
         float4 v[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = ld_nc4(src_s + i + u * stride);
+        for (int u = 0; u < kUnroll; ++u)
+            v[u] = chk(src_s + i + u * stride, 16, a.cap_state, a.ext_cap_state) ? ld_nc4(src_s + i + u * stride)
+                                                                                : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) dst_s[i + u * stride] = v[u];
+        for (int u = 0; u < kUnroll; ++u)
+            if (chk(dst_s + i + u * stride, 16, a.state, a.ext_state)) dst_s[i + u * stride] = v[u];
     }
     for (; i < total; i += stride) {
-        if (i < n4_state) dst_s[i] = ld_nc4(src_s + i);
-        else dst_c[i - n4_state] = ld_nc4(src_c + (i - n4_state));
+        if (i < n4_state) {
+            if (chk(src_s + i, 16, a.cap_state, a.ext_cap_state) && chk(dst_s + i, 16, a.state, a.ext_state))
+                dst_s[i] = ld_nc4(src_s + i);
+        } else {
+            const long long j = i - n4_state;
+            if (chk(src_c + j, 16, a.cap_conv, a.ext_cap_conv) && chk(dst_c + j, 16, a.conv_state, a.ext_conv_state))
+                dst_c[j] = ld_nc4(src_c + j);
+        }
     }
 }
 

@@ -264,6 +264,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     const uint32_t redbar = smem_u32(smem_raw + L.redbar);
     int *tpar = reinterpret_cast<int *>(smem_raw + L.arow);     // tree: [T] parents, then [T][4] window rows
     int *trow = tpar + T;
+    // a checked build tests each global access against its buffer first (compiled away otherwise)
+    auto chk = [&](const void *ptr, size_t bytes, const void *base, size_t ext) -> bool {
+        return in_bounds(ptr, bytes, base, ext, a.d_status);
+    };
     const int NCH = L.NCH;
 
     // local channel c -> global conv channel
@@ -292,13 +296,18 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         // segments (q, k of the key head, its own v and z rows), one 128-byte line per prefetch
         constexpr int kLine = 128;
         const float *st = a.state + ((size_t(s) * Hv + h) * DV + j0) * DK;
+        const float *st_base = ROLLED ? a.cap_state : a.state;
+        const size_t st_ext = ROLLED ? a.ext_cap_state : a.ext_state;
         if constexpr (ROLLED) {
-            int tr = a.trim ? ld_relaxed_s32(a.trim + s) : 0;
+            int tr = a.trim && chk(a.trim + s, 4, a.trim, a.ext_trim) ? ld_relaxed_s32(a.trim + s) : 0;
             tr = tr < 0 ? 0 : (tr >= T ? T - 1 : tr);
             st = a.cap_state + ((size_t(s) * T + (T - 1 - tr)) * Hv + h) * DV * DK + size_t(j0) * DK;
         }
         const int st_lines = ROWS * DK * 4 / kLine;
-        for (int i = tid; i < st_lines; i += nthr) prefetch_l2(reinterpret_cast<const char *>(st) + size_t(i) * kLine);
+        for (int i = tid; i < st_lines; i += nthr) {
+            const char *line = reinterpret_cast<const char *>(st) + size_t(i) * kLine;
+            if (chk(line, 1, st_base, st_ext)) prefetch_l2(line);
+        }
         constexpr int qk_lines = DK * int(sizeof(Act)) / kLine;          // 0 when a segment is below a line
         const int seg = qk_lines > 0 ? 2 * qk_lines + 2 : 4;
         const Act *qkv = static_cast<const Act *>(a.qkv);
@@ -307,17 +316,21 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
             const int t = i / seg, w = i % seg;
             const size_t rw = size_t(s) * a.Ts + t;
             const Act *p;
+            bool ok;
             if (w < seg - 2) {
                 const int half = qk_lines > 0 ? qk_lines : 1;
                 const int part = w / half, l = w % half;
                 p = qkv + rw * a.ld_qkv + size_t(part ? Hk + kh : kh) * DK + size_t(l) * (kLine / sizeof(Act));
+                ok = chk(p, 1, qkv, a.ext_qkv);
             } else if (w == seg - 2) {
                 p = qkv + rw * a.ld_qkv + size_t(2 * Hk) * DK + size_t(h) * DV + j0;
+                ok = chk(p, 1, qkv, a.ext_qkv);
             } else {
                 if (COMMIT) continue;
                 p = zp + rw * a.ld_z + size_t(h) * DV + j0;
+                ok = chk(p, 1, zp, a.ext_z);
             }
-            prefetch_l2(p);
+            if (ok) prefetch_l2(p);
         }
     }
     // everything below may read what the previous kernel in the stream wrote
@@ -327,7 +340,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     int src_tok = 0;                            // rolled: the previous batch's accepted token
     if constexpr (COMMIT || LAZY || ROLLED) {
         if (a.trim) {
-            const int tr = a.trim[s];           // uniform over the cluster: one slot
+            // uniform over the cluster: one slot (an unreadable trim counts as out of range)
+            const int tr = chk(a.trim + s, 4, a.trim, a.ext_trim) ? a.trim[s] : -1;
             if (tr < 0 || tr >= T) {            // reported; the slot is left untouched
                 if (tid == 0 && blockIdx.x == 0 && a.d_status)
                     atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TRIM_RANGE));
@@ -357,7 +371,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         for (int rho = 0; rho < RPG; ++rho)
 #pragma unroll
             for (int m = 0; m < NCL; ++m) {
-                const float4 v = ld_na4(src + size_t(rho) * DK + 4 * LR * m);
+                const float *q = src + size_t(rho) * DK + 4 * LR * m;
+                const float4 v = chk(q, 16, ROLLED ? a.cap_state : a.state, ROLLED ? a.ext_cap_state : a.ext_state)
+                                     ? ld_na4(q) : make_float4(0.f, 0.f, 0.f, 0.f);
                 S[rho][m][0] = v.x; S[rho][m][1] = v.y; S[rho][m][2] = v.z; S[rho][m][3] = v.w;
             }
     }
@@ -375,6 +391,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
             const size_t rw = size_t(s) * a.Ts + (pend ? t : t - n_prev);
             const Act *src;
             Act *dst;
+            const void *base = qkv;
+            size_t ext = a.ext_qkv;
             if (w < vq) {
                 src = qkv + rw * a.ld_qkv + size_t(kh) * DK + w * kPer16;
                 dst = xs + size_t(t) * NCH + w * kPer16;
@@ -388,8 +406,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
                 if (pend) continue;                 // no outputs for the pending tokens
                 src = z + rw * a.ld_z + size_t(h) * DV + j0 + (w - 2 * vq - vv) * kPer16;
                 dst = zs + size_t(t - n_prev) * ROWS + (w - 2 * vq - vv) * kPer16;
+                base = z;
+                ext = a.ext_z;
             }
-            cp_async16(dst, src);
+            if (chk(src, 16, base, ext)) cp_async16(dst, src);
         }
         // conv weights (4 rows) and old conv state (3 rows), per segment in float4s
         const int fq = DK / 4, fv = ROWS / 4, per_row = 2 * fq + fv;
@@ -397,27 +417,38 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
             const int rrow = i / per_row, w = i % per_row;
             const int c0 = w < fq ? w * 4 : (w < 2 * fq ? DK + (w - fq) * 4 : 2 * DK + (w - 2 * fq) * 4);
             const int g0 = gchan(c0);
-            if (rrow < 4) cp_async16(cw + rrow * NCH + c0, a.conv_w + size_t(rrow) * C + g0);
-            else if (ROLLED)        // window rows after the accepted token of the previous batch
-                cp_async16(cs + (rrow - 4) * NCH + c0,
-                           a.cap_conv + (size_t(s) * (3 + T) + src_tok + 1 + (rrow - 4)) * C + g0);
-            else cp_async16(cs + (rrow - 4) * NCH + c0, a.conv_state + (size_t(s) * 3 + (rrow - 4)) * C + g0);
+            if (rrow < 4) {
+                const float *q = a.conv_w + size_t(rrow) * C + g0;
+                if (chk(q, 16, a.conv_w, a.ext_conv_w)) cp_async16(cw + rrow * NCH + c0, q);
+            } else if (ROLLED) {    // window rows after the accepted token of the previous batch
+                const float *q = a.cap_conv + (size_t(s) * (3 + T) + src_tok + 1 + (rrow - 4)) * C + g0;
+                if (chk(q, 16, a.cap_conv, a.ext_cap_conv)) cp_async16(cs + (rrow - 4) * NCH + c0, q);
+            } else {
+                const float *q = a.conv_state + (size_t(s) * 3 + (rrow - 4)) * C + g0;
+                if (chk(q, 16, a.conv_state, a.ext_conv_state)) cp_async16(cs + (rrow - 4) * NCH + c0, q);
+            }
         }
         if constexpr (!COMMIT)
-            for (int i = tid; i < ROWS / 4; i += nthr) cp_async16(nw + i * 4, a.norm_w + j0 + i * 4);
+            for (int i = tid; i < ROWS / 4; i += nthr)
+                if (chk(a.norm_w + j0 + i * 4, 16, a.norm_w, a.ext_norm_w)) cp_async16(nw + i * 4, a.norm_w + j0 + i * 4);
     }
     // (3) gates for this head, one token per thread
     for (int t = tid; t < TT; t += nthr) {
         const bool pend = t < n_prev;
         const size_t idx = (size_t(s) * a.Ts + (pend ? t : t - n_prev)) * a.ld_ab + h;
-        const float al = to_f32(static_cast<const Act *>(pend ? a.alpha_prev : a.alpha)[idx]);
-        const float br = to_f32(static_cast<const Act *>(pend ? a.beta_prev : a.beta_raw)[idx]);
-        const float x = al + __ldg(a.dt_bias + h);
+        const Act *ap = static_cast<const Act *>(pend ? a.alpha_prev : a.alpha) + idx;
+        const Act *bp = static_cast<const Act *>(pend ? a.beta_prev : a.beta_raw) + idx;
+        const float al = chk(ap, sizeof(Act), ap - idx, a.ext_ab) ? to_f32(*ap) : 0.f;
+        const float br = chk(bp, sizeof(Act), bp - idx, a.ext_ab) ? to_f32(*bp) : 0.f;
+        const float dtb = chk(a.dt_bias + h, 4, a.dt_bias, a.ext_head) ? __ldg(a.dt_bias + h) : 0.f;
+        const float alg = chk(a.A_log + h, 4, a.A_log, a.ext_head) ? __ldg(a.A_log + h) : 0.f;
+        const float x = al + dtb;
         const float sp = x > 20.0f ? x : log1pf(expf(x));               // softplus
-        gs[t] = expf(-expf(__ldg(a.A_log + h)) * sp);
+        gs[t] = expf(-expf(alg) * sp);
         bs[t] = 1.0f / (1.0f + expf(-br));
         if constexpr (TREE) {
-            int pt = __ldg(a.parent + size_t(s) * T + t);
+            int pt = chk(a.parent + size_t(s) * T + t, 4, a.parent, a.ext_parent) ? __ldg(a.parent + size_t(s) * T + t)
+                                                                                  : -1;
             if (pt < -1 || pt >= t) {                   // not a tree in token order: reported, root used
                 if (a.d_status) atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TREE));
                 pt = -1;
@@ -534,11 +565,14 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
                 if (pt != t - 1) {
                     const float *src = pt < 0 ? a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b
                                               : cap_row + (size_t(s) * T + pt) * cap_token_stride;
+                    const float *sbase = pt < 0 ? a.state : a.cap_state;
+                    const size_t sext = pt < 0 ? a.ext_state : a.ext_cap_state;
 #pragma unroll
                     for (int rho = 0; rho < RPG; ++rho)
 #pragma unroll
                         for (int m = 0; m < NCL; ++m) {
-                            const float4 v = ld_na4(src + size_t(rho) * DK + 4 * LR * m);
+                            const float *q = src + size_t(rho) * DK + 4 * LR * m;
+                            const float4 v = chk(q, 16, sbase, sext) ? ld_na4(q) : make_float4(0.f, 0.f, 0.f, 0.f);
                             S[rho][m][0] = v.x; S[rho][m][1] = v.y; S[rho][m][2] = v.z; S[rho][m][3] = v.w;
                         }
                 }
@@ -603,18 +637,22 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
 #pragma unroll
                 for (int rho = 0; rho < RPG; ++rho)
 #pragma unroll
-                    for (int m = 0; m < NCL; ++m)
-                        store4(dst + size_t(rho) * DK + 4 * LR * m,
-                               make_float4(S[rho][m][0], S[rho][m][1], S[rho][m][2], S[rho][m][3]));
+                    for (int m = 0; m < NCL; ++m) {
+                        float *q = dst + size_t(rho) * DK + 4 * LR * m;
+                        if (chk(q, 16, a.state, a.ext_state))
+                            store4(q, make_float4(S[rho][m][0], S[rho][m][1], S[rho][m][2], S[rho][m][3]));
+                    }
             }
             if (capture) {
                 float *dst = cap_row + (size_t(s) * T + t) * cap_token_stride;
 #pragma unroll
                 for (int rho = 0; rho < RPG; ++rho)
 #pragma unroll
-                    for (int m = 0; m < NCL; ++m)
-                        st_stream4(dst + size_t(rho) * DK + 4 * LR * m, S[rho][m][0], S[rho][m][1], S[rho][m][2],
-                                   S[rho][m][3]);
+                    for (int m = 0; m < NCL; ++m) {
+                        float *q = dst + size_t(rho) * DK + 4 * LR * m;
+                        if (chk(q, 16, a.cap_state, a.ext_cap_state))
+                            st_stream4(q, S[rho][m][0], S[rho][m][1], S[rho][m][2], S[rho][m][3]);
+                    }
             }
         }
         // the next kernel in the stream may start launching (it waits for this grid's completion itself)
@@ -627,7 +665,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
             float *base = a.cap_conv + size_t(s) * T * 3 * C;
             for (int i = tid; i < T * 3 * n4; i += nthr) {
                 const int t = i / (3 * n4), rr = (i / n4) % 3, c = c_first + 4 * (i % n4);
-                store4(base + (size_t(t) * 3 + rr) * C + gchan(c), win4(trow[t * 4 + 1 + rr], c));
+                float *q = base + (size_t(t) * 3 + rr) * C + gchan(c);
+                if (chk(q, 16, a.cap_conv, a.ext_cap_conv)) store4(q, win4(trow[t * 4 + 1 + rr], c));
             }
         }
         __syncwarp();
@@ -655,7 +694,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
             float *base = a.cap_conv + size_t(s) * (3 + T) * C;
             for (int i = tid; i < (3 + T) * n4; i += nthr) {
                 const int rho = i / n4, c = c_first + 4 * (i % n4);
-                store4(base + size_t(rho) * C + gchan(c), win4(rho, c));
+                float *q = base + size_t(rho) * C + gchan(c);
+                if (chk(q, 16, a.cap_conv, a.ext_cap_conv)) store4(q, win4(rho, c));
             }
         }
         if constexpr (!TREE && !LAZY) {    // a tree or lazy verify leaves the state as it was
@@ -663,9 +703,11 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
 #pragma unroll
             for (int rho = 0; rho < RPG; ++rho)
 #pragma unroll
-                for (int m = 0; m < NCL; ++m)
-                    store4(dst + size_t(rho) * DK + 4 * LR * m,
-                           make_float4(S[rho][m][0], S[rho][m][1], S[rho][m][2], S[rho][m][3]));
+                for (int m = 0; m < NCL; ++m) {
+                    float *q = dst + size_t(rho) * DK + 4 * LR * m;
+                    if (chk(q, 16, a.state, a.ext_state))
+                        store4(q, make_float4(S[rho][m][0], S[rho][m][1], S[rho][m][2], S[rho][m][3]));
+                }
         }
     }
 
@@ -677,7 +719,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         float *base = a.conv_state + size_t(s) * 3 * C;
         for (int i = tid; i < 3 * n4; i += nthr) {
             const int rr = i / n4, c = c_first + 4 * (i % n4);
-            store4(base + size_t(rr) * C + gchan(c), win4(TT + rr, c));
+            float *q = base + size_t(rr) * C + gchan(c);
+            if (chk(q, 16, a.conv_state, a.ext_conv_state)) store4(q, win4(TT + rr, c));
         }
         return;
     }
@@ -701,7 +744,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
             const float ri = rinv[t];
             const float4 y = make_float4(oo.x * ri * ww.x * silu(zz.x), oo.y * ri * ww.y * silu(zz.y),
                                          oo.z * ri * ww.z * silu(zz.z), oo.w * ri * ww.w * silu(zz.w));
-            store4(out + (size_t(s) * a.Ts + t) * size_t(Hv) * DV + size_t(h) * DV + j0 + c, y);
+            Act *q = out + (size_t(s) * a.Ts + t) * size_t(Hv) * DV + size_t(h) * DV + j0 + c;
+            if (chk(q, 4 * sizeof(Act), out, a.ext_out)) store4(q, y);
         }
     }
     if (LAZY && n_prev > 0) {
@@ -711,7 +755,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         float *base = a.conv_state + size_t(s) * 3 * C;
         for (int i = tid; i < 3 * n4; i += nthr) {
             const int rr = i / n4, c = c_first + 4 * (i % n4);
-            store4(base + size_t(rr) * C + gchan(c), win4(n_prev + rr, c));
+            float *q = base + size_t(rr) * C + gchan(c);
+            if (chk(q, 16, a.conv_state, a.ext_conv_state)) store4(q, win4(n_prev + rr, c));
         }
     }
     if constexpr (MODE == kChain || ROLLED) {
@@ -721,7 +766,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         float *base = a.conv_state + size_t(s) * 3 * C;
         for (int i = tid; i < 3 * n4; i += nthr) {
             const int rr = i / n4, c = c_first + 4 * (i % n4);
-            store4(base + size_t(rr) * C + gchan(c), win4(T + rr, c));
+            float *q = base + size_t(rr) * C + gchan(c);
+            if (chk(q, 16, a.conv_state, a.ext_conv_state)) store4(q, win4(T + rr, c));
         }
     }
 }

@@ -73,7 +73,8 @@ typedef enum {
     GDN_ERR_LAUNCH = 7,      /* the CUDA launch itself failed (message in gdn_last_error) */
     GDN_ERR_TIMEOUT = 8,     /* (device) a bounded wait gave up */
     GDN_ERR_WORKSPACE = 9,   /* workspace missing or smaller than the query returned */
-    GDN_ERR_TREE = 10        /* (device) a parent id is outside [-1, t-1]; that token ran from the root */
+    GDN_ERR_TREE = 10,       /* (device) a parent id is outside [-1, t-1]; that token ran from the root */
+    GDN_ERR_BOUNDS = 11      /* (device, checked builds only) an access fell outside its buffer and was skipped */
 } gdn_status;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;

@@ -1,0 +1,90 @@
+"""Cases run through both the ordinary and the bounds-checked library (see
+test_checked_gpu.py): every verify mode, the rollbacks and the layer step on
+small seeded shapes.  ``python -m tests.checked_cases OUT.npz`` runs them on
+the checked library and saves the results and status words."""
+import sys
+
+import numpy as np
+import torch
+
+import gated_deltanet_verify_gb300 as gdn
+from tests.gpu_util import dims_of, params_of, upload
+from workloads.device import act_host, empty_outputs, to_f64
+from workloads.synth import Shape, make_inputs, make_parents, make_proj
+
+
+def _shape(**kw):
+    base = dict(name="chk", n_slots=3, n_qk_heads=2, n_v_heads=6, d_k=128, d_v=128, n_tokens=7, act="bf16", seed=71)
+    base.update(kw)
+    return Shape(**base)
+
+
+def run_all() -> dict:
+    torch.cuda.set_device(0)
+    res = {}
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def keep(prefix, **tensors):
+        for k, v in tensors.items():
+            res[f"{prefix}.{k}"] = to_f64(v)
+
+    for name, shape in (("chain", _shape()), ("f32_dk32", _shape(d_k=32, d_v=32, act="f32", n_tokens=4)),
+                        ("dk64_r4", _shape(d_k=64, d_v=64, n_qk_heads=2, n_v_heads=8, n_tokens=5))):
+        x = upload(make_inputs(shape))
+        o = empty_outputs(shape, "cuda")
+        d = dims_of(shape)
+        gdn.gdn_verify_forward(d, params_of(x), x["qkv"], x["z"], x["alpha"], x["beta_raw"], x["state"],
+                               x["conv_state"], o["cap_state"], o["cap_conv"], o["out"], status)
+        trims = torch.tensor([0, 2, shape.n_tokens - 1][:shape.n_slots], dtype=torch.int32, device="cuda")
+        gdn.gdn_rollback(d, trims, x["state"], x["conv_state"], o["cap_state"], o["cap_conv"], status)
+        # the rolled verify from those captures, then a lazy verify committing that batch, then a commit
+        y = upload(make_inputs(shape, seed=72))
+        gdn.gdn_verify_after_rollback(d, params_of(x), trims, y["qkv"], y["z"], y["alpha"], y["beta_raw"],
+                                      x["state"], x["conv_state"], o["cap_state"], o["cap_conv"], o["out"], status)
+        keep(name, out=o["out"], cap_state=o["cap_state"], cap_conv=o["cap_conv"], state=x["state"],
+             conv_state=x["conv_state"])
+        lz = upload(make_inputs(shape, seed=73))
+        out2 = empty_outputs(shape, "cuda", capture=False)["out"]
+        gdn.gdn_verify_lazy(d, params_of(x), lz["qkv"], lz["z"], lz["alpha"], lz["beta_raw"], x["state"],
+                            x["conv_state"], out2, status, prev_trim=trims, prev_qkv=y["qkv"], prev_alpha=y["alpha"],
+                            prev_beta_raw=y["beta_raw"])
+        gdn.gdn_commit_lazy(d, params_of(x), trims, lz["qkv"], lz["alpha"], lz["beta_raw"], x["state"],
+                            x["conv_state"], status)
+        keep(name + ".lazy", out=out2, state=x["state"], conv_state=x["conv_state"])
+        # tree verify and the rollback to the accepted node
+        xt = upload(make_inputs(shape, seed=74))
+        ot = empty_outputs(shape, "cuda")
+        cap_conv_t = torch.empty((shape.n_slots, shape.n_tokens, 3, shape.conv_channels), dtype=torch.float32,
+                                 device="cuda")
+        par = torch.from_numpy(make_parents(shape, "random", seed=75).astype(np.int32)).to("cuda")
+        gdn.gdn_verify_tree(d, params_of(xt), xt["qkv"], xt["z"], xt["alpha"], xt["beta_raw"], par, xt["state"],
+                            xt["conv_state"], ot["cap_state"], cap_conv_t, ot["out"], status)
+        acc = torch.tensor([-1, 0, shape.n_tokens - 1][:shape.n_slots], dtype=torch.int32, device="cuda")
+        gdn.gdn_rollback_tree(d, acc, xt["state"], xt["conv_state"], ot["cap_state"], cap_conv_t, status)
+        keep(name + ".tree", out=ot["out"], cap_state=ot["cap_state"], cap_conv=cap_conv_t, state=xt["state"],
+             conv_state=xt["conv_state"])
+
+    # the layer step with its projections
+    shape = _shape(n_v_heads=8, d_k=64, d_v=64, n_embd=256)
+    x = upload(make_inputs(shape))
+    p = {k: act_host(v, shape).to("cuda") for k, v in make_proj(shape).items()}
+    d = dims_of(shape)
+    w = gdn.proj_weights(shape.n_embd, p["w_in"], p["w_out"])
+    o = empty_outputs(shape, "cuda")
+    ws_bytes = gdn.gdn_layer_workspace_bytes(d, shape.n_embd)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    yv = torch.empty((shape.n_slots, shape.n_tokens, shape.n_embd), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_layer_verify(d, params_of(x), w, p["x"], x["state"], x["conv_state"], o["cap_state"], o["cap_conv"], yv,
+                         ws, ws_bytes, status)
+    keep("layer", y=yv, cap_state=o["cap_state"], state=x["state"])
+    torch.cuda.synchronize()
+    res["status"] = np.array([int(status.item())])
+    return res
+
+
+if __name__ == "__main__":
+    from gated_deltanet_verify_gb300 import _build
+    gdn.LIB_PATH = _build.CHECKED_LIB
+    r = run_all()
+    r["version"] = np.frombuffer(gdn.gdn_version().encode(), dtype=np.uint8)
+    np.savez(sys.argv[1], **r)
