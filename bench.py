@@ -10,13 +10,14 @@ a 64-layer hybrid target, 1 slot, 16 QK / 48 V heads, d_k = d_v = 128, K+1 =
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
                     [--workload layer_verify|multislot_verify|stack_verify|prefill|tree_verify|
-                                rolled_verify|rolled_multislot_verify|lazy_verify|lazy_multislot_verify|
-                                lazy_stack_verify|proj_verify]
+                                rolled_verify|rolled_multislot_verify|rolled_stack_verify|
+                                lazy_verify|lazy_multislot_verify|lazy_stack_verify|proj_verify]
 
 The tree_verify workload verifies a draft tree and rolls back to the accepted
 node; the rolled_* workloads fold each step's rollback into the next verify
-(one launch per step); the lazy_* workloads run lazy capture on the same inputs as their
-capture counterparts: one launch per step commits the pending batch (re-runs
+(one launch per step); the lazy_* workloads run lazy capture on the same
+inputs as their capture counterparts: one launch per step commits the pending
+batch (re-runs
 its accepted tokens) and writes the new batch's outputs, nothing captured.
 
 Prints one JSON line.  ``value`` = verified tokens/s over all ranks (device
@@ -631,7 +632,7 @@ def run_cuda(args):
         return
 
     graph_len = max(1, min(args.graph_len, args.steps))
-    if args.workload in ("stack_verify", "lazy_stack_verify", "prefill"):
+    if args.workload in ("stack_verify", "lazy_stack_verify", "rolled_stack_verify", "prefill"):
         graph_len = 1
     g_full, n_full, g_rem = time_graph_steps(torch, wl, args.steps, graph_len)
     g_warm, nw_full, g_wrem = time_graph_steps(torch, wl, args.warmup, graph_len)

@@ -173,6 +173,7 @@ WORKLOADS: Dict[str, Shape] = {
     # the layer shape with each step's rollback folded into the next verify (one launch per step)
     "rolled_verify": Shape("rolled_verify", 1, 16, 48, 128, 128, 16, "bf16", seed=1),
     "rolled_multislot_verify": Shape("rolled_multislot_verify", 32, 16, 48, 128, 128, 16, "bf16", seed=2),
+    "rolled_stack_verify": Shape("rolled_stack_verify", 8, 16, 48, 128, 128, 16, "bf16", n_layers=48, seed=3),
     # the layer with its projections (hidden 5120): x -> [qkv | z | alpha | beta] -> verify -> y
     "proj_verify": Shape("proj_verify", 1, 16, 48, 128, 128, 16, "bf16", seed=1, n_embd=5120),
 }
