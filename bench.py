@@ -17,8 +17,9 @@ The tree_verify workload verifies a draft tree and rolls back to the accepted
 node; the rolled_* workloads fold each step's rollback into the next verify
 (one launch per step); the lazy_* workloads run lazy capture on the same
 inputs as their capture counterparts: one launch per step commits the pending
-batch (re-runs
-its accepted tokens) and writes the new batch's outputs, nothing captured.
+batch (re-runs its accepted tokens) and writes the new batch's outputs,
+nothing captured.  proj_verify adds the projections around the block
+(hidden 5120; cuBLASLt GEMMs).
 
 Prints one JSON line.  ``value`` = verified tokens/s over all ranks (device
 time, CUDA events, steps replayed from CUDA graphs over rotating buffer sets
