@@ -437,7 +437,52 @@ class VerifyWorkload:
         moved = (self.trims[k] >= 0) if self.tree else self.trims[k]     # slots whose rollback copies
         return sum(vb + rollback_bytes(self.shape, moved[li]) for li in range(self.layers))
 
+    def e2e_step_host(self, steps, device):
+        """One C-ABI call per step with host buffers (gdn_verify_step_host): the
+        packed pinned input block goes to the device in one copy, the verify and
+        the rollback (or the rolled verify) run, the outputs come back in one copy;
+        one host wait per step.  The ctypes arguments are marshalled once."""
+        import ctypes
+        torch, gdn = self.torch, self.gdn
+        from workloads.device import act_host
+        s = self.shape
+        io = gdn.gdn_step_io_layout(self.dims)
+        inp = self.host_inputs[0]
+        host_in = torch.zeros(io.in_bytes, dtype=torch.uint8).pin_memory()
+        for off, t in ((io.qkv, act_host(inp.qkv, s)), (io.z, act_host(inp.z, s)), (io.alpha, act_host(inp.alpha, s)),
+                       (io.beta_raw, act_host(inp.beta_raw, s)),
+                       (io.trim, torch.from_numpy(self.trims[0, 0].astype(np.int32)))):
+            b = t.contiguous().view(torch.uint8).reshape(-1)
+            host_in[off:off + b.numel()].copy_(b)
+        host_out = torch.empty(io.out_bytes, dtype=torch.uint8).pin_memory()
+        d_io = torch.empty(io.in_bytes + io.out_bytes, dtype=torch.uint8, device=device)
+        x = self.sets[0][0]
+        stream = torch.cuda.current_stream()
+        fn = gdn.lib().gdn_verify_step_host
+        args = (ctypes.byref(self.dims), ctypes.byref(x["params"]), 1 if self.rolled else 0, host_in.data_ptr(),
+                host_out.data_ptr(), d_io.data_ptr(), d_io.numel(), x["state"].data_ptr(), x["conv_state"].data_ptr(),
+                x["cap_state"].data_ptr(), x["cap_conv"].data_ptr(), x["status"].data_ptr(), stream.cuda_stream)
+
+        def one(k):
+            rc = fn(*args)
+            if rc != 0:
+                raise RuntimeError(f"gdn_verify_step_host: {rc} {gdn.gdn_last_error()}")
+            stream.synchronize()
+
+        for k in range(10):
+            one(k)
+        t0 = time.perf_counter()
+        for k in range(steps):
+            one(k)
+        dt = time.perf_counter() - t0
+        return dt, io.in_bytes, io.out_bytes
+
     def e2e(self, steps, device):
+        if self.layers == 1 and not (self.tree or self.lazy or self.proj):
+            return self.e2e_step_host(steps, device)
+        return self.e2e_staged(steps, device)
+
+    def e2e_staged(self, steps, device):
         """Public-API loop with host buffers: every step copies all its inputs (every
         layer's activations, trims, parent ids or hidden state) host -> device as one
         pinned buffer, runs verify + rollback per layer through the C ABI, copies all
@@ -786,7 +831,10 @@ def run_cuda(args):
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
                       "timing": ("wall clock, host sync per step; one H2D copy of all the step's inputs "
                                  "and one D2H copy of its outputs" if args.workload != "prefill"
-                                 else "wall clock, host sync per step")}
+                                 else "wall clock, host sync per step"),
+                      "api": ("gdn_verify_step_host (one C-ABI call per step with host buffers)"
+                              if args.workload != "prefill" and wl.layers == 1
+                              and not (wl.tree or wl.lazy or wl.proj) else "the calls of the step")}
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(shape, args.cpu_seconds)
     if world > 1:

@@ -37,7 +37,8 @@ GDN_F32 = 0
 GDN_BF16 = 1
 
 EXPORTED_SYMBOLS = ("gdn_verify_forward", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_tree",
-                    "gdn_verify_after_rollback", "gdn_verify_lazy", "gdn_commit_lazy", "gdn_proj_in_ld", "gdn_layer_workspace_bytes",
+                    "gdn_verify_after_rollback", "gdn_verify_lazy", "gdn_commit_lazy", "gdn_step_io_layout",
+                    "gdn_verify_step_host", "gdn_proj_in_ld", "gdn_layer_workspace_bytes",
                     "gdn_project_in", "gdn_project_out", "gdn_layer_verify", "gdn_prefill_workspace_bytes",
                     "gdn_prefill_chunked", "gdn_prefill_chunked_static", "gdn_last_error", "gdn_version")
 
@@ -61,6 +62,12 @@ class Dims(ctypes.Structure):
 class LayerParams(ctypes.Structure):
     _fields_ = [("conv_w", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
                 ("norm_w", ctypes.c_void_p)]
+
+
+class StepIO(ctypes.Structure):
+    _fields_ = [("qkv", ctypes.c_size_t), ("z", ctypes.c_size_t), ("alpha", ctypes.c_size_t),
+                ("beta_raw", ctypes.c_size_t), ("trim", ctypes.c_size_t), ("in_bytes", ctypes.c_size_t),
+                ("out_bytes", ctypes.c_size_t)]
 
 
 class ProjWeights(ctypes.Structure):
@@ -96,6 +103,11 @@ def lib() -> ctypes.CDLL:
         L.gdn_rollback_tree.restype = ip
         L.gdn_verify_after_rollback.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 12
         L.gdn_verify_after_rollback.restype = ip
+        L.gdn_step_io_layout.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(StepIO)]
+        L.gdn_step_io_layout.restype = ip
+        L.gdn_verify_step_host.argtypes = ([ctypes.POINTER(Dims), ctypes.POINTER(LayerParams), ip] + [vp] * 3 +
+                                           [ctypes.c_size_t] + [vp] * 6)
+        L.gdn_verify_step_host.restype = ip
         L.gdn_verify_lazy.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 13
         L.gdn_verify_lazy.restype = ip
         L.gdn_commit_lazy.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 8
@@ -192,6 +204,20 @@ def gdn_verify_after_rollback(dims: Dims, params: LayerParams, d_prev_trim, qkv,
                                            _ptr(z), _ptr(alpha), _ptr(beta_raw), _ptr(state), _ptr(conv_state),
                                            _ptr(cap_state), _ptr(cap_conv), _ptr(out), _ptr(d_status),
                                            _stream(stream)))
+
+
+def gdn_step_io_layout(dims: Dims) -> StepIO:
+    io = StepIO()
+    _check(lib().gdn_step_io_layout(ctypes.byref(dims), ctypes.byref(io)))
+    return io
+
+
+def gdn_verify_step_host(dims: Dims, params: LayerParams, rollback_first: int, h_in, h_out, d_io, d_io_bytes: int,
+                         state, conv_state, cap_state, cap_conv, d_status=None, stream=None) -> None:
+    """One verify step from host memory (packed pinned input block, output block)."""
+    _check(lib().gdn_verify_step_host(ctypes.byref(dims), ctypes.byref(params), int(rollback_first), _ptr(h_in),
+                                      _ptr(h_out), _ptr(d_io), int(d_io_bytes), _ptr(state), _ptr(conv_state),
+                                      _ptr(cap_state), _ptr(cap_conv), _ptr(d_status), _stream(stream)))
 
 
 def gdn_verify_lazy(dims: Dims, params: LayerParams, qkv, z, alpha, beta_raw, state, conv_state, out,

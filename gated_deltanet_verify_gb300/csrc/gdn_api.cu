@@ -345,6 +345,59 @@ int gdn_prefill_chunked_static(const gdn_dims *dims, const gdn_layer_params *par
                                need > 0 ? (size_t)GDN_PREFILL_STATIC_SCRATCH_BYTES : 0, d_status, stream);
 }
 
+// ---- one verify step from host memory ---------------------------------------
+
+int gdn_step_io_layout(const gdn_dims *dims, gdn_step_io *io) {
+    g_err.clear();
+    int rc = check_common(dims);
+    if (rc) return rc;
+    if (!io) return fail(GDN_ERR_ARG, "io is NULL");
+    const gdn_dims &d = *dims;
+    const size_t ab = d.act_dtype == GDN_BF16 ? 2 : 4, M = size_t(d.n_slots) * d.n_tokens;
+    const size_t V = size_t(d.n_v_heads) * d.d_v;
+    auto up = [](size_t n) { return (n + 255) & ~size_t(255); };
+    size_t off = 0;
+    io->qkv = off; off += up(M * size_t(conv_channels(&d)) * ab);
+    io->z = off; off += up(M * V * ab);
+    io->alpha = off; off += up(M * size_t(d.n_v_heads) * ab);
+    io->beta_raw = off; off += up(M * size_t(d.n_v_heads) * ab);
+    io->trim = off; off += up(size_t(d.n_slots) * 4);
+    io->in_bytes = off;
+    io->out_bytes = up(M * V * ab);
+    return GDN_OK;
+}
+
+int gdn_verify_step_host(const gdn_dims *dims, const gdn_layer_params *params, int rollback_first,
+                         const void *h_in, void *h_out, void *d_io, size_t d_io_bytes, float *state,
+                         float *conv_state, float *cap_state, float *cap_conv, int *d_status, void *stream) {
+    gdn_step_io io;
+    int rc = gdn_step_io_layout(dims, &io);
+    if (rc) return rc;
+    if (!h_in || !h_out || !d_io) return fail(GDN_ERR_ARG, "h_in, h_out or d_io is NULL");
+    if (d_io_bytes < io.in_bytes + io.out_bytes)
+        return fail(GDN_ERR_WORKSPACE, "d_io of %zu bytes needed (got %zu)", io.in_bytes + io.out_bytes, d_io_bytes);
+    if (reinterpret_cast<uintptr_t>(d_io) & 255u) return fail(GDN_ERR_ALIGN, "d_io must be 256-byte aligned");
+    if (rollback_first != 0 && rollback_first != 1) return fail(GDN_ERR_ARG, "rollback_first must be 0 or 1");
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned char *din = static_cast<unsigned char *>(d_io), *dout = din + io.in_bytes;
+    cudaError_t e = cudaMemcpyAsync(din, h_in, io.in_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "input copy failed: %s", cudaGetErrorString(e));
+    const int32_t *trim = reinterpret_cast<const int32_t *>(din + io.trim);
+    if (rollback_first) {
+        rc = gdn_verify_after_rollback(dims, params, trim, din + io.qkv, din + io.z, din + io.alpha,
+                                       din + io.beta_raw, state, conv_state, cap_state, cap_conv, dout, d_status,
+                                       stream);
+    } else {
+        rc = gdn_verify_forward(dims, params, din + io.qkv, din + io.z, din + io.alpha, din + io.beta_raw, state,
+                                conv_state, cap_state, cap_conv, dout, d_status, stream);
+        if (rc == GDN_OK) rc = gdn_rollback(dims, trim, state, conv_state, cap_state, cap_conv, d_status, stream);
+    }
+    if (rc) return rc;
+    e = cudaMemcpyAsync(h_out, dout, io.out_bytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "output copy failed: %s", cudaGetErrorString(e));
+    return GDN_OK;
+}
+
 // ---- projections around the block and the layer step ----------------------
 
 static long long proj_in_cols(const gdn_dims &d) {

@@ -289,6 +289,33 @@ int gdn_layer_verify(const gdn_dims *dims, const gdn_layer_params *params, const
                      const void *x, float *state, float *conv_state, float *cap_state, float *cap_conv,
                      void *y, void *workspace, size_t ws_bytes, int *d_status, void *stream);
 
+/*
+ * One verify step from host memory: the inputs of the step arrive as one
+ * packed host block, the outputs leave as one host block, and everything in
+ * between is enqueued on `stream` by this one call (the caller synchronises
+ * the stream when it needs h_out).  The packed input block holds qkv, z,
+ * alpha, beta_raw (the layouts above, act_dtype) and the int32 trims [B], each
+ * section starting at the offset gdn_step_io_layout gives (256-byte aligned);
+ * the output block is out.  d_io is caller-owned device staging of
+ * in_bytes + out_bytes (256-byte aligned).  rollback_first = 0: verify with
+ * capture, then gdn_rollback with the staged trims (the trims of this batch);
+ * rollback_first = 1: gdn_verify_after_rollback (the trims of the previous
+ * batch, whose captures cap_state / cap_conv still hold).  h_in and h_out
+ * should be pinned for the copies to be asynchronous.  Errors as the calls it
+ * makes; a copy that cannot be enqueued is GDN_ERR_LAUNCH.
+ */
+typedef struct {
+    size_t qkv, z, alpha, beta_raw, trim;   /* byte offsets in the packed input block */
+    size_t in_bytes, out_bytes;             /* sizes of the input and output blocks */
+} gdn_step_io;
+
+int gdn_step_io_layout(const gdn_dims *dims, gdn_step_io *io);
+
+int gdn_verify_step_host(const gdn_dims *dims, const gdn_layer_params *params, int rollback_first,
+                         const void *h_in, void *h_out, void *d_io, size_t d_io_bytes,
+                         float *state, float *conv_state, float *cap_state, float *cap_conv,
+                         int *d_status, void *stream);
+
 /* Bytes of device workspace gdn_prefill_chunked needs for these dims (0 on bad dims). */
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims);
 
