@@ -124,3 +124,65 @@ def test_binding_raises_on_error(lib):
     with pytest.raises(gdn.GdnError) as ei:
         gdn.gdn_rollback(_dims(), A, A, A, None, A, stream=0)
     assert ei.value.status == gdn.GDN_ERR_NO_CAPTURE
+
+
+def test_step_io_layout(lib):
+    d = _dims(n_slots=3, n_tokens=5, act_dtype=gdn.GDN_BF16)
+    io = gdn.gdn_step_io_layout(d)
+    C, V, H, M = 2 * 2 * 32 + 4 * 32, 4 * 32, 4, 15
+    up = lambda n: -(-n // 256) * 256
+    assert (io.qkv, io.z) == (0, up(M * C * 2))
+    assert io.alpha == io.z + up(M * V * 2) and io.beta_raw == io.alpha + up(M * H * 2)
+    assert io.trim == io.beta_raw + up(M * H * 2) and io.in_bytes == io.trim + up(3 * 4)
+    assert io.out_bytes == up(M * V * 2)
+    assert all(v % 256 == 0 for v in (io.qkv, io.z, io.alpha, io.beta_raw, io.trim, io.in_bytes))
+
+
+def test_step_host_validation(lib):
+    d = _dims()
+    io = gdn.gdn_step_io_layout(d)
+    L = gdn.lib()
+
+    def call(rf=0, h_in=A, d_io=A, n=None):
+        return L.gdn_verify_step_host(ctypes.byref(d), ctypes.byref(_params()), rf, h_in, A, d_io,
+                                      io.in_bytes + io.out_bytes if n is None else n, A, A, A, A, None, None)
+
+    assert call(h_in=None) == gdn.GDN_ERR_ARG
+    assert call(n=io.in_bytes) == gdn.GDN_ERR_WORKSPACE
+    assert call(d_io=A + 16) == gdn.GDN_ERR_ALIGN
+    assert call(rf=2) == gdn.GDN_ERR_ARG
+
+
+def test_lazy_and_rolled_host_validation(lib):
+    d = _dims()
+    L = gdn.lib()
+    p = ctypes.byref(_params())
+    # commit without trims; lazy verify with a pending batch but no pending activations
+    assert L.gdn_commit_lazy(ctypes.byref(d), p, None, A, A, A, A, A, None, None) == gdn.GDN_ERR_ARG
+    assert L.gdn_verify_lazy(ctypes.byref(d), p, A, None, A, A, A, A, A, A, A, A, A, None, None) == gdn.GDN_ERR_ARG
+    # the rolled verify needs the previous captures and trims
+    assert L.gdn_verify_after_rollback(ctypes.byref(d), p, A, A, A, A, A, A, A, None, A, A, None,
+                                       None) == gdn.GDN_ERR_NO_CAPTURE
+    assert L.gdn_verify_after_rollback(ctypes.byref(d), p, None, A, A, A, A, A, A, A, A, A, None,
+                                       None) == gdn.GDN_ERR_ARG
+
+
+def test_projection_host_validation(lib):
+    L = gdn.lib()
+    bf = _dims(n_v_heads=8, act_dtype=gdn.GDN_BF16)
+    w = gdn.ProjWeights(64, A, A)
+    need = gdn.gdn_layer_workspace_bytes(bf, 64)
+    M, ld = 4, gdn.gdn_proj_in_ld(bf)
+    assert ld % 8 == 0 and ld >= 2 * 2 * 32 + 8 * 32 + 8 * 32 + 16
+    assert need >= M * ld * 2 + M * 8 * 32 * 2 + (32 << 20)
+
+    def call(d=bf, ww=w, n=need, ws=A):
+        return L.gdn_layer_verify(ctypes.byref(d), ctypes.byref(_params()), ctypes.byref(ww), A, A, A, None, None,
+                                  A, ws, n, None, None)
+
+    assert call(d=_dims(n_v_heads=8)) == gdn.GDN_ERR_DTYPE                          # f32 activations
+    assert call(ww=gdn.ProjWeights(60, A, A)) == gdn.GDN_ERR_SHAPE                  # n_embd not a multiple of 8
+    assert call(d=_dims(n_v_heads=4, act_dtype=gdn.GDN_BF16)) == gdn.GDN_ERR_SHAPE  # H_v not a multiple of 8
+    assert call(n=need - 1) == gdn.GDN_ERR_WORKSPACE
+    assert call(ws=A + 16) == gdn.GDN_ERR_ALIGN
+    assert call(ww=gdn.ProjWeights(64, None, A)) == gdn.GDN_ERR_ARG
