@@ -71,7 +71,6 @@ struct PrefillArgs {
     void *out;
     float *scratch;                   // the caller's workspace (ring flags first), prefill_workspace_bytes
     size_t ring_offset;               // bytes from the workspace start to the ring slots
-    float *scratch_vt;                // per-(slot, value head, preparation CTA) v^T scratch
     int *d_status;
 };
 

@@ -61,7 +61,7 @@ constexpr int kSpinLimit = 1 << 20;    // try_wait rounds before an mbarrier wai
 constexpr int kFlagSpin = 1 << 21;     // polls (with back-off, about a second) before a ring-flag wait gives up
 constexpr int kTmemCols = 512;
 constexpr int kRing = 4;               // ring slots per (slot, value head)
-constexpr int kMaxPrep = 8;            // preparation CTAs per key head, at most
+constexpr int kMaxPrep = 8;            // preparation CTAs per key head, at most (more would only wait)
 
 // dynamic shared memory carve-up (bytes)
 constexpr uint32_t kRA = 0;                    // 128 KB: A operand planes; raw chunk inputs at chunk start
@@ -107,8 +107,12 @@ constexpr size_t kSlotBytes = 256 * 1024;
 // per (slot, value head): ring flags and the chunk decays (ints: full[4], empty[4], Gamma_C[4] bits)
 constexpr size_t kFlagWords = 32;
 static_assert(kFlagWords >= 3 * kRing, "flag words");
-// per (slot, key head, preparation CTA): v^T scratch (128 channels x 64 tokens)
-constexpr size_t kVtFloats = 128 * 64;
+// v^T of the current value head (128 channels x 64 tokens, rows padded to 68 floats so that a warp's 16-byte
+// row accesses fall in distinct banks) lives in the upper half of the A region: free from the end of the G
+// product until the A2 operand build, by which time every thread holds its row in registers
+constexpr uint32_t kVt = kRA + 64 * 1024;
+constexpr int kVtStride = kC + 4;
+static_assert(64 * 1024 + 128 * kVtStride * 4 <= 128 * 1024, "v^T fits the upper half of the A region");
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -364,7 +368,7 @@ struct Ctx {
 // the group, each published to that head's ring
 // ---------------------------------------------------------------------------
 template <typename Act>
-__device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) {
+__device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x) {
     unsigned char *sm = x.sm;
     const int tid = x.tid, lane = x.lane, wid = x.wid, tl = x.tl, half = x.half;
     const int Hk = a.Hk, Hv = a.Hv, L = a.L, C = a.C, R = a.r;
@@ -385,7 +389,7 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) 
     const uint32_t sRA = smem_u32(RA), sRB = smem_u32(RB);
     const uint32_t rawbar = smem_u32(sm + kRawBar);
     uint32_t raw_phase = 0;
-    float *vT = a.scratch_vt + (size_t)pidx * kVtFloats;      // [128 channels][64 tokens]
+    float *vT = reinterpret_cast<float *>(sm + kVt);           // [128 channels][64 tokens, padded]
     constexpr uint32_t kTile = kWin * kD * sizeof(Act);
 
     // raw window rows t0-3 .. t0+63 of chunk cc: 128-channel tiles of the qkv tensor map, one thread.
@@ -601,7 +605,7 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) 
                 const int ch = it % kD, tb = 16 * (it / kD);
                 float yv[16];
                 conv16(rawA + ch, hist + ch, kD, 2 * Hk * kD + h * kD + ch, tb, c, n, yv);
-                float4 *dv = reinterpret_cast<float4 *>(vT + ch * kC + tb);
+                float4 *dv = reinterpret_cast<float4 *>(vT + ch * kVtStride + tb);
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
                     dv[q4] = make_float4(yv[4 * q4], yv[4 * q4 + 1], yv[4 * q4 + 2], yv[4 * q4 + 3]);
@@ -612,7 +616,7 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x, int pidx) 
             // this thread's row of v^T for the A2 operand below, fetched ahead of the readout
             float4 vpre[8];
             {
-                const float4 *vrow = reinterpret_cast<const float4 *>(vT + tl * kC + 32 * half);
+                const float4 *vrow = reinterpret_cast<const float4 *>(vT + tl * kVtStride + 32 * half);
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) vpre[q4] = vrow[q4];
             }
@@ -1015,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     x.tmem = *reinterpret_cast<volatile uint32_t *>(sm + kTmemSlot);
     x.tq = (uint32_t)(32 * (x.wid & 3)) << 16;        // this warp's TMEM lane quarter
 
-    if (prep) prepare<Act>(a, x, blockIdx.x);
+    if (prep) prepare<Act>(a, x);
     else advance_state<Act>(a, x, a.slot0 + sidx / a.Hv, sidx % a.Hv);
 
     if (x.timed_out && x.tid == 0 && a.d_status) atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TIMEOUT));
@@ -1075,8 +1079,7 @@ static size_t ring_offset_bytes(const gdn_dims &d) {
 
 size_t prefill_workspace_bytes(const gdn_dims &d) {
     const size_t pairs = (size_t)d.n_slots * d.n_v_heads;
-    return ring_offset_bytes(d) + pairs * kRing * kSlotBytes +
-           (size_t)d.n_slots * d.n_qk_heads * kMaxPrep * kVtFloats * sizeof(float);
+    return ring_offset_bytes(d) + pairs * kRing * kSlotBytes;
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once
@@ -1106,8 +1109,6 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
     a.state = state; a.conv_state = conv_state; a.out = out;
     a.scratch = static_cast<float *>(workspace);
     a.ring_offset = ring_offset_bytes(d);
-    a.scratch_vt = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + a.ring_offset +
-                                             (size_t)d.n_slots * d.n_v_heads * kRing * kSlotBytes);
     a.n_prep = 1;
     a.d_status = d_status;
     // Fault injection for tests, on the host: GDN_FAULT_DROP_CHUNK=<c> makes the preparation CTAs never
@@ -1159,7 +1160,7 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
         a.ns = ns;
         a.counter = counters + li;
         int n_prep = max_ctas - ns * a.Hv;
-        if (n_prep > ns * a.Hk * kMaxPrep) n_prep = ns * a.Hk * kMaxPrep;       // v^T scratch areas
+        if (n_prep > ns * a.Hk * kMaxPrep) n_prep = ns * a.Hk * kMaxPrep;
         a.n_prep = n_prep;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(n_prep + ns * a.Hv, 1, 1);

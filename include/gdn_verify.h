@@ -326,9 +326,9 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims *dims);
  * rollback tensors: internal.h, create_target_cache, prefill_only).  Updates
  * state and conv_state in place.  workspace: caller-owned device scratch of
  * at least gdn_prefill_workspace_bytes(dims) bytes, 256-byte aligned (1 MiB
- * per (slot, value head): a ring of operand slots with its flags; 256 KiB per
- * (slot, key head): v scratch); its contents need no initialisation and are
- * garbage afterwards.  The call enqueues, on `stream`, a memset of the ring
+ * per (slot, value head): a ring of operand slots, plus its flags and a work
+ * counter per launch); its contents need no initialisation and are garbage
+ * afterwards.  The call enqueues, on `stream`, a memset of the ring
  * flags, one cooperative launch per group of slots that fits on the device
  * at once, and a small kernel that advances conv_state; calls sharing a
  * workspace must be ordered.  Supported:
