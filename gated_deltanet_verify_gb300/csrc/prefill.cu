@@ -19,25 +19,25 @@
 // becomes an error of 10-60 % in the outputs; with the split it is ~1e-5.
 //
 // Work split.  Everything but U, O and S depends only on the chunk itself, so
-// three CTAs serve one (slot, value head):
+// one state CTA per (slot, value head) is fed by a shared pool:
 //   * preparation CTAs (every SM the state CTAs leave) claim (chunk, key head) work items
 //     in chunk order from a counter; per item the q/k work is done once for
 //     the r value heads that share the key head (raw window by TMA,
 //     conv + SiLU into TMEM, L2 norms, G = [K; Q] K^T kept in TMEM), then per
-//     value head its gates, v conv, A and the masked, decayed P, T = (I + A)^-1
-//     (16 x 16 blocks), W^T and U~^T; they publish the ready-split operands
-//     (-W, Gamma Q, P, Gamma_C/Gamma K planes and U~) to that head's ring of
-//     eight slots in the caller's workspace (L2-resident) and release a
-//     per-slot flag;
+//     value head its gates, v conv (into shared memory), A and the masked,
+//     decayed P, T = (I + A)^-1 (16 x 16 blocks), W^T and U~^T; they publish
+//     the ready-split operands ([-W; Gamma Q] as one operand, P, Gamma_C/Gamma
+//     K planes and U~) to that head's ring of four slots in the caller's
+//     workspace (L2-resident) and release a per-slot flag;
 //   * the state CTA holds the fp32 state in registers and, chunk by chunk,
 //     acquires a slot, pulls it in with bulk copies and runs only the
 //     state-dependent products and the epilogue:
-//       X^T = S0^T (-W)^T, U^T = U~^T + X^T          (N 64, K 128)
-//       O^T = S0^T (Gamma Q)^T + U^T P^T             (N 64)
+//       [X^T | O^T] = S0^T [-W; Gamma Q]^T          (one N 128 product, A from TMEM)
+//       U^T = U~^T + X^T,  O^T += U^T P^T            (N 64)
 //       D2  = U^T (diag(Gamma_C / Gamma) K)          (N 128, K 64);  S^T <- Gamma_C S^T + D2
 //     then the gated RMSNorm.  It frees the slot once its bulk copies landed.
 // The launch is cooperative (every CTA resident at once), so the flag waits
-// between the three CTAs cannot starve; (slot, head) pairs beyond what fits
+// between the CTAs cannot starve; (slot, head) pairs beyond what fits
 // at once go to further launches.  Every wait is bounded and reports
 // GDN_ERR_TIMEOUT instead of hanging.  The ring flags are zeroed by a
 // stream-ordered memset before each launch.  The conv state (shared by the

@@ -32,17 +32,23 @@
 //     (token, q|k, 16-channel chunk); a chunk's channels are interleaved
 //     (4 channels every 4*chunks) so the vector loads of a warp are
 //     conflict-free, and the sums of squares need three shuffle levels.
-//   * The RMSNorm partials travel by st.async into the peers' shared memory,
+//   * The RMSNorm partials travel by st.async into the peers' shared memory
+//     right after the recurrence (before the conv-window capture is written),
 //     completing a transaction-counted mbarrier there; no release fence has
 //     to wait behind the capture stores still in flight.  The one cluster
-//     barrier sits right after the loads: it orders every CTA's read of the
-//     old conv state before the in-place rewrite, and publishes the
-//     initialised mbarriers before any peer writes to them.
+//     barrier arrives right after the loads and completes after the
+//     recurrence: it orders every CTA's read of the old conv state before the
+//     in-place rewrite, and publishes the initialised mbarriers before any
+//     peer writes to them.
 //   * Every wait is bounded; a wait that gives up writes GDN_ERR_TIMEOUT to
 //     the caller's status word instead of hanging.
 //   * Programmatic dependent launch: the kernel waits on its predecessor only
 //     right before its first global read, so its launch overlaps the tail of
-//     the previous kernel in the stream.
+//     the previous kernel in the stream; meanwhile it prefetches its state
+//     rows and activation segments into L2 (a prefetch returns nothing to the
+//     SM, so lines the previous kernel is still writing stay coherent).
+//   * A checked build (-DGDN_CHECKED=1) tests every global access against its
+//     buffer first (check.cuh); the ordinary build compiles the tests away.
 //
 // Modes (one template instance each)
 //   kChain  the (K+1)-token chain: outputs, optional captures, state and conv
