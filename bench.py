@@ -142,6 +142,17 @@ def rollback_bytes(s, trims) -> int:
     return int(np.count_nonzero(np.asarray(trims))) * per_slot + 4 * s.n_slots
 
 
+def resident_bytes(s) -> int:
+    """Bytes of one layer's buffers that stay in L2 between steps: the state, conv state, conv window,
+    activations, outputs and parameters -- every buffer but the captured states, which the kernels
+    stream out evict-first."""
+    a = 2 if s.act == "bf16" else 4
+    B, T, C, Hv, dk, dv, W = s.n_slots, s.n_tokens, s.conv_channels, s.n_v_heads, s.d_k, s.d_v, s.conv_width
+    n = B * Hv * dv * dk * 4 + B * (W - 1) * C * 4 + B * (W - 1 + T) * C * 4
+    n += B * T * C * a + 2 * B * T * Hv * dv * a + 2 * B * T * Hv * a
+    return n + W * C * 4 + 2 * Hv * 4 + dv * 4
+
+
 def prefill_bytes(s) -> int:
     return verify_bytes(s, capture=False)
 
@@ -320,11 +331,13 @@ class VerifyWorkload:
         self.proj = s.n_embd > 0
         # the rollback of each step folded into the next verify: one launch per step
         self.rolled = s.name.startswith("rolled")
-        per_set = (tree_verify_bytes(s) if self.tree else
-                   lazy_step_bytes(s, [0] * s.n_slots) if self.lazy else verify_bytes(s)) * self.layers
+        # the rotation is sized on what a step leaves in L2: everything but the captured states (streamed
+        # out with evict-first stores), so that each step reads its state and activations from DRAM
+        per_set = resident_bytes(s) * self.layers
         if self.proj:
             per_set += (proj_in_bytes(s) + proj_out_bytes(s)) * self.layers
-        self.n_sets = 1 if per_set > 3 * l2_bytes else int(min(64, -(-3 * l2_bytes // per_set) + 1))
+        self.n_sets = 1 if per_set > 3 * l2_bytes else int(min(128, -(-3 * l2_bytes // per_set) + 1))
+        self.resident_per_set = per_set
         self.dims = gdn.make_dims(s.n_slots, s.n_qk_heads, s.n_v_heads, s.d_k, s.d_v, s.n_tokens,
                                   gdn.GDN_BF16 if s.act == "bf16" else gdn.GDN_F32)
         self.sets = []
@@ -561,7 +574,8 @@ class PrefillWorkload:
         self.dims = gdn.make_dims(s.n_slots, s.n_qk_heads, s.n_v_heads, s.d_k, s.d_v, s.n_tokens,
                                   gdn.GDN_BF16 if s.act == "bf16" else gdn.GDN_F32)
         per_set = prefill_bytes(s)
-        self.n_sets = 1 if per_set > 3 * l2_bytes else 2
+        self.n_sets = 1 if per_set > 3 * l2_bytes else int(-(-3 * l2_bytes // per_set) + 1)
+        self.resident_per_set = per_set
         inp = make_inputs(s)
         self.host_inputs = [inp]
         self.ws_bytes = gdn.gdn_prefill_workspace_bytes(self.dims)
@@ -638,17 +652,20 @@ def capture_graph(torch, fn_list):
     return g
 
 
-def time_graph_steps(torch, wl, steps, graph_len):
-    """Replay graphs of `graph_len` steps (rotating buffer sets) covering exactly `steps` steps."""
+def time_graph_steps(torch, wl, steps, graph_len, first=0):
+    """Graphs of `graph_len` steps over rotating buffer sets (starting at set `first`) covering exactly
+    `steps` steps."""
     n_full, rem = divmod(steps, graph_len)
-    fns = [lambda sp, k=k: wl.step(k % wl.n_sets, sp) for k in range(graph_len)]
+    fns = [lambda sp, k=k: wl.step((first + k) % wl.n_sets, sp) for k in range(graph_len)]
     g_full = capture_graph(torch, fns) if n_full else None
     g_rem = capture_graph(torch, fns[:rem]) if rem else None
     return g_full, n_full, g_rem
 
 
-def kernel_duration(torch, wl, which, n_launch):
-    """Average duration of one kernel kind: CUDA events around a graph of n_launch back-to-back launches."""
+def kernel_duration(torch, wl, which, n_launch, flush=None):
+    """Average duration of one kernel kind: CUDA events around a graph of n_launch back-to-back
+    launches cycling over the buffer sets and layers (each set's data evicted from L2 by the others
+    before it comes round again)."""
     fns = []
     for k in range(n_launch):
         kk, li = k % wl.n_sets, (k // wl.n_sets) % wl.layers
@@ -656,6 +673,8 @@ def kernel_duration(torch, wl, which, n_launch):
     g = capture_graph(torch, fns)
     for _ in range(3):
         g.replay()
+    if flush is not None:
+        flush()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps = 5
@@ -665,6 +684,170 @@ def kernel_duration(torch, wl, which, n_launch):
     e1.record()
     e1.synchronize()
     return e0.elapsed_time(e1) / 1e3 / (reps * n_launch)
+
+
+def describe(shape) -> str:
+    return (f"{shape.name}: {shape.n_layers} layer(s) x {shape.n_slots} slot(s), {shape.n_qk_heads} QK / "
+            f"{shape.n_v_heads} V heads, d_k=d_v={shape.d_k}, {shape.n_tokens} tokens")
+
+
+# steps a per-config entry times at least (about 10 ms of device work or more)
+MIN_STEPS = {"layer_verify": 1000, "multislot_verify": 64, "prefill": 20}
+HEADLINE = "stack_verify"                                   # 48 layers x 8 slots: the largest configuration
+PER_CONFIG = ("layer_verify", "multislot_verify", "prefill")
+
+
+def measure(name, steps, warmup, device, world, l2, clocks, with_e2e, graph_len_max=64):
+    """Time `steps` steps of one workload (after `warmup` untimed ones) and its kernels; returns the
+    fields of a bench line (without the CPU baseline)."""
+    import torch
+    import torch.distributed as dist
+    shape = WORKLOADS[name]
+    wl = PrefillWorkload(shape, device, l2) if name == "prefill" else VerifyWorkload(shape, device, l2)
+    torch.cuda.synchronize()
+    # a step graph covers at most one rotation of the buffer sets, so no set comes round twice in a graph
+    graph_len = max(1, min(graph_len_max, steps, wl.n_sets))
+    if wl.layers > 1 or name == "prefill":
+        graph_len = 1
+    g_full, n_full, g_rem = time_graph_steps(torch, wl, steps, graph_len)
+    g_warm, nw_full, g_wrem = time_graph_steps(torch, wl, warmup, max(1, min(graph_len, warmup)),
+                                               first=wl.n_sets // 2)
+    # a buffer larger than L2, written between the warm-up and the timed steps
+    flush_buf = torch.empty(int(3 * l2), dtype=torch.uint8, device=device)
+    flush = lambda: flush_buf.fill_(1)
+    for _ in range(nw_full):
+        g_warm.replay()
+    if g_wrem:
+        g_wrem.replay()
+    flush()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(n_full):
+        g_full.replay()
+    if g_rem:
+        g_rem.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    dt = e0.elapsed_time(e1) / 1e3
+    bad = [int(x["status"].item()) for layers in wl.sets for x in layers if int(x["status"].item()) != 0]
+
+    # per-kernel durations (own timed regions, graphs of back-to-back launches over every set and layer)
+    n_launch = max(8, min(256, wl.n_sets * wl.layers))
+    if name == "prefill":
+        kdur = {"prefill": kernel_duration(torch, wl, "prefill", max(2, wl.n_sets), flush)}
+    elif wl.lazy:
+        kdur = {"lazy_verify": kernel_duration(torch, wl, "verify", n_launch, flush)}
+    elif wl.rolled:
+        kdur = {"verify": kernel_duration(torch, wl, "verify", n_launch, flush)}
+    elif wl.proj:
+        # the layer call is GEMM + verify + GEMM; what it takes beyond the two GEMMs timed alone is the
+        # verify plus the launch gaps between the library's kernels and it
+        kdur = {"layer": kernel_duration(torch, wl, "verify", n_launch, flush),
+                "gemm_in": kernel_duration(torch, wl, "gemm_in", n_launch, flush),
+                "gemm_out": kernel_duration(torch, wl, "gemm_out", n_launch, flush),
+                "rollback": kernel_duration(torch, wl, "rollback", n_launch, flush)}
+        kdur["verify_and_launch_gaps"] = max(0.0, kdur["layer"] - kdur["gemm_in"] - kdur["gemm_out"])
+    else:
+        kdur = {"verify": kernel_duration(torch, wl, "verify", n_launch, flush),
+                "rollback": kernel_duration(torch, wl, "rollback", n_launch, flush)}
+    t_wall2 = time.time()
+
+    dt = max_over_ranks(dt, device)
+    value = job_throughput(wl.tokens_per_step, steps, world, dt)
+    hbm, peak_kind = peaks()
+    if name == "prefill":
+        dom, dom_bytes, dom_src = "prefill", prefill_bytes(shape), ["prefill.cu", "internal.cuh"]
+    elif wl.proj:
+        dom, dom_bytes, dom_src = "gemm_in", proj_in_bytes(shape), ["proj.cu"]
+    elif wl.lazy:
+        dom = "lazy_verify"
+        dom_bytes = float(np.mean([lazy_step_bytes(shape, t) for t in wl.trims.reshape(-1, shape.n_slots)]))
+        dom_src = ["verify.cu", "internal.cuh"]
+    else:
+        dom, dom_bytes, dom_src = "verify", (tree_verify_bytes(shape) if getattr(wl, "tree", False)
+                                             else verify_bytes(shape)), ["verify.cu", "internal.cuh"]
+    achieved = dom_bytes / kdur[dom] / 1e9
+    sha = kernel_source_sha(dom_src)
+    traffic = recorded_traffic(dom, sha, name)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": traffic, "kernel": dom, "bytes_per_launch": dom_bytes, "launch_us": kdur[dom] * 1e6,
+            "peak_source": f"{peak_kind} hbm_gbs" + (" (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                                                     else " (recipe fallback)")}
+    if traffic:
+        # the same launch judged on the DRAM bytes ncu counted for it (L2 hits excluded)
+        roof["dram_gbs"] = traffic / kdur[dom] / 1e9
+        roof["dram_frac"] = roof["dram_gbs"] / hbm
+        roof["traffic_over_algorithmic"] = traffic / dom_bytes
+    if name == "prefill":
+        # the chunkwise products at the tf32 tensor rate take longer than the algorithmic bytes at the
+        # copy rate: the prefill is tensor-bound
+        flops = prefill_flops(shape)
+        tpk, tkind = tf32_peak()
+        t_ach = flops / kdur[dom] / 1e12
+        roof = {"bound": "tensor", "achieved": t_ach, "peak": tpk, "unit": "TFLOP/s", "frac": t_ach / tpk,
+                "traffic": traffic, "kernel": dom, "flops_per_launch": flops, "bytes_per_launch": dom_bytes,
+                "launch_us": kdur[dom] * 1e6, "hbm_gbs": achieved, "hbm_frac": achieved / hbm,
+                "peak_source": (f"{tkind} bf16_tflops x nominal tf32/bf16 ratio 1.1/2.25"
+                                + (" (MEASURED_PEAKS.json)" if tkind == "measured" else " (recipe fallback)")),
+                "note": "operands run as 3xTF32 (three tf32 products per fp32 product); flops counted once"}
+        if traffic:
+            roof["traffic_over_algorithmic"] = traffic / dom_bytes
+    step = ("chunked prefill" if name == "prefill" else
+            "layer: input projection GEMM + verify + output projection GEMM, then rollback" if wl.proj else
+            "verify with the previous step's rollback folded in (one launch)" if wl.rolled else
+            "lazy verify: commit of the pending batch (accepted-prefix re-run) + outputs of the new one"
+            if wl.lazy else "verify+rollback" + (" per layer, all layers" if wl.layers > 1 else ""))
+    res = {
+        "value": value, "unit": "tokens/s", "steps": steps, "warmup": warmup,
+        "ms_per_step": dt / steps * 1e3,
+        "config": {
+            "workload": describe(shape), "act_dtype": shape.act, "state_dtype": "f32", "step": step,
+            "l2": (f"{wl.n_sets} rotating buffer set(s), {wl.resident_per_set / 1e6:.0f} MB left in L2 per set "
+                   f"(state, conv state and window, activations; captures stream out evict-first); every set "
+                   f"is evicted by the others before it comes round again (> 3x L2 {l2 / 2**20:.0f} MiB), "
+                   f"and a {3 * l2 / 2**20:.0f} MiB buffer is written between the warm-up and the timed steps"),
+            "timing": f"CUDA events around CUDA-graph replays of {graph_len} step(s)",
+        },
+        "roofline": roof,
+        "kernels_us": {k: v * 1e6 for k, v in kdur.items()},
+        "step_bytes": wl.step_bytes(0),
+        "step_gbs": wl.step_bytes(0) * steps / dt / 1e9,
+        "gpu_launches": (wl.kernels_per_step if wl.kernels_per_step is not None
+                         else 1 + -(-shape.n_slots * shape.n_v_heads * 3 // 152)) * steps,
+        "clocks": clocks.summary(t_wall0 - 0.5, t_wall1 + 0.5),
+        "kernel_clocks": clocks.summary(t_wall1, t_wall2 + 0.5),
+    }
+    if wl.layers > 1:
+        res["config"]["units"] = (f"tokens/s = slots x {shape.n_tokens} verify tokens through all "
+                                  f"{shape.n_layers} layers per step")
+    if bad:
+        res["device_status_errors"] = bad
+    if with_e2e:
+        e_steps = max(20, min(steps, 500)) if name != "prefill" else max(5, min(steps, 50))
+        if wl.layers > 1:
+            e_steps = max(5, min(steps, 50))
+        edt, h2d, d2h = wl.e2e(e_steps, device)
+        edt = max_over_ranks(edt, device)
+        res["e2e"] = {"value": wl.tokens_per_step * e_steps * world / edt, "unit": "tokens/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+                      "timing": ("wall clock, host sync per step; one H2D copy of all the step's inputs "
+                                 "and one D2H copy of its outputs" if name != "prefill"
+                                 else "wall clock, host sync per step"),
+                      "api": ("gdn_verify_step_host (one C-ABI call per step with host buffers)"
+                              if name != "prefill" and wl.layers == 1
+                              and not (wl.tree or wl.lazy or wl.proj) else "the C-ABI calls of the step")}
+    del wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_cuda(args):
@@ -685,156 +868,44 @@ def run_cuda(args):
     gdn.lib()
 
     shape = WORKLOADS[args.workload]
-    if args.slots:
-        shape = shape.with_(n_slots=args.slots)
     props = torch.cuda.get_device_properties(local)
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
-    wl = PrefillWorkload(shape, device, l2) if args.workload == "prefill" else VerifyWorkload(shape, device, l2)
-    torch.cuda.synchronize()
     if args.profile:
-        # profiling mode (for ncu): eager steps on the current stream, no timing, no output
+        # profiling mode (for ncu): eager steps over the rotating sets on the current stream, no timing
+        if args.slots:
+            shape = shape.with_(n_slots=args.slots)
+        wl = (PrefillWorkload(shape, device, l2) if args.workload == "prefill"
+              else VerifyWorkload(shape, device, l2))
+        torch.cuda.synchronize()
         sp = torch.cuda.current_stream().cuda_stream
         for k in range(args.profile):
             wl.step(k % wl.n_sets, sp)
         torch.cuda.synchronize()
         return
 
-    graph_len = max(1, min(args.graph_len, args.steps))
-    if args.workload in ("stack_verify", "lazy_stack_verify", "rolled_stack_verify", "prefill"):
-        graph_len = 1
-    g_full, n_full, g_rem = time_graph_steps(torch, wl, args.steps, graph_len)
-    g_warm, nw_full, g_wrem = time_graph_steps(torch, wl, args.warmup, graph_len)
-
     vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
     clocks = ClockSampler(int(vis[local]) if len(vis) > local and vis[local].strip().isdigit() else local)
     clocks.start()
-    # warm-up steps (untimed)
-    for _ in range(nw_full):
-        g_warm.replay()
-    if g_wrem:
-        g_wrem.replay()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clocks.once()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
-    torch.cuda.synchronize()
-    e0.record()
-    for _ in range(n_full):
-        g_full.replay()
-    if g_rem:
-        g_rem.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    if world > 1:
-        dist.barrier()
-    clocks.once()
-    dt = e0.elapsed_time(e1) / 1e3
-    # the status words must still read GDN_OK
-    bad = [int(x["status"].item()) for layers in wl.sets for x in layers if int(x["status"].item()) != 0]
-
-    # per-kernel durations (own timed regions, graphs of back-to-back launches)
-    n_launch = max(1, min(64, 8 * wl.n_sets * wl.layers))
-    if args.workload == "prefill":
-        kdur = {"prefill": kernel_duration(torch, wl, "prefill", 2)}
-    elif wl.lazy:
-        kdur = {"lazy_verify": kernel_duration(torch, wl, "verify", n_launch)}
-    elif wl.rolled:
-        kdur = {"verify": kernel_duration(torch, wl, "verify", n_launch)}
-    elif wl.proj:
-        # the layer call is GEMM + verify + GEMM; what it takes beyond the two GEMMs timed alone is the
-        # verify plus the launch gaps between the library's kernels and it
-        kdur = {"layer": kernel_duration(torch, wl, "verify", n_launch),
-                "gemm_in": kernel_duration(torch, wl, "gemm_in", n_launch),
-                "gemm_out": kernel_duration(torch, wl, "gemm_out", n_launch),
-                "rollback": kernel_duration(torch, wl, "rollback", n_launch)}
-        kdur["verify_and_launch_gaps"] = max(0.0, kdur["layer"] - kdur["gemm_in"] - kdur["gemm_out"])
-    else:
-        kdur = {"verify": kernel_duration(torch, wl, "verify", n_launch),
-                "rollback": kernel_duration(torch, wl, "rollback", n_launch)}
+    glm = max(args.graph_len, 128)
+    head = measure(args.workload, args.steps, args.warmup, device, world, l2, clocks, not args.no_e2e, glm)
+    per_config = {}
+    if args.workload == HEADLINE and not args.no_per_config:
+        for name in PER_CONFIG:
+            k = max(args.steps, MIN_STEPS[name])
+            per_config[name] = measure(name, k, max(args.warmup, 3), device, world, l2, clocks, False, glm)
     clocks.stop()
 
-    dt = max_over_ranks(dt, device)
-    value = job_throughput(wl.tokens_per_step, args.steps, world, dt)
-    hbm, peak_kind = peaks()
-    if args.workload == "prefill":
-        dom, dom_bytes, dom_src = "prefill", prefill_bytes(shape), ["prefill.cu", "internal.cuh"]
-    elif wl.proj:
-        # dominant: the input projection GEMM (cuBLASLt), streaming the fused weights
-        dom, dom_bytes, dom_src = "gemm_in", proj_in_bytes(shape), ["proj.cu"]
-    elif wl.lazy:
-        # the timed launches cycle over every buffer set's pending trims: their mean bytes
-        dom = "lazy_verify"
-        dom_bytes = float(np.mean([lazy_step_bytes(shape, t) for t in wl.trims.reshape(-1, shape.n_slots)]))
-        dom_src = ["verify.cu", "internal.cuh"]
-    else:
-        dom, dom_bytes, dom_src = "verify", (tree_verify_bytes(shape) if getattr(wl, "tree", False)
-                                             else verify_bytes(shape)), ["verify.cu", "internal.cuh"]
-    achieved = dom_bytes / kdur[dom] / 1e9
-    sha = kernel_source_sha(dom_src)
-    traffic = recorded_traffic(dom, sha, args.workload)
-
-    res = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded splitmix64/Box-Muller)",
-        "config": {
-            "workload": (f"{shape.name}: {shape.n_layers} layer(s) x {shape.n_slots} slot(s), "
-                         f"{shape.n_qk_heads} QK / {shape.n_v_heads} V heads, d_k=d_v={shape.d_k}, "
-                         f"{shape.n_tokens} tokens"),
-            "act_dtype": shape.act, "state_dtype": "f32",
-            "step": ("chunked prefill" if args.workload == "prefill" else
-                     "layer: input projection GEMM + verify + output projection GEMM, then rollback" if wl.proj else
-                     "verify with the previous step's rollback folded in (one launch)" if wl.rolled else
-                     "lazy verify: commit of the pending batch (accepted-prefix re-run) + outputs of the new one"
-                     if wl.lazy else
-                     "verify+rollback"),
-            "l2": (f"rotating {wl.n_sets} buffer sets, {wl.n_sets * wl.step_bytes(0) / 1e6:.0f} MB "
-                   f"touched per rotation (> 3x L2 {l2 / 2**20:.0f} MiB)"),
-            "timing": f"CUDA events around CUDA-graph replays of {graph_len} steps",
-            "parallelism": f"replicas x{world}",
-        },
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic, "kernel": dom,
-                     "bytes_per_launch": dom_bytes, "launch_us": kdur[dom] * 1e6,
-                     "peak_source": f"{peak_kind} hbm_gbs" + (" (MEASURED_PEAKS.json)" if peak_kind == "measured"
-                                                               else " (recipe fallback)")},
-        "kernels_us": {k: v * 1e6 for k, v in kdur.items()},
-        "step_bytes": wl.step_bytes(0),
-        "step_gbs": wl.step_bytes(0) * args.steps / dt / 1e9,
-        "gpu_launches": (wl.kernels_per_step if wl.kernels_per_step is not None
-                         else 1 + -(-shape.n_slots * shape.n_v_heads * 3 // 152)) * args.steps,
-        "clocks": clocks.summary(t_wall0 - 0.5, t_wall1 + 0.5),
-    }
-    if args.workload == "prefill":
-        # the chunkwise products at the tf32 tensor rate take longer than the
-        # algorithmic bytes at the copy rate: the prefill is tensor-bound
-        flops = prefill_flops(shape)
-        tpk, tkind = tf32_peak()
-        t_ach = flops / kdur[dom] / 1e12
-        res["roofline"] = {
-            "bound": "tensor", "achieved": t_ach, "peak": tpk, "unit": "TFLOP/s", "frac": t_ach / tpk,
-            "traffic": traffic, "kernel": dom, "flops_per_launch": flops, "bytes_per_launch": dom_bytes,
-            "launch_us": kdur[dom] * 1e6, "hbm_gbs": achieved, "hbm_frac": achieved / hbm,
-            "peak_source": (f"{tkind} bf16_tflops x nominal tf32/bf16 ratio 1.1/2.25"
-                            + (" (MEASURED_PEAKS.json)" if tkind == "measured" else " (recipe fallback)")),
-            "note": "operands run as 3xTF32 (three tf32 products per fp32 product); flops counted once"}
-    if bad:
-        res["device_status_errors"] = bad
-    if not args.no_e2e:
-        e_steps = max(20, min(args.steps, 500)) if args.workload != "prefill" else max(5, min(args.steps, 50))
-        edt, h2d, d2h = wl.e2e(e_steps, device)
-        edt = max_over_ranks(edt, device)
-        res["e2e"] = {"value": wl.tokens_per_step * e_steps * world / edt, "unit": "tokens/s",
-                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
-                      "timing": ("wall clock, host sync per step; one H2D copy of all the step's inputs "
-                                 "and one D2H copy of its outputs" if args.workload != "prefill"
-                                 else "wall clock, host sync per step"),
-                      "api": ("gdn_verify_step_host (one C-ABI call per step with host buffers)"
-                              if args.workload != "prefill" and wl.layers == 1
-                              and not (wl.tree or wl.lazy or wl.proj) else "the calls of the step")}
+    res = {"metric": METRIC, "value": head.pop("value"), "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": head.pop("ms_per_step"),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic (seeded splitmix64/Box-Muller)"}
+    head.pop("steps")
+    head.pop("warmup")
+    res.update(head)
+    res["config"]["parallelism"] = f"replicas x{world}"
+    res["gpu_launches"] = head["gpu_launches"]
+    if per_config:
+        res["per_config"] = per_config
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(shape, args.cpu_seconds)
     if world > 1:
@@ -881,31 +952,40 @@ def _oracle_pass(shape, x, heads, n_threads, trims):
     oracle.rollback(shape, trims, r["state"], r["conv_state"], r["cap_state"], r["cap_conv"])
 
 
+def _layer_inputs(shape, n):
+    """Inputs of the first n layers of a workload (one layer: the workload's own)."""
+    one = shape.with_(n_layers=1)
+    return one, [make_inputs(one, layer=li) for li in range(max(1, min(n, shape.n_layers)))]
+
+
+def _oracle_layers(one, layers, n_passes, cores):
+    """n_passes whole passes of the step (every slot and every head) over the given layers in turn."""
+    for k in range(n_passes):
+        inp = layers[k % len(layers)]
+        _oracle_pass(one, inp.as_f64(), None, cores, inp.trim)
+
+
 def cpu_baseline(shape, seconds):
-    """fp64 oracle, all host cores, on whole value heads of the same workload
-    until about `seconds` of CPU work; tokens/s scaled by the fraction of heads."""
+    """The fp64 oracle as it stands on all host cores: whole passes of the step over every slot and
+    head of one layer, repeated (over the workload's layers in turn) for about `seconds`; tokens/s
+    counts a token once it has been through every layer of the workload."""
     import oracle
     oracle.build()
-    one = shape.with_(n_layers=1)
-    inp = make_inputs(one)
-    x = inp.as_f64()
     cores = os.cpu_count() or 1
-    heads = list(range(min(cores, shape.n_v_heads)))
+    one, layers = _layer_inputs(shape, 4)
     t0 = time.perf_counter()
-    _oracle_pass(one, x, heads, cores, inp.trim)
+    _oracle_layers(one, layers, 1, cores)
     t_pass = time.perf_counter() - t0
     reps = max(1, int(seconds / max(t_pass, 1e-3)))
     t0 = time.perf_counter()
-    for _ in range(reps):
-        _oracle_pass(one, x, heads, cores, inp.trim)
+    _oracle_layers(one, layers, reps, cores)
     dt = time.perf_counter() - t0
-    frac = len(heads) / shape.n_v_heads
-    tok = one.n_slots * one.n_tokens * frac * reps / shape.n_layers
-    return {"value": tok / dt, "unit": "tokens/s", "cores": min(cores, len(heads)) if shape.n_slots == 1 else cores,
-            "kind": "oracle",
-            "sample": (f"{reps} passes of verify+rollback over {len(heads)} of {shape.n_v_heads} value heads "
-                       f"(all {one.n_slots} slot(s), {one.n_tokens} tokens, 1 layer) of the same workload, fp64, "
-                       f"{dt:.1f} s")}
+    tok = one.n_slots * one.n_tokens * reps / shape.n_layers
+    return {"value": tok / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": (f"{reps} whole pass(es) of the step (verify+rollback, or the prefill) over all "
+                       f"{one.n_slots} slot(s) and {shape.n_v_heads} value heads of one layer, "
+                       f"{one.n_tokens} tokens, fp64, {cores} threads, {dt:.1f} s; a token counts once it has "
+                       f"been through all {shape.n_layers} layer(s)")}
 
 
 def run_reference(args):
@@ -915,34 +995,31 @@ def run_reference(args):
     import oracle
     oracle.build()
     shape = WORKLOADS[args.workload]
-    one = shape.with_(n_layers=1)
-    inp = make_inputs(one)
-    x = inp.as_f64()
     cores = os.cpu_count() or 1
-    # size each step so the whole run stays within ~2 minutes
+    one, layers = _layer_inputs(shape, 4)
+    # each step: whole layer passes of the workload, as many as keep the run within about two minutes
     budget = 120.0 / max(1, args.steps + args.warmup)
     t0 = time.perf_counter()
-    _oracle_pass(one, x, [0], 1, inp.trim)
-    t_head = time.perf_counter() - t0
-    n_heads = int(max(1, min(shape.n_v_heads, cores * max(1.0, budget / max(t_head, 1e-4)))))
-    n_heads = min(n_heads, shape.n_v_heads)
-    heads = list(range(n_heads))
+    _oracle_layers(one, layers, 1, cores)
+    t_pass = time.perf_counter() - t0
+    per_step = int(max(1, min(shape.n_layers, budget / max(t_pass, 1e-4))))
     for _ in range(args.warmup):
-        _oracle_pass(one, x, heads, cores, inp.trim)
+        _oracle_layers(one, layers, per_step, cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_pass(one, x, heads, cores, inp.trim)
+        _oracle_layers(one, layers, per_step, cores)
     dt = time.perf_counter() - t0
-    tok = one.n_slots * one.n_tokens * (n_heads / shape.n_v_heads) * args.steps / shape.n_layers
+    tok = one.n_slots * one.n_tokens * per_step * args.steps / shape.n_layers
     value = tok / dt
-    sample = (f"each step: verify+rollback over {n_heads} of {shape.n_v_heads} value heads of {shape.name} "
-              f"(fp64 oracle, {min(cores, n_heads * one.n_slots)} threads)")
+    sample = (f"each step: {per_step} whole pass(es) of the step over all {one.n_slots} slot(s) and "
+              f"{shape.n_v_heads} value heads of one layer of {shape.name} (fp64 oracle, {cores} threads); "
+              f"a token counts once it has been through all {shape.n_layers} layer(s)")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded splitmix64/Box-Muller)",
-        "config": {"workload": shape.name, "act_dtype": shape.act, "parallelism": "host cores"},
+        "config": {"workload": describe(shape), "act_dtype": shape.act, "parallelism": "host cores"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
@@ -951,14 +1028,16 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
-    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
-    ap.add_argument("--workload", choices=list(WORKLOADS), default="layer_verify")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default=HEADLINE)
     ap.add_argument("--graph-len", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the chosen workload (by default the headline also times configs 1, 2, 4)")
     ap.add_argument("--slots", type=int, default=0, help="override the workload's slot count (profiling cases)")
     ap.add_argument("--profile", type=int, default=0, metavar="K",
                     help="run K untimed eager steps and exit (for ncu captures)")

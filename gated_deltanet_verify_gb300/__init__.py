@@ -40,10 +40,8 @@ EXPORTED_SYMBOLS = ("gdn_verify_forward", "gdn_verify_tree", "gdn_rollback", "gd
                     "gdn_verify_after_rollback", "gdn_verify_lazy", "gdn_commit_lazy", "gdn_step_io_layout",
                     "gdn_verify_step_host", "gdn_proj_in_ld", "gdn_layer_workspace_bytes",
                     "gdn_project_in", "gdn_project_out", "gdn_layer_verify", "gdn_prefill_workspace_bytes",
-                    "gdn_prefill_chunked", "gdn_prefill_chunked_static", "gdn_last_error", "gdn_version")
-
-# size of the library's built-in prefill scratch (GDN_PREFILL_STATIC_SCRATCH_BYTES)
-PREFILL_STATIC_SCRATCH_BYTES = 16 << 20
+                    "gdn_prefill_chunked", "gdn_prefill_chunked_static", "gdn_prefill_static_scratch_bytes",
+                    "gdn_last_error", "gdn_version")
 
 
 class GdnError(RuntimeError):
@@ -129,6 +127,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_prefill_chunked.restype = ip
         L.gdn_prefill_chunked_static.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 9
         L.gdn_prefill_chunked_static.restype = ip
+        L.gdn_prefill_static_scratch_bytes.argtypes = []
+        L.gdn_prefill_static_scratch_bytes.restype = ctypes.c_size_t
         L.gdn_last_error.restype = ctypes.c_char_p
         L.gdn_version.restype = ctypes.c_char_p
         _lib = L
@@ -280,6 +280,11 @@ def gdn_prefill_chunked(dims: Dims, params: LayerParams, qkv, z, alpha, beta_raw
                                      _ptr(alpha), _ptr(beta_raw), _ptr(state), _ptr(conv_state), _ptr(out),
                                      _ptr(workspace), ctypes.c_size_t(ws_bytes), _ptr(d_status),
                                      _stream(stream)))
+
+
+def prefill_static_scratch_bytes() -> int:
+    """Size of the library's built-in prefill scratch (GDN_PREFILL_STATIC_SCRATCH_BYTES), read from the library."""
+    return int(lib().gdn_prefill_static_scratch_bytes())
 
 
 def gdn_prefill_chunked_static(dims: Dims, params: LayerParams, qkv, z, alpha, beta_raw, state, conv_state, out,

@@ -2,7 +2,7 @@
 
 Each translation unit is compiled in parallel, then linked into one shared
 library (CUDA runtime linked statically, so the library only needs the
-driver).  Rebuilds only what changed.
+driver; no other CUDA library is linked).  Rebuilds only what changed.
 """
 from __future__ import annotations
 
@@ -34,17 +34,6 @@ def nvcc() -> str:
         if cand and os.path.exists(cand):
             return cand
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libgdn_verify.so")
-
-
-def link_flags(cc: str) -> List[str]:
-    """cuBLASLt (the projection GEMMs), found through an rpath to the toolkit's
-    library directory so the library loads without LD_LIBRARY_PATH."""
-    home = os.path.dirname(os.path.dirname(os.path.realpath(cc)))
-    libdir = next((d for d in (os.path.join(home, "lib64"), os.path.join(home, "lib"))
-                   if os.path.exists(os.path.join(d, "libcublasLt.so"))), None)
-    if libdir is None:
-        raise RuntimeError(f"libcublasLt.so not found under {home}: the CUDA toolkit's cuBLAS is required")
-    return ["-L", libdir, "-lcublasLt", "-Xlinker", "-rpath=" + libdir]
 
 
 def _headers() -> List[str]:
@@ -110,7 +99,7 @@ def build(verbose: bool = False, extra_flags: List[str] = (), checked: bool = Fa
         list(ex.map(run, jobs))
     if jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        run([cc, *ARCH, "-shared", "-o", tmp, *objs, *link_flags(cc)])
+        run([cc, *ARCH, "-shared", "-o", tmp, *objs])
         os.replace(tmp, LIB)
     return LIB
 

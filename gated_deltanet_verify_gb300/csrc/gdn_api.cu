@@ -9,6 +9,8 @@
 #include <mutex>
 #include <string>
 
+#include <cudaTypedefs.h>
+
 namespace gdn {
 size_t verify_smem_bytes(int T, int dk, int dv, int P, int act_bytes, bool tree);
 }  // namespace gdn
@@ -98,29 +100,68 @@ int verify_parts_per_head(int B, int Hv, int r, int dv, int sm_count) {
 
 }  // namespace gdn
 
+namespace gdn {
+
+// cuCtxGetCurrent / cuCtxGetId from the driver, looked up once (the library links only the runtime)
+bool current_context_id(unsigned long long *id) {
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace gdn
+
 // ---- prefill with library-owned scratch -----------------------------------
-// One fixed scratch array per device (the module's device globals are per
-// context); its device address is looked up once per device and cached.
+// One fixed scratch array, which every context that loads this library's
+// device code holds (module globals are per context).  Its device address is
+// looked up with cudaGetSymbolAddress once per context -- in practice once per
+// device, on the first static call with that device current -- and cached
+// under the context's id, so a reset device (a new context, a new address) is
+// looked up again instead of being handed a stale pointer.
 namespace {
 __device__ __align__(256) unsigned char g_prefill_scratch[GDN_PREFILL_STATIC_SCRATCH_BYTES];
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices];
+gdn::PerContext<void *> g_scratch_addr;
 
 int static_scratch(void **addr) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "cudaGetDevice failed: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices) return fail(GDN_ERR_ARG, "device ordinal %d out of range", dev);
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_prefill_scratch);
-        if (e != cudaSuccess || !p)
-            return fail(GDN_ERR_LAUNCH, "looking up the prefill scratch array failed: %s", cudaGetErrorString(e));
-        g_scratch_addr[dev] = p;
-    }
-    *addr = g_scratch_addr[dev];
+    unsigned long long ctx = 0;
+    const bool known = gdn::current_context_id(&ctx);
+    if (known && g_scratch_addr.get(ctx, addr)) return GDN_OK;
+    void *p = nullptr;
+    // initialises the runtime's context on the current device if none is current yet
+    cudaError_t e = cudaGetSymbolAddress(&p, g_prefill_scratch);
+    if (e != cudaSuccess || !p)
+        return fail(GDN_ERR_LAUNCH, "looking up the prefill scratch array failed: %s", cudaGetErrorString(e));
+    if (gdn::current_context_id(&ctx)) g_scratch_addr.put(ctx, p);
+    *addr = p;
     return GDN_OK;
 }
 }  // namespace
@@ -327,6 +368,17 @@ int gdn_prefill_chunked(const gdn_dims *dims, const gdn_layer_params *params, co
     return GDN_OK;
 }
 
+size_t gdn_prefill_static_scratch_bytes(void) { return GDN_PREFILL_STATIC_SCRATCH_BYTES; }
+
+#if GDN_CHECKED
+// Test build only: the scratch address gdn_prefill_chunked_static would use in the current context
+// (NULL on failure), so a test can check that each context gets its own.
+void *gdn_test_static_scratch_address(void) {
+    void *p = nullptr;
+    return static_scratch(&p) == GDN_OK ? p : nullptr;
+}
+#endif
+
 int gdn_prefill_chunked_static(const gdn_dims *dims, const gdn_layer_params *params, const void *qkv,
                                const void *z, const void *alpha, const void *beta_raw, float *state,
                                float *conv_state, void *out, int *d_status, void *stream) {
@@ -406,8 +458,6 @@ static long long proj_in_cols(const gdn_dims &d) {
 
 static size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
-static constexpr size_t kLtWorkspace = size_t(32) << 20;
-
 // checks shared by the projection calls; M = B * T rows
 static int check_proj(const gdn_dims *dims, const gdn_proj_weights *w) {
     int rc = check_common(dims);
@@ -434,42 +484,49 @@ long long gdn_proj_in_ld(const gdn_dims *dims) {
 size_t gdn_layer_workspace_bytes(const gdn_dims *dims, int n_embd) {
     if (!dims || n_embd < 1) return 0;
     const size_t M = size_t(dims->n_slots) * size_t(dims->n_tokens);
-    return align256(M * size_t(gdn_proj_in_ld(dims)) * 2) + align256(M * size_t(dims->n_v_heads) * dims->d_v * 2) +
-           kLtWorkspace;
+    return align256(M * size_t(gdn_proj_in_ld(dims)) * 2) + align256(M * size_t(dims->n_v_heads) * dims->d_v * 2);
+}
+
+static int project_in(const gdn_dims *dims, const gdn_proj_weights *w, const void *x, void *act, int *d_status,
+                      void *stream) {
+    int rc = check_proj(dims, w);
+    if (rc) return rc;
+    if (!x || !act) return fail(GDN_ERR_ARG, "x or act is NULL");
+    if (!aligned16(x) || !aligned16(act)) return fail(GDN_ERR_ALIGN, "x and act must be 16-byte aligned");
+    std::string why;
+    const int M = dims->n_slots * dims->n_tokens;
+    if (!gdn::gemm_xwt_bf16(w->w_in, x, act, M, int(proj_in_cols(*dims)), w->n_embd, gdn_proj_in_ld(dims), d_status,
+                            static_cast<cudaStream_t>(stream), why))
+        return fail(GDN_ERR_LAUNCH, "input projection: %s", why.c_str());
+    return GDN_OK;
+}
+
+static int project_out(const gdn_dims *dims, const gdn_proj_weights *w, const void *out, void *y, int *d_status,
+                       void *stream) {
+    int rc = check_proj(dims, w);
+    if (rc) return rc;
+    if (!out || !y) return fail(GDN_ERR_ARG, "out or y is NULL");
+    if (!aligned16(out) || !aligned16(y)) return fail(GDN_ERR_ALIGN, "out and y must be 16-byte aligned");
+    std::string why;
+    const int M = dims->n_slots * dims->n_tokens;
+    if (!gdn::gemm_xwt_bf16(w->w_out, out, y, M, w->n_embd, dims->n_v_heads * dims->d_v, w->n_embd, d_status,
+                            static_cast<cudaStream_t>(stream), why))
+        return fail(GDN_ERR_LAUNCH, "output projection: %s", why.c_str());
+    return GDN_OK;
 }
 
 int gdn_project_in(const gdn_dims *dims, const gdn_proj_weights *w, const void *x, void *act, void *workspace,
                    size_t ws_bytes, void *stream) {
     g_err.clear();
-    int rc = check_proj(dims, w);
-    if (rc) return rc;
-    if (!x || !act) return fail(GDN_ERR_ARG, "x or act is NULL");
-    if (!aligned16(x) || !aligned16(act)) return fail(GDN_ERR_ALIGN, "x and act must be 16-byte aligned");
-    if (!workspace || ws_bytes < kLtWorkspace)
-        return fail(GDN_ERR_WORKSPACE, "the GEMM needs %zu bytes of workspace (got %zu)", kLtWorkspace, ws_bytes);
-    std::string why;
-    const int M = dims->n_slots * dims->n_tokens;
-    if (!gdn::gemm_xwt_bf16(w->w_in, x, act, M, int(proj_in_cols(*dims)), w->n_embd, gdn_proj_in_ld(dims), workspace,
-                            kLtWorkspace, static_cast<cudaStream_t>(stream), why))
-        return fail(GDN_ERR_LAUNCH, "input projection: %s", why.c_str());
-    return GDN_OK;
+    (void)workspace; (void)ws_bytes;            // the GEMM needs no scratch
+    return project_in(dims, w, x, act, nullptr, stream);
 }
 
 int gdn_project_out(const gdn_dims *dims, const gdn_proj_weights *w, const void *out, void *y, void *workspace,
                     size_t ws_bytes, void *stream) {
     g_err.clear();
-    int rc = check_proj(dims, w);
-    if (rc) return rc;
-    if (!out || !y) return fail(GDN_ERR_ARG, "out or y is NULL");
-    if (!aligned16(out) || !aligned16(y)) return fail(GDN_ERR_ALIGN, "out and y must be 16-byte aligned");
-    if (!workspace || ws_bytes < kLtWorkspace)
-        return fail(GDN_ERR_WORKSPACE, "the GEMM needs %zu bytes of workspace (got %zu)", kLtWorkspace, ws_bytes);
-    std::string why;
-    const int M = dims->n_slots * dims->n_tokens;
-    if (!gdn::gemm_xwt_bf16(w->w_out, out, y, M, w->n_embd, dims->n_v_heads * dims->d_v, w->n_embd, workspace,
-                            kLtWorkspace, static_cast<cudaStream_t>(stream), why))
-        return fail(GDN_ERR_LAUNCH, "output projection: %s", why.c_str());
-    return GDN_OK;
+    (void)workspace; (void)ws_bytes;
+    return project_out(dims, w, out, y, nullptr, stream);
 }
 
 int gdn_layer_verify(const gdn_dims *dims, const gdn_layer_params *params, const gdn_proj_weights *w,
@@ -487,15 +544,14 @@ int gdn_layer_verify(const gdn_dims *dims, const gdn_layer_params *params, const
     const long long ld = gdn_proj_in_ld(dims);
     unsigned char *act = static_cast<unsigned char *>(workspace);
     unsigned char *out = act + align256(M * size_t(ld) * 2);
-    unsigned char *lt = out + align256(M * size_t(d.n_v_heads) * d.d_v * 2);
-    if ((rc = gdn_project_in(dims, w, x, act, lt, kLtWorkspace, stream))) return rc;
+    if ((rc = project_in(dims, w, x, act, d_status, stream))) return rc;
     // the verify reads q|k|v, z, alpha and beta_raw as column blocks of the activation matrix
     const long long C = conv_channels(dims), V = (long long)d.n_v_heads * d.d_v;
     unsigned char *z = act + C * 2, *alpha = act + (C + V) * 2, *beta = alpha + size_t(d.n_v_heads) * 2;
     if ((rc = verify_impl(dims, params, act, z, alpha, beta, nullptr, state, conv_state, cap_state, cap_conv, out,
                           d_status, stream, gdn::kChain, nullptr, nullptr, nullptr, nullptr, ld)))
         return rc;
-    return gdn_project_out(dims, w, out, y, lt, kLtWorkspace, stream);
+    return project_out(dims, w, out, y, d_status, stream);
 }
 
 }  // extern "C"

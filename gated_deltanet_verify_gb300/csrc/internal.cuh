@@ -3,9 +3,11 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <string>
 
 #include "gdn_verify.h"
@@ -87,11 +89,56 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
                            void *out, void *workspace, int *d_status, cudaStream_t stream);
 
 // Row-major C[M][N] (row stride ldc) = X[M][K] @ W[N][K]^T, bf16 in and out,
-// fp32 accumulation (cuBLASLt).  false with the reason in why.
-bool gemm_xwt_bf16(const void *W, const void *X, void *C, int M, int N, int K, long long ldc, void *ws,
-                   size_t ws_bytes, cudaStream_t stream, std::string &why);
+// fp32 accumulation (proj.cu; no scratch).  d_status (may be NULL) receives
+// GDN_ERR_TIMEOUT if a bounded wait gave up.  false with the reason in why.
+bool gemm_xwt_bf16(const void *W, const void *X, void *C, int M, int N, int K, long long ldc, int *d_status,
+                   cudaStream_t stream, std::string &why);
+
+// cuTensorMapEncodeTiled from the driver, looked up once (NULL if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Choice of CTAs per value head for a verify launch (host heuristic).
 int verify_parts_per_head(int B, int Hv, int r, int dv, int sm_count);
+
+// Identity of the CUDA context current on the calling thread (cuCtxGetId: unique for the life of the
+// process).  Host-side caches of per-context facts -- function attributes, device-symbol addresses --
+// are keyed on it, so that a device reset or another context on the same device never reads an entry
+// made for a context that no longer exists.  false if no context is current (or the driver lacks the
+// entry points).
+bool current_context_id(unsigned long long *id);
+
+// A small thread-safe map from context id to one cached value; the oldest entry gives way when full.
+template <typename V, int N = 16>
+class PerContext {
+  public:
+    bool get(unsigned long long id, V *v) {
+        std::lock_guard<std::mutex> lock(mu_);
+        for (int i = 0; i < N; ++i)
+            if (used_[i] && ids_[i] == id) {
+                *v = vals_[i];
+                return true;
+            }
+        return false;
+    }
+    void put(unsigned long long id, const V &v) {
+        std::lock_guard<std::mutex> lock(mu_);
+        for (int i = 0; i < N; ++i)
+            if (used_[i] && ids_[i] == id) {
+                vals_[i] = v;
+                return;
+            }
+        ids_[next_] = id;
+        vals_[next_] = v;
+        used_[next_] = true;
+        next_ = (next_ + 1) % N;
+    }
+
+  private:
+    std::mutex mu_;
+    unsigned long long ids_[N] = {};
+    V vals_[N] = {};
+    bool used_[N] = {};
+    int next_ = 0;
+};
 
 }  // namespace gdn

@@ -10,10 +10,11 @@
 //   W = T diag(beta Gamma) K,   U~ = T diag(beta) V,   U = U~ - W S0
 //   O = diag(Gamma) Q S0 + (Q K^T (.) M) U,   M[r][s] = Gamma_r / Gamma_s (s <= r)
 //   S = Gamma_C S0 + (diag(Gamma_C / Gamma) K)^T U
-// Every dense product runs on tcgen05.mma (kind::tf32, fp32 accumulators in
-// tensor memory) with 3xTF32 operands: each fp32 operand is split into a
-// tf32-exact high part and the remainder, and A.B is taken as hi.hi + hi.lo +
-// lo.hi.  Single-pass tf32 (or bf16) operands are not accurate enough here:
+// Every dense product but G = [K; Q] K^T (fp32 CUDA-core FMA chains, see the
+// preparation phase) runs on tcgen05.mma (kind::tf32, fp32 accumulators in
+// tensor memory) with 3xTF32 operands: each fp32 operand is split into its
+// nearest tf32 value and the nearest tf32 value of the remainder, and A.B is
+// taken as hi.hi + hi.lo + lo.hi.  Single-pass tf32 (or bf16) operands are not accurate enough here:
 // the delta rule subtracts nearly equal predictions (U~ against W S0) and the
 // per-token RMSNorm rescales small outputs, so an operand rounding of 2^-11
 // becomes an error of 10-60 % in the outputs; with the split it is ~1e-5.
@@ -23,7 +24,8 @@
 //   * preparation CTAs (every SM the state CTAs leave) claim (chunk, key head) work items
 //     in chunk order from a counter; per item the q/k work is done once for
 //     the r value heads that share the key head (raw window by TMA,
-//     conv + SiLU into TMEM, L2 norms, G = [K; Q] K^T kept in TMEM), then per
+//     conv + SiLU into TMEM, L2 norms, G = [K; Q] K^T in fp32 FMA chains, kept
+//     in TMEM), then per
 //     value head its gates, v conv (into shared memory), A and the masked,
 //     decayed P, T = (I + A)^-1 (16 x 16 blocks), W^T and U~^T; they publish
 //     the ready-split operands ([-W; Gamma Q] as one operand, P, Gamma_C/Gamma
@@ -33,7 +35,7 @@
 //     acquires a slot, pulls it in with bulk copies and runs only the
 //     state-dependent products and the epilogue:
 //       [X^T | O^T] = S0^T [-W; Gamma Q]^T          (one N 128 product, A from TMEM)
-//       U^T = U~^T + X^T,  O^T += U^T P^T            (N 64)
+//       U^T = U~^T + X^T,  O^T = (Gamma Q S0)^T + U^T P^T   (N 64)
 //       D2  = U^T (diag(Gamma_C / Gamma) K)          (N 128, K 64);  S^T <- Gamma_C S^T + D2
 //     then the gated RMSNorm.  It frees the slot once its bulk copies landed.
 // The launch is cooperative (every CTA resident at once), so the flag waits
@@ -94,8 +96,10 @@ constexpr uint32_t kSsqOff = 8 * 1024;         // 8 channel blocks (q, k) x 64 t
 // chunk's conv outputs q and k (lane = channel, column = token; not normalised).
 constexpr uint32_t kColG = 0, kColUT = 64, kColWT = 128, kColQ = 192, kColK = 256;
 static_assert(kColK + 64 <= kTmemCols, "TMEM columns");
-// State CTA: X^T (then U^T hi) | O^T | U^T lo | S^T hi (then D2) | S^T lo
-constexpr uint32_t kSX = 64, kSO = 128, kSUlo = 192, kSShi = 256, kSSlo = 384;
+// State CTA: (U^T P^T) | X^T (then U^T hi) | (Gamma Q S0)^T | U^T lo | S^T hi (then D2) | S^T lo.  The two
+// parts of O^T have accumulators of their own and are added in fp32 on the CUDA cores (a product added
+// onto an accumulator that already holds a large value truncates relative to that value)
+constexpr uint32_t kSO2 = 0, kSX = 64, kSO = 128, kSUlo = 192, kSShi = 256, kSSlo = 384;
 static_assert(kSSlo + 128 <= kTmemCols, "TMEM columns of the state CTA");
 
 // One ring slot: the chunk's operands in the exact shared-memory layout the state CTA uses.
@@ -112,6 +116,10 @@ static_assert(kFlagWords >= 3 * kRing, "flag words");
 // product until the A2 operand build, by which time every thread holds its row in registers
 constexpr uint32_t kVt = kRA + 64 * 1024;
 constexpr int kVtStride = kC + 4;
+// fp32 K^ / Q^ rows for the G product (start of the A region), padded so that a warp's 16-byte row reads
+// at rows r .. r+7 fall in distinct banks
+constexpr int kXStride = kD + 4;
+static_assert(2 * kC * kXStride * 4 <= 128 * 1024, "K^ / Q^ rows fit the A region");
 static_assert(64 * 1024 + 128 * kVtStride * 4 <= 128 * 1024, "v^T fits the upper half of the A region");
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
@@ -132,11 +140,26 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 __device__ __forceinline__ uint32_t plane_off(int r, int k4, int K) {
     return (uint32_t)((((r >> 3) * (K >> 2) + k4) << 7) + ((r & 7) << 4));
 }
-__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+// x rounded to the nearest tf32 value (ties to even).  A kind::tf32 MMA reads only the upper 19 bits of
+// each fp32 operand, so both parts of a split are made exact tf32 values: hi = tf32(x), lo = tf32(x - hi).
+// Rounding both (instead of cutting the low bits off, which the tensor core would do to an unrounded
+// remainder) keeps the split's error symmetric and about four times smaller.
+__device__ __forceinline__ float tf32_rn(float x) {
+    uint32_t u = __float_as_uint(x);
+    u += 0xFFFu + ((u >> 13) & 1u);
+    return __uint_as_float(u & 0xFFFFE000u);
+}
+__device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
+    hi = tf32_rn(x);
+    lo = tf32_rn(x - hi);
+}
 // 4 consecutive k of row r: the tf32 part into the hi plane, the remainder into the lo plane
 __device__ __forceinline__ void put4(unsigned char *hi, unsigned char *lo, int r, int k4, int K, float4 v) {
-    const float4 h = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
-    const float4 l = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
+    float4 h, l;
+    split_tf32(v.x, h.x, l.x);
+    split_tf32(v.y, h.y, l.y);
+    split_tf32(v.z, h.z, l.z);
+    split_tf32(v.w, h.w, l.w);
     const uint32_t off = plane_off(r, k4, K);
     *reinterpret_cast<float4 *>(hi + off) = h;
     *reinterpret_cast<float4 *>(lo + off) = l;
@@ -192,18 +215,20 @@ __device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t a, uint64_t b, uin
                  "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
                  "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
-// D (128 x N, fp32 in TMEM) (+)= A (128 x K) . B (N x K)^T with 3xTF32 planes
+// D (128 x N, fp32 in TMEM) (+)= A (128 x K) . B (N x K)^T with 3xTF32 planes.  The tensor core truncates
+// its fp32 accumulator at every step, relative to the accumulator's magnitude, so the small cross terms
+// (hi.lo, lo.hi) go in first while the accumulator is still small and the large hi.hi products last:
+// measured on the GB300 for K = 128 dot products, this order errs at most ~4 units of 2^-24 of sum |a b|
+// (an fp32 FMA chain: ~3.7), against ~18 with the three products interleaved per K step.
 __device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo, int K,
                                      int N, bool accumulate) {
     const uint32_t id = idesc_tf32(N);
-    for (int ks = 0; ks < K / 8; ++ks) {
-        const uint32_t o = (uint32_t)ks * 256u;                // 8 tf32 = two core matrices along K
-        const uint64_t ah = make_desc(a_hi + o, K), al = make_desc(a_lo + o, K);
-        const uint64_t bh = make_desc(b_hi + o, K), bl = make_desc(b_lo + o, K);
-        mma_tf32(d, ah, bh, id, (ks > 0 || accumulate) ? 1u : 0u);
-        mma_tf32(d, ah, bl, id, 1u);
-        mma_tf32(d, al, bh, id, 1u);
-    }
+    for (int pass = 0; pass < 3; ++pass)
+        for (int ks = 0; ks < K / 8; ++ks) {
+            const uint32_t o = (uint32_t)ks * 256u;            // 8 tf32 = two core matrices along K
+            const uint32_t a = pass == 1 ? a_lo : a_hi, b = pass == 0 ? b_lo : b_hi;
+            mma_tf32(d, make_desc(a + o, K), make_desc(b + o, K), id, (pass > 0 || ks > 0 || accumulate) ? 1u : 0u);
+        }
 }
 // D (128 x N) (+)= A (128 x K, tf32 columns of TMEM: lane = row) . B (N x K, smem)^T, 3xTF32
 __device__ __forceinline__ void mma_tf32_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -211,16 +236,16 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d, uint32_t a, uint64_t b, 
                  "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d),
                  "r"(a), "l"(b), "r"(idesc), "r"(acc));
 }
+// (the same pass order as mma3: cross terms first, hi.hi last)
 __device__ __forceinline__ void mma3_ts(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo, int K,
                                         int N, bool accumulate) {
     const uint32_t id = idesc_tf32(N);
-    for (int ks = 0; ks < K / 8; ++ks) {
-        const uint32_t o = (uint32_t)ks * 256u;
-        const uint64_t bh = make_desc(b_hi + o, K), bl = make_desc(b_lo + o, K);
-        mma_tf32_ts(d, a_hi + 8 * ks, bh, id, (ks > 0 || accumulate) ? 1u : 0u);
-        mma_tf32_ts(d, a_hi + 8 * ks, bl, id, 1u);
-        mma_tf32_ts(d, a_lo + 8 * ks, bh, id, 1u);
-    }
+    for (int pass = 0; pass < 3; ++pass)
+        for (int ks = 0; ks < K / 8; ++ks) {
+            const uint32_t o = (uint32_t)ks * 256u;
+            const uint32_t a = pass == 1 ? a_lo : a_hi, b = pass == 0 ? b_lo : b_hi;
+            mma_tf32_ts(d, a + 8 * ks, make_desc(b + o, K), id, (pass > 0 || ks > 0 || accumulate) ? 1u : 0u);
+        }
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
@@ -541,22 +566,51 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x) {
         }
         __syncthreads();
         {
-            // this thread holds channel i = tl of 32 tokens: the rows of [K^; Q^] get column i
+            // K^ and Q^ as fp32 rows of RA (rows 0-63: K^ tokens, rows 64-127: Q^ tokens; the raw window is
+            // consumed): this thread holds channel i = tl of 32 tokens and writes column i
+            float *Xr = reinterpret_cast<float *>(RA);
             float x32[32];
             tmem_ld16(tmem + tq + kColK + 32 * half, x32);
             tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) x32[q] *= invk[32 * half + q];
-            put_col32(RA, RA + 64 * 1024, 32 * half, tl, x32);
+            for (int q = 0; q < 32; ++q) Xr[(32 * half + q) * kXStride + tl] = x32[q] * invk[32 * half + q];
             tmem_ld16(tmem + tq + kColQ + 32 * half, x32);
             tmem_ld16(tmem + tq + kColQ + 32 * half + 16, x32 + 16);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) x32[q] *= invq[32 * half + q];
-            put_col32(RA, RA + 64 * 1024, kC + 32 * half, tl, x32);
+            for (int q = 0; q < 32; ++q) Xr[(kC + 32 * half + q) * kXStride + tl] = x32[q] * invq[32 * half + q];
         }
-        x.publish();
-        if (tid == 0) mma3(tmem + kColG, sRA, sRA + 64 * 1024, sRA, sRA + 64 * 1024, 128, 64, false);
-        x.commit_wait();                                    // G stays in TMEM for every value head
+        __syncthreads();
+        {
+            // G = [K^; Q^] K^T in fp32 FMA chains, thread (row r = tl, column half) taking G[r][32 half ..
+            // 32 half + 31].  These are dot products of unit vectors that nearly cancel (q.k ~ 1e-2 from terms
+            // summing to ~1 in magnitude), and the per-token RMSNorm rescales tokens whose output is small:
+            // with the tensor core's split operands (error ~2^-22 of the terms) and its truncating
+            // accumulation, rare outputs of the 8192-token layer were measured outside the tolerance, so this
+            // product is taken at full fp32 precision.  The result goes to TMEM where the value-head phases
+            // read it (lane = row r, column = s).
+            const float *Xr = reinterpret_cast<const float *>(RA);
+            const float4 *xrow = reinterpret_cast<const float4 *>(Xr + tl * kXStride);
+            const float *krows = Xr + 32 * half * kXStride;
+            float acc[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) acc[q] = 0.f;
+#pragma unroll 2
+            for (int i4 = 0; i4 < kD / 4; ++i4) {
+                const float4 xv = xrow[i4];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const float4 kv = *reinterpret_cast<const float4 *>(krows + q * kXStride + 4 * i4);
+                    acc[q] = fmaf(xv.x, kv.x, acc[q]);
+                    acc[q] = fmaf(xv.y, kv.y, acc[q]);
+                    acc[q] = fmaf(xv.z, kv.z, acc[q]);
+                    acc[q] = fmaf(xv.w, kv.w, acc[q]);
+                }
+            }
+            tmem_st16(tmem + tq + kColG + 32 * half, acc);
+            tmem_st16(tmem + tq + kColG + 32 * half + 16, acc + 16);
+            tmem_wait_st();
+        }
+        x.publish();                                        // G stays in TMEM for every value head
         if (tid == 0) issue_v(c, s, kh * R);
 
         for (int hi = 0; hi < R; ++hi) {
@@ -868,10 +922,7 @@ __device__ __forceinline__ void advance_state(const PrefillArgs &a, Ctx &x, int 
         for (int q4 = 0; q4 < 4; ++q4) {
             float hi16[16], lo16[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                hi16[e] = tf32_hi(St[16 * q4 + e]);
-                lo16[e] = St[16 * q4 + e] - hi16[e];
-            }
+            for (int e = 0; e < 16; ++e) split_tf32(St[16 * q4 + e], hi16[e], lo16[e]);
             tmem_st16(tmem + tq + kSShi + 64 * half + 16 * q4, hi16);
             tmem_st16(tmem + tq + kSSlo + 64 * half + 16 * q4, lo16);
         }
@@ -896,10 +947,7 @@ __device__ __forceinline__ void advance_state(const PrefillArgs &a, Ctx &x, int 
             for (int q2 = 0; q2 < 2; ++q2) {
                 float hi16[16], lo16[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    hi16[e] = tf32_hi(u32[16 * q2 + e]);
-                    lo16[e] = u32[16 * q2 + e] - hi16[e];
-                }
+                for (int e = 0; e < 16; ++e) split_tf32(u32[16 * q2 + e], hi16[e], lo16[e]);
                 tmem_st16(tmem + tq + kSX + 32 * half + 16 * q2, hi16);
                 tmem_st16(tmem + tq + kSUlo + 32 * half + 16 * q2, lo16);
             }
@@ -908,9 +956,9 @@ __device__ __forceinline__ void advance_state(const PrefillArgs &a, Ctx &x, int 
         x.wait_bar(ldbar, ld_phase);
         if (tid == 0) st_release(ring.empty + slot, c + 1);     // the slot's bytes are all on chip
         x.publish();
-        // O^T += U^T P^T;  D2 = U^T (diag(Gamma_C / Gamma) K)
+        // O2^T = U^T P^T (its own accumulator);  D2 = U^T (diag(Gamma_C / Gamma) K)
         if (tid == 0) {
-            mma3_ts(tmem + kSO, tmem + kSX, tmem + kSUlo, sRB, sRB + 16 * 1024, 64, 64, true);
+            mma3_ts(tmem + kSO2, tmem + kSX, tmem + kSUlo, sRB, sRB + 16 * 1024, 64, 64, false);
             mma3_ts(tmem + kSShi, tmem + kSX, tmem + kSUlo, sRA, sRA + 32 * 1024, 64, 128, false);
         }
         float zg[32];
@@ -930,9 +978,13 @@ __device__ __forceinline__ void advance_state(const PrefillArgs &a, Ctx &x, int 
 
         // ---------------- outputs (gated RMSNorm) and the state update
         {
-            float o32[32];
+            float o32[32], p32[32];
             tmem_ld16(tmem + tq + kSO + 32 * half, o32);
             tmem_ld16(tmem + tq + kSO + 32 * half + 16, o32 + 16);
+            tmem_ld16(tmem + tq + kSO2 + 32 * half, p32);
+            tmem_ld16(tmem + tq + kSO2 + 32 * half + 16, p32 + 16);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o32[q] += p32[q];
             // per-token sums of squares over this warp's 32 columns: reduce-scatter, lane l ends with token l
             float v[32];
 #pragma unroll
@@ -1082,21 +1134,6 @@ size_t prefill_workspace_bytes(const gdn_dims &d) {
     return ring_offset_bytes(d) + pairs * kRing * kSlotBytes;
 }
 
-// cuTensorMapEncodeTiled from the driver, looked up once
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const void *qkv, const void *z,
                            const void *alpha, const void *beta_raw, float *state, float *conv_state,
                            void *out, void *workspace, int *d_status, cudaStream_t stream) {
@@ -1111,11 +1148,16 @@ cudaError_t launch_prefill(const gdn_dims &d, const gdn_layer_params &p, const v
     a.ring_offset = ring_offset_bytes(d);
     a.n_prep = 1;
     a.d_status = d_status;
-    // Fault injection for tests, on the host: GDN_FAULT_DROP_CHUNK=<c> makes the preparation CTAs never
-    // publish chunk c, so the state CTA's bounded wait runs out and the call reports GDN_ERR_TIMEOUT
-    // through d_status (the outputs are then undefined; nothing faults or hangs).
+#if GDN_CHECKED
+    // Test build only (the ordinary library never reads the environment): fault injection on the host.
+    // GDN_FAULT_DROP_CHUNK=<c> makes the preparation CTAs never publish chunk c, so the state CTA's
+    // bounded wait runs out and the call reports GDN_ERR_TIMEOUT through d_status (the outputs are then
+    // undefined; nothing faults or hangs).
     const char *drop = getenv("GDN_FAULT_DROP_CHUNK");
     a.drop_chunk = drop ? atoi(drop) : -1;
+#else
+    a.drop_chunk = -1;
+#endif
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const bool bf = d.act_dtype == GDN_BF16;

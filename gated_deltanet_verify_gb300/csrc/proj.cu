@@ -1,131 +1,362 @@
-// proj.cu -- the projections either side of the GDN block as plain bf16 GEMMs
-// through cuBLASLt (fp32 accumulation): the fused input projection
-// x -> [qkv | z | alpha | beta_raw] and the output projection out -> y.
+// proj.cu -- the projections either side of the GDN block: the fused input
+// projection x -> [qkv | z | alpha | beta_raw] and the output projection
+// out -> y, as one hand-written sm_103a GEMM kernel.
 //
-// Row-major C[M][N] (row stride ldc) = X[M][K] @ W[N][K]^T is, in cuBLAS's
-// column-major terms, D (N x M, ld ldc) = op_T(A) (N x K) * B (K x M) with A
-// the weight stored K x N (ld K) and B the activations stored K x M (ld K):
-// the "TN" form, weights K-major.  The matmul descriptor, layouts and the
-// algorithm of a shape are chosen once per device and cached.
+// Row-major C[M][N] (row stride ldc, bf16) = X[M][K] @ W[N][K]^T, bf16
+// operands, fp32 accumulation.  In a verify step M = slots x tokens is small
+// (16 rows for one slot) while W holds tens of MB, so the GEMM streams the
+// weights: the weight rows are the tensor core's M dimension and the
+// activation rows its N.
+//
+//   * One CTA per 128-row tile of W (and per split of K when the tiles are
+//     too few to cover the SMs; a 256-row block of X per grid row).  The tile
+//     is D = W_tile X^T (128 x Mt), fp32 in tensor memory (tcgen05.mma
+//     kind::f16, bf16 A and B, both K-major from shared memory).
+//   * Warp 0 is the TMA producer: each stage holds 64 columns of K (128
+//     bytes per row) of the W tile and of X, one TMA box each, in the
+//     128-byte swizzled K-major layout the tensor core reads directly.
+//     Warp 1 issues the MMAs (4 per stage) and frees each stage through
+//     tcgen05.commit on the stage's "empty" barrier.
+//   * Programmatic dependent launch: the weight tiles of the first stages
+//     are requested before the grid-dependency wait (the weights do not
+//     depend on the previous kernel; X does), so the stream of weights starts
+//     while the previous kernel finishes.
+//   * Epilogue: thread t of the 128 reads TMEM lane t (weight row n0 + t)
+//     and writes column n0 + t of every output row.  With K split S ways the
+//     S CTAs of a tile form a thread-block cluster: after a cluster barrier
+//     (every split's MMAs are done, so the first split's pipeline buffers are
+//     free) the other splits write their fp32 partial tiles into the first
+//     split's shared memory (distributed shared memory), and after a second
+//     barrier the first split adds them to its own in split order and writes
+//     bf16.  No global scratch, and the sum's order is fixed.
+//   * Every wait is bounded; a wait that gives up reports GDN_ERR_TIMEOUT on
+//     the caller's status word (when one is given) and the tile is skipped.
 #include "internal.cuh"
 
-#include <cublasLt.h>
-
-#include <deque>
-#include <mutex>
+#include <cuda_bf16.h>
 
 namespace gdn {
 namespace {
 
-constexpr int kMaxDevices = 64;
+constexpr int kTileN = 128;             // weight rows per CTA (MMA M)
+constexpr int kKBlk = 64;               // K columns per pipeline stage
+constexpr int kMaxMt = 256;             // activation rows per CTA (MMA N)
+constexpr int kThreads = 128;
+constexpr int kSpin = 1 << 22;          // mbarrier polls before a wait gives up
 
-struct Plan {
-    int dev, M, N, K;
+struct GemmArgs {
+    CUtensorMap w_map, x_map;
+    int M, N, K, Mt;                    // Mt: activation rows per CTA (multiple of 16, <= 256)
+    int n_kb, kb_per_split, splits, stages;
     long long ldc;
-    cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t a = nullptr, b = nullptr, d = nullptr;
-    cublasLtMatmulAlgo_t algo;
-    size_t ws_bytes = 0;
+    __nv_bfloat16 *C;
+    int *d_status;
 };
 
-std::mutex g_mu;
-cublasLtHandle_t g_handle[kMaxDevices];
-std::deque<Plan> g_plans;           // a deque: references stay valid as plans are added
-
-const char *lt_name(cublasStatus_t s) {
-    switch (s) {
-        case CUBLAS_STATUS_SUCCESS: return "success";
-        case CUBLAS_STATUS_NOT_INITIALIZED: return "not initialised";
-        case CUBLAS_STATUS_ALLOC_FAILED: return "allocation failed";
-        case CUBLAS_STATUS_INVALID_VALUE: return "invalid value";
-        case CUBLAS_STATUS_ARCH_MISMATCH: return "architecture mismatch";
-        case CUBLAS_STATUS_EXECUTION_FAILED: return "execution failed";
-        case CUBLAS_STATUS_INTERNAL_ERROR: return "internal error";
-        case CUBLAS_STATUS_NOT_SUPPORTED: return "not supported";
-        default: return "error";
-    }
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-
-#define LT_TRY(call, what)                                                            \
-    do {                                                                              \
-        cublasStatus_t st_ = (call);                                                  \
-        if (st_ != CUBLAS_STATUS_SUCCESS) {                                           \
-            why = std::string(what) + ": cuBLASLt " + lt_name(st_);                   \
-            return false;                                                             \
-        }                                                                             \
-    } while (0)
-
-void free_plan(Plan &p) {
-    if (p.d) cublasLtMatrixLayoutDestroy(p.d);
-    if (p.b) cublasLtMatrixLayoutDestroy(p.b);
-    if (p.a) cublasLtMatrixLayoutDestroy(p.a);
-    if (p.op) cublasLtMatmulDescDestroy(p.op);
-    p.op = nullptr; p.a = p.b = p.d = nullptr;
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
 }
-
-bool make_plan_steps(Plan &p, cublasLtHandle_t h, std::string &why) {
-    LT_TRY(cublasLtMatmulDescCreate(&p.op, CUBLAS_COMPUTE_32F, CUDA_R_32F), "matmul descriptor");
-    const cublasOperation_t tA = CUBLAS_OP_T, tB = CUBLAS_OP_N;
-    LT_TRY(cublasLtMatmulDescSetAttribute(p.op, CUBLASLT_MATMUL_DESC_TRANSA, &tA, sizeof(tA)), "transa");
-    LT_TRY(cublasLtMatmulDescSetAttribute(p.op, CUBLASLT_MATMUL_DESC_TRANSB, &tB, sizeof(tB)), "transb");
-    LT_TRY(cublasLtMatrixLayoutCreate(&p.a, CUDA_R_16BF, uint64_t(p.K), uint64_t(p.N), int64_t(p.K)), "A layout");
-    LT_TRY(cublasLtMatrixLayoutCreate(&p.b, CUDA_R_16BF, uint64_t(p.K), uint64_t(p.M), int64_t(p.K)), "B layout");
-    LT_TRY(cublasLtMatrixLayoutCreate(&p.d, CUDA_R_16BF, uint64_t(p.N), uint64_t(p.M), int64_t(p.ldc)), "D layout");
-    cublasLtMatmulPreference_t pref = nullptr;
-    LT_TRY(cublasLtMatmulPreferenceCreate(&pref), "preference");
-    const uint64_t ws = p.ws_bytes;
-    cublasStatus_t st = cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws,
-                                                             sizeof(ws));
-    cublasLtMatmulHeuristicResult_t res = {};
-    int n = 0;
-    if (st == CUBLAS_STATUS_SUCCESS)
-        st = cublasLtMatmulAlgoGetHeuristic(h, p.op, p.a, p.b, p.d, p.d, pref, 1, &res, &n);
-    cublasLtMatmulPreferenceDestroy(pref);
-    if (st != CUBLAS_STATUS_SUCCESS || n < 1) {
-        why = std::string("no cuBLASLt algorithm for the projection GEMM: ") + lt_name(st);
-        return false;
-    }
-    p.algo = res.algo;
-    return true;
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], %1;\n\t}\n" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
 }
-
-// a plan whose setup failed half way releases what it created
-bool make_plan(Plan &p, cublasLtHandle_t h, std::string &why) {
-    if (make_plan_steps(p, h, why)) return true;
-    free_plan(p);
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}\n"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+// bounded wait; false if it gave up
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (int i = 0; i < kSpin; ++i)
+        if (mbar_try(bar, parity)) return true;
     return false;
+}
+__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+// shared-memory matrix descriptor of a K-major tile with 128-byte rows in the 128-byte swizzle (the layout a
+// SWIZZLE_128B TMA box of 64 bf16 columns leaves): 8-row groups 1024 bytes apart, the leading offset unused
+// (one MMA's 16 columns lie inside a row); saddr may point 32 * j bytes into a 1024-aligned tile to select
+// columns 16 j .. 16 j + 15
+__device__ __forceinline__ uint64_t make_desc_sw128(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;                                    // leading byte offset 16 (unused)
+    d |= (uint64_t)(1024 >> 4) << 32;                          // stride byte offset: next 8-row group
+    d |= (uint64_t)1 << 46;                                    // descriptor version (sm_100 family)
+    d |= (uint64_t)2 << 61;                                    // layout: 128-byte swizzle
+    return d;
+}
+// instruction descriptor: kind::f16 with bf16 A and B, fp32 D, both K-major, M = 128
+__host__ __device__ constexpr uint32_t idesc_bf16(int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+                 "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+                 : "memory");
+}
+// 16 fp32 columns of this thread's TMEM lane (activation rows come in multiples of 16)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ uint32_t map_cluster(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// bytes of one pipeline stage: the W tile (128 rows) and the X block (Mt rows), 64 K-columns each
+__host__ __device__ constexpr uint32_t w_stage_bytes() { return kTileN * kKBlk * 2; }
+__host__ __device__ inline uint32_t x_stage_bytes(int Mt) { return (uint32_t)Mt * kKBlk * 2; }
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs a) {
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __shared__ __align__(8) uint64_t bars[2 * 8 + 1];          // full[stages], empty[stages], done
+    __shared__ uint32_t tslot;
+    const int tid = threadIdx.x, wid = tid >> 5;
+    const int nt = blockIdx.x, mb = blockIdx.y, split = blockIdx.z;   // the splits of a tile: one cluster
+    const int n0 = nt * kTileN, m0 = mb * a.Mt;
+    const int kb0 = split * a.kb_per_split;
+    const int kb1 = min(a.n_kb, kb0 + a.kb_per_split);
+    const int S = a.stages;
+    const uint32_t wbytes = w_stage_bytes(), xbytes = x_stage_bytes(a.Mt);
+    const uint32_t stage_bytes = wbytes + xbytes;
+    const uint32_t sbase = (smem_u32(sm) + 1023u) & ~1023u;   // swizzled tiles start on 1024 bytes
+    auto full = [&](int s) { return smem_u32(&bars[s]); };
+    auto empty = [&](int s) { return smem_u32(&bars[8 + s]); };
+    const uint32_t done = smem_u32(&bars[16]);
+
+    if (wid == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&tslot)),
+                     "r"(kMaxMt));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+    }
+    if (tid == 32) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tslot;
+    bool ok = true;
+
+    if (tid == 0) {
+        // ---- producer: the weight boxes of the first stages go out before the dependency wait
+        const int pre = min(S, kb1 - kb0);
+        for (int i = 0; i < pre; ++i) {
+            const uint32_t st = sbase + (uint32_t)i * stage_bytes;
+            mbar_expect_tx(full(i), stage_bytes);
+            tma_box(st, &a.w_map, (kb0 + i) * kKBlk, n0, full(i));
+        }
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
+        for (int i = 0; i < pre; ++i)
+            tma_box(sbase + (uint32_t)i * stage_bytes + wbytes, &a.x_map, (kb0 + i) * kKBlk, m0, full(i));
+        for (int i = pre; i < kb1 - kb0 && ok; ++i) {
+            const int s = i % S;
+            ok = mbar_wait(empty(s), ((i / S) - 1) & 1);       // the MMAs of stage use i - S are done
+            const uint32_t st = sbase + (uint32_t)s * stage_bytes;
+            mbar_expect_tx(full(s), stage_bytes);
+            tma_box(st, &a.w_map, (kb0 + i) * kKBlk, n0, full(s));
+            tma_box(st + wbytes, &a.x_map, (kb0 + i) * kKBlk, m0, full(s));
+        }
+    } else if (tid == 32) {
+        // ---- MMA issuer: 4 MMAs of K = 16 per stage; each stage is freed when its MMAs complete
+        const uint32_t id = idesc_bf16(a.Mt);
+        for (int i = 0; i < kb1 - kb0 && ok; ++i) {
+            const int s = i % S;
+            ok = mbar_wait(full(s), (i / S) & 1);
+            fence_after_sync();
+            const uint32_t st = sbase + (uint32_t)s * stage_bytes;
+#pragma unroll
+            for (int j = 0; j < kKBlk / 16; ++j)            // 16 columns (32 bytes of each row) per MMA
+                mma_bf16(tmem, make_desc_sw128(st + 32 * j), make_desc_sw128(st + wbytes + 32 * j), id,
+                         (i > 0 || j > 0) ? 1u : 0u);
+            mma_commit(empty(s));
+        }
+        mma_commit(done);
+    }
+    __syncwarp();
+    // ---- epilogue: the accumulator of weight row n0 + tid, every activation row of the block
+    const bool got = mbar_wait(done, 0);
+    fence_after_sync();
+    const bool good = got && ok;
+    if (!good && a.d_status) atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TIMEOUT));
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    const int n = n0 + tid;
+    const uint32_t taddr = tmem + ((uint32_t)(32 * wid) << 16);
+    if (a.splits == 1) {
+        if (good)
+            for (int c0 = 0; c0 < a.Mt; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr + c0, v);
+                if (n < a.N)
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int m = m0 + c0 + q;
+                        if (m < a.M) a.C[(size_t)m * a.ldc + n] = __float2bfloat16_rn(v[q]);
+                    }
+            }
+    } else {
+        // partial tiles of splits 1 .. S-1 -> the first split's shared memory, [split-1][column][row]
+        cluster_sync();                            // every split's MMAs are done: split 0's buffers are free
+        if (split > 0) {
+            const uint32_t dst = map_cluster(sbase, 0) + (uint32_t)((split - 1) * a.Mt * kTileN + tid) * 4u;
+            for (int c0 = 0; c0 < a.Mt; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr + c0, v);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) st_cluster_f32(dst + (uint32_t)((c0 + q) * kTileN) * 4u, good ? v[q] : 0.f);
+            }
+        }
+        cluster_sync();                            // every partial has landed
+        if (split == 0 && good) {
+            const float *red = reinterpret_cast<const float *>(sm + (sbase - smem_u32(sm)));
+            for (int c0 = 0; c0 < a.Mt; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr + c0, v);
+                if (n < a.N)
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int m = m0 + c0 + q;
+                        float acc = v[q];
+                        for (int sp = 1; sp < a.splits; ++sp) acc += red[((sp - 1) * a.Mt + c0 + q) * kTileN + tid];
+                        if (m < a.M) a.C[(size_t)m * a.ldc + n] = __float2bfloat16_rn(acc);
+                    }
+            }
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (wid == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kMaxMt));
 }
 
 }  // namespace
 
-bool gemm_xwt_bf16(const void *W, const void *X, void *C, int M, int N, int K, long long ldc, void *ws,
-                   size_t ws_bytes, cudaStream_t stream, std::string &why) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+// K splits of a tile: enough CTAs to cover the SMs when the output tiles are few, while the other
+// splits' partial tiles fit the first split's pipeline buffers (the reduction space)
+static int gemm_splits(int n_tiles, int m_blocks, int n_kb, int Mt, size_t smem, int sms) {
+    int splits = sms / (n_tiles * m_blocks);
+    if (splits > 8) splits = 8;
+    if (splits > n_kb) splits = n_kb;
+    while (splits > 1 && (size_t)(splits - 1) * Mt * kTileN * 4 > smem) --splits;
+    return splits < 1 ? 1 : splits;
+}
+
+bool gemm_xwt_bf16(const void *W, const void *X, void *C, int M, int N, int K, long long ldc, int *d_status,
+                   cudaStream_t stream, std::string &why) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) {
+        why = "the driver's tensor-map encoder is unavailable";
+        return false;
+    }
+    if (K % 8 || K < 8) {
+        why = "K must be a positive multiple of 8";
+        return false;
+    }
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                   cudaSuccess) {
         why = "no usable CUDA device";
         return false;
     }
-    const Plan *plan = nullptr;
-    cublasLtHandle_t h = nullptr;
+    GemmArgs a{};
+    a.M = M; a.N = N; a.K = K; a.ldc = ldc;
+    a.Mt = M >= kMaxMt ? kMaxMt : ((M + 15) / 16) * 16;
+    const int m_blocks = (M + a.Mt - 1) / a.Mt;
+    const int n_tiles = (N + kTileN - 1) / kTileN;
+    a.n_kb = (K + kKBlk - 1) / kKBlk;
+    const uint32_t stage = w_stage_bytes() + x_stage_bytes(a.Mt);
+    a.stages = (int)((200u * 1024u) / stage);
+    if (a.stages > 8) a.stages = 8;
+    const size_t smem = (size_t)a.stages * stage + 1024;          // + room to align the tiles to 1024 bytes
+    const int splits = gemm_splits(n_tiles, m_blocks, a.n_kb, a.Mt, smem - 1024, sms);
+    a.kb_per_split = (a.n_kb + splits - 1) / splits;
+    a.splits = (a.n_kb + a.kb_per_split - 1) / a.kb_per_split;
+    a.C = static_cast<__nv_bfloat16 *>(C);
+    a.d_status = d_status;
+    // tensor maps: 64-column (128-byte) boxes in the 128-byte swizzle
+    const cuuint32_t estr[2] = {1, 1};
     {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_handle[dev]) LT_TRY(cublasLtCreate(&g_handle[dev]), "handle");
-        h = g_handle[dev];
-        for (const Plan &p : g_plans)
-            if (p.dev == dev && p.M == M && p.N == N && p.K == K && p.ldc == ldc && p.ws_bytes == ws_bytes)
-                plan = &p;
-        if (!plan) {
-            Plan p;
-            p.dev = dev; p.M = M; p.N = N; p.K = K; p.ldc = ldc; p.ws_bytes = ws_bytes;
-            if (!make_plan(p, h, why)) return false;
-            g_plans.push_back(p);
-            plan = &g_plans.back();
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)kKBlk, (cuuint32_t)kTileN};
+        if (encode(&a.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(W), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            why = "weight tensor map";
+            return false;
         }
     }
-    const float one = 1.0f, zero = 0.0f;
-    LT_TRY(cublasLtMatmul(h, plan->op, &one, W, plan->a, X, plan->b, &zero, C, plan->d, C, plan->d, &plan->algo, ws,
-                          ws_bytes, stream),
-           "projection GEMM");
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)kKBlk, (cuuint32_t)a.Mt};
+        if (encode(&a.x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(X), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            why = "activation tensor map";
+            return false;
+        }
+    }
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(n_tiles, m_blocks, a.splits);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 1;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = a.splits;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelEx(&cfg, gemm_kernel, a);
+    }
+    if (e != cudaSuccess) {
+        why = std::string("projection GEMM launch: ") + cudaGetErrorString(e);
+        return false;
+    }
     return true;
 }
 

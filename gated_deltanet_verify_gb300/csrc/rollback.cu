@@ -19,7 +19,7 @@ namespace gdn {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;
 
 __device__ __forceinline__ float4 ld_nc4(const float4 *p) {
     float4 v;
@@ -30,15 +30,16 @@ __device__ __forceinline__ float4 ld_nc4(const float4 *p) {
 }
 
 __global__ void __launch_bounds__(kThreads) rollback_kernel(const RollbackArgs a) {
-    // programmatic dependent launch: wait for the previous kernel's writes
-    // (captures, trims), then let the next kernel start launching
+    // programmatic dependent launch: wait for the previous kernel's writes (captures, trims); the next
+    // kernel may start launching once every block has issued its copies (signalled at the end, so that
+    // its CTAs do not take SM slots from the copy blocks still waiting to run)
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int s = blockIdx.y;
     // a checked build tests each global access against its buffer first (compiled away otherwise)
     auto chk = [&](const void *p, size_t bytes, const void *base, size_t ext) -> bool {
         return in_bounds(p, bytes, base, ext, a.d_status);
     };
+    auto launch_next = []() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); };
     if (!chk(a.trim + s, 4, a.trim, size_t(a.B) * 4)) return;
     const int idx = __ldg(a.trim + s);
     int accepted_idx;
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(kThreads) rollback_kernel(const RollbackArgs a
                 dst_c[j] = ld_nc4(src_c + j);
         }
     }
+    launch_next();
 }
 
 }  // namespace

@@ -83,7 +83,6 @@ constexpr int kRowsPerWarp = 8;
 constexpr int kMaxWarps = 8;
 constexpr int kMaxThreads = 32 * kMaxWarps;
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kMaxDevices = 64;
 constexpr int kSpinLimit = 1 << 22;     // try_wait rounds before a wait gives up
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
@@ -784,23 +783,33 @@ cudaError_t launch_t(const VerifyArgs &a, cudaStream_t stream) {
     const int warps = rows / kRowsPerWarp;
     const Smem L(a.Tm, DK, rows, warps, a.P, sizeof(Act), MODE == kTree);
     auto kern = verify_kernel<DK, Act, MODE>;
-    // Function attributes are set once per device (and raised when a launch needs more).
-    static int smem_set[kMaxDevices] = {};
-    static bool nonportable_set[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const int slot = dev < kMaxDevices ? dev : kMaxDevices - 1;
-    if (int(L.total) > smem_set[slot] || dev >= kMaxDevices) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.total));
-        if (e != cudaSuccess) return e;
-        smem_set[slot] = int(L.total);
-    }
+    // Function attributes belong to the context: the dynamic shared memory limit set so far (raised
+    // when a launch needs more) and the non-portable cluster permission are cached per context id,
+    // shared by the host threads under a lock.
+    struct Attrs {
+        int smem = 0;
+        bool nonportable = false;
+    };
+    static PerContext<Attrs> attrs;
+    unsigned long long ctx = 0;
+    Attrs have;
+    const bool known = current_context_id(&ctx) && attrs.get(ctx, &have);
     const int cluster = a.r * a.P;
-    if (cluster > 8 && (!nonportable_set[slot] || dev >= kMaxDevices)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        nonportable_set[slot] = true;
+    const bool need_np = cluster > 8;
+    cudaError_t e = cudaSuccess;
+    if (!known || int(L.total) > have.smem || (need_np && !have.nonportable)) {
+        Attrs now = have;
+        if (int(L.total) > now.smem) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.total));
+            if (e != cudaSuccess) return e;
+            now.smem = int(L.total);
+        }
+        if (need_np && !now.nonportable) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+            now.nonportable = true;
+        }
+        if (current_context_id(&ctx)) attrs.put(ctx, now);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.Hv * a.P, a.B, 1);

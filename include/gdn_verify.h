@@ -104,8 +104,9 @@ typedef struct {
  * Verify forward over T positions.  Reads qkv/z/alpha/beta_raw and the layer
  * params; updates state and conv_state IN PLACE to "after all T tokens";
  * writes out.  If cap_state is non-NULL it receives, for every position t,
- * the state after token t (internal.h, ssm_intermediate: "element t ... holds
- * the DeltaNet recurrent state after processing verify token t"), so
+ * the state after token t (internal.h, "Target cache", the ssm_intermediate
+ * comment: entry t of that per-layer buffer is the recurrent state once the
+ * verify has run token t), so
  * cap_state[:, T-1] equals the new state bit for bit.  If cap_conv is non-NULL
  * it receives the concat(old conv_state, qkv) window (internal.h,
  * conv_input_cache).  Supported: 1 <= T <= 64, d_k in {32,64,128}, d_v % 8 ==
@@ -235,9 +236,10 @@ int gdn_commit_lazy(const gdn_dims *dims, const gdn_layer_params *params, const 
                     float *state, float *conv_state, int *d_status, void *stream);
 
 /*
- * The projections either side of the block, as plain bf16 GEMMs (fp32
- * accumulation; cuBLASLt), and the layer step that chains them around the
- * verify.  They follow the GDN tensors of internal.h, Target weights
+ * The projections either side of the block, as bf16 GEMMs with fp32
+ * accumulation (this library's own tensor-core kernel: the weight rows
+ * stream through shared memory while the B*T activation rows stay resident),
+ * and the layer step that chains them around the verify.  They follow the GDN tensors of internal.h, Target weights
  * (TargetLayer: wqkv, the fused Q/K/V projection; wqkv_gate, the z
  * projection; ssm_alpha and ssm_beta, the per-token gate inputs; ssm_out, the
  * output projection), each weight stored as its output rows with n_embd
@@ -261,17 +263,17 @@ typedef struct {
 /* Row stride (elements) of gdn_project_in's output: C + H_v*d_v + 2*H_v rounded up to 8. */
 long long gdn_proj_in_ld(const gdn_dims *dims);
 
-/* Device workspace of gdn_layer_verify: the activation matrix, the block's
- * output and 32 MiB of GEMM workspace (0 on bad arguments).  The GEMM-only
- * calls below need 32 MiB. */
+/* Device workspace of gdn_layer_verify: the activation matrix and the block's
+ * output (0 on bad arguments).  The GEMMs themselves need no scratch. */
 size_t gdn_layer_workspace_bytes(const gdn_dims *dims, int n_embd);
 
 /* act[B*T][gdn_proj_in_ld] = x @ w_in^T: columns [0, C) are qkv, then z, then
- * alpha, then beta_raw, per row (bf16).  workspace >= 32 MiB of GEMM scratch. */
+ * alpha, then beta_raw, per row (bf16).  workspace / ws_bytes are not used (the
+ * GEMM needs no scratch; pass NULL, 0). */
 int gdn_project_in(const gdn_dims *dims, const gdn_proj_weights *w, const void *x, void *act,
                    void *workspace, size_t ws_bytes, void *stream);
 
-/* y[B*T][n_embd] = out @ w_out^T (bf16). */
+/* y[B*T][n_embd] = out @ w_out^T (bf16).  workspace / ws_bytes are not used. */
 int gdn_project_out(const gdn_dims *dims, const gdn_proj_weights *w, const void *out, void *y,
                     void *workspace, size_t ws_bytes, void *stream);
 
@@ -316,7 +318,18 @@ int gdn_verify_step_host(const gdn_dims *dims, const gdn_layer_params *params, i
                          float *state, float *conv_state, float *cap_state, float *cap_conv,
                          int *d_status, void *stream);
 
-/* Bytes of device workspace gdn_prefill_chunked needs for these dims (0 on bad dims). */
+/*
+ * Bytes of device workspace gdn_prefill_chunked needs for these dims (0 on bad
+ * dims).  internal.h, "Target cache", create_target_cache: a cache made with
+ * prefill_only holds only the persistent recurrent and conv state (the
+ * rollback tensors -- snapshots, per-step intermediates -- are skipped), and
+ * migrate_prefill_cache later promotes it to a full decode cache.  The
+ * prefill therefore runs over exactly the state / conv_state buffers that
+ * gdn_verify_forward and gdn_rollback use; the workspace sized here is
+ * transient scratch of the chunkwise form (operand rings, flags, a work
+ * counter), which has no counterpart on the pages: the caller owns it, as the
+ * page's caller owns the cache.
+ */
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims);
 
 /*
@@ -348,24 +361,42 @@ int gdn_prefill_chunked(const gdn_dims *dims, const gdn_layer_params *params,
  * budget whose allocator must not grow -- and so have no workspace to pass.
  *
  * Limit: the call needs gdn_prefill_workspace_bytes(dims) bytes of scratch and
- * the built-in array holds GDN_PREFILL_STATIC_SCRATCH_BYTES (16 MiB, one array
- * per device, reserved when the call is first used on that device); larger
- * dims are rejected with GDN_ERR_WORKSPACE before anything is enqueued.  The
- * scratch needs no initialisation.
+ * the built-in array holds GDN_PREFILL_STATIC_SCRATCH_BYTES (16 MiB; also
+ * returned by gdn_prefill_static_scratch_bytes); larger dims are rejected with
+ * GDN_ERR_WORKSPACE before anything is enqueued.  The scratch needs no
+ * initialisation.  The array is reserved on a device when this library's
+ * device code is loaded into a context there: under CUDA's default lazy
+ * module loading that is the first call into the library that runs its
+ * device code on the device; with CUDA_MODULE_LOADING=EAGER it is when the
+ * context is created.  Each context holds its own copy until it is destroyed
+ * (and the bounds-checked build of the library holds another).
  *
- * The first call on a device looks the array's device address up (with that
- * device current) and caches it, so make that first call before any stream
- * capture on the device.  Calls that overlap on one device -- different
+ * The first call in a context (normally: the first call on a device, with
+ * that device current) looks the array's device address up and caches it
+ * under the context's id, so make that first call before any stream capture
+ * on the device.  After cudaDeviceReset, or in another context, the address
+ * is looked up again.  Calls that overlap on one device -- different
  * streams, or host threads, with no ordering between them -- share the one
  * array and race: order them (one stream, or events).  Everything else,
  * including the error codes, is as for gdn_prefill_chunked.
  */
 #define GDN_PREFILL_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+/* The size of that built-in array (GDN_PREFILL_STATIC_SCRATCH_BYTES), for
+ * bindings that cannot read the macro. */
+size_t gdn_prefill_static_scratch_bytes(void);
 int gdn_prefill_chunked_static(const gdn_dims *dims, const gdn_layer_params *params,
                                const void *qkv, const void *z, const void *alpha, const void *beta_raw,
                                float *state, float *conv_state, void *out, int *d_status, void *stream);
 
-/* Message for the last non-OK return on this thread ("" if none). */
+/*
+ * Message for the last non-OK return on this thread ("" if none).  internal.h,
+ * top of the file: one error channel for the whole library, into which every
+ * loader and graph builder writes through set_last_error(...), and whose
+ * builders "return false and set last_error on failure" ("Target forward
+ * graph").  Here every call returns a gdn_status and, when it is not GDN_OK,
+ * leaves the reason in this per-thread string (valid until the thread's next
+ * call into the library).
+ */
 const char *gdn_last_error(void);
 
 /* Library version string. */

@@ -1,7 +1,10 @@
 """Cases run through both the ordinary and the bounds-checked library (see
 test_checked_gpu.py): every verify mode, the rollbacks and the layer step on
-small seeded shapes.  ``python -m tests.checked_cases OUT.npz`` runs them on
-the checked library and saves the results and status words."""
+small seeded shapes.  ``python -m tests.checked_cases OUT.npz [all|lost_chunk|scratch_contexts]``
+runs them on the checked library -- the test build, which also carries the
+test hooks (the prefill's host-side fault injection, the static-scratch
+address lookup) -- and saves the results and status words."""
+import os
 import sys
 
 import numpy as np
@@ -82,9 +85,69 @@ def run_all() -> dict:
     return res
 
 
+LOST_CHUNK_SHAPE = Shape("prefill_small", n_slots=1, n_qk_heads=2, n_v_heads=6, d_k=128, d_v=128, n_tokens=300,
+                         act="bf16", seed=46)
+
+
+def _prefill(shape, x, status):
+    d = dims_of(shape)
+    ws_bytes = gdn.gdn_prefill_workspace_bytes(d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((shape.n_slots, shape.n_tokens, shape.n_v_heads * shape.d_v), dtype=torch.bfloat16,
+                      device="cuda")
+    gdn.gdn_prefill_chunked(d, params_of(x), x["qkv"], x["z"], x["alpha"], x["beta_raw"], x["state"],
+                            x["conv_state"], out, ws, ws_bytes, status)
+    torch.cuda.synchronize()
+    return out
+
+
+def run_lost_chunk() -> dict:
+    """A fault injected on the host (test build only): with GDN_FAULT_DROP_CHUNK=2 the prefill never
+    publishes chunk 2, the state CTA's bounded wait gives up and the call reports GDN_ERR_TIMEOUT; then a
+    clean call on the same device."""
+    torch.cuda.set_device(0)
+    inp = make_inputs(LOST_CHUNK_SHAPE)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    os.environ["GDN_FAULT_DROP_CHUNK"] = "2"
+    _prefill(LOST_CHUNK_SHAPE, upload(inp), status)
+    first = int(status.item())
+    del os.environ["GDN_FAULT_DROP_CHUNK"]
+    status.zero_()
+    x = upload(inp)
+    out = _prefill(LOST_CHUNK_SHAPE, x, status)
+    return {"status_dropped": np.array([first]), "status_clean": np.array([int(status.item())]),
+            "state": to_f64(x["state"]), "out": to_f64(out)}
+
+
+def run_scratch_contexts() -> dict:
+    """The static-scratch address the library uses in the primary context, in a second context made
+    current on the same device, and in the primary context again.  Only the address lookup runs in the
+    second context (no kernel is launched there)."""
+    import ctypes
+    torch.cuda.set_device(0)
+    torch.zeros(1, device="cuda")                      # the primary context is current
+    L = gdn.lib()
+    f = L.gdn_test_static_scratch_address
+    f.restype = ctypes.c_void_p
+    f.argtypes = []
+    cu = ctypes.CDLL("libcuda.so.1")
+    a0, a1 = f(), f()
+    dev = ctypes.c_int()
+    assert cu.cuCtxGetDevice(ctypes.byref(dev)) == 0
+    ctx = ctypes.c_void_p()
+    assert cu.cuCtxCreate_v2(ctypes.byref(ctx), 0, dev) == 0     # pushed: current on this thread
+    b0, b1 = f(), f()
+    popped = ctypes.c_void_p()
+    assert cu.cuCtxPopCurrent_v2(ctypes.byref(popped)) == 0
+    a2 = f()
+    assert cu.cuCtxDestroy_v2(ctx) == 0
+    return {"addr": np.array([a0 or 0, a1 or 0, b0 or 0, b1 or 0, a2 or 0], dtype=np.uint64)}
+
+
 if __name__ == "__main__":
     from gated_deltanet_verify_gb300 import _build
     gdn.LIB_PATH = _build.CHECKED_LIB
-    r = run_all()
+    case = sys.argv[2] if len(sys.argv) > 2 else "all"
+    r = {"all": run_all, "lost_chunk": run_lost_chunk, "scratch_contexts": run_scratch_contexts}[case]()
     r["version"] = np.frombuffer(gdn.gdn_version().encode(), dtype=np.uint8)
     np.savez(sys.argv[1], **r)

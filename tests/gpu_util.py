@@ -1,5 +1,8 @@
 """Helpers for the GPU tests: run the CUDA path through the C ABI on seeded
 inputs and read the results back as fp64 numpy arrays."""
+import os
+import subprocess
+import sys
 from typing import Dict, Optional
 
 import numpy as np
@@ -49,3 +52,19 @@ def as_f64(d: Dict[str, torch.Tensor]) -> Dict[str, np.ndarray]:
 
 def upload(inp: Inputs, device="cuda") -> Dict[str, torch.Tensor]:
     return to_device(inp, device)
+
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_test_build(tmp_path, case: str) -> dict:
+    """Run one case of tests/checked_cases.py in a child process on the test build."""
+    import __graft_entry__
+    __graft_entry__.build()
+    from gated_deltanet_verify_gb300 import _build
+    _build.build(checked=True)
+    out = tmp_path / f"{case}.npz"
+    r = subprocess.run([sys.executable, "-m", "tests.checked_cases", str(out), case], cwd=ROOT,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    return dict(np.load(out))

@@ -39,6 +39,41 @@ def test_header_declares_the_boundary():
     assert set(names) <= set(gdn.EXPORTED_SYMBOLS)
 
 
+def _doc_block(name):
+    """The comment block that documents a declaration: the last /* ... */ before it with nothing but
+    other declarations in between."""
+    text = open(os.path.join(ROOT, "include", "gdn_verify.h")).read()
+    m = re.search(r"^(?![ \t]*(?:/\*|\*))[^\n]*\b" + name + r"\s*\(", text, flags=re.M)
+    assert m, name
+    before = text[:m.start()]
+    i = before.rfind("/*")
+    return before[i:before.index("*/", i) + 2]
+
+
+# the calls of the boundary, each with the page and the section (or the function on it) that defines it
+BOUNDARY = {
+    "gdn_verify_forward": ("internal.h", "ssm_intermediate"),
+    "gdn_rollback": ("qwen35_target.rs", "rollback_kv"),
+    "gdn_prefill_chunked": ("internal.h", "create_target_cache"),
+    "gdn_prefill_workspace_bytes": ("internal.h", "create_target_cache"),
+    "gdn_last_error": ("internal.h", "set_last_error"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BOUNDARY))
+def test_boundary_calls_cite_their_passage(name):
+    page, section = BOUNDARY[name]
+    doc = _doc_block(name)
+    assert page in doc and section in doc, (name, doc)
+
+
+def test_static_scratch_size_matches_the_header(lib):
+    text = open(os.path.join(ROOT, "include", "gdn_verify.h")).read()
+    m = re.search(r"#define\s+GDN_PREFILL_STATIC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", text)
+    assert m
+    assert gdn.prefill_static_scratch_bytes() == int(m.group(1)) << int(m.group(2))
+
+
 def test_library_exports_every_declared_symbol(lib):
     for n in _declared_functions():
         assert hasattr(lib, n), n
@@ -174,7 +209,7 @@ def test_projection_host_validation(lib):
     need = gdn.gdn_layer_workspace_bytes(bf, 64)
     M, ld = 4, gdn.gdn_proj_in_ld(bf)
     assert ld % 8 == 0 and ld >= 2 * 2 * 32 + 8 * 32 + 8 * 32 + 16
-    assert need >= M * ld * 2 + M * 8 * 32 * 2 + (32 << 20)
+    assert need >= M * ld * 2 + M * 8 * 32 * 2
 
     def call(d=bf, ww=w, n=need, ws=A):
         return L.gdn_layer_verify(ctypes.byref(d), ctypes.byref(_params()), ctypes.byref(ww), A, A, A, None, None,

@@ -144,6 +144,36 @@ def test_project_calls_alone():
     assert np.all(np.abs(to_f64(y) - ref) <= bound)
 
 
+@pytest.mark.parametrize("kw", [
+    dict(n_slots=1, n_tokens=1, n_embd=72),                  # one activation row; K below one pipeline stage
+    dict(n_slots=3, n_tokens=7, n_embd=200),                 # ragged M (21), K not a multiple of 64
+    dict(n_slots=20, n_tokens=15, n_embd=136),               # 300 rows: two blocks of activation rows
+    dict(n_slots=1, n_tokens=16, n_qk_heads=16, n_v_heads=48, d_k=128, d_v=128, n_embd=1024),   # split K on out
+])
+def test_projection_gemm_shapes(kw):
+    # both projections on their own against the fp64 product, over the tilings the GEMM kernel uses: weight
+    # tiles with a ragged last tile, 16-row activation blocks (M padded), one or two blocks of up to 256
+    # rows, K tails, and K split across a cluster when the output tiles are few
+    shape = _shape(**kw)
+    pr = make_proj(shape)
+    p = _upload_proj(pr)
+    dims = dims_of(shape)
+    w = gdn.proj_weights(shape.n_embd, p["w_in"], p["w_out"])
+    M = shape.n_slots * shape.n_tokens
+    act = torch.empty((M, gdn.gdn_proj_in_ld(dims)), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_project_in(dims, w, p["x"], act, None, 0)
+    out = torch.from_numpy(np.ascontiguousarray(make_inputs(shape).z)).view(torch.bfloat16).to("cuda")
+    y = torch.empty((M, shape.n_embd), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_project_out(dims, w, out, y, None, 0)
+    torch.cuda.synchronize()
+    hidden, w_in, w_out = (bf16_bits_to_f64(pr[k]) for k in ("x", "w_in", "w_out"))
+    _check_act(shape, act, hidden, w_in)
+    o64 = to_f64(out).reshape(M, -1)
+    ref = oracle.project(o64, w_out)
+    bound = 2.0 ** -8 * np.abs(ref) + shape.value_dim * 2.0 ** -23 * (np.abs(o64) @ np.abs(w_out).T)
+    assert np.all(np.abs(to_f64(y) - ref) <= bound)
+
+
 def test_layer_full_size():
     # one slot of the layer shape with hidden 5120: all of y and the state against the oracle
     shape = WORKLOADS["proj_verify"]

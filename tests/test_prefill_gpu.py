@@ -61,16 +61,17 @@ def test_prefill_matches_sequential_oracle(case):
     assert np.array_equal(gpu["conv_state"], ref["conv_state"])
 
 
-def test_prefill_full_size_sampled_heads():
+def test_prefill_full_size_all_heads():
+    # the 8192-token layer as the bench runs it, every head (so every key-head group of the work split)
+    # against the sequential oracle
     shape = WORKLOADS["prefill"]
     inp = make_inputs(shape)
     gpu = run_prefill(shape, upload(inp))
-    heads = [0, 47]
-    ref = oracle.verify(shape, inp.as_f64(), capture=False, head_mask=heads, n_threads=2)
-    for h in heads:
+    ref = oracle.verify(shape, inp.as_f64(), capture=False, n_threads=16)
+    assert_f32_close(gpu["state"], ref["state"], "state")
+    assert_act_close(gpu["out"], ref["out"], shape.act, "out")
+    for h in range(shape.n_v_heads):      # per head as well: each head's state at its own scale
         assert_f32_close(gpu["state"][:, h], ref["state"][:, h], f"state h{h}")
-        sl = slice(h * shape.d_v, (h + 1) * shape.d_v)
-        assert_act_close(gpu["out"][:, :, sl], ref["out"][:, :, sl], shape.act, f"out h{h}")
     assert np.array_equal(gpu["conv_state"], ref["conv_state"])
 
 
@@ -92,30 +93,8 @@ def test_prefill_more_pairs_than_one_launch():
     inp = make_inputs(shape)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     gpu = run_prefill(shape, upload(inp), status=status)
-    heads = [0, 23, 47]
-    ref = oracle.verify(shape, inp.as_f64(), capture=False, head_mask=heads, n_threads=8)
-    for h in heads:
-        assert_f32_close(gpu["state"][:, h], ref["state"][:, h], f"state h{h}")
-        sl = slice(h * shape.d_v, (h + 1) * shape.d_v)
-        assert_act_close(gpu["out"][:, :, sl], ref["out"][:, :, sl], shape.act, f"out h{h}")
+    ref = oracle.verify(shape, inp.as_f64(), capture=False, n_threads=16)
+    assert_f32_close(gpu["state"], ref["state"], "state")
+    assert_act_close(gpu["out"], ref["out"], shape.act, "out")
     assert np.array_equal(gpu["conv_state"], ref["conv_state"])
     assert int(status.item()) == gdn.GDN_OK
-
-
-def test_prefill_lost_chunk_reports_timeout(monkeypatch):
-    # fault injected on the host: chunk 2 is never published to the state CTA, whose bounded wait
-    # (about a second) then gives up and writes GDN_ERR_TIMEOUT to the status word; the device stays
-    # usable and the next clean call matches the oracle
-    shape = _shape(n_tokens=300, seed=46)
-    inp = make_inputs(shape)
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    monkeypatch.setenv("GDN_FAULT_DROP_CHUNK", "2")
-    run_prefill(shape, upload(inp), status=status)
-    assert int(status.item()) == gdn.GDN_ERR_TIMEOUT
-    monkeypatch.delenv("GDN_FAULT_DROP_CHUNK")
-    status.zero_()
-    gpu = run_prefill(shape, upload(inp), status=status)
-    assert int(status.item()) == gdn.GDN_OK
-    ref = oracle.verify(shape, inp.as_f64(), capture=False, n_threads=8)
-    assert_f32_close(gpu["state"], ref["state"], "state after recovery")
-    assert_act_close(gpu["out"], ref["out"], shape.act, "out after recovery")

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import gated_deltanet_verify_gb300 as gdn
-from tests.gpu_util import as_f64, dims_of, params_of, upload
+from tests.gpu_util import as_f64, dims_of, params_of, run_test_build, upload
 from tests.tolerance import assert_act_close, assert_f32_close
 from workloads.device import act_torch_dtype
 from workloads.synth import Shape, make_inputs
@@ -52,7 +52,7 @@ def _static(shape, inp, status):
 
 
 def test_static_scratch_prefill_matches_workspace_prefill_on_two_calls():
-    assert gdn.gdn_prefill_workspace_bytes(dims_of(SHAPE)) <= gdn.PREFILL_STATIC_SCRATCH_BYTES
+    assert gdn.gdn_prefill_workspace_bytes(dims_of(SHAPE)) <= gdn.prefill_static_scratch_bytes()
     inp = make_inputs(SHAPE)
     ref = _with_workspace(SHAPE, inp)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -67,8 +67,19 @@ def test_static_scratch_prefill_matches_workspace_prefill_on_two_calls():
 def test_static_scratch_rejects_dims_beyond_its_size():
     big = SHAPE.with_(n_slots=400, n_qk_heads=16, n_v_heads=48)
     d = dims_of(big)
-    assert gdn.gdn_prefill_workspace_bytes(d) > gdn.PREFILL_STATIC_SCRATCH_BYTES
+    assert gdn.gdn_prefill_workspace_bytes(d) > gdn.prefill_static_scratch_bytes()
     with pytest.raises(gdn.GdnError) as ei:
         # rejected on the host before any pointer is looked at or any work is enqueued
         gdn.gdn_prefill_chunked_static(d, gdn.LayerParams(), None, None, None, None, None, None, None)
     assert ei.value.status == gdn.GDN_ERR_WORKSPACE
+
+
+def test_static_scratch_address_is_looked_up_per_context(tmp_path):
+    # the address is cached per CUDA context: a second context on the same device gets its own copy of
+    # the array (a different address), and the first context keeps its cached one; only the lookup runs
+    # in the second context, no kernel
+    a = [int(v) for v in run_test_build(tmp_path, "scratch_contexts")["addr"]]
+    assert all(a), a
+    assert a[0] == a[1] == a[4]
+    assert a[2] == a[3]
+    assert a[2] != a[0]
