@@ -1,17 +1,21 @@
 #!/usr/bin/env python3
 """Benchmark of the GDN verify hot path on GB300.
 
-One step = one verify forward (conv + SiLU, q/k L2 norm, gates, gated
-delta-rule recurrence with per-position state capture, gated RMSNorm,
-conv-state advance) followed by one rollback, over one batch of seeded
-synthetic inputs already resident in HBM.  Default workload: one GDN layer of
-a 64-layer hybrid target, 1 slot, 16 QK / 48 V heads, d_k = d_v = 128, K+1 =
-16 verify tokens, bf16 activations, fp32 state.
+Default (the largest single-GPU configuration): a 48-layer x 8-slot stack of
+the GDN block of a 64-layer hybrid target (16 QK / 48 V heads, d_k = d_v =
+128, K+1 = 16 verify tokens, bf16 activations, fp32 state); one step = one
+verify forward (conv + SiLU, q/k L2 norm, gates, gated delta-rule recurrence
+with per-position state capture, gated RMSNorm, conv-state advance) followed
+by one rollback, for every layer, over seeded synthetic inputs already
+resident in HBM.  The same JSON line carries per-config entries for one layer
+at 1 slot and at 32 slots, the 8192-token chunked prefill and the layer with
+its projections.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
                     [--workload layer_verify|multislot_verify|stack_verify|prefill|tree_verify|
                                 rolled_verify|rolled_multislot_verify|rolled_stack_verify|
                                 lazy_verify|lazy_multislot_verify|lazy_stack_verify|proj_verify]
+                    [--no-per-config] [--no-e2e] [--no-cpu-baseline]
 
 The tree_verify workload verifies a draft tree and rolls back to the accepted
 node; the rolled_* workloads fold each step's rollback into the next verify
@@ -19,12 +23,14 @@ node; the rolled_* workloads fold each step's rollback into the next verify
 inputs as their capture counterparts: one launch per step commits the pending
 batch (re-runs its accepted tokens) and writes the new batch's outputs,
 nothing captured.  proj_verify adds the projections around the block
-(hidden 5120; cuBLASLt GEMMs).
+(hidden 5120; the library's own tcgen05 GEMM).
 
 Prints one JSON line.  ``value`` = verified tokens/s over all ranks (device
-time, CUDA events, steps replayed from CUDA graphs over rotating buffer sets
-whose total exceeds 3x L2).  ``roofline`` is for the dominant kernel
-(verify): algorithmic bytes per launch / its average launch duration.
+time, CUDA events, steps replayed from CUDA graphs over rotating buffer sets:
+each set is evicted from L2 by the others before it comes round again).  A
+token counts once it has been through every layer of the workload.
+``roofline`` is for the dominant kernel (verify): algorithmic bytes per launch
+/ its average launch duration.
 ``e2e`` = the same metric through the public API with pinned host buffers,
 host->device copies of each step's activations and a device->host read of
 its output inside the timed region.  ``cpu_baseline`` = the fp64 oracle on
@@ -692,9 +698,10 @@ def describe(shape) -> str:
 
 
 # steps a per-config entry times at least (about 10 ms of device work or more)
-MIN_STEPS = {"layer_verify": 1000, "multislot_verify": 64, "prefill": 20}
+MIN_STEPS = {"layer_verify": 1000, "multislot_verify": 64, "prefill": 20, "proj_verify": 500}
 HEADLINE = "stack_verify"                                   # 48 layers x 8 slots: the largest configuration
-PER_CONFIG = ("layer_verify", "multislot_verify", "prefill")
+# configs 1, 2 and 4, and the layer with its projections around the block (hidden 5120, the library's GEMM)
+PER_CONFIG = ("layer_verify", "multislot_verify", "prefill", "proj_verify")
 
 
 def measure(name, steps, warmup, device, world, l2, clocks, with_e2e, graph_len_max=64):
@@ -1037,7 +1044,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
-                    help="time only the chosen workload (by default the headline also times configs 1, 2, 4)")
+                    help="time only the chosen workload (by default the headline also times configs 1, 2, 4 and "
+                         "the layer with its projections)")
     ap.add_argument("--slots", type=int, default=0, help="override the workload's slot count (profiling cases)")
     ap.add_argument("--profile", type=int, default=0, metavar="K",
                     help="run K untimed eager steps and exit (for ncu captures)")

@@ -84,7 +84,8 @@ constexpr uint32_t kRinv = kGam + 256;
 constexpr uint32_t kInvQ = kRinv + 256;        // 1 / ||q_t||, 1 / ||k_t||
 constexpr uint32_t kInvK = kInvQ + 256;
 constexpr uint32_t kRed = kInvK + 256;         // 4 lane quarters x 64 tokens
-constexpr uint32_t kSmemBytes = kRed + 4 * 64 * 4;
+constexpr uint32_t kLogLo = kRed + 4 * 64 * 4;  // low parts of the cumulative log decays (64 floats)
+constexpr uint32_t kSmemBytes = kLogLo + 256;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 constexpr int kWin = kC + 3;                   // window rows of a chunk (3 rows of history)
 static_assert(kWin * kCh * 4 <= 128 * 1024, "raw chunk window fits the A region");
@@ -135,23 +136,38 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// (ah + al) + (bh + bl) as a normalised pair of floats (Knuth's two-sum on the high parts): the
+// cumulative log decay of a chunk reaches a few hundred in magnitude, and the decay between two nearby
+// tokens is exp of the difference of two such sums, so a plain fp32 sum would leave that difference with
+// an error of |sum| * 2^-24 (~1e-5 relative in the decay); the pair keeps it to fp32 precision of the
+// difference itself
+__device__ __forceinline__ void add_pair(float ah, float al, float bh, float bl, float &h, float &l) {
+    const float s = ah + bh, bb = s - ah;
+    const float e = (ah - (s - bb)) + (bh - bb);
+    const float lo = al + bl + e;
+    h = s + lo;
+    l = lo - (h - s);
+}
+
 // ---- 3xTF32 operand planes: canonical K-major, no swizzle -----------------
 // 16-byte group (r, k4) of an R x K operand: core matrix (r/8, k4) of 8 rows x 16 B
 __device__ __forceinline__ uint32_t plane_off(int r, int k4, int K) {
     return (uint32_t)((((r >> 3) * (K >> 2) + k4) << 7) + ((r & 7) << 4));
 }
-// x rounded to the nearest tf32 value (ties to even).  A kind::tf32 MMA reads only the upper 19 bits of
-// each fp32 operand, so both parts of a split are made exact tf32 values: hi = tf32(x), lo = tf32(x - hi).
-// Rounding both (instead of cutting the low bits off, which the tensor core would do to an unrounded
-// remainder) keeps the split's error symmetric and about four times smaller.
+// x rounded to the nearest tf32 value (ties away from zero; one cvt instruction).
 __device__ __forceinline__ float tf32_rn(float x) {
-    uint32_t u = __float_as_uint(x);
-    u += 0xFFFu + ((u >> 13) & 1u);
-    return __uint_as_float(u & 0xFFFFE000u);
+    uint32_t u;
+    asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(u) : "f"(x));
+    return __uint_as_float(u);
 }
+// x = hi + lo exactly, hi the nearest tf32 value.  A kind::tf32 MMA reads only the upper 19 bits of an fp32
+// operand, so it cuts lo's last bits off: an error below 2^-23 |x| whose sign is that of lo, i.e. as often
+// toward x as away from it.  (Cutting the bits of x itself to form hi, as a plain mask does, leaves lo with
+// x's sign and makes both cuts err toward zero: a one-sided error up to 2^-21 |x|, which the all-heads
+// parity test of the 8192-token layer showed in its outputs.)
 __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
     hi = tf32_rn(x);
-    lo = tf32_rn(x - hi);
+    lo = x - hi;
 }
 // 4 consecutive k of row r: the tf32 part into the hi plane, the remainder into the lo plane
 __device__ __forceinline__ void put4(unsigned char *hi, unsigned char *lo, int r, int k4, int K, float4 v) {
@@ -405,7 +421,8 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x) {
     float *Pt = reinterpret_cast<float *>(sm + kPT);
     float *Tm = reinterpret_cast<float *>(sm + kRB + 32 * 1024);      // T (fp32, 64 x 64, row-major)
     float *Xb = reinterpret_cast<float *>(sm + kRB + 48 * 1024);      // block-inversion temporaries
-    float *logG = reinterpret_cast<float *>(sm + kLogG);
+    float *logG = reinterpret_cast<float *>(sm + kLogG);          // cumulative log decays: high parts
+    float *logLo = reinterpret_cast<float *>(sm + kLogLo);        // and low parts
     float *betas = reinterpret_cast<float *>(sm + kBeta);
     float *gam = reinterpret_cast<float *>(sm + kGam);
     float *invq = reinterpret_cast<float *>(sm + kInvQ);
@@ -639,19 +656,28 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x) {
             }
             x.wait_bar(rawbar, raw_phase);
             __syncthreads();
-            if (wid == 0) {                    // Gamma = exp(cumsum(log g)): lane l owns tokens 2l, 2l+1
+            if (wid == 0) {
+                // cumulative log decays as (hi, lo) pairs, Gamma = exp(cumsum(log g)): lane l owns tokens
+                // 2l, 2l+1; an inclusive scan of the lane totals, then each token from the previous lane's
                 const float l0 = logG[2 * lane], l1 = logG[2 * lane + 1];
-                float incl = l0 + l1;
+                float h, lo;
+                add_pair(l0, 0.f, l1, 0.f, h, lo);
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, incl, off);
-                    if (lane >= off) incl += y;
+                    const float yh = __shfl_up_sync(0xffffffffu, h, off), yl = __shfl_up_sync(0xffffffffu, lo, off);
+                    if (lane >= off) add_pair(h, lo, yh, yl, h, lo);
                 }
-                const float c0 = incl - l1;
-                logG[2 * lane] = c0;
-                logG[2 * lane + 1] = incl;
-                gam[2 * lane] = expf(c0);
-                gam[2 * lane + 1] = expf(incl);
+                float ph = __shfl_up_sync(0xffffffffu, h, 1), pl = __shfl_up_sync(0xffffffffu, lo, 1);
+                if (lane == 0) ph = pl = 0.f;
+                float h0, lo0, h1, lo1;
+                add_pair(ph, pl, l0, 0.f, h0, lo0);
+                add_pair(h0, lo0, l1, 0.f, h1, lo1);
+                logG[2 * lane] = h0;
+                logG[2 * lane + 1] = h1;
+                logLo[2 * lane] = lo0;
+                logLo[2 * lane + 1] = lo1;
+                gam[2 * lane] = expf(h0 + lo0);
+                gam[2 * lane + 1] = expf(h1 + lo1);
             }
 #pragma unroll 1
             for (int k = 0; k < 2; ++k) {
@@ -682,19 +708,19 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x) {
                 tmem_ld16(tmem + tq + kColG + 32 * half + 16, g32 + 16);
                 if (tl < kC) {                 // A[r][s] = beta_r Gamma_r / Gamma_s k_r.k_s for s < r
                     const int r = tl;
-                    const float br = betas[r], lr = logG[r];
+                    const float br = betas[r], lr = logG[r], lrl = logLo[r];
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
                         const int sc = 32 * half + q;
-                        AMt[sc * kC + r] = sc < r ? br * __expf(lr - logG[sc]) * g32[q] : 0.f;
+                        AMt[sc * kC + r] = sc < r ? br * __expf((lr - logG[sc]) + (lrl - logLo[sc])) * g32[q] : 0.f;
                     }
                 } else {                       // P[r][s] = q_r.k_s Gamma_r / Gamma_s for s <= r
                     const int r = tl - kC;
-                    const float lr = logG[r];
+                    const float lr = logG[r], lrl = logLo[r];
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
                         const int sc = 32 * half + q;
-                        Pt[sc * kC + r] = sc <= r ? __expf(lr - logG[sc]) * g32[q] : 0.f;
+                        Pt[sc * kC + r] = sc <= r ? __expf((lr - logG[sc]) + (lrl - logLo[sc])) * g32[q] : 0.f;
                     }
                 }
             }
@@ -820,14 +846,14 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x) {
                 // (Gamma_C / Gamma) K^ planes, as (128 x 64): row i = tl, tokens along K
                 tmem_ld16(tmem + tq + kColK + 32 * half, x32);
                 tmem_ld16(tmem + tq + kColK + 32 * half + 16, x32 + 16);
-                const float lc = logG[kC - 1];
+                const float lc = logG[kC - 1], lcl = logLo[kC - 1];
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) {
                     float ka[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int sr = 32 * half + 4 * q4 + e;
-                        ka[e] = __expf(lc - logG[sr]) * invk[sr] * x32[4 * q4 + e];
+                        ka[e] = __expf((lc - logG[sr]) + (lcl - logLo[sr])) * invk[sr] * x32[4 * q4 + e];
                     }
                     put4(dst_slot + kSlotKd, dst_slot + kSlotKd + 32 * 1024, tl, 8 * half + q4, 64,
                          make_float4(ka[0], ka[1], ka[2], ka[3]));

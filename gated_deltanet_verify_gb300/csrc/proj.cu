@@ -12,9 +12,9 @@
 //     too few to cover the SMs; a 256-row block of X per grid row).  The tile
 //     is D = W_tile X^T (128 x Mt), fp32 in tensor memory (tcgen05.mma
 //     kind::f16, bf16 A and B, both K-major from shared memory).
-//   * Warp 0 is the TMA producer: each stage holds 64 columns of K (128
-//     bytes per row) of the W tile and of X, one TMA box each, in the
-//     128-byte swizzled K-major layout the tensor core reads directly.
+//   * Warp 0 is the TMA producer: each stage holds kKBlk columns of K of the
+//     W tile and of X as 64-column (128-byte) TMA boxes in the 128-byte
+//     swizzled K-major layout the tensor core reads directly.
 //     Warp 1 issues the MMAs (4 per stage) and frees each stage through
 //     tcgen05.commit on the stage's "empty" barrier.
 //   * Programmatic dependent launch: the weight tiles of the first stages
@@ -39,10 +39,16 @@ namespace gdn {
 namespace {
 
 constexpr int kTileN = 128;             // weight rows per CTA (MMA M)
-constexpr int kKBlk = 64;               // K columns per pipeline stage
+#ifndef GDN_GEMM_KBLK
+#define GDN_GEMM_KBLK 128
+#endif
+constexpr int kKBlk = GDN_GEMM_KBLK;    // K columns per pipeline stage (a multiple of 64: one TMA box per 64)
+constexpr int kBoxes = kKBlk / 64;      // 64-column (128-byte) boxes per operand per stage
+static_assert(kKBlk % 64 == 0, "whole 128-byte boxes");
 constexpr int kMaxMt = 256;             // activation rows per CTA (MMA N)
 constexpr int kThreads = 128;
 constexpr int kSpin = 1 << 22;          // mbarrier polls before a wait gives up
+constexpr int kMaxStages = 16;
 
 struct GemmArgs {
     CUtensorMap w_map, x_map;
@@ -143,7 +149,7 @@ __host__ __device__ inline uint32_t x_stage_bytes(int Mt) { return (uint32_t)Mt 
 
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
-    __shared__ __align__(8) uint64_t bars[2 * 8 + 1];          // full[stages], empty[stages], done
+    __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 1];   // full[stages], empty[stages], done
     __shared__ uint32_t tslot;
     const int tid = threadIdx.x, wid = tid >> 5;
     const int nt = blockIdx.x, mb = blockIdx.y, split = blockIdx.z;   // the splits of a tile: one cluster
@@ -155,8 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const uint32_t stage_bytes = wbytes + xbytes;
     const uint32_t sbase = (smem_u32(sm) + 1023u) & ~1023u;   // swizzled tiles start on 1024 bytes
     auto full = [&](int s) { return smem_u32(&bars[s]); };
-    auto empty = [&](int s) { return smem_u32(&bars[8 + s]); };
-    const uint32_t done = smem_u32(&bars[16]);
+    auto empty = [&](int s) { return smem_u32(&bars[kMaxStages + s]); };
+    const uint32_t done = smem_u32(&bars[2 * kMaxStages]);
 
     if (wid == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&tslot)),
@@ -180,21 +186,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (tid == 0) {
         // ---- producer: the weight boxes of the first stages go out before the dependency wait
         const int pre = min(S, kb1 - kb0);
+        const uint32_t xbox = (uint32_t)a.Mt * 128;            // bytes of one X box
         for (int i = 0; i < pre; ++i) {
             const uint32_t st = sbase + (uint32_t)i * stage_bytes;
             mbar_expect_tx(full(i), stage_bytes);
-            tma_box(st, &a.w_map, (kb0 + i) * kKBlk, n0, full(i));
+            for (int b = 0; b < kBoxes; ++b) tma_box(st + b * 16384u, &a.w_map, (kb0 + i) * kKBlk + 64 * b, n0, full(i));
         }
         asm volatile("griddepcontrol.wait;\n" ::: "memory");
         for (int i = 0; i < pre; ++i)
-            tma_box(sbase + (uint32_t)i * stage_bytes + wbytes, &a.x_map, (kb0 + i) * kKBlk, m0, full(i));
+            for (int b = 0; b < kBoxes; ++b)
+                tma_box(sbase + (uint32_t)i * stage_bytes + wbytes + b * xbox, &a.x_map, (kb0 + i) * kKBlk + 64 * b, m0,
+                        full(i));
         for (int i = pre; i < kb1 - kb0 && ok; ++i) {
             const int s = i % S;
             ok = mbar_wait(empty(s), ((i / S) - 1) & 1);       // the MMAs of stage use i - S are done
             const uint32_t st = sbase + (uint32_t)s * stage_bytes;
             mbar_expect_tx(full(s), stage_bytes);
-            tma_box(st, &a.w_map, (kb0 + i) * kKBlk, n0, full(s));
-            tma_box(st + wbytes, &a.x_map, (kb0 + i) * kKBlk, m0, full(s));
+            for (int b = 0; b < kBoxes; ++b) tma_box(st + b * 16384u, &a.w_map, (kb0 + i) * kKBlk + 64 * b, n0, full(s));
+            for (int b = 0; b < kBoxes; ++b)
+                tma_box(st + wbytes + b * xbox, &a.x_map, (kb0 + i) * kKBlk + 64 * b, m0, full(s));
         }
     } else if (tid == 32) {
         // ---- MMA issuer: 4 MMAs of K = 16 per stage; each stage is freed when its MMAs complete
@@ -205,9 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             fence_after_sync();
             const uint32_t st = sbase + (uint32_t)s * stage_bytes;
 #pragma unroll
-            for (int j = 0; j < kKBlk / 16; ++j)            // 16 columns (32 bytes of each row) per MMA
-                mma_bf16(tmem, make_desc_sw128(st + 32 * j), make_desc_sw128(st + wbytes + 32 * j), id,
-                         (i > 0 || j > 0) ? 1u : 0u);
+            for (int j = 0; j < kKBlk / 16; ++j) {          // 16 columns (32 bytes of each row) per MMA
+                const uint32_t b = j >> 2, c = 32u * (j & 3);
+                mma_bf16(tmem, make_desc_sw128(st + b * 16384u + c),
+                         make_desc_sw128(st + wbytes + b * (uint32_t)a.Mt * 128u + c), id, (i > 0 || j > 0) ? 1u : 0u);
+            }
             mma_commit(empty(s));
         }
         mma_commit(done);
@@ -303,8 +315,14 @@ bool gemm_xwt_bf16(const void *W, const void *X, void *C, int M, int N, int K, l
     const int n_tiles = (N + kTileN - 1) / kTileN;
     a.n_kb = (K + kKBlk - 1) / kKBlk;
     const uint32_t stage = w_stage_bytes() + x_stage_bytes(a.Mt);
+    // as many stages as 200 KB hold: the weight stream needs ~200 KB in flight per SM to cover the DRAM
+    // latency at the copy rate
     a.stages = (int)((200u * 1024u) / stage);
-    if (a.stages > 8) a.stages = 8;
+    if (a.stages > kMaxStages) a.stages = kMaxStages;
+    if (a.stages < 1) {
+        why = "pipeline stage larger than shared memory";
+        return false;
+    }
     const size_t smem = (size_t)a.stages * stage + 1024;          // + room to align the tiles to 1024 bytes
     const int splits = gemm_splits(n_tiles, m_blocks, a.n_kb, a.Mt, smem - 1024, sms);
     a.kb_per_split = (a.n_kb + splits - 1) / splits;
@@ -316,7 +334,7 @@ bool gemm_xwt_bf16(const void *W, const void *X, void *C, int M, int N, int K, l
     {
         const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
         const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        const cuuint32_t box[2] = {(cuuint32_t)kKBlk, (cuuint32_t)kTileN};
+        const cuuint32_t box[2] = {64u, (cuuint32_t)kTileN};
         if (encode(&a.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(W), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
@@ -327,7 +345,7 @@ bool gemm_xwt_bf16(const void *W, const void *X, void *C, int M, int N, int K, l
     {
         const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
         const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        const cuuint32_t box[2] = {(cuuint32_t)kKBlk, (cuuint32_t)a.Mt};
+        const cuuint32_t box[2] = {64u, (cuuint32_t)a.Mt};
         if (encode(&a.x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(X), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
