@@ -12,7 +12,7 @@
 #include <cudaTypedefs.h>
 
 namespace gdn {
-size_t verify_smem_bytes(int T, int dk, int dv, int P, int act_bytes, bool tree);
+size_t verify_smem_bytes(int Tm, int T, int dk, int dv, int P, int act_bytes, bool tree);
 }  // namespace gdn
 
 namespace {
@@ -205,7 +205,7 @@ static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, con
     const int act_bytes = d.act_dtype == GDN_BF16 ? 2 : 4;
     // a lazy verify with a pending batch runs up to 2T tokens through shared memory
     const int Tm = pending ? 2 * d.n_tokens : d.n_tokens;
-    const size_t smem = gdn::verify_smem_bytes(Tm, d.d_k, d.d_v, P, act_bytes, mode == gdn::kTree);
+    const size_t smem = gdn::verify_smem_bytes(Tm, d.n_tokens, d.d_k, d.d_v, P, act_bytes, mode == gdn::kTree);
     if (info.smem_optin > 0 && smem > size_t(info.smem_optin))
         return fail(GDN_ERR_SHAPE, "verify needs %zu bytes of shared memory per CTA (max %d)", smem,
                     info.smem_optin);
@@ -241,6 +241,26 @@ static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, con
         a.ext_norm_w = size_t(d.d_v) * 4;
         a.ext_parent = M * 4;
         a.ext_trim = size_t(d.n_slots) * 4;
+    }
+    {   // the batch's activations as 2-D tensors for the kernel's TMA boxes (T tokens of a slot per box)
+        PFN_cuTensorMapEncodeTiled_v12000 encode = gdn::tensor_map_encoder();
+        if (!encode) return fail(GDN_ERR_LAUNCH, "the driver's tensor-map encoder is unavailable");
+        const CUtensorMapDataType dt = d.act_dtype == GDN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        const cuuint32_t estr[2] = {1, 1};
+        const cuuint64_t rows = cuuint64_t(d.n_slots) * cuuint64_t(d.n_tokens);
+        auto make = [&](CUtensorMap *map, const void *base, cuuint64_t cols, long long ld, int box_x) {
+            const cuuint64_t dims[2] = {cols, rows};
+            const cuuint64_t strides[1] = {cuuint64_t(ld) * cuuint64_t(act_bytes)};
+            const cuuint32_t box[2] = {cuuint32_t(box_x), cuuint32_t(d.n_tokens)};
+            return encode(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        };
+        if (!make(&a.qk_map, qkv, cuuint64_t(a.C), a.ld_qkv, d.d_k) ||
+            !make(&a.v_map, qkv, cuuint64_t(a.C), a.ld_qkv, d.d_v / P) ||
+            (z && !make(&a.z_map, z, cuuint64_t(d.n_v_heads) * d.d_v, a.ld_z, d.d_v / P)))
+            return fail(GDN_ERR_LAUNCH, "encoding the activation tensor maps failed");
     }
     cudaError_t e = gdn::launch_verify(a, d.act_dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "verify launch failed: %s", cudaGetErrorString(e));

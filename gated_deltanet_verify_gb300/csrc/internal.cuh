@@ -22,6 +22,9 @@ enum VerifyMode { kChain = 0, kTree = 1, kLazy = 2, kCommit = 3, kRolled = 4 };
 
 // Everything one verify launch needs, validated on the host.
 struct VerifyArgs {
+    CUtensorMap qk_map;               // the q|k|v channels as a 2-D tensor [B*Ts rows][C], box d_k x T tokens
+    CUtensorMap v_map;                // the same tensor, box (d_v / P) x T: a CTA's value rows
+    CUtensorMap z_map;                // z as [B*Ts rows][H_v*d_v], box (d_v / P) x T (not used by a commit)
     int B, Hk, Hv, dk, dv, T, C, r;   // C: conv channels; r = Hv / Hk
     int Ts;                           // tokens per slot in the activation buffers (>= T)
     int Tm;                           // tokens the shared memory holds (T; 2T for a lazy verify with a pending batch)

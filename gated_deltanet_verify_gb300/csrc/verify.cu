@@ -42,6 +42,12 @@
 //     peer writes to them.
 //   * Every wait is bounded; a wait that gives up writes GDN_ERR_TIMEOUT to
 //     the caller's status word instead of hanging.
+//   * The batch's activations arrive as TMA boxes, one per segment (q and k
+//     of the key head, this CTA's v and z rows, T tokens each) into their own
+//     128-byte aligned areas of shared memory, completing on an mbarrier; the
+//     state rows go straight into registers; the pending tokens of a lazy
+//     verify and the small parameter / conv-state rows come by 16-byte async
+//     copies.
 //   * Programmatic dependent launch: the kernel waits on its predecessor only
 //     right before its first global read, so its launch overlaps the tail of
 //     the previous kernel in the stream; meanwhile it prefetches its state
@@ -170,6 +176,23 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
                  : "memory");
     return ok != 0;
 }
+__device__ __forceinline__ bool mbar_try_wait_cta(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}\n"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+// 2-D tile of a tensor map -> own shared memory, completion counted in bytes on an mbarrier
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
 // Bounded waits: after kSpinLimit rounds the wait gives up and reports.
 __device__ __forceinline__ void report_timeout(int *status) {
     if (status) atomicCAS(status, int(GDN_OK), int(GDN_ERR_TIMEOUT));
@@ -177,6 +200,11 @@ __device__ __forceinline__ void report_timeout(int *status) {
 __device__ __forceinline__ void mbar_wait_cluster(uint32_t bar, uint32_t parity, int *status) {
     for (int i = 0; i < kSpinLimit; ++i)
         if (mbar_try_wait_cluster(bar, parity)) return;
+    report_timeout(status);
+}
+__device__ __forceinline__ void mbar_wait_cta(uint32_t bar, uint32_t parity, int *status) {
+    for (int i = 0; i < kSpinLimit; ++i)
+        if (mbar_try_wait_cta(bar, parity)) return;
     report_timeout(status);
 }
 __device__ __forceinline__ void fence_mbarrier_init_cluster() {
@@ -199,11 +227,14 @@ __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
-// Shared-memory carve-up; identical on host and device.
+// Shared-memory carve-up; identical on host and device.  The raw q, k and v segments of the window each
+// have an area for the batch's Tb tokens, written by one TMA box, and in front of it an area for the
+// Tm - Tb pending tokens of a lazy verify (16-byte async copies); TMA destinations start on 128 bytes.
 struct Smem {
     int NCH;
-    size_t xs, zs, cw, cs, nw, ys, os, gs, bs, kqs, rinv, allp, redbar, arow, total;
-    __host__ __device__ Smem(int T, int dk, int rows, int warps, int P, int act_bytes, bool tree)
+    size_t xq_p, xq_c, xk_p, xk_c, xv_p, xv_c, zs, cw, cs, nw, ys, os, gs, bs, kqs, rinv, allp, redbar, loadbar, arow,
+        total;
+    __host__ __device__ Smem(int Tm, int Tb, int dk, int rows, int warps, int P, int act_bytes, bool tree)
         : NCH(2 * dk + rows) {
         size_t off = 0;
         auto take = [&](size_t bytes) {
@@ -211,26 +242,37 @@ struct Smem {
             off += (bytes + 15) & ~size_t(15);
             return o;
         };
-        xs = take(size_t(T) * NCH * act_bytes);    // raw q | k | v inputs
-        zs = take(size_t(T) * rows * act_bytes);   // raw z for own rows
+        auto take128 = [&](size_t bytes) {
+            off = (off + 127) & ~size_t(127);
+            return take(bytes);
+        };
+        const size_t pend = size_t(Tm - Tb), ab = size_t(act_bytes);
+        xq_p = take128(pend * dk * ab);             // raw q of the pending tokens
+        xq_c = take128(size_t(Tb) * dk * ab);       // raw q of the batch (TMA)
+        xk_p = take128(pend * dk * ab);
+        xk_c = take128(size_t(Tb) * dk * ab);
+        xv_p = take128(pend * rows * ab);           // raw v of own rows
+        xv_c = take128(size_t(Tb) * rows * ab);
+        zs = take128(size_t(Tb) * rows * ab);       // raw z for own rows (TMA)
         cw = take(size_t(4) * NCH * 4);             // conv weights
         cs = take(size_t(3) * NCH * 4);             // old conv state
         nw = take(size_t(rows) * 4);                // norm weight for own rows
-        ys = take(size_t(T) * NCH * 4);             // post conv+SiLU (q, k normalised)
-        os = take(size_t(T) * rows * 4);            // o before the RMSNorm
-        gs = take(size_t(T) * 4);
-        bs = take(size_t(T) * 4);
-        kqs = take(size_t(T) * 4);
-        rinv = take(size_t(T) * 4);
-        allp = take(size_t(T) * P * warps * 4);     // per-warp sums of o^2 of the whole head
+        ys = take(size_t(Tm) * NCH * 4);            // post conv+SiLU (q, k normalised)
+        os = take(size_t(Tm) * rows * 4);           // o before the RMSNorm
+        gs = take(size_t(Tm) * 4);
+        bs = take(size_t(Tm) * 4);
+        kqs = take(size_t(Tm) * 4);
+        rinv = take(size_t(Tm) * 4);
+        allp = take(size_t(Tm) * P * warps * 4);    // per-warp sums of o^2 of the whole head
         redbar = take(8);                           // all RMSNorm partials of the head arrived
-        arow = take(tree ? size_t(T) * 5 * 4 : 0);  // tree: parent and the window row of each conv tap
+        loadbar = take(8);                          // the batch's activation boxes landed
+        arow = take(tree ? size_t(Tm) * 5 * 4 : 0); // tree: parent and the window row of each conv tap
         total = off;
     }
 };
 
 template <int DK, typename Act, int MODE>
-__global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs a) {
+__global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_constant__ VerifyArgs a) {
     static_assert(DK == 32 || DK == 64 || DK == 128, "d_k must be 32, 64 or 128");
     constexpr bool TREE = MODE == kTree, LAZY = MODE == kLazy, COMMIT = MODE == kCommit, ROLLED = MODE == kRolled;
     constexpr int LR = DK >= 64 ? 16 : 8;          // lanes per row group
@@ -240,7 +282,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     constexpr int NCL = DK / (4 * LR);             // 16-byte chunks per lane per row
     static_assert(NV == LR / 2, "lane layout");
 
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];   // no static shared memory: the base is aligned
 
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, wid = tid >> 5;
@@ -253,8 +295,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     const int j0 = p * ROWS;                                   // first value row of this CTA
     const bool qk_writer = (h % a.r == 0) && (p == 0);        // writes the shared q/k conv channels
 
-    const Smem L(LAZY ? a.Tm : T, DK, ROWS, WARPS, P, sizeof(Act), TREE);   // only a lazy launch holds 2T
-    Act *xs = reinterpret_cast<Act *>(smem_raw + L.xs);
+    const Smem L(LAZY ? a.Tm : T, T, DK, ROWS, WARPS, P, sizeof(Act), TREE);   // only a lazy launch holds 2T
     Act *zs = reinterpret_cast<Act *>(smem_raw + L.zs);
     float *cw = reinterpret_cast<float *>(smem_raw + L.cw);
     float *cs = reinterpret_cast<float *>(smem_raw + L.cs);
@@ -267,6 +308,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     float *rinv = reinterpret_cast<float *>(smem_raw + L.rinv);
     float *allp = reinterpret_cast<float *>(smem_raw + L.allp);
     const uint32_t redbar = smem_u32(smem_raw + L.redbar);
+    const uint32_t loadbar = smem_u32(smem_raw + L.loadbar);
     int *tpar = reinterpret_cast<int *>(smem_raw + L.arow);     // tree: [T] parents, then [T][4] window rows
     int *trow = tpar + T;
     // a checked build tests each global access against its buffer first (compiled away otherwise)
@@ -281,16 +323,28 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         if (c < 2 * DK) return Hk * DK + kh * DK + (c - DK);            // k of key head kh
         return 2 * Hk * DK + h * DV + j0 + (c - 2 * DK);                 // v rows of this CTA
     };
-    // window row rho (0..T+2) of local channel c: old conv state, then the new tokens
-    auto win = [&](int rho, int c) -> float {
-        return rho < 3 ? cs[rho * NCH + c] : to_f32(xs[size_t(rho - 3) * NCH + c]);
+    int n_prev = 0;                             // lazy: the pending batch's accepted tokens, run first
+    // raw input of token t (0..TT-1) at local channel c: the q, k or v area, pending or batch part
+    auto xsrc = [&](int t, int c) -> const Act * {
+        const bool pend = t < n_prev;
+        const size_t r = size_t(pend ? t : t - n_prev);
+        if (c < DK) return reinterpret_cast<const Act *>(smem_raw + (pend ? L.xq_p : L.xq_c)) + r * DK + c;
+        if (c < 2 * DK) return reinterpret_cast<const Act *>(smem_raw + (pend ? L.xk_p : L.xk_c)) + r * DK + (c - DK);
+        return reinterpret_cast<const Act *>(smem_raw + (pend ? L.xv_p : L.xv_c)) + r * ROWS + (c - 2 * DK);
     };
+    // window row rho (0..TT+2) of local channel c: old conv state, then the tokens
+    auto win = [&](int rho, int c) -> float { return rho < 3 ? cs[rho * NCH + c] : to_f32(*xsrc(rho - 3, c)); };
     auto win4 = [&](int rho, int c) -> float4 {
-        return rho < 3 ? load4(cs + rho * NCH + c) : load4(xs + size_t(rho - 3) * NCH + c);
+        return rho < 3 ? load4(cs + rho * NCH + c) : load4(xsrc(rho - 3, c));
     };
 
+    if (smem_u32(smem_raw) & 127u) {            // TMA destinations need 128-byte alignment (uniform: every CTA)
+        if (tid == 0 && a.d_status) atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_LAUNCH));
+        return;
+    }
     if (tid == 0) {
         mbar_init(redbar, 1);
+        mbar_init(loadbar, 1);
         fence_mbarrier_init_cluster();
         // the single arrival; the phase completes once every partial of the head has landed
         mbar_arrive_expect_tx(redbar, uint32_t(T * P * WARPS * 4));
@@ -341,7 +395,6 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
     // everything below may read what the previous kernel in the stream wrote
     grid_dependency_wait();
     int TT = T;                                 // tokens run for this slot
-    int n_prev = 0;                             // lazy: the pending batch's accepted tokens, run first
     int src_tok = 0;                            // rolled: the previous batch's accepted token
     if constexpr (COMMIT || LAZY || ROLLED) {
         if (a.trim) {
@@ -382,39 +435,39 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
                 S[rho][m][0] = v.x; S[rho][m][1] = v.y; S[rho][m][2] = v.z; S[rho][m][3] = v.w;
             }
     }
-    // (2) activations, conv weights / state, norm weight: 16-byte async copies to smem
+    // (2) the batch's activations: one TMA box per segment (q and k of the key head, this CTA's v and z
+    // rows, T tokens each), completing on loadbar; the pending tokens of a lazy verify, the conv weights /
+    // state and the norm weight: 16-byte async copies
+    if (tid == 0) {
+        const uint32_t seg = uint32_t(T) * sizeof(Act);
+        mbar_arrive_expect_tx(loadbar, seg * (2 * DK + ROWS + (COMMIT ? 0 : ROWS)));
+        const int y = s * a.Ts;
+        tma_load_2d(smem_u32(smem_raw + L.xq_c), &a.qk_map, kh * DK, y, loadbar);
+        tma_load_2d(smem_u32(smem_raw + L.xk_c), &a.qk_map, (Hk + kh) * DK, y, loadbar);
+        tma_load_2d(smem_u32(smem_raw + L.xv_c), &a.v_map, 2 * Hk * DK + h * DV + j0, y, loadbar);
+        if constexpr (!COMMIT) tma_load_2d(smem_u32(smem_raw + L.zs), &a.z_map, h * DV + j0, y, loadbar);
+    }
     {
         constexpr int kPer16 = 16 / sizeof(Act);
         const int vq = DK / kPer16, vv = ROWS / kPer16;     // 16-byte vectors per segment
-        const int per_t = 2 * vq + vv + (COMMIT ? 0 : vv);  // q, k, v, z (no z in a commit)
-        const Act *z = static_cast<const Act *>(a.z);
-        for (int i = tid; i < TT * per_t; i += nthr) {
+        const int per_t = 2 * vq + vv;                      // q, k, v of a pending token
+        const Act *qkv = static_cast<const Act *>(a.qkv_prev);
+        for (int i = tid; i < n_prev * per_t; i += nthr) {
             const int t = i / per_t, w = i % per_t;
-            // tokens of the pending batch come first (lazy), then the batch itself
-            const bool pend = t < n_prev;
-            const Act *qkv = static_cast<const Act *>(pend ? a.qkv_prev : a.qkv);
-            const size_t rw = size_t(s) * a.Ts + (pend ? t : t - n_prev);
+            const size_t rw = size_t(s) * a.Ts + t;
             const Act *src;
             Act *dst;
-            const void *base = qkv;
-            size_t ext = a.ext_qkv;
             if (w < vq) {
                 src = qkv + rw * a.ld_qkv + size_t(kh) * DK + w * kPer16;
-                dst = xs + size_t(t) * NCH + w * kPer16;
+                dst = reinterpret_cast<Act *>(smem_raw + L.xq_p) + size_t(t) * DK + w * kPer16;
             } else if (w < 2 * vq) {
                 src = qkv + rw * a.ld_qkv + size_t(Hk + kh) * DK + (w - vq) * kPer16;
-                dst = xs + size_t(t) * NCH + DK + (w - vq) * kPer16;
-            } else if (w < 2 * vq + vv) {
-                src = qkv + rw * a.ld_qkv + size_t(2 * Hk) * DK + size_t(h) * DV + j0 + (w - 2 * vq) * kPer16;
-                dst = xs + size_t(t) * NCH + 2 * DK + (w - 2 * vq) * kPer16;
+                dst = reinterpret_cast<Act *>(smem_raw + L.xk_p) + size_t(t) * DK + (w - vq) * kPer16;
             } else {
-                if (pend) continue;                 // no outputs for the pending tokens
-                src = z + rw * a.ld_z + size_t(h) * DV + j0 + (w - 2 * vq - vv) * kPer16;
-                dst = zs + size_t(t - n_prev) * ROWS + (w - 2 * vq - vv) * kPer16;
-                base = z;
-                ext = a.ext_z;
+                src = qkv + rw * a.ld_qkv + size_t(2 * Hk) * DK + size_t(h) * DV + j0 + (w - 2 * vq) * kPer16;
+                dst = reinterpret_cast<Act *>(smem_raw + L.xv_p) + size_t(t) * ROWS + (w - 2 * vq) * kPer16;
             }
-            if (chk(src, 16, base, ext)) cp_async16(dst, src);
+            if (chk(src, 16, qkv, a.ext_qkv)) cp_async16(dst, src);
         }
         // conv weights (4 rows) and old conv state (3 rows), per segment in float4s
         const int fq = DK / 4, fv = ROWS / 4, per_row = 2 * fq + fv;
@@ -462,6 +515,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const VerifyArgs
         }
     }
     cp_async_wait_all();
+    mbar_wait_cta(loadbar, 0, a.d_status);      // the batch's activation boxes
     __syncthreads();
     // cluster phase 1: this CTA has read the old conv state (the copies above have
     // landed) and initialised its mbarrier (published by fence.mbarrier_init)
@@ -781,7 +835,7 @@ template <int DK, typename Act, int MODE>
 cudaError_t launch_t(const VerifyArgs &a, cudaStream_t stream) {
     const int rows = a.dv / a.P;
     const int warps = rows / kRowsPerWarp;
-    const Smem L(a.Tm, DK, rows, warps, a.P, sizeof(Act), MODE == kTree);
+    const Smem L(a.Tm, a.T, DK, rows, warps, a.P, sizeof(Act), MODE == kTree);
     auto kern = verify_kernel<DK, Act, MODE>;
     // Function attributes belong to the context: the dynamic shared memory limit set so far (raised
     // when a launch needs more) and the non-portable cluster permission are cached per context id,
@@ -830,9 +884,9 @@ cudaError_t launch_t(const VerifyArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
-size_t verify_smem_bytes(int T, int dk, int dv, int P, int act_bytes, bool tree) {
+size_t verify_smem_bytes(int Tm, int T, int dk, int dv, int P, int act_bytes, bool tree) {
     const int rows = dv / P;
-    return Smem(T, dk, rows, rows / kRowsPerWarp, P, act_bytes, tree).total;
+    return Smem(Tm, T, dk, rows, rows / kRowsPerWarp, P, act_bytes, tree).total;
 }
 
 template <int MODE>
