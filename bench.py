@@ -669,9 +669,9 @@ def time_graph_steps(torch, wl, steps, graph_len, first=0):
 
 
 def kernel_duration(torch, wl, which, n_launch, flush=None):
-    """Average duration of one kernel kind: CUDA events around a graph of n_launch back-to-back
-    launches cycling over the buffer sets and layers (each set's data evicted from L2 by the others
-    before it comes round again)."""
+    """Duration of one kernel kind: CUDA events around each of five replays of a graph of n_launch
+    back-to-back launches cycling over the buffer sets and layers (each set's data evicted from L2 by
+    the others before it comes round again); the median replay, per launch."""
     fns = []
     for k in range(n_launch):
         kk, li = k % wl.n_sets, (k // wl.n_sets) % wl.layers
@@ -682,14 +682,32 @@ def kernel_duration(torch, wl, which, n_launch, flush=None):
     if flush is not None:
         flush()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps = 5
-    e0.record()
-    for _ in range(reps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record()
+    for i in range(reps):
         g.replay()
+        ev[i + 1].record()
+    ev[-1].synchronize()
+    per = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(reps))
+    return per[reps // 2] / 1e3 / n_launch
+
+
+def eager_step_duration(torch, wl, n):
+    """Launch-to-launch time of a step issued eagerly (no graph): n steps back to back on one stream,
+    cycling over the buffer sets, each step one or two C-ABI calls from Python; CUDA events around the
+    burst.  Against the graph replays this shows what the host's launch path costs a short step."""
+    sp = torch.cuda.current_stream().cuda_stream
+    for k in range(3):
+        wl.step(k % wl.n_sets, sp)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for k in range(n):
+        wl.step(k % wl.n_sets, sp)
     e1.record()
     e1.synchronize()
-    return e0.elapsed_time(e1) / 1e3 / (reps * n_launch)
+    return e0.elapsed_time(e1) / 1e3 / n
 
 
 def describe(shape) -> str:
@@ -835,6 +853,16 @@ def measure(name, steps, warmup, device, world, l2, clocks, with_e2e, graph_len_
     if wl.layers > 1:
         res["config"]["units"] = (f"tokens/s = slots x {shape.n_tokens} verify tokens through all "
                                   f"{shape.n_layers} layers per step")
+    if name != "prefill" and not wl.tree:
+        # accepted tokens: per slot T - trim of the step's rollback (averaged over the sets and layers)
+        frac = float(np.mean(shape.n_tokens - wl.trims)) / shape.n_tokens
+        res["accepted"] = {"value": value * frac, "unit": "accepted tokens/s",
+                           "fraction": frac, "note": "the trims are drawn U{0..T-1} per slot, set and layer"}
+    if name != "prefill" and wl.layers == 1 and not wl.proj:
+        n_eager = 200
+        res["eager"] = {"us_per_step": eager_step_duration(torch, wl, n_eager) * 1e6, "steps": n_eager,
+                        "timing": "the same step launched eagerly from Python (no CUDA graph), back to back; "
+                                  "ms_per_step above is the graph-amortised figure"}
     if bad:
         res["device_status_errors"] = bad
     if with_e2e:
@@ -988,7 +1016,16 @@ def cpu_baseline(shape, seconds):
     _oracle_layers(one, layers, reps, cores)
     dt = time.perf_counter() - t0
     tok = one.n_slots * one.n_tokens * reps / shape.n_layers
+    # one whole pass on a single thread as well, when it is expected to take under half a minute
+    single = None
+    if t_pass * cores < 30.0:
+        t0 = time.perf_counter()
+        _oracle_layers(one, layers, 1, 1)
+        t1 = time.perf_counter() - t0
+        single = {"value": one.n_slots * one.n_tokens / shape.n_layers / t1, "unit": "tokens/s",
+                  "seconds": t1, "sample": "one whole pass of the step, 1 thread"}
     return {"value": tok / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "single_thread": single,
             "sample": (f"{reps} whole pass(es) of the step (verify+rollback, or the prefill) over all "
                        f"{one.n_slots} slot(s) and {shape.n_v_heads} value heads of one layer, "
                        f"{one.n_tokens} tokens, fp64, {cores} threads, {dt:.1f} s; a token counts once it has "
