@@ -315,10 +315,10 @@ bool gemm_xwt_bf16(const void *W, const void *X, void *C, int M, int N, int K, l
     const int n_tiles = (N + kTileN - 1) / kTileN;
     a.n_kb = (K + kKBlk - 1) / kKBlk;
     const uint32_t stage = w_stage_bytes() + x_stage_bytes(a.Mt);
-    // ~200 KB of weights in flight per SM covers the DRAM latency at the copy rate (two CTAs per SM with
-    // 100 KB each, the K splits spread over every SM, measured slower for the output projection: 26 us
-    // against 15 us)
-    a.stages = (int)((200u * 1024u) / stage);
+    // as many stages as fit in ~216 KB: a stage is held until its MMAs complete, so the bytes in flight per
+    // SM set the intake (six 36 KB stages: output projection 14.6 us against 14.9 with five; two CTAs per SM
+    // with 100 KB each, the K splits spread over every SM, measured slower: 26 us)
+    a.stages = (int)((216u * 1024u) / stage);
     if (a.stages > kMaxStages) a.stages = kMaxStages;
     if (a.stages < 1) {
         why = "pipeline stage larger than shared memory";
