@@ -200,6 +200,19 @@ def kernel_source_sha(names) -> str:
     return h.hexdigest()[:16]
 
 
+def recorded_step_traffic(workload: str, sha: str):
+    """DRAM bytes per step over a long range of steps (ncu range capture: the captured states' write-backs
+    included), if taken on this exact source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        e = json.load(f).get("step", {}).get(workload)
+    if not e or e.get("source_sha") != sha:
+        return None
+    return e.get("dram_bytes_per_step")
+
+
 def recorded_traffic(kernel: str, sha: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     this exact kernel source and workload; else None."""
@@ -850,6 +863,12 @@ def measure(name, steps, warmup, device, world, l2, clocks, with_e2e, graph_len_
         "clocks": clocks.summary(t_wall0 - 0.5, t_wall1 + 0.5),
         "kernel_clocks": clocks.summary(t_wall1, t_wall2 + 0.5),
     }
+    st = recorded_step_traffic(name, kernel_source_sha(["verify.cu", "internal.cuh", "rollback.cu"]))
+    if st and name != "prefill":
+        sb = wl.step_bytes(0)
+        res["step_traffic"] = {"dram_bytes_per_step": st, "over_algorithmic": st / sb,
+                               "dram_gbs": st * steps / dt / 1e9, "dram_frac": st * steps / dt / 1e9 / hbm,
+                               "how": "ncu range capture over many steps (profiles/traffic.json, key step)"}
     if wl.layers > 1:
         res["config"]["units"] = (f"tokens/s = slots x {shape.n_tokens} verify tokens through all "
                                   f"{shape.n_layers} layers per step")
@@ -913,9 +932,18 @@ def run_cuda(args):
               else VerifyWorkload(shape, device, l2))
         torch.cuda.synchronize()
         sp = torch.cuda.current_stream().cuda_stream
+        if args.profile_range:
+            # one rotation first (every set touched, L2 in its steady state), then the K steps inside one
+            # cudaProfilerStart/Stop range, so that a range capture sees the captures' write-backs too
+            for k in range(wl.n_sets):
+                wl.step(k, sp)
+            torch.cuda.synchronize()
+            torch.cuda.profiler.start()
         for k in range(args.profile):
             wl.step(k % wl.n_sets, sp)
         torch.cuda.synchronize()
+        if args.profile_range:
+            torch.cuda.profiler.stop()
         return
 
     vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
@@ -1086,6 +1114,8 @@ def main():
     ap.add_argument("--slots", type=int, default=0, help="override the workload's slot count (profiling cases)")
     ap.add_argument("--profile", type=int, default=0, metavar="K",
                     help="run K untimed eager steps and exit (for ncu captures)")
+    ap.add_argument("--profile-range", action="store_true",
+                    help="with --profile: the K steps inside one profiler start/stop range (ncu range capture)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
