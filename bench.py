@@ -365,8 +365,9 @@ class VerifyWorkload:
         for li in range(n_layer_inputs):
             inp = make_inputs(s, layer=li)
             self.host_inputs.append(inp)
-        trims = randint(s.seed, 12, self.n_sets * self.layers * s.n_slots, s.n_tokens).reshape(
-            self.n_sets, self.layers, s.n_slots)
+        # a slot's trim is decided once per step (after every layer has verified) and rolls back every layer
+        trims = np.repeat(randint(s.seed, 12, self.n_sets * s.n_slots, s.n_tokens).reshape(self.n_sets, 1, s.n_slots),
+                          self.layers, axis=1)
         if self.tree:                                # accepted node per slot, -1 .. T-1
             trims = trims.astype(np.int64) - 1
         self.trims = trims
@@ -452,8 +453,10 @@ class VerifyWorkload:
         fn(self.dims, x["trim"], x["state"], x["conv_state"], x["cap_state"], x["cap_conv"], x["status"], stream)
 
     def step(self, k, stream):
+        # the verify pass through every layer, then (the accepted lengths known) the rollback of every layer
         for li in range(self.layers):
             self.verify(k, li, stream)
+        for li in range(self.layers):
             self.rollback(k, li, stream)
 
     def step_bytes(self, k):
@@ -521,11 +524,16 @@ class VerifyWorkload:
         outputs device -> host as one buffer, and synchronises the host once.  The
         device tensors the calls read and write are views into the two staging
         buffers (each view 256-byte aligned).  (Replaying the step from a CUDA
-        graph instead measured slower at one slot: 352K against 387K tokens/s.)"""
+        graph instead measured slower at one slot: 352K against 387K tokens/s.)
+        A multi-layer chain step runs as a serving step would: the verify of every
+        layer, the outputs back to the host and a host synchronisation (the accepted
+        lengths are decided there), then the trims host -> device and the rollback
+        of every layer."""
         torch = self.torch
         from workloads.device import act_host
         s = self.shape
         out_key = "y" if self.proj else "out"
+        split_rollback = self.layers > 1 and not (self.lazy or self.rolled or self.tree or self.proj)
         hosts = []
         for li in range(self.layers):
             inp = self.host_inputs[li if self.layers > 1 else 0]
@@ -534,7 +542,8 @@ class VerifyWorkload:
             else:
                 h = {"qkv": act_host(inp.qkv, s), "z": act_host(inp.z, s), "alpha": act_host(inp.alpha, s),
                      "beta_raw": act_host(inp.beta_raw, s)}
-            h["trim"] = torch.from_numpy(self.trims[0, li].astype(np.int32))
+            if not split_rollback:
+                h["trim"] = torch.from_numpy(self.trims[0, li].astype(np.int32))
             if self.tree:
                 h["parent"] = torch.from_numpy(self.parents)
             hosts.append(h)
@@ -564,9 +573,23 @@ class VerifyWorkload:
             xs[li][out_key] = dev_out[off:off + nb].view(ref.dtype).view(ref.shape)
         stream = torch.cuda.current_stream()
         sp = stream.cuda_stream
+        host_trim = torch.from_numpy(self.trims[0, 0].astype(np.int32)).pin_memory()
+        dev_trim = torch.empty_like(host_trim, device=device)
+        if split_rollback:
+            for li in range(self.layers):
+                xs[li]["trim"] = dev_trim
 
         def one(k):
             dev_in.copy_(host_in, non_blocking=True)
+            if split_rollback:
+                for li in range(self.layers):
+                    self.verify(0, li, sp, xs[li])
+                host_out.copy_(dev_out, non_blocking=True)
+                stream.synchronize()
+                dev_trim.copy_(host_trim, non_blocking=True)
+                for li in range(self.layers):
+                    self.rollback(0, li, sp, xs[li])
+                return
             for li in range(self.layers):
                 self.verify(0, li, sp, xs[li])
                 self.rollback(0, li, sp, xs[li])
@@ -575,11 +598,13 @@ class VerifyWorkload:
 
         for k in range(10):
             one(k)
+        stream.synchronize()
         t0 = time.perf_counter()
         for k in range(steps):
             one(k)
+        stream.synchronize()
         dt = time.perf_counter() - t0
-        return dt, in_bytes, out_bytes
+        return dt, in_bytes + (host_trim.numel() * 4 if split_rollback else 0), out_bytes
 
 
 class PrefillWorkload:
@@ -842,7 +867,8 @@ def measure(name, steps, warmup, device, world, l2, clocks, with_e2e, graph_len_
             "layer: input projection GEMM + verify + output projection GEMM, then rollback" if wl.proj else
             "verify with the previous step's rollback folded in (one launch)" if wl.rolled else
             "lazy verify: commit of the pending batch (accepted-prefix re-run) + outputs of the new one"
-            if wl.lazy else "verify+rollback" + (" per layer, all layers" if wl.layers > 1 else ""))
+            if wl.lazy else ("the verify of every layer, then the rollback of every layer (one trim per slot)"
+                             if wl.layers > 1 else "verify+rollback"))
     res = {
         "value": value, "unit": "tokens/s", "steps": steps, "warmup": warmup,
         "ms_per_step": dt / steps * 1e3,
