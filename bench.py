@@ -408,6 +408,13 @@ class VerifyWorkload:
                                            x["state"], x["conv_state"], x["cap_state"], x["cap_conv"], x["out"])
         self.tokens_per_step = s.n_slots * s.n_tokens
         self.kernels_per_step = (1 if self.lazy or self.rolled else 2) * self.layers
+        # a multi-layer chain step rolls every layer back in one launch (gdn_rollback_layers, device pointer
+        # tables of each set's layers)
+        self.tabs = None
+        if self.layers > 1 and not (self.lazy or self.rolled or self.tree or self.proj):
+            self.tabs = [[gdn.pointer_table([x[key] for x in layers], device)
+                          for key in ("state", "conv_state", "cap_state", "cap_conv")] for layers in self.sets]
+            self.kernels_per_step = self.layers + 1
 
     def verify(self, k, li, stream, x=None):
         x = self.sets[k][li] if x is None else x
@@ -452,10 +459,19 @@ class VerifyWorkload:
         fn = self.gdn.gdn_rollback_tree if self.tree else self.gdn.gdn_rollback
         fn(self.dims, x["trim"], x["state"], x["conv_state"], x["cap_state"], x["cap_conv"], x["status"], stream)
 
+    def rollback_all(self, k, li, stream, tabs=None, trim=None):
+        """Every layer of set k rolled back in one launch (li unused: the signature of the per-kernel timer)."""
+        x = self.sets[k][0]
+        self.gdn.gdn_rollback_layers(self.dims, self.layers, x["trim"] if trim is None else trim,
+                                     *(self.tabs[k] if tabs is None else tabs), x["status"], stream)
+
     def step(self, k, stream):
         # the verify pass through every layer, then (the accepted lengths known) the rollback of every layer
         for li in range(self.layers):
             self.verify(k, li, stream)
+        if self.tabs is not None:
+            self.rollback_all(k, 0, stream)
+            return
         for li in range(self.layers):
             self.rollback(k, li, stream)
 
@@ -587,8 +603,7 @@ class VerifyWorkload:
                 host_out.copy_(dev_out, non_blocking=True)
                 stream.synchronize()
                 dev_trim.copy_(host_trim, non_blocking=True)
-                for li in range(self.layers):
-                    self.rollback(0, li, sp, xs[li])
+                self.rollback_all(0, 0, sp, trim=dev_trim)
                 return
             for li in range(self.layers):
                 self.verify(0, li, sp, xs[li])
@@ -821,6 +836,8 @@ def measure(name, steps, warmup, device, world, l2, clocks, with_e2e, graph_len_
     else:
         kdur = {"verify": kernel_duration(torch, wl, "verify", n_launch, flush),
                 "rollback": kernel_duration(torch, wl, "rollback", n_launch, flush)}
+        if wl.tabs is not None:     # the step's one rollback launch over every layer
+            kdur["rollback_all_layers"] = kernel_duration(torch, wl, "rollback_all", max(2, wl.n_sets), flush)
     t_wall2 = time.time()
 
     dt = max_over_ranks(dt, device)

@@ -36,7 +36,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_A
 GDN_F32 = 0
 GDN_BF16 = 1
 
-EXPORTED_SYMBOLS = ("gdn_verify_forward", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_tree",
+EXPORTED_SYMBOLS = ("gdn_verify_forward", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_tree", "gdn_rollback_layers",
                     "gdn_verify_after_rollback", "gdn_verify_lazy", "gdn_commit_lazy", "gdn_step_io_layout",
                     "gdn_verify_step_host", "gdn_proj_in_ld", "gdn_layer_workspace_bytes",
                     "gdn_project_in", "gdn_project_out", "gdn_layer_verify", "gdn_prefill_workspace_bytes",
@@ -99,6 +99,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_verify_tree.restype = ip
         L.gdn_rollback_tree.argtypes = [ctypes.POINTER(Dims)] + [vp] * 7
         L.gdn_rollback_tree.restype = ip
+        L.gdn_rollback_layers.argtypes = [ctypes.POINTER(Dims), ctypes.c_int] + [vp] * 7
+        L.gdn_rollback_layers.restype = ip
         L.gdn_verify_after_rollback.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 12
         L.gdn_verify_after_rollback.restype = ip
         L.gdn_step_io_layout.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(StepIO)]
@@ -181,6 +183,20 @@ def gdn_rollback(dims: Dims, d_trim, state, conv_state, cap_state, cap_conv, d_s
                  stream=None) -> None:
     _check(lib().gdn_rollback(ctypes.byref(dims), _ptr(d_trim), _ptr(state), _ptr(conv_state),
                               _ptr(cap_state), _ptr(cap_conv), _ptr(d_status), _stream(stream)))
+
+
+def pointer_table(tensors, device="cuda"):
+    """A DEVICE int64 array of the tensors' data pointers (the tables gdn_rollback_layers reads)."""
+    import torch
+    return torch.tensor([t.data_ptr() for t in tensors], dtype=torch.int64, device=device)
+
+
+def gdn_rollback_layers(dims: Dims, n_layers: int, d_trim, tab_state, tab_conv_state, tab_cap_state, tab_cap_conv,
+                        d_status=None, stream=None) -> None:
+    """gdn_rollback of n_layers layers in one launch; the tab_* are device pointer tables (pointer_table)."""
+    _check(lib().gdn_rollback_layers(ctypes.byref(dims), int(n_layers), _ptr(d_trim), _ptr(tab_state),
+                                     _ptr(tab_conv_state), _ptr(tab_cap_state), _ptr(tab_cap_conv), _ptr(d_status),
+                                     _stream(stream)))
 
 
 def gdn_verify_tree(dims: Dims, params: LayerParams, qkv, z, alpha, beta_raw, d_parent, state, conv_state,

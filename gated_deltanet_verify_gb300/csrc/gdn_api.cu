@@ -356,6 +356,41 @@ int gdn_rollback_tree(const gdn_dims *dims, const int32_t *d_accept, float *stat
     return rollback_impl(dims, d_accept, state, conv_state, cap_state, cap_conv, d_status, stream, 1);
 }
 
+int gdn_rollback_layers(const gdn_dims *dims, int n_layers, const int32_t *d_trim, float *const *d_state,
+                        float *const *d_conv_state, const float *const *d_cap_state, const float *const *d_cap_conv,
+                        int *d_status, void *stream) {
+    g_err.clear();
+    int rc = check_common(dims);
+    if (rc) return rc;
+    const gdn_dims &d = *dims;
+    if (n_layers < 1 || n_layers > 65535) return fail(GDN_ERR_SHAPE, "n_layers must be in [1, 65535] (got %d)", n_layers);
+    if (d.n_slots > 65535) return fail(GDN_ERR_SHAPE, "n_slots must be <= 65535");
+    if ((d.d_k % 4) || (d.d_v % 8)) return fail(GDN_ERR_SHAPE, "d_k must be a multiple of 4 and d_v of 8");
+    if (!d_trim || !d_state || !d_conv_state) return fail(GDN_ERR_ARG, "trim or a state table is NULL");
+    if (!d_cap_state || !d_cap_conv) return fail(GDN_ERR_NO_CAPTURE, "rollback needs both capture tables");
+    if (!aligned16(d_trim)) return fail(GDN_ERR_ALIGN, "d_trim is not 16-byte aligned");
+    const void *tabs[] = {d_state, d_conv_state, d_cap_state, d_cap_conv};
+    for (const void *p : tabs)
+        if (reinterpret_cast<uintptr_t>(p) & 7u) return fail(GDN_ERR_ALIGN, "pointer table %p is not 8-byte aligned", p);
+    gdn::RollbackArgs a{};
+    a.B = d.n_slots; a.T = d.n_tokens; a.W1 = d.conv_width - 1;
+    a.C = conv_channels(&d);
+    a.state_elems = (long long)d.n_v_heads * d.d_v * d.d_k;
+    a.conv_elems = (long long)a.W1 * a.C;
+    a.trim = d_trim;
+    a.d_status = d_status;
+    a.tree = 0;
+    a.ext_state = size_t(a.B) * size_t(a.state_elems) * 4;
+    a.ext_conv_state = size_t(a.B) * size_t(a.conv_elems) * 4;
+    a.ext_cap_state = size_t(a.B) * a.T * size_t(a.state_elems) * 4;
+    a.ext_cap_conv = size_t(a.B) * size_t(a.W1 + a.T) * size_t(a.C) * 4;
+    a.n_layers = n_layers;
+    a.tab_state = d_state; a.tab_conv_state = d_conv_state; a.tab_cap_state = d_cap_state; a.tab_cap_conv = d_cap_conv;
+    cudaError_t e = gdn::launch_rollback(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "rollback launch failed: %s", cudaGetErrorString(e));
+    return GDN_OK;
+}
+
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims) {
     if (!dims) return 0;
     std::string why;

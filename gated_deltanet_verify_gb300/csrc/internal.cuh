@@ -58,6 +58,13 @@ struct RollbackArgs {
     int *d_status;
     int tree;                         // 1: cap_conv holds per-node conv states [B][T][W-1][C]
     size_t ext_state, ext_conv_state, ext_cap_state, ext_cap_conv;   // bytes, for a checked build
+    // several layers in one launch (grid z = layer): device tables of n_layers pointers replace the four
+    // buffers above (NULL tables: one layer, the buffers above)
+    int n_layers;
+    float *const *tab_state;
+    float *const *tab_conv_state;
+    const float *const *tab_cap_state;
+    const float *const *tab_cap_conv;
 };
 
 // Everything one chunkwise prefill launch needs (d_k = d_v = 128, W = 4).

@@ -8,11 +8,14 @@
 // After a tree verify the slot moves to its accepted node instead: state and
 // conv state come from that node's captures (-1: nothing accepted, no-op).
 //
-// A pure copy, so HBM-bound: grid (blocks_per_slot, B); every block reads the
-// slot's trim (or node) from device memory (the call can live in a CUDA graph),
-// and copies its share of the 16-byte vectors with several loads in flight per
-// thread.  A slot with an invalid index is left untouched and reported through
-// the status word.
+// A pure copy, so HBM-bound: grid (blocks_per_slot, B, layers); every block
+// reads the slot's trim (or node) from device memory (the call can live in a
+// CUDA graph), and copies its share of the 16-byte vectors with several loads
+// in flight per thread.  A slot with an invalid index is left untouched and
+// reported through the status word.  The layers of a serving step roll back
+// with the same trims once the whole pass has verified, so one launch can take
+// them all: the layer's four buffers then come from device pointer tables (an
+// entry that is NULL or not 16-byte aligned skips that layer and is reported).
 #include "internal.cuh"
 
 namespace gdn {
@@ -35,6 +38,22 @@ __global__ void __launch_bounds__(kThreads) rollback_kernel(const RollbackArgs a
     // its CTAs do not take SM slots from the copy blocks still waiting to run)
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const int s = blockIdx.y;
+    float *state = a.state, *conv_state = a.conv_state;
+    const float *cap_state = a.cap_state, *cap_conv = a.cap_conv;
+    if (a.tab_state) {
+        const int l = blockIdx.z;
+        state = a.tab_state[l];
+        conv_state = a.tab_conv_state[l];
+        cap_state = a.tab_cap_state[l];
+        cap_conv = a.tab_cap_conv[l];
+        const uintptr_t any = reinterpret_cast<uintptr_t>(state) | reinterpret_cast<uintptr_t>(conv_state) |
+                              reinterpret_cast<uintptr_t>(cap_state) | reinterpret_cast<uintptr_t>(cap_conv);
+        if (!state || !conv_state || !cap_state || !cap_conv || (any & 15u)) {
+            if (blockIdx.x == 0 && s == 0 && threadIdx.x == 0 && a.d_status)
+                atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_ARG));
+            return;
+        }
+    }
     // a checked build tests each global access against its buffer first (compiled away otherwise)
     auto chk = [&](const void *p, size_t bytes, const void *base, size_t ext) -> bool {
         return in_bounds(p, bytes, base, ext, a.d_status);
@@ -56,13 +75,13 @@ __global__ void __launch_bounds__(kThreads) rollback_kernel(const RollbackArgs a
         return;
     }
     const long long n4_state = a.state_elems / 4, n4_conv = a.conv_elems / 4;
-    const float4 *src_s = reinterpret_cast<const float4 *>(a.cap_state + (size_t(s) * a.T + accepted_idx) * a.state_elems);
-    float4 *dst_s = reinterpret_cast<float4 *>(a.state + size_t(s) * a.state_elems);
+    const float4 *src_s = reinterpret_cast<const float4 *>(cap_state + (size_t(s) * a.T + accepted_idx) * a.state_elems);
+    float4 *dst_s = reinterpret_cast<float4 *>(state + size_t(s) * a.state_elems);
     // chain: window rows accepted_idx + 1 .. + W-1; tree: the node's own conv state
     const float4 *src_c = reinterpret_cast<const float4 *>(
-        a.tree ? a.cap_conv + (size_t(s) * a.T + accepted_idx) * a.W1 * a.C
-               : a.cap_conv + (size_t(s) * (a.W1 + a.T) + accepted_idx + 1) * a.C);
-    float4 *dst_c = reinterpret_cast<float4 *>(a.conv_state + size_t(s) * a.conv_elems);
+        a.tree ? cap_conv + (size_t(s) * a.T + accepted_idx) * a.W1 * a.C
+               : cap_conv + (size_t(s) * (a.W1 + a.T) + accepted_idx + 1) * a.C);
+    float4 *dst_c = reinterpret_cast<float4 *>(conv_state + size_t(s) * a.conv_elems);
 
     const long long total = n4_state + n4_conv;
     const long long stride = (long long)gridDim.x * kThreads;
@@ -71,19 +90,19 @@ __global__ void __launch_bounds__(kThreads) rollback_kernel(const RollbackArgs a
         float4 v[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
-            v[u] = chk(src_s + i + u * stride, 16, a.cap_state, a.ext_cap_state) ? ld_nc4(src_s + i + u * stride)
-                                                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[u] = chk(src_s + i + u * stride, 16, cap_state, a.ext_cap_state) ? ld_nc4(src_s + i + u * stride)
+                                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
-            if (chk(dst_s + i + u * stride, 16, a.state, a.ext_state)) dst_s[i + u * stride] = v[u];
+            if (chk(dst_s + i + u * stride, 16, state, a.ext_state)) dst_s[i + u * stride] = v[u];
     }
     for (; i < total; i += stride) {
         if (i < n4_state) {
-            if (chk(src_s + i, 16, a.cap_state, a.ext_cap_state) && chk(dst_s + i, 16, a.state, a.ext_state))
+            if (chk(src_s + i, 16, cap_state, a.ext_cap_state) && chk(dst_s + i, 16, state, a.ext_state))
                 dst_s[i] = ld_nc4(src_s + i);
         } else {
             const long long j = i - n4_state;
-            if (chk(src_c + j, 16, a.cap_conv, a.ext_cap_conv) && chk(dst_c + j, 16, a.conv_state, a.ext_conv_state))
+            if (chk(src_c + j, 16, cap_conv, a.ext_cap_conv) && chk(dst_c + j, 16, conv_state, a.ext_conv_state))
                 dst_c[j] = ld_nc4(src_c + j);
         }
     }
@@ -98,7 +117,7 @@ cudaError_t launch_rollback(const RollbackArgs &a, cudaStream_t stream) {
     if (per_slot < 1) per_slot = 1;
     if (per_slot > 65535) per_slot = 65535;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(per_slot), unsigned(a.B), 1);
+    cfg.gridDim = dim3(unsigned(per_slot), unsigned(a.B), unsigned(a.tab_state ? a.n_layers : 1));
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

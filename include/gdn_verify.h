@@ -134,6 +134,23 @@ int gdn_rollback(const gdn_dims *dims, const int32_t *d_trim, float *state, floa
                  const float *cap_state, const float *cap_conv, int *d_status, void *stream);
 
 /*
+ * gdn_rollback of n_layers layers in one launch, with the same trims: the
+ * target cache keeps one DeltaNetCapture per DeltaNet layer (internal.h,
+ * Target cache, create_target_cache), and a serving step rolls every layer
+ * back once the verify of the whole pass has decided how many tokens each
+ * slot accepted (hf2q qwen35_target.rs, rollback_kv).  d_state,
+ * d_conv_state, d_cap_state and d_cap_conv are DEVICE arrays of n_layers
+ * pointers (8-byte aligned), entry l being layer l's buffer as gdn_rollback
+ * takes it (same dims for every layer); the tables are read on the device, so
+ * the call can sit in a CUDA graph.  Per layer and slot exactly gdn_rollback
+ * (bit-identical); a table entry that is NULL or not 16-byte aligned skips
+ * that layer and writes GDN_ERR_ARG to *d_status.  The caller owns the tables.
+ */
+int gdn_rollback_layers(const gdn_dims *dims, int n_layers, const int32_t *d_trim, float *const *d_state,
+                        float *const *d_conv_state, const float *const *d_cap_state, const float *const *d_cap_conv,
+                        int *d_status, void *stream);
+
+/*
  * Tree (DDTree) verify: the T = dims->n_tokens tokens of each slot form a
  * draft tree in token order (internal.h, Target forward graph:
  * QwenGraphInputs::parent_ids, "tree mode when non-null"; the capture is sized
