@@ -66,6 +66,19 @@ def run_all() -> dict:
         gdn.gdn_rollback_tree(d, acc, xt["state"], xt["conv_state"], ot["cap_state"], cap_conv_t, status)
         keep(name + ".tree", out=ot["out"], cap_state=ot["cap_state"], cap_conv=cap_conv_t, state=xt["state"],
              conv_state=xt["conv_state"])
+        # two layers verified, then rolled back in one launch from device pointer tables
+        lay = []
+        for li in range(2):
+            xl = upload(make_inputs(shape, layer=li + 1))
+            ol = empty_outputs(shape, "cuda")
+            gdn.gdn_verify_forward(d, params_of(xl), xl["qkv"], xl["z"], xl["alpha"], xl["beta_raw"], xl["state"],
+                                   xl["conv_state"], ol["cap_state"], ol["cap_conv"], ol["out"], status)
+            lay.append((xl, ol))
+        tabs = [gdn.pointer_table([xl["state"] for xl, _ in lay]), gdn.pointer_table([xl["conv_state"] for xl, _ in lay]),
+                gdn.pointer_table([ol["cap_state"] for _, ol in lay]), gdn.pointer_table([ol["cap_conv"] for _, ol in lay])]
+        gdn.gdn_rollback_layers(d, 2, trims, *tabs, status)
+        for li, (xl, _) in enumerate(lay):
+            keep(f"{name}.layers{li}", state=xl["state"], conv_state=xl["conv_state"])
 
     # the layer step with its projections
     shape = _shape(n_v_heads=8, d_k=64, d_v=64, n_embd=256)
