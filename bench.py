@@ -234,7 +234,7 @@ def recorded_traffic(kernel: str, sha: str, workload: str):
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_power_cap,clocks.mem,clocks.max.mem,temperature.memory")
 
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
@@ -247,8 +247,14 @@ class ClockSampler:
         if len(parts) < 8:
             return None
         try:
-            return {"sm": float(parts[0]), "max": float(parts[1]), "hw": parts[4], "hw_thermal": parts[5],
-                    "sw_thermal": parts[6], "sw_power": parts[7], "t": time.time()}
+            s = {"sm": float(parts[0]), "max": float(parts[1]), "hw": parts[4], "hw_thermal": parts[5],
+                 "sw_thermal": parts[6], "sw_power": parts[7], "t": time.time()}
+            for key, i in (("mem", 8), ("mem_max", 9), ("mem_temp", 10)):     # context: HBM clock, temperature
+                try:
+                    s[key] = float(parts[i])
+                except (IndexError, ValueError):
+                    pass
+            return s
         except ValueError:
             return None
 
@@ -299,9 +305,14 @@ class ClockSampler:
                               ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
                 if s[key].lower().startswith("active"):
                     reasons.add(name)
-        return {"sm_mhz": float(np.median([s["sm"] for s in inside])),
-                "sm_max_mhz": float(max(s["max"] for s in inside)), "reasons": sorted(reasons),
-                "samples": len(inside)}
+        res = {"sm_mhz": float(np.median([s["sm"] for s in inside])),
+               "sm_max_mhz": float(max(s["max"] for s in inside)), "reasons": sorted(reasons),
+               "samples": len(inside)}
+        for key, name in (("mem", "mem_mhz"), ("mem_max", "mem_max_mhz"), ("mem_temp", "mem_temp_c")):
+            vals = [s[key] for s in inside if key in s]
+            if vals:
+                res[name] = float(np.median(vals)) if key != "mem_max" else float(max(vals))
+        return res
 
 
 # ---------------------------------------------------------------------------
