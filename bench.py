@@ -555,7 +555,9 @@ class VerifyWorkload:
         A multi-layer chain step runs as a serving step would: the verify of every
         layer, the outputs back to the host and a host synchronisation (the accepted
         lengths are decided there), then the trims host -> device and the rollback
-        of every layer."""
+        of every layer.  With several layers the copies are pipelined on a second
+        stream: layer l's inputs go host -> device while the layers before it run,
+        and its outputs come back while the layers after it run."""
         torch = self.torch
         from workloads.device import act_host
         s = self.shape
@@ -606,7 +608,40 @@ class VerifyWorkload:
             for li in range(self.layers):
                 xs[li]["trim"] = dev_trim
 
+        # per-layer byte ranges of the staging buffers (the inputs are laid out layer by layer)
+        in_rng = []
+        for li in range(self.layers):
+            offs = [(off, t.numel() * t.element_size()) for (l2, _, t), off in zip(ins, in_offs) if l2 == li]
+            in_rng.append((min(o for o, _ in offs), max(o + n for o, n in offs)))
+        out_rng = [(off, off + ref.numel() * ref.element_size()) for ref, off in zip(outs_ref, out_offs)]
+        copy_stream = torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(self.layers)]
+        ev_done = [torch.cuda.Event() for _ in range(self.layers)]
+
+        def one_pipelined(k):
+            with torch.cuda.stream(copy_stream):
+                for li, (a, b) in enumerate(in_rng):
+                    dev_in[a:b].copy_(host_in[a:b], non_blocking=True)
+                    ev_in[li].record(copy_stream)
+            for li in range(self.layers):
+                stream.wait_event(ev_in[li])
+                self.verify(0, li, sp, xs[li])
+                if not split_rollback:
+                    self.rollback(0, li, sp, xs[li])
+                ev_done[li].record(stream)
+                copy_stream.wait_event(ev_done[li])
+                with torch.cuda.stream(copy_stream):
+                    a, b = out_rng[li]
+                    host_out[a:b].copy_(dev_out[a:b], non_blocking=True)
+            copy_stream.synchronize()
+            if split_rollback:
+                dev_trim.copy_(host_trim, non_blocking=True)
+                self.rollback_all(0, 0, sp, trim=dev_trim)
+
         def one(k):
+            if self.layers > 1:
+                one_pipelined(k)
+                return
             dev_in.copy_(host_in, non_blocking=True)
             if split_rollback:
                 for li in range(self.layers):
