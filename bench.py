@@ -817,7 +817,8 @@ def describe(shape) -> str:
 # steps a per-config entry times at least (about 10 ms of device work or more)
 MIN_STEPS = {"layer_verify": 1000, "multislot_verify": 64, "prefill": 20, "proj_verify": 500}
 HEADLINE = "stack_verify"                                   # 48 layers x 8 slots: the largest configuration
-# configs 1, 2 and 4, and the layer with its projections around the block (hidden 5120, the library's GEMM)
+# one layer at one slot, 32 slots, the 8192-token prefill, and the layer with its projections around the block
+# (hidden 5120, the library's GEMM)
 PER_CONFIG = ("layer_verify", "multislot_verify", "prefill", "proj_verify")
 
 
@@ -1213,8 +1214,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
-                    help="time only the chosen workload (by default the headline also times configs 1, 2, 4 and "
-                         "the layer with its projections)")
+                    help="time only the chosen workload (by default the headline also times one slot, 32 slots, "
+                         "the prefill and the layer with its projections)")
     ap.add_argument("--slots", type=int, default=0, help="override the workload's slot count (profiling cases)")
     ap.add_argument("--profile", type=int, default=0, metavar="K",
                     help="run K untimed eager steps and exit (for ncu captures)")
