@@ -13,6 +13,7 @@
 
 namespace gdn {
 size_t verify_smem_bytes(int Tm, int T, int dk, int dv, int P, int act_bytes, bool tree);
+int verify_part_rows(int dv, int P);
 }  // namespace gdn
 
 namespace {
@@ -78,9 +79,12 @@ int check_params(const gdn_layer_params *p) {
 
 namespace gdn {
 
-// CTAs per value head: as many as the cluster allows (portable size 8) while a
-// CTA keeps at most 8 consumer warps of 8 rows; more CTAs spread a small
-// batch over more SMs.
+// CTAs per value head: as many equal parts (a power of two) as the cluster
+// allows (portable size 8) while a CTA keeps at most 8 warps of 8 rows; more
+// CTAs spread a small batch over more SMs.  Failing that, equal parts within a
+// non-portable cluster of up to 16; failing that (d_v/8 warps with no such
+// divisor, e.g. 9 or 30), the fewest parts of unequal width (floor or ceil of
+// d_v/8 / P warps) that keep a CTA at 8 warps and the cluster at 16.
 int verify_parts_per_head(int B, int Hv, int r, int dv, int sm_count) {
     (void)B; (void)Hv; (void)sm_count;
     const int warps_head = dv / 8;
@@ -95,7 +99,8 @@ int verify_parts_per_head(int B, int Hv, int r, int dv, int sm_count) {
         if (warps_head % P || warps_head / P > 8) continue;
         if (r * P <= 16) return P;
     }
-    return 0;
+    const int P = (warps_head + 7) / 8;
+    return r * P <= 16 ? P : 0;
 }
 
 }  // namespace gdn
@@ -201,7 +206,9 @@ static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, con
     const int r = d.n_v_heads / d.n_qk_heads;
     const DevInfo info = dev_info();
     const int P = gdn::verify_parts_per_head(d.n_slots, d.n_v_heads, r, d.d_v, info.sms);
-    if (P == 0) return fail(GDN_ERR_SHAPE, "H_v/H_k = %d is too large for one thread-block cluster", r);
+    if (P == 0)
+        return fail(GDN_ERR_SHAPE, "H_v/H_k = %d heads of d_v = %d need more than 16 CTAs per thread-block cluster "
+                    "(at most 8 warps of 8 value rows per CTA)", r, d.d_v);
     const int act_bytes = d.act_dtype == GDN_BF16 ? 2 : 4;
     // a lazy verify with a pending batch runs up to 2T tokens through shared memory
     const int Tm = pending ? 2 * d.n_tokens : d.n_tokens;
@@ -242,7 +249,9 @@ static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, con
         a.ext_parent = M * 4;
         a.ext_trim = size_t(d.n_slots) * 4;
     }
-    {   // the batch's activations as 2-D tensors for the kernel's TMA boxes (T tokens of a slot per box)
+    {   // the batch's activations as 2-D tensors for the kernel's TMA boxes (T tokens of a slot per box); the v
+        // and z boxes are as wide as the widest part of a head (the last), so a narrower part also reads the
+        // first rows of the next part of its own head
         PFN_cuTensorMapEncodeTiled_v12000 encode = gdn::tensor_map_encoder();
         if (!encode) return fail(GDN_ERR_LAUNCH, "the driver's tensor-map encoder is unavailable");
         const CUtensorMapDataType dt = d.act_dtype == GDN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -258,8 +267,8 @@ static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, con
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
         };
         if (!make(&a.qk_map, qkv, cuuint64_t(a.C), a.ld_qkv, d.d_k) ||
-            !make(&a.v_map, qkv, cuuint64_t(a.C), a.ld_qkv, d.d_v / P) ||
-            (z && !make(&a.z_map, z, cuuint64_t(d.n_v_heads) * d.d_v, a.ld_z, d.d_v / P)))
+            !make(&a.v_map, qkv, cuuint64_t(a.C), a.ld_qkv, gdn::verify_part_rows(d.d_v, P)) ||
+            (z && !make(&a.z_map, z, cuuint64_t(d.n_v_heads) * d.d_v, a.ld_z, gdn::verify_part_rows(d.d_v, P))))
             return fail(GDN_ERR_LAUNCH, "encoding the activation tensor maps failed");
     }
     cudaError_t e = gdn::launch_verify(a, d.act_dtype, static_cast<cudaStream_t>(stream));

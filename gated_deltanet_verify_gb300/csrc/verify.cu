@@ -8,8 +8,12 @@
 // Work decomposition
 //   * A thread-block cluster covers one (slot, key-head group): the r = H_v/H_k
 //     value heads that share key head kh, each split into P CTAs along d_v.
-//     Columns j of S (value dims) evolve independently, so a CTA owns d_v/P
-//     of them; only the per-head RMSNorm needs all d_v.  Its partial sums are
+//     Columns j of S (value dims) evolve independently, so a CTA owns a part
+//     of them: the head's d_v/8 warps of 8 rows are dealt out in P contiguous
+//     parts of floor or ceil(d_v/8 / P) warps (unequal when P does not divide
+//     them; the block has the widest part's warps and a narrower part leaves
+//     its last warp idle in the recurrence); only the per-head RMSNorm needs
+//     all d_v.  Its partial sums are
 //     exchanged through distributed shared memory inside the cluster; the
 //     q/k conv channels are read by every CTA of the group, and the cluster
 //     also orders their in-place conv_state rewrite after all those reads.
@@ -234,7 +238,9 @@ struct Smem {
     int NCH;
     size_t xq_p, xq_c, xk_p, xk_c, xv_p, xv_c, zs, cw, cs, nw, ys, os, gs, bs, kqs, rinv, allp, redbar, loadbar, arow,
         total;
-    __host__ __device__ Smem(int Tm, int Tb, int dk, int rows, int warps, int P, int act_bytes, bool tree)
+    // rows: the widest part's rows (the stride of the per-CTA row tables, the TMA box width); head_warps: the
+    // warps of a whole head (the RMSNorm partials of every part land in every CTA of the head)
+    __host__ __device__ Smem(int Tm, int Tb, int dk, int rows, int head_warps, int act_bytes, bool tree)
         : NCH(2 * dk + rows) {
         size_t off = 0;
         auto take = [&](size_t bytes) {
@@ -263,7 +269,7 @@ struct Smem {
         bs = take(size_t(Tm) * 4);
         kqs = take(size_t(Tm) * 4);
         rinv = take(size_t(Tm) * 4);
-        allp = take(size_t(Tm) * P * warps * 4);    // per-warp sums of o^2 of the whole head
+        allp = take(size_t(Tm) * head_warps * 4);   // per-warp sums of o^2 of the whole head
         redbar = take(8);                           // all RMSNorm partials of the head arrived
         loadbar = take(8);                          // the batch's activation boxes landed
         arow = take(tree ? size_t(Tm) * 5 * 4 : 0); // tree: parent and the window row of each conv tap
@@ -286,16 +292,21 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
 
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, wid = tid >> 5;
-    const int WARPS = nthr >> 5;
-    const int ROWS = WARPS * kRowsPerWarp;
+    const int WARPS = nthr >> 5;                               // warps of the widest part (the block)
+    const int ROWS = WARPS * kRowsPerWarp;                     // its rows: the stride of the row tables
     const int T = a.T, Hv = a.Hv, Hk = a.Hk, DV = a.dv, C = a.C, P = a.P;
+    const int HW = DV / kRowsPerWarp;                          // warps of a whole head
     const int s = blockIdx.y;
     const int h = blockIdx.x / P, p = blockIdx.x % P;
     const int kh = h / a.r;
-    const int j0 = p * ROWS;                                   // first value row of this CTA
+    const int w0 = (p * HW) / P;                               // this part: head warps w0 .. w0 + MYW - 1
+    const int MYW = ((p + 1) * HW) / P - w0;
+    const int MY_ROWS = MYW * kRowsPerWarp;
+    const bool active = wid < MYW;                             // warp-uniform: owns rows in the recurrence
+    const int j0 = w0 * kRowsPerWarp;                          // first value row of this CTA
     const bool qk_writer = (h % a.r == 0) && (p == 0);        // writes the shared q/k conv channels
 
-    const Smem L(LAZY ? a.Tm : T, T, DK, ROWS, WARPS, P, sizeof(Act), TREE);   // only a lazy launch holds 2T
+    const Smem L(LAZY ? a.Tm : T, T, DK, ROWS, HW, sizeof(Act), TREE);   // only a lazy launch holds 2T
     Act *zs = reinterpret_cast<Act *>(smem_raw + L.zs);
     float *cw = reinterpret_cast<float *>(smem_raw + L.cw);
     float *cs = reinterpret_cast<float *>(smem_raw + L.cs);
@@ -315,7 +326,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
     auto chk = [&](const void *ptr, size_t bytes, const void *base, size_t ext) -> bool {
         return in_bounds(ptr, bytes, base, ext, a.d_status);
     };
-    const int NCH = L.NCH;
+    const int NCH = L.NCH;                      // channel stride of the conv tables (widest part)
+    const int MY_NCH = 2 * DK + MY_ROWS;        // channels of this CTA: q, k of the key head, its own v rows
 
     // local channel c -> global conv channel
     auto gchan = [&](int c) -> int {
@@ -347,7 +359,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
         mbar_init(loadbar, 1);
         fence_mbarrier_init_cluster();
         // the single arrival; the phase completes once every partial of the head has landed
-        mbar_arrive_expect_tx(redbar, uint32_t(T * P * WARPS * 4));
+        mbar_arrive_expect_tx(redbar, uint32_t(T * HW * 4));
     }
     {
         // while the previous kernel finishes: L2 prefetch of this CTA's state rows (for a rolled verify the
@@ -362,7 +374,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
             tr = tr < 0 ? 0 : (tr >= T ? T - 1 : tr);
             st = a.cap_state + ((size_t(s) * T + (T - 1 - tr)) * Hv + h) * DV * DK + size_t(j0) * DK;
         }
-        const int st_lines = ROWS * DK * 4 / kLine;
+        const int st_lines = MY_ROWS * DK * 4 / kLine;
         for (int i = tid; i < st_lines; i += nthr) {
             const char *line = reinterpret_cast<const char *>(st) + size_t(i) * kLine;
             if (chk(line, 1, st_base, st_ext)) prefetch_l2(line);
@@ -421,7 +433,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
     const int my_kind = (b & NV) ? 1 : 0;                       // after the reduce-scatter
     const int my_rho = (b >> 1) & (RPG - 1);
     float S[RPG][NCL][4];
-    {
+    if (!active) {
+#pragma unroll
+        for (int rho = 0; rho < RPG; ++rho)
+#pragma unroll
+            for (int m = 0; m < NCL; ++m) S[rho][m][0] = S[rho][m][1] = S[rho][m][2] = S[rho][m][3] = 0.f;
+    } else {
         const float *src = ROLLED ? a.cap_state + ((size_t(s) * T + src_tok) * Hv + h) * DV * DK +
                                         size_t(j0 + row0) * DK + 4 * b
                                   : a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b;
@@ -449,7 +466,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
     }
     {
         constexpr int kPer16 = 16 / sizeof(Act);
-        const int vq = DK / kPer16, vv = ROWS / kPer16;     // 16-byte vectors per segment
+        const int vq = DK / kPer16, vv = MY_ROWS / kPer16;  // 16-byte vectors per segment
         const int per_t = 2 * vq + vv;                      // q, k, v of a pending token
         const Act *qkv = static_cast<const Act *>(a.qkv_prev);
         for (int i = tid; i < n_prev * per_t; i += nthr) {
@@ -470,7 +487,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
             if (chk(src, 16, qkv, a.ext_qkv)) cp_async16(dst, src);
         }
         // conv weights (4 rows) and old conv state (3 rows), per segment in float4s
-        const int fq = DK / 4, fv = ROWS / 4, per_row = 2 * fq + fv;
+        const int fq = DK / 4, fv = MY_ROWS / 4, per_row = 2 * fq + fv;
         for (int i = tid; i < 7 * per_row; i += nthr) {
             const int rrow = i / per_row, w = i % per_row;
             const int c0 = w < fq ? w * 4 : (w < 2 * fq ? DK + (w - fq) * 4 : 2 * DK + (w - 2 * fq) * 4);
@@ -487,7 +504,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
             }
         }
         if constexpr (!COMMIT)
-            for (int i = tid; i < ROWS / 4; i += nthr)
+            for (int i = tid; i < MY_ROWS / 4; i += nthr)
                 if (chk(a.norm_w + j0 + i * 4, 16, a.norm_w, a.ext_norm_w)) cp_async16(nw + i * 4, a.norm_w + j0 + i * 4);
     }
     // (3) gates for this head, one token per thread
@@ -595,8 +612,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
         }
     }
     // v: four channels of one token per item
-    for (int i = tid; i < TT * (ROWS / 4); i += nthr) {
-        const int t = i / (ROWS / 4), c = 2 * DK + 4 * (i % (ROWS / 4));
+    for (int i = tid; i < TT * (MY_ROWS / 4); i += nthr) {
+        const int t = i / (MY_ROWS / 4), c = 2 * DK + 4 * (i % (MY_ROWS / 4));
         float4 acc;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -616,7 +633,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
         const size_t cap_token_stride = size_t(Hv) * DV * DK;
         const float q_scale = a.q_scale;
 
-        for (int t = 0; t < TT; ++t) {
+        for (int t = 0; t < TT && active; ++t) {
             if constexpr (TREE) {
                 // the token runs from its parent's state: already in registers when the parent is t-1,
                 // else this thread's own rows of the parent's capture (or of the state before the batch)
@@ -720,7 +737,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
             // conv state after each node: the window rows of its taps 1, 2, 3, channels this CTA owns (a large
             // store burst, measured to be better issued before the RMSNorm exchange)
             const int c_first = qk_writer ? 0 : 2 * DK;
-            const int n4 = (NCH - c_first) / 4;
+            const int n4 = (MY_NCH - c_first) / 4;
             float *base = a.cap_conv + size_t(s) * T * 3 * C;
             for (int i = tid; i < T * 3 * n4; i += nthr) {
                 const int t = i / (3 * n4), rr = (i / n4) % 3, c = c_first + 4 * (i % n4);
@@ -730,7 +747,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
         }
         __syncwarp();
         cluster_wait_acquire();            // phase 1: every peer's mbarrier is initialised, every old conv row read
-        if constexpr (!COMMIT) {
+        if (!COMMIT && active) {
             // this warp's sums of o^2 per token, sent to the allp table of every CTA of this head
             const int first_rank = (h - kh * a.r) * P;
             const uint32_t allp_local = smem_u32(allp);
@@ -741,7 +758,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
 #pragma unroll
                 for (int r = 1; r < kRowsPerWarp; ++r) acc = fmaf(o[r], o[r], acc);
                 const uint32_t rank = uint32_t(first_rank + dst_p);
-                const uint32_t off = uint32_t((size_t(t) * P * WARPS + p * WARPS + wid) * 4);
+                const uint32_t off = uint32_t((size_t(t) * HW + w0 + wid) * 4);   // slot: warp of the head
                 st_async_f32(map_cluster(allp_local + off, rank), acc, map_cluster(redbar, rank));
             }
         }
@@ -749,7 +766,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
             // conv window capture: concat(old conv state, new tokens) of the channels this CTA owns (a rolled
             // verify read its old conv rows from these very rows: after cluster phase 1 like everything here)
             const int c_first = qk_writer ? 0 : 2 * DK;
-            const int n4 = (NCH - c_first) / 4;
+            const int n4 = (MY_NCH - c_first) / 4;
             float *base = a.cap_conv + size_t(s) * (3 + T) * C;
             for (int i = tid; i < (3 + T) * n4; i += nthr) {
                 const int rho = i / n4, c = c_first + 4 * (i % n4);
@@ -757,7 +774,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
                 if (chk(q, 16, a.cap_conv, a.ext_cap_conv)) store4(q, win4(rho, c));
             }
         }
-        if constexpr (!TREE && !LAZY) {    // a tree or lazy verify leaves the state as it was
+        if (!TREE && !LAZY && active) {    // a tree or lazy verify leaves the state as it was
             float *dst = a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b;
 #pragma unroll
             for (int rho = 0; rho < RPG; ++rho)
@@ -774,7 +791,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
     if constexpr (COMMIT) {
         // conv state <- window rows TT .. TT+2 (after cluster phase 1: every reader is done)
         const int c_first = qk_writer ? 0 : 2 * DK;
-        const int n4 = (NCH - c_first) / 4;
+        const int n4 = (MY_NCH - c_first) / 4;
         float *base = a.conv_state + size_t(s) * 3 * C;
         for (int i = tid; i < 3 * n4; i += nthr) {
             const int rr = i / n4, c = c_first + 4 * (i % n4);
@@ -786,15 +803,15 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
     if (tid < T) {
         mbar_wait_cluster(redbar, 0, a.d_status);   // every partial of this head has landed
         const int t = tid;
-        const float *ap = allp + size_t(t) * P * WARPS;
+        const float *ap = allp + size_t(t) * HW;
         float tot = 0.f;
-        for (int i = 0; i < P * WARPS; ++i) tot += ap[i];              // head-level warp order: fixed
+        for (int i = 0; i < HW; ++i) tot += ap[i];                     // head-level warp order: fixed
         rinv[t] = 1.0f / sqrtf(tot / float(DV) + a.rms_eps);
     }
     __syncthreads();
     {
         Act *out = static_cast<Act *>(a.out);
-        const int n4 = ROWS / 4;
+        const int n4 = MY_ROWS / 4;
         for (int i = tid; i < T * n4; i += nthr) {
             const int t = i / n4, c = 4 * (i % n4);
             const float4 zz = load4(zs + size_t(t) * ROWS + c);
@@ -810,7 +827,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
     if (LAZY && n_prev > 0) {
         // conv state after the committed tokens: window rows n_prev .. n_prev+2 (after cluster phase 1)
         const int c_first = qk_writer ? 0 : 2 * DK;
-        const int n4 = (NCH - c_first) / 4;
+        const int n4 = (MY_NCH - c_first) / 4;
         float *base = a.conv_state + size_t(s) * 3 * C;
         for (int i = tid; i < 3 * n4; i += nthr) {
             const int rr = i / n4, c = c_first + 4 * (i % n4);
@@ -821,7 +838,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
     if constexpr (MODE == kChain || ROLLED) {
         // conv state <- window rows T .. T+2 (after cluster phase 1: every reader is done)
         const int c_first = qk_writer ? 0 : 2 * DK;
-        const int n4 = (NCH - c_first) / 4;
+        const int n4 = (MY_NCH - c_first) / 4;
         float *base = a.conv_state + size_t(s) * 3 * C;
         for (int i = tid; i < 3 * n4; i += nthr) {
             const int rr = i / n4, c = c_first + 4 * (i % n4);
@@ -833,9 +850,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
 
 template <int DK, typename Act, int MODE>
 cudaError_t launch_t(const VerifyArgs &a, cudaStream_t stream) {
-    const int rows = a.dv / a.P;
-    const int warps = rows / kRowsPerWarp;
-    const Smem L(a.Tm, a.T, DK, rows, warps, a.P, sizeof(Act), MODE == kTree);
+    const int head_warps = a.dv / kRowsPerWarp;
+    const int warps = (head_warps + a.P - 1) / a.P;            // the widest part
+    const Smem L(a.Tm, a.T, DK, warps * kRowsPerWarp, head_warps, sizeof(Act), MODE == kTree);
     auto kern = verify_kernel<DK, Act, MODE>;
     // Function attributes belong to the context: the dynamic shared memory limit set so far (raised
     // when a launch needs more) and the non-portable cluster permission are cached per context id,
@@ -884,9 +901,14 @@ cudaError_t launch_t(const VerifyArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
+// rows of the widest of the P parts of a head (the last): the block's warps x 8, the TMA box width
+int verify_part_rows(int dv, int P) {
+    const int head_warps = dv / kRowsPerWarp;
+    return ((head_warps + P - 1) / P) * kRowsPerWarp;
+}
+
 size_t verify_smem_bytes(int Tm, int T, int dk, int dv, int P, int act_bytes, bool tree) {
-    const int rows = dv / P;
-    return Smem(Tm, T, dk, rows, rows / kRowsPerWarp, P, act_bytes, tree).total;
+    return Smem(Tm, T, dk, verify_part_rows(dv, P), dv / kRowsPerWarp, act_bytes, tree).total;
 }
 
 template <int MODE>

@@ -110,7 +110,9 @@ typedef struct {
  * cap_state[:, T-1] equals the new state bit for bit.  If cap_conv is non-NULL
  * it receives the concat(old conv_state, qkv) window (internal.h,
  * conv_input_cache).  Supported: 1 <= T <= 64, d_k in {32,64,128}, d_v % 8 ==
- * 0 and d_v <= 256, H_v/H_k <= 16, W == 4, act_dtype f32 or bf16.
+ * 0 and d_v <= 256, (H_v/H_k) * ceil(d_v / 64) <= 16 (the value heads of a key
+ * head share one thread-block cluster, a CTA holding at most 64 value rows;
+ * GDN_ERR_SHAPE otherwise), W == 4, act_dtype f32 or bf16.
  * d_status may be NULL (the verify kernel reports nothing through it).
  */
 int gdn_verify_forward(const gdn_dims *dims, const gdn_layer_params *params,

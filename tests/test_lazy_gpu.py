@@ -76,6 +76,7 @@ CASES = {
     "T1": (_shape(n_slots=2, n_tokens=1), [0, 0]),
     "T5_dk64_r4": (_shape(n_slots=3, n_tokens=5, d_k=64, d_v=64, n_qk_heads=2, n_v_heads=8), [4, 2, 0]),
     "T64_max": (_shape(n_slots=1, n_tokens=64), [17]),
+    "dv240_unequal": (_shape(n_slots=2, n_tokens=9, d_v=240, n_qk_heads=2, n_v_heads=2), [3, 0]),
 }
 
 

@@ -49,6 +49,7 @@ CASES = {
     "layer": (WORKLOADS["layer_verify"], [[5], [0], [15]]),
     "tiny_f32": (WORKLOADS["tiny"].with_(n_slots=2), [[3, 0], [1, 2]]),
     "T7_dk64_r4": (_shape(n_slots=3, n_tokens=7, d_k=64, d_v=64, n_qk_heads=2, n_v_heads=8), [[6, 0, 3], [1, 5, 2]]),
+    "dv72_unequal": (_shape(n_slots=2, n_tokens=6, d_k=64, d_v=72, n_qk_heads=2, n_v_heads=4), [[5, 1], [0, 3]]),
 }
 
 

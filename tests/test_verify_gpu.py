@@ -50,6 +50,9 @@ CASES = {
     "r4_f32": _shape(n_qk_heads=2, n_v_heads=8, act="f32", n_tokens=9),
     "r8": _shape(d_k=64, d_v=32, n_qk_heads=1, n_v_heads=8, n_tokens=6),
     "r12_nonportable": _shape(d_k=32, d_v=32, n_qk_heads=1, n_v_heads=12, n_tokens=4, n_slots=1),
+    # d_v/8 warps with no power-of-two split of at most 8 warps: parts of unequal width (5 + 4, 8 + 7 + 8 + 7)
+    "dv72_unequal": _shape(d_k=64, d_v=72, n_qk_heads=2, n_v_heads=4, n_tokens=6, n_slots=2),
+    "dv240_unequal": _shape(d_v=240, n_qk_heads=2, n_v_heads=2, n_tokens=11, n_slots=2),
 }
 
 
