@@ -1,5 +1,5 @@
-"""Seeded random shapes through the chain verify, the rollback and the tree
-verify, against the fp64 oracle: slot counts, head counts and ratios, d_k,
+"""Seeded random shapes through the chain verify, the rollback, the tree verify
+and the chunkwise prefill, against the fp64 oracle: slot counts, head counts and ratios, d_k,
 d_v, batch lengths and activation dtypes drawn from everything the verify
 accepts (d_k 32/64/128, d_v a multiple of 8 up to 256, T up to 64, H_v/H_k up
 to 12), so that launch shapes the fixed cases do not reach (parts per head,
@@ -98,3 +98,31 @@ def test_random_shape_verify_rollback_tree(i):
     assert_act_close(to_f64(ot["out"]), rt["out"], shape.act, f"{what} tree out")
     assert_f32_close(to_f64(ot["cap_state"]), rt["cap_state"], f"{what} tree cap_state")
     assert np.array_equal(to_f64(cap_conv_t), rt["cap_conv"]), f"{what} tree cap_conv"
+
+
+N_PREFILL = 8
+
+
+def _draw_prefill(i):
+    rng = np.random.default_rng(5000 + i)
+    hk = int(rng.integers(1, 5))
+    r = int(rng.choice([1, 2, 3, 4, 6, 8]))
+    while hk * r > 24:
+        hk -= 1
+    return Shape(f"fuzz_prefill{i}", n_slots=int(rng.integers(1, 4)), n_qk_heads=hk, n_v_heads=hk * r, d_k=128,
+                 d_v=128, n_tokens=int(rng.integers(1, 400)), act=str(rng.choice(["bf16", "f32"])), seed=6000 + i)
+
+
+@pytest.mark.parametrize("i", range(N_PREFILL))
+def test_random_shape_prefill(i):
+    # the chunkwise prefill (d_k = d_v = 128) on random slot and head counts, ratios and prompt lengths (partial
+    # last chunks, prompts shorter than the conv window) against the sequential oracle
+    from tests.test_prefill_gpu import run_prefill
+    shape = _draw_prefill(i)
+    inp = make_inputs(shape)
+    gpu = run_prefill(shape, upload(inp))
+    ref = oracle.verify(shape, inp.as_f64(), capture=False, n_threads=8)
+    what = f"{shape.name} B{shape.n_slots} Hk{shape.n_qk_heads} Hv{shape.n_v_heads} L{shape.n_tokens} {shape.act}"
+    assert_f32_close(gpu["state"], ref["state"], f"{what} state")
+    assert_act_close(gpu["out"], ref["out"], shape.act, f"{what} out")
+    assert np.array_equal(gpu["conv_state"], ref["conv_state"]), what
