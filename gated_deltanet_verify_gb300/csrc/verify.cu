@@ -800,9 +800,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
         }
         return;
     }
-    if (tid < T) {
-        mbar_wait_cluster(redbar, 0, a.d_status);   // every partial of this head has landed
-        const int t = tid;
+    // one token per thread, in rounds when the block has fewer threads than tokens (one warp of 8 value rows
+    // per CTA with T > 32)
+    if (tid < T) mbar_wait_cluster(redbar, 0, a.d_status);   // every partial of this head has landed
+    for (int t = tid; t < T; t += nthr) {
         const float *ap = allp + size_t(t) * HW;
         float tot = 0.f;
         for (int i = 0; i < HW; ++i) tot += ap[i];                     // head-level warp order: fixed

@@ -42,6 +42,36 @@ def _draw(i):
                  seed=2000 + i)
 
 
+def verify_parts(r, dv):
+    """CTAs per value head the library picks for a ratio r and d_v (its host rule, restated); 0: refused."""
+    w = dv // 8
+    best, p = 0, 1
+    while p <= w:
+        if w % p == 0 and w // p <= 8 and r * p <= 8:
+            best = p
+        p *= 2
+    if best:
+        return best
+    p = 1
+    while p <= w:
+        if w % p == 0 and w // p <= 8 and r * p <= 16:
+            return p
+        p *= 2
+    p = (w + 7) // 8
+    return p if r * p <= 16 else 0
+
+
+def supported_draws(n, first):
+    """n random shapes the verify accepts, drawn from seeds first, first + 1, ..."""
+    out, i = [], first
+    while len(out) < n:
+        s = _draw(i)
+        if verify_parts(s.n_v_heads // s.n_qk_heads, s.d_v):
+            out.append(s)
+        i += 1
+    return out
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _built():
     import __graft_entry__

@@ -8,6 +8,7 @@ import torch
 
 import gated_deltanet_verify_gb300 as gdn
 import oracle
+from tests.test_fuzz_shapes_gpu import supported_draws
 from tests.gpu_util import as_f64, dims_of, params_of, run_verify, upload
 from tests.tolerance import assert_act_close, assert_f32_close
 from workloads.device import empty_outputs, to_f64
@@ -78,6 +79,8 @@ CASES = {
     "T64_max": (_shape(n_slots=1, n_tokens=64), [17]),
     "dv240_unequal": (_shape(n_slots=2, n_tokens=9, d_v=240, n_qk_heads=2, n_v_heads=2), [3, 0]),
 }
+for _s in supported_draws(3, 200):            # random shapes the verify accepts, their own drawn trims
+    CASES[_s.name] = (_s, None)
 
 
 @pytest.mark.parametrize("case", list(CASES))

@@ -7,6 +7,7 @@ import torch
 
 import gated_deltanet_verify_gb300 as gdn
 import oracle
+from tests.test_fuzz_shapes_gpu import supported_draws
 from tests.gpu_util import dims_of, params_of, run_verify, upload
 from tests.tolerance import assert_act_close, assert_f32_close
 from workloads.device import empty_outputs, to_f64
@@ -51,6 +52,9 @@ CASES = {
     "T7_dk64_r4": (_shape(n_slots=3, n_tokens=7, d_k=64, d_v=64, n_qk_heads=2, n_v_heads=8), [[6, 0, 3], [1, 5, 2]]),
     "dv72_unequal": (_shape(n_slots=2, n_tokens=6, d_k=64, d_v=72, n_qk_heads=2, n_v_heads=4), [[5, 1], [0, 3]]),
 }
+for _s in supported_draws(3, 100):            # random shapes the verify accepts, two steps of random trims
+    _rng = np.random.default_rng(_s.seed)
+    CASES[_s.name] = (_s, [[int(t) for t in _rng.integers(0, _s.n_tokens, _s.n_slots)] for _ in range(2)])
 
 
 @pytest.mark.parametrize("case", list(CASES))

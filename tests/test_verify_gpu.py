@@ -53,6 +53,9 @@ CASES = {
     # d_v/8 warps with no power-of-two split of at most 8 warps: parts of unequal width (5 + 4, 8 + 7 + 8 + 7)
     "dv72_unequal": _shape(d_k=64, d_v=72, n_qk_heads=2, n_v_heads=4, n_tokens=6, n_slots=2),
     "dv240_unequal": _shape(d_v=240, n_qk_heads=2, n_v_heads=2, n_tokens=11, n_slots=2),
+    # one warp per CTA (8 value rows) and more tokens than threads: the RMSNorm's per-token sums in rounds
+    "dv16_T53_one_warp": _shape(d_v=16, n_qk_heads=2, n_v_heads=8, n_tokens=53, n_slots=2, act="f32"),
+    "dv8_T64_one_warp": _shape(d_k=64, d_v=8, n_qk_heads=1, n_v_heads=2, n_tokens=64, n_slots=1),
 }
 
 
