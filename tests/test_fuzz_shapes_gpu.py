@@ -156,3 +156,50 @@ def test_random_shape_prefill(i):
     assert_f32_close(gpu["state"], ref["state"], f"{what} state")
     assert_act_close(gpu["out"], ref["out"], shape.act, f"{what} out")
     assert np.array_equal(gpu["conv_state"], ref["conv_state"]), what
+
+
+N_LAYER = 4
+
+
+def _draw_layer(i):
+    rng = np.random.default_rng(7000 + i)
+    while True:
+        hk = int(rng.integers(1, 4))
+        r = int(rng.choice([1, 2, 4, 8]))
+        hv = hk * r
+        dk = int(rng.choice([32, 64, 128]))
+        dv = int(8 * rng.integers(1, 17))
+        if hv % 8 == 0 and verify_parts(r, dv):           # the layer step wants H_v a multiple of 8
+            break
+    return Shape(f"fuzz_layer{i}", n_slots=int(rng.integers(1, 4)), n_qk_heads=hk, n_v_heads=hv, d_k=dk, d_v=dv,
+                 n_tokens=int(rng.integers(1, 17)), act="bf16", seed=8000 + i, n_embd=int(8 * rng.integers(1, 97)))
+
+
+@pytest.mark.parametrize("i", range(N_LAYER))
+def test_random_shape_layer_step(i):
+    # the layer with its projections (hidden size, heads, d_k, d_v, slots, tokens drawn): each stage on its own
+    # GPU input within the verify's bar, as for the fixed layer shapes
+    from tests.test_layer_gpu import _check_act, _run_layer, _upload_proj
+    from workloads.synth import bf16_bits_to_f64, make_proj
+    shape = _draw_layer(i)
+    inp = make_inputs(shape)
+    pr = make_proj(shape)
+    x, p = upload(inp), _upload_proj(pr)
+    y, act, out, cap = _run_layer(shape, x, p)
+    hidden, w_in, w_out = (bf16_bits_to_f64(pr[k]) for k in ("x", "w_in", "w_out"))
+    _check_act(shape, act, hidden, w_in)
+    C, V, H = shape.conv_channels, shape.value_dim, shape.n_v_heads
+    a = to_f64(act).reshape(shape.n_slots, shape.n_tokens, -1)
+    xin = inp.as_f64()
+    xin["qkv"], xin["z"] = a[:, :, :C], a[:, :, C:C + V]
+    xin["alpha"], xin["beta_raw"] = a[:, :, C + V:C + V + H], a[:, :, C + V + H:C + V + 2 * H]
+    ref = oracle.verify(shape, xin, n_threads=8)
+    what = f"{shape.name} B{shape.n_slots} Hk{shape.n_qk_heads} Hv{H} dk{shape.d_k} dv{shape.d_v} T{shape.n_tokens} " \
+           f"E{shape.n_embd}"
+    assert_act_close(to_f64(out), ref["out"], "bf16", f"{what} block output")
+    assert_f32_close(to_f64(x["state"]), ref["state"], f"{what} state")
+    M = shape.n_slots * shape.n_tokens
+    o64 = to_f64(out).reshape(M, -1)
+    y_ref = oracle.project(o64, w_out)
+    bound = 2.0 ** -8 * np.abs(y_ref) + V * 2.0 ** -23 * (np.abs(o64) @ np.abs(w_out).T)
+    assert np.all(np.abs(to_f64(y).reshape(M, -1) - y_ref) <= bound), f"{what} y"

@@ -123,6 +123,9 @@ FUSED = {
     "tiny_f32": (WORKLOADS["tiny"].with_(n_slots=2), [[3, 0], [1, 2], [0, 3]]),
     "T32_dk64": (_shape(n_slots=2, n_tokens=32, d_k=64, d_v=64, n_qk_heads=1, n_v_heads=3), [[31, 0], [9, 20]]),
 }
+for _s in supported_draws(3, 400):            # random shapes the verify accepts, three steps of random trims
+    _rng = np.random.default_rng(_s.seed)
+    FUSED[_s.name] = (_s, [[int(t) for t in _rng.integers(0, _s.n_tokens, _s.n_slots)] for _ in range(3)])
 
 
 @pytest.mark.parametrize("case", list(FUSED))

@@ -5,6 +5,7 @@ import torch
 
 import gated_deltanet_verify_gb300 as gdn
 import oracle
+from tests.test_fuzz_shapes_gpu import supported_draws
 from tests.gpu_util import as_f64, dims_of, params_of, run_verify, upload
 from tests.tolerance import assert_act_close, assert_f32_close
 from workloads.device import act_torch_dtype
@@ -47,6 +48,8 @@ CASES = {
     "random_dk32_tiny": (WORKLOADS["tiny"].with_(n_slots=3, n_tokens=7), "random"),
     "random_dk64": (_shape(d_k=64, d_v=64, seed=66), "random"),
 }
+for _s, _kind in zip(supported_draws(3, 300), ("random", "spine", "star")):   # random shapes the verify accepts
+    CASES[_s.name] = (_s, _kind)
 
 
 @pytest.mark.parametrize("case", list(CASES))
