@@ -31,14 +31,21 @@ def run_all() -> dict:
         for k, v in tensors.items():
             res[f"{prefix}.{k}"] = to_f64(v)
 
-    for name, shape in (("chain", _shape()), ("f32_dk32", _shape(d_k=32, d_v=32, act="f32", n_tokens=4)),
-                        ("dk64_r4", _shape(d_k=64, d_v=64, n_qk_heads=2, n_v_heads=8, n_tokens=5))):
+    from tests.test_fuzz_shapes_gpu import supported_draws
+    shapes = [("chain", _shape()), ("f32_dk32", _shape(d_k=32, d_v=32, act="f32", n_tokens=4)),
+              ("dk64_r4", _shape(d_k=64, d_v=64, n_qk_heads=2, n_v_heads=8, n_tokens=5)),
+              ("dv72_unequal", _shape(d_k=64, d_v=72, n_qk_heads=2, n_v_heads=4, n_tokens=6)),
+              ("dv16_T40_one_warp", _shape(d_v=16, n_qk_heads=2, n_v_heads=8, n_tokens=40, act="f32"))]
+    shapes += [(s.name, s) for s in supported_draws(4, 500)]      # random shapes the verify accepts
+    for name, shape in shapes:
         x = upload(make_inputs(shape))
         o = empty_outputs(shape, "cuda")
         d = dims_of(shape)
         gdn.gdn_verify_forward(d, params_of(x), x["qkv"], x["z"], x["alpha"], x["beta_raw"], x["state"],
                                x["conv_state"], o["cap_state"], o["cap_conv"], o["out"], status)
-        trims = torch.tensor([0, 2, shape.n_tokens - 1][:shape.n_slots], dtype=torch.int32, device="cuda")
+        T = shape.n_tokens
+        trims = torch.tensor([[0, min(2, T - 1), T - 1][b % 3] for b in range(shape.n_slots)], dtype=torch.int32,
+                             device="cuda")
         gdn.gdn_rollback(d, trims, x["state"], x["conv_state"], o["cap_state"], o["cap_conv"], status)
         # the rolled verify from those captures, then a lazy verify committing that batch, then a commit
         y = upload(make_inputs(shape, seed=72))
@@ -62,7 +69,7 @@ def run_all() -> dict:
         par = torch.from_numpy(make_parents(shape, "random", seed=75).astype(np.int32)).to("cuda")
         gdn.gdn_verify_tree(d, params_of(xt), xt["qkv"], xt["z"], xt["alpha"], xt["beta_raw"], par, xt["state"],
                             xt["conv_state"], ot["cap_state"], cap_conv_t, ot["out"], status)
-        acc = torch.tensor([-1, 0, shape.n_tokens - 1][:shape.n_slots], dtype=torch.int32, device="cuda")
+        acc = torch.tensor([[-1, 0, T - 1][b % 3] for b in range(shape.n_slots)], dtype=torch.int32, device="cuda")
         gdn.gdn_rollback_tree(d, acc, xt["state"], xt["conv_state"], ot["cap_state"], cap_conv_t, status)
         keep(name + ".tree", out=ot["out"], cap_state=ot["cap_state"], cap_conv=cap_conv_t, state=xt["state"],
              conv_state=xt["conv_state"])
