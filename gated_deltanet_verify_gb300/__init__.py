@@ -36,8 +36,8 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_A
 GDN_F32 = 0
 GDN_BF16 = 1
 
-EXPORTED_SYMBOLS = ("gdn_verify_forward", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_tree", "gdn_rollback_layers",
-                    "gdn_verify_after_rollback", "gdn_verify_lazy", "gdn_commit_lazy", "gdn_step_io_layout",
+EXPORTED_SYMBOLS = ("gdn_verify_forward", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_tree",
+                    "gdn_rollback_layers", "gdn_rollback_tree_layers", "gdn_verify_after_rollback", "gdn_verify_lazy", "gdn_commit_lazy", "gdn_step_io_layout",
                     "gdn_verify_step_host", "gdn_proj_in_ld", "gdn_layer_workspace_bytes",
                     "gdn_project_in", "gdn_project_out", "gdn_layer_verify", "gdn_prefill_workspace_bytes",
                     "gdn_prefill_chunked", "gdn_prefill_chunked_static", "gdn_prefill_static_scratch_bytes",
@@ -101,6 +101,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_rollback_tree.restype = ip
         L.gdn_rollback_layers.argtypes = [ctypes.POINTER(Dims), ctypes.c_int] + [vp] * 7
         L.gdn_rollback_layers.restype = ip
+        L.gdn_rollback_tree_layers.argtypes = [ctypes.POINTER(Dims), ctypes.c_int] + [vp] * 7
+        L.gdn_rollback_tree_layers.restype = ip
         L.gdn_verify_after_rollback.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(LayerParams)] + [vp] * 12
         L.gdn_verify_after_rollback.restype = ip
         L.gdn_step_io_layout.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(StepIO)]
@@ -197,6 +199,14 @@ def gdn_rollback_layers(dims: Dims, n_layers: int, d_trim, tab_state, tab_conv_s
     _check(lib().gdn_rollback_layers(ctypes.byref(dims), int(n_layers), _ptr(d_trim), _ptr(tab_state),
                                      _ptr(tab_conv_state), _ptr(tab_cap_state), _ptr(tab_cap_conv), _ptr(d_status),
                                      _stream(stream)))
+
+
+def gdn_rollback_tree_layers(dims: Dims, n_layers: int, d_accept, tab_state, tab_conv_state, tab_cap_state,
+                             tab_cap_conv, d_status=None, stream=None) -> None:
+    """gdn_rollback_tree of n_layers layers in one launch; the tab_* are device pointer tables (pointer_table)."""
+    _check(lib().gdn_rollback_tree_layers(ctypes.byref(dims), int(n_layers), _ptr(d_accept), _ptr(tab_state),
+                                          _ptr(tab_conv_state), _ptr(tab_cap_state), _ptr(tab_cap_conv),
+                                          _ptr(d_status), _stream(stream)))
 
 
 def gdn_verify_tree(dims: Dims, params: LayerParams, qkv, z, alpha, beta_raw, d_parent, state, conv_state,

@@ -365,9 +365,9 @@ int gdn_rollback_tree(const gdn_dims *dims, const int32_t *d_accept, float *stat
     return rollback_impl(dims, d_accept, state, conv_state, cap_state, cap_conv, d_status, stream, 1);
 }
 
-int gdn_rollback_layers(const gdn_dims *dims, int n_layers, const int32_t *d_trim, float *const *d_state,
-                        float *const *d_conv_state, const float *const *d_cap_state, const float *const *d_cap_conv,
-                        int *d_status, void *stream) {
+static int rollback_layers_impl(const gdn_dims *dims, int n_layers, const int32_t *d_trim, float *const *d_state,
+                                float *const *d_conv_state, const float *const *d_cap_state,
+                                const float *const *d_cap_conv, int *d_status, void *stream, int tree) {
     g_err.clear();
     int rc = check_common(dims);
     if (rc) return rc;
@@ -388,16 +388,30 @@ int gdn_rollback_layers(const gdn_dims *dims, int n_layers, const int32_t *d_tri
     a.conv_elems = (long long)a.W1 * a.C;
     a.trim = d_trim;
     a.d_status = d_status;
-    a.tree = 0;
+    a.tree = tree;
     a.ext_state = size_t(a.B) * size_t(a.state_elems) * 4;
     a.ext_conv_state = size_t(a.B) * size_t(a.conv_elems) * 4;
     a.ext_cap_state = size_t(a.B) * a.T * size_t(a.state_elems) * 4;
-    a.ext_cap_conv = size_t(a.B) * size_t(a.W1 + a.T) * size_t(a.C) * 4;
+    a.ext_cap_conv = size_t(a.B) * (tree ? size_t(a.T) * a.W1 : size_t(a.W1 + a.T)) * size_t(a.C) * 4;
     a.n_layers = n_layers;
     a.tab_state = d_state; a.tab_conv_state = d_conv_state; a.tab_cap_state = d_cap_state; a.tab_cap_conv = d_cap_conv;
     cudaError_t e = gdn::launch_rollback(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "rollback launch failed: %s", cudaGetErrorString(e));
     return GDN_OK;
+}
+
+int gdn_rollback_layers(const gdn_dims *dims, int n_layers, const int32_t *d_trim, float *const *d_state,
+                        float *const *d_conv_state, const float *const *d_cap_state, const float *const *d_cap_conv,
+                        int *d_status, void *stream) {
+    return rollback_layers_impl(dims, n_layers, d_trim, d_state, d_conv_state, d_cap_state, d_cap_conv, d_status,
+                                stream, 0);
+}
+
+int gdn_rollback_tree_layers(const gdn_dims *dims, int n_layers, const int32_t *d_accept, float *const *d_state,
+                             float *const *d_conv_state, const float *const *d_cap_state,
+                             const float *const *d_cap_conv, int *d_status, void *stream) {
+    return rollback_layers_impl(dims, n_layers, d_accept, d_state, d_conv_state, d_cap_state, d_cap_conv, d_status,
+                                stream, 1);
 }
 
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims) {

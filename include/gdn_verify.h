@@ -186,6 +186,17 @@ int gdn_rollback_tree(const gdn_dims *dims, const int32_t *d_accept, float *stat
                       const float *cap_state, const float *cap_conv, int *d_status, void *stream);
 
 /*
+ * gdn_rollback_tree of n_layers layers in one launch, with the same accepted
+ * nodes: the tables as for gdn_rollback_layers (each layer's cap_conv holding
+ * its per-node conv states, as gdn_verify_tree writes them).  Per layer and
+ * slot exactly gdn_rollback_tree (bit-identical); a bad table entry skips that
+ * layer and writes GDN_ERR_ARG to *d_status.
+ */
+int gdn_rollback_tree_layers(const gdn_dims *dims, int n_layers, const int32_t *d_accept, float *const *d_state,
+                             float *const *d_conv_state, const float *const *d_cap_state,
+                             const float *const *d_cap_conv, int *d_status, void *stream);
+
+/*
  * gdn_verify_after_rollback: a verify step with the previous step's rollback
  * folded in (one launch per step instead of a verify and a rollback).
  * cap_state / cap_conv hold the previous gdn_verify_forward (or

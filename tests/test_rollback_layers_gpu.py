@@ -96,3 +96,31 @@ def test_rollback_layers_host_checks():
                                  None) == gdn.GDN_ERR_ARG
     assert L.gdn_rollback_layers(d, 2, trim.data_ptr(), t.data_ptr(), t.data_ptr(), None, t.data_ptr(), None,
                                  None) == gdn.GDN_ERR_NO_CAPTURE
+
+
+def test_rollback_tree_layers_is_per_layer_tree_rollback_bit_for_bit():
+    from workloads.synth import make_parents
+    d = dims_of(SHAPE)
+    acc = torch.tensor([-1, 0, 3, SHAPE.n_tokens - 1], dtype=torch.int32, device="cuda")   # nothing .. last node
+    layers = []
+    for li in range(LAYERS):
+        x = upload(make_inputs(SHAPE, layer=li))
+        o = empty_outputs(SHAPE, "cuda")
+        cap_conv = torch.empty((SHAPE.n_slots, SHAPE.n_tokens, 3, SHAPE.conv_channels), dtype=torch.float32,
+                               device="cuda")
+        par = torch.from_numpy(make_parents(SHAPE, "random", layer=li).astype("int32")).to("cuda")
+        gdn.gdn_verify_tree(d, params_of(x), x["qkv"], x["z"], x["alpha"], x["beta_raw"], par, x["state"],
+                            x["conv_state"], o["cap_state"], cap_conv, o["out"])
+        layers.append({"state": x["state"], "conv_state": x["conv_state"], "cap_state": o["cap_state"],
+                       "cap_conv": cap_conv})
+    torch.cuda.synchronize()
+    ref = _copy(layers)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for layer in ref:
+        gdn.gdn_rollback_tree(d, acc, layer["state"], layer["conv_state"], layer["cap_state"], layer["cap_conv"],
+                              status)
+    gdn.gdn_rollback_tree_layers(d, LAYERS, acc, *_tables(layers), status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for la, lr in zip(layers, ref):
+        assert torch.equal(la["state"], lr["state"]) and torch.equal(la["conv_state"], lr["conv_state"])
