@@ -169,6 +169,7 @@ def prefill_bytes(s) -> int:
 PREFILL_FLOPS_PER_CHUNK = 2 * (128 * 64 * 128 + 2 * 128 * 64 * 64 + 128 * 64 * 128 + 128 * 64 * 128
                                + 128 * 64 * 64 + 128 * 128 * 64)
 TF32_PER_BF16 = 1.1 / 2.25      # nominal dense tf32 / bf16 tensor rate of the part
+HBM_NOMINAL_GBS = 7900.0        # the part's nominal HBM3e rate (the measured copy rate is the roofline's peak)
 
 
 def prefill_flops(s) -> int:
@@ -921,6 +922,7 @@ def measure(name, steps, warmup, device, world, l2, clocks, with_e2e, graph_len_
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "traffic": traffic, "kernel": dom, "bytes_per_launch": dom_bytes, "launch_us": t_launch * 1e6,
             "launch_us_alone": kdur[dom] * 1e6, "launch_time": how,
+            "frac_of_nominal": achieved / HBM_NOMINAL_GBS, "nominal_gbs": HBM_NOMINAL_GBS,
             "peak_source": f"{peak_kind} hbm_gbs" + (" (MEASURED_PEAKS.json)" if peak_kind == "measured"
                                                      else " (recipe fallback)")}
     if traffic:
