@@ -304,7 +304,11 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
     const int MY_ROWS = MYW * kRowsPerWarp;
     const bool active = wid < MYW;                             // warp-uniform: owns rows in the recurrence
     const int j0 = w0 * kRowsPerWarp;                          // first value row of this CTA
-    const bool qk_writer = (h % a.r == 0) && (p == 0);        // writes the shared q/k conv channels
+    // the q/k conv channels of the key head are read by every CTA of the cluster (its r value heads x P
+    // parts); their stores (conv window or per-node capture, conv state) are dealt out in equal runs of
+    // 4-channel units, CTA (h mod r, p) taking its run besides its own v channels
+    const int crank = (h % a.r) * P + p, csize = a.r * P;
+    const int q_u0 = (crank * (DK / 2)) / csize, q_nu = ((crank + 1) * (DK / 2)) / csize - q_u0;
 
     const Smem L(LAZY ? a.Tm : T, T, DK, ROWS, HW, sizeof(Act), TREE);   // only a lazy launch holds 2T
     Act *zs = reinterpret_cast<Act *>(smem_raw + L.zs);
@@ -328,6 +332,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
     };
     const int NCH = L.NCH;                      // channel stride of the conv tables (widest part)
     const int MY_NCH = 2 * DK + MY_ROWS;        // channels of this CTA: q, k of the key head, its own v rows
+    const int n_own4 = q_nu + MY_ROWS / 4;      // 4-channel units this CTA stores: its q/k run, its v rows
+    auto own_chan = [&](int u) -> int { return u < q_nu ? 4 * (q_u0 + u) : 2 * DK + 4 * (u - q_nu); };
 
     // local channel c -> global conv channel
     auto gchan = [&](int c) -> int {
@@ -633,25 +639,40 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
         const size_t cap_token_stride = size_t(Hv) * DV * DK;
         const float q_scale = a.q_scale;
 
+        // tree: this thread's own rows of a parent's state -- the parent's capture, or the state before
+        // the batch -- for a token whose parent is not the token before it
+        auto parent_rows = [&](int pt, float (&D)[RPG][NCL][4]) {
+            const float *src = pt < 0 ? a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b
+                                      : cap_row + (size_t(s) * T + pt) * cap_token_stride;
+            const float *sbase = pt < 0 ? a.state : a.cap_state;
+            const size_t sext = pt < 0 ? a.ext_state : a.ext_cap_state;
+#pragma unroll
+            for (int rho = 0; rho < RPG; ++rho)
+#pragma unroll
+                for (int m = 0; m < NCL; ++m) {
+                    const float *q = src + size_t(rho) * DK + 4 * LR * m;
+                    const float4 v = chk(q, 16, sbase, sext) ? ld_na4(q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    D[rho][m][0] = v.x; D[rho][m][1] = v.y; D[rho][m][2] = v.z; D[rho][m][3] = v.w;
+                }
+        };
+        // the next token's parent rows, requested one token ahead (the parent is then at most the token
+        // before this one, so this thread stored its capture in an earlier iteration; token 0's parent is
+        // the state before the batch, already in registers)
+        float Sn[TREE ? RPG : 1][TREE ? NCL : 1][4];
+
         for (int t = 0; t < TT && active; ++t) {
             if constexpr (TREE) {
                 // the token runs from its parent's state: already in registers when the parent is t-1,
-                // else this thread's own rows of the parent's capture (or of the state before the batch)
-                const int pt = tpar[t];
-                if (pt != t - 1) {
-                    const float *src = pt < 0 ? a.state + ((size_t(s) * Hv + h) * DV + j0 + row0) * DK + 4 * b
-                                              : cap_row + (size_t(s) * T + pt) * cap_token_stride;
-                    const float *sbase = pt < 0 ? a.state : a.cap_state;
-                    const size_t sext = pt < 0 ? a.ext_state : a.ext_cap_state;
+                // else the rows requested during the previous token
+                if (tpar[t] != t - 1) {
 #pragma unroll
                     for (int rho = 0; rho < RPG; ++rho)
 #pragma unroll
-                        for (int m = 0; m < NCL; ++m) {
-                            const float *q = src + size_t(rho) * DK + 4 * LR * m;
-                            const float4 v = chk(q, 16, sbase, sext) ? ld_na4(q) : make_float4(0.f, 0.f, 0.f, 0.f);
-                            S[rho][m][0] = v.x; S[rho][m][1] = v.y; S[rho][m][2] = v.z; S[rho][m][3] = v.w;
-                        }
+                        for (int m = 0; m < NCL; ++m)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) S[rho][m][e] = Sn[rho][m][e];
                 }
+                if (t + 1 < TT && tpar[t + 1] != t) parent_rows(tpar[t + 1], Sn);
             }
             const float *yt = ys + size_t(t) * NCH;
             const float g = gs[t], beta = bs[t], kq = kqs[t];
@@ -736,11 +757,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
         if constexpr (TREE) {
             // conv state after each node: the window rows of its taps 1, 2, 3, channels this CTA owns (a large
             // store burst, measured to be better issued before the RMSNorm exchange)
-            const int c_first = qk_writer ? 0 : 2 * DK;
-            const int n4 = (MY_NCH - c_first) / 4;
+            const int n4 = n_own4;
             float *base = a.cap_conv + size_t(s) * T * 3 * C;
             for (int i = tid; i < T * 3 * n4; i += nthr) {
-                const int t = i / (3 * n4), rr = (i / n4) % 3, c = c_first + 4 * (i % n4);
+                const int t = i / (3 * n4), rr = (i / n4) % 3, c = own_chan(i % n4);
                 float *q = base + (size_t(t) * 3 + rr) * C + gchan(c);
                 if (chk(q, 16, a.cap_conv, a.ext_cap_conv)) store4(q, win4(trow[t * 4 + 1 + rr], c));
             }
@@ -765,11 +785,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
         if constexpr (!TREE) if (a.cap_conv) {
             // conv window capture: concat(old conv state, new tokens) of the channels this CTA owns (a rolled
             // verify read its old conv rows from these very rows: after cluster phase 1 like everything here)
-            const int c_first = qk_writer ? 0 : 2 * DK;
-            const int n4 = (MY_NCH - c_first) / 4;
+            const int n4 = n_own4;
             float *base = a.cap_conv + size_t(s) * (3 + T) * C;
             for (int i = tid; i < (3 + T) * n4; i += nthr) {
-                const int rho = i / n4, c = c_first + 4 * (i % n4);
+                const int rho = i / n4, c = own_chan(i % n4);
                 float *q = base + size_t(rho) * C + gchan(c);
                 if (chk(q, 16, a.cap_conv, a.ext_cap_conv)) store4(q, win4(rho, c));
             }
@@ -790,11 +809,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
     // ------------------------------------------------------------- epilogue
     if constexpr (COMMIT) {
         // conv state <- window rows TT .. TT+2 (after cluster phase 1: every reader is done)
-        const int c_first = qk_writer ? 0 : 2 * DK;
-        const int n4 = (MY_NCH - c_first) / 4;
+        const int n4 = n_own4;
         float *base = a.conv_state + size_t(s) * 3 * C;
         for (int i = tid; i < 3 * n4; i += nthr) {
-            const int rr = i / n4, c = c_first + 4 * (i % n4);
+            const int rr = i / n4, c = own_chan(i % n4);
             float *q = base + size_t(rr) * C + gchan(c);
             if (chk(q, 16, a.conv_state, a.ext_conv_state)) store4(q, win4(TT + rr, c));
         }
@@ -827,22 +845,20 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
     }
     if (LAZY && n_prev > 0) {
         // conv state after the committed tokens: window rows n_prev .. n_prev+2 (after cluster phase 1)
-        const int c_first = qk_writer ? 0 : 2 * DK;
-        const int n4 = (MY_NCH - c_first) / 4;
+        const int n4 = n_own4;
         float *base = a.conv_state + size_t(s) * 3 * C;
         for (int i = tid; i < 3 * n4; i += nthr) {
-            const int rr = i / n4, c = c_first + 4 * (i % n4);
+            const int rr = i / n4, c = own_chan(i % n4);
             float *q = base + size_t(rr) * C + gchan(c);
             if (chk(q, 16, a.conv_state, a.ext_conv_state)) store4(q, win4(n_prev + rr, c));
         }
     }
     if constexpr (MODE == kChain || ROLLED) {
         // conv state <- window rows T .. T+2 (after cluster phase 1: every reader is done)
-        const int c_first = qk_writer ? 0 : 2 * DK;
-        const int n4 = (MY_NCH - c_first) / 4;
+        const int n4 = n_own4;
         float *base = a.conv_state + size_t(s) * 3 * C;
         for (int i = tid; i < 3 * n4; i += nthr) {
-            const int rr = i / n4, c = c_first + 4 * (i % n4);
+            const int rr = i / n4, c = own_chan(i % n4);
             float *q = base + size_t(rr) * C + gchan(c);
             if (chk(q, 16, a.conv_state, a.ext_conv_state)) store4(q, win4(T + rr, c));
         }
