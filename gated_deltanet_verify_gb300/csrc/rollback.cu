@@ -33,6 +33,14 @@ __device__ __forceinline__ float4 ld_nc4(const float4 *p) {
 }
 
 __global__ void __launch_bounds__(kThreads) rollback_kernel(const RollbackArgs a) {
+    // while the previous kernel finishes: an L2 prefetch of the line holding this slot's trim (and of the
+    // layer's table entries), so that the read after the wait does not go to DRAM; a prefetch returns
+    // nothing to the SM, so a trim the previous kernel is still writing is read correctly below
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.trim + blockIdx.y));
+        if (a.tab_state)
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.tab_state + blockIdx.z));
+    }
     // programmatic dependent launch: wait for the previous kernel's writes (captures, trims); the next
     // kernel may start launching once every block has issued its copies (signalled at the end, so that
     // its CTAs do not take SM slots from the copy blocks still waiting to run)
