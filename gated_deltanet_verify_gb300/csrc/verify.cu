@@ -331,7 +331,6 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
         return in_bounds(ptr, bytes, base, ext, a.d_status);
     };
     const int NCH = L.NCH;                      // channel stride of the conv tables (widest part)
-    const int MY_NCH = 2 * DK + MY_ROWS;        // channels of this CTA: q, k of the key head, its own v rows
     const int n_own4 = q_nu + MY_ROWS / 4;      // 4-channel units this CTA stores: its q/k run, its v rows
     auto own_chan = [&](int u) -> int { return u < q_nu ? 4 * (q_u0 + u) : 2 * DK + 4 * (u - q_nu); };
 
