@@ -271,7 +271,7 @@ static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, con
             (z && !make(&a.z_map, z, cuuint64_t(d.n_v_heads) * d.d_v, a.ld_z, gdn::verify_part_rows(d.d_v, P))))
             return fail(GDN_ERR_LAUNCH, "encoding the activation tensor maps failed");
     }
-    cudaError_t e = gdn::launch_verify(a, d.act_dtype, static_cast<cudaStream_t>(stream));
+    cudaError_t e = gdn::launch_verify(a, d.act_dtype, info.sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(GDN_ERR_LAUNCH, "verify launch failed: %s", cudaGetErrorString(e));
     return GDN_OK;
 }

@@ -87,7 +87,7 @@ struct PrefillArgs {
 };
 
 // Returns a cudaError_t of the launch (cudaSuccess when enqueued).
-cudaError_t launch_verify(const VerifyArgs &a, gdn_dtype act, cudaStream_t stream);
+cudaError_t launch_verify(const VerifyArgs &a, gdn_dtype act, int sm_count, cudaStream_t stream);
 cudaError_t launch_rollback(const RollbackArgs &a, cudaStream_t stream);
 
 // Prefill: shape check (GDN_OK or a status, reason in why), workspace size,

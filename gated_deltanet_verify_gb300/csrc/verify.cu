@@ -277,8 +277,13 @@ struct Smem {
     }
 };
 
-template <int DK, typename Act, int MODE>
-__global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_constant__ VerifyArgs a) {
+// MINB: resident CTAs per SM the register budget is sized for.  Two everywhere; three (80 registers, no
+// spills) for chain and rolled launches with more CTAs than two per SM, where a third resident CTA keeps
+// the SM's stores going while another loads, convolves or normalises (a 48-layer x 8-slot stack layer
+// 77.7 -> 75.2 us).  A launch that fits at two per SM keeps the roomier build (one slot: 17.0 us against
+// 18.3 us under the tighter budget); so does the lazy mode, slower under it at every size.
+template <int DK, typename Act, int MODE, int MINB>
+__global__ void __launch_bounds__(kMaxThreads, MINB) verify_kernel(const __grid_constant__ VerifyArgs a) {
     static_assert(DK == 32 || DK == 64 || DK == 128, "d_k must be 32, 64 or 128");
     constexpr bool TREE = MODE == kTree, LAZY = MODE == kLazy, COMMIT = MODE == kCommit, ROLLED = MODE == kRolled;
     constexpr int LR = DK >= 64 ? 16 : 8;          // lanes per row group
@@ -864,12 +869,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2) verify_kernel(const __grid_con
     }
 }
 
-template <int DK, typename Act, int MODE>
+template <int DK, typename Act, int MODE, int MINB>
 cudaError_t launch_t(const VerifyArgs &a, cudaStream_t stream) {
     const int head_warps = a.dv / kRowsPerWarp;
     const int warps = (head_warps + a.P - 1) / a.P;            // the widest part
     const Smem L(a.Tm, a.T, DK, warps * kRowsPerWarp, head_warps, sizeof(Act), MODE == kTree);
-    auto kern = verify_kernel<DK, Act, MODE>;
+    auto kern = verify_kernel<DK, Act, MODE, MINB>;
     // Function attributes belong to the context: the dynamic shared memory limit set so far (raised
     // when a launch needs more) and the non-portable cluster permission are cached per context id,
     // shared by the host threads under a lock.
@@ -927,24 +932,29 @@ size_t verify_smem_bytes(int Tm, int T, int dk, int dv, int P, int act_bytes, bo
     return Smem(Tm, T, dk, verify_part_rows(dv, P), dv / kRowsPerWarp, act_bytes, tree).total;
 }
 
-template <int MODE>
+template <int MODE, int MINB>
 static cudaError_t launch_mode(const VerifyArgs &a, bool bf, cudaStream_t stream) {
     switch (a.dk) {
-        case 128: return bf ? launch_t<128, __nv_bfloat16, MODE>(a, stream) : launch_t<128, float, MODE>(a, stream);
-        case 64: return bf ? launch_t<64, __nv_bfloat16, MODE>(a, stream) : launch_t<64, float, MODE>(a, stream);
-        case 32: return bf ? launch_t<32, __nv_bfloat16, MODE>(a, stream) : launch_t<32, float, MODE>(a, stream);
+        case 128:
+            return bf ? launch_t<128, __nv_bfloat16, MODE, MINB>(a, stream) : launch_t<128, float, MODE, MINB>(a, stream);
+        case 64:
+            return bf ? launch_t<64, __nv_bfloat16, MODE, MINB>(a, stream) : launch_t<64, float, MODE, MINB>(a, stream);
+        case 32:
+            return bf ? launch_t<32, __nv_bfloat16, MODE, MINB>(a, stream) : launch_t<32, float, MODE, MINB>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_verify(const VerifyArgs &a, gdn_dtype act, cudaStream_t stream) {
+cudaError_t launch_verify(const VerifyArgs &a, gdn_dtype act, int sm_count, cudaStream_t stream) {
     const bool bf = act == GDN_BF16;
+    // more CTAs than two per SM: the three-per-SM build of the chain and rolled modes
+    const bool dense = (long long)a.Hv * a.P * a.B > 2LL * sm_count;
     switch (a.mode) {
-        case kChain: return launch_mode<kChain>(a, bf, stream);
-        case kTree: return launch_mode<kTree>(a, bf, stream);
-        case kLazy: return launch_mode<kLazy>(a, bf, stream);
-        case kCommit: return launch_mode<kCommit>(a, bf, stream);
-        case kRolled: return launch_mode<kRolled>(a, bf, stream);
+        case kChain: return dense ? launch_mode<kChain, 3>(a, bf, stream) : launch_mode<kChain, 2>(a, bf, stream);
+        case kTree: return launch_mode<kTree, 2>(a, bf, stream);
+        case kLazy: return launch_mode<kLazy, 2>(a, bf, stream);
+        case kCommit: return launch_mode<kCommit, 2>(a, bf, stream);
+        case kRolled: return dense ? launch_mode<kRolled, 3>(a, bf, stream) : launch_mode<kRolled, 2>(a, bf, stream);
         default: return cudaErrorInvalidValue;
     }
 }

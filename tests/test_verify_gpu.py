@@ -117,6 +117,22 @@ def test_slot_isolation_bitwise():
             assert np.array_equal(rb[k][0], full[k][b]), (b, k)
 
 
+def test_dense_launch_is_bit_identical_to_one_slot_launches():
+    # 8 slots of the layer shape launch 768 CTAs (more than two per SM: the three-per-SM build of the
+    # kernel); one slot launches 96 (the two-per-SM build).  Every result must be the same bits.
+    shape = WORKLOADS["layer_verify"].with_(n_slots=8, seed=17)
+    inp = make_inputs(shape)
+    x = upload(inp)
+    full = as_f64(run_verify(shape, {k: v.clone() for k, v in x.items()}))
+    one = shape.with_(n_slots=1)
+    for b in (0, 5, 7):
+        xb = {k: (v[b:b + 1].clone() if k in ("qkv", "z", "alpha", "beta_raw", "state", "conv_state", "trim")
+                  else v) for k, v in x.items()}
+        rb = as_f64(run_verify(one, xb))
+        for k in ("state", "conv_state", "out", "cap_state", "cap_conv"):
+            assert np.array_equal(rb[k][0], full[k][b]), (b, k)
+
+
 def _rollback(shape, x, o, trims, status=None):
     d_trim = torch.tensor(trims, dtype=torch.int32, device=x["qkv"].device)
     gdn.gdn_rollback(dims_of(shape), d_trim, x["state"], x["conv_state"], o["cap_state"], o["cap_conv"], status)
