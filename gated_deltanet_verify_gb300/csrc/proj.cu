@@ -15,8 +15,14 @@
 //   * Warp 0 is the TMA producer: each stage holds kKBlk columns of K of the
 //     W tile and of X as 64-column (128-byte) TMA boxes in the 128-byte
 //     swizzled K-major layout the tensor core reads directly.
-//     Warp 1 issues the MMAs (4 per stage) and frees each stage through
-//     tcgen05.commit on the stage's "empty" barrier.
+//     Two threads issue the MMAs (8 per stage), warp 1 the even stages into
+//     one tensor-memory accumulator and warp 2 the odd ones into a second, and
+//     free each stage through tcgen05.commit on its "empty" barrier: one
+//     thread's MMAs follow each other ~150 cycles apart whatever their size
+//     (measured from M = 64, N = 16 to M = 128, N = 256), and two issuing
+//     threads on an SM each keep that pace, so a second issuer doubles the
+//     rate of these N = 16 MMAs.  The epilogue adds the two accumulators in a
+//     fixed order.
 //   * Programmatic dependent launch: the weight tiles of the first stages
 //     are requested before the grid-dependency wait (the weights do not
 //     depend on the previous kernel; X does), so the stream of weights starts
@@ -129,6 +135,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// the same 16 columns summed over the n accumulators (Mt columns apart), in accumulator order
+__device__ __forceinline__ void tmem_ld16_sum(uint32_t taddr, int n, int Mt, float *v) {
+    tmem_ld16(taddr, v);
+    for (int q = 1; q < n; ++q) {
+        float w[16];
+        tmem_ld16(taddr + (uint32_t)(q * Mt), w);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] += w[i];
+    }
+}
 __device__ __forceinline__ uint32_t map_cluster(uint32_t local, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(local), "r"(rank));
@@ -149,7 +165,7 @@ __host__ __device__ inline uint32_t x_stage_bytes(int Mt) { return (uint32_t)Mt 
 
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
-    __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 1];   // full[stages], empty[stages], done
+    __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 1];   // full[stages], empty[stages], done (2 arrivals)
     __shared__ uint32_t tslot;
     const int tid = threadIdx.x, wid = tid >> 5;
     const int nt = blockIdx.x, mb = blockIdx.y, split = blockIdx.z;   // the splits of a tile: one cluster
@@ -166,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
     if (wid == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&tslot)),
-                     "r"(kMaxMt));
+                     "r"(2 * kMaxMt));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
     if (tid == 32) {
@@ -174,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
-        mbar_init(done, 1);
+        mbar_init(done, 2);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     fence_before_sync();
@@ -206,10 +222,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (int b = 0; b < kBoxes; ++b)
                 tma_box(st + wbytes + b * xbox, &a.x_map, (kb0 + i) * kKBlk + 64 * b, m0, full(s));
         }
-    } else if (tid == 32) {
-        // ---- MMA issuer: 4 MMAs of K = 16 per stage; each stage is freed when its MMAs complete
+    } else if (tid == 32 || tid == 64) {
+        // ---- MMA issuers: stages e, e + 2, ... into accumulator e (8 MMAs of K = 16 per stage); each stage is
+        // freed when its MMAs complete
+        const int e = wid - 1;
+        const uint32_t acc = tmem + (uint32_t)(e * a.Mt);
         const uint32_t id = idesc_bf16(a.Mt);
-        for (int i = 0; i < kb1 - kb0 && ok; ++i) {
+        for (int i = e; i < kb1 - kb0 && ok; i += 2) {
             const int s = i % S;
             ok = mbar_wait(full(s), (i / S) & 1);
             fence_after_sync();
@@ -217,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
             for (int j = 0; j < kKBlk / 16; ++j) {          // 16 columns (32 bytes of each row) per MMA
                 const uint32_t b = j >> 2, c = 32u * (j & 3);
-                mma_bf16(tmem, make_desc_sw128(st + b * 16384u + c),
-                         make_desc_sw128(st + wbytes + b * (uint32_t)a.Mt * 128u + c), id, (i > 0 || j > 0) ? 1u : 0u);
+                mma_bf16(acc, make_desc_sw128(st + b * 16384u + c),
+                         make_desc_sw128(st + wbytes + b * (uint32_t)a.Mt * 128u + c), id, (i > e || j > 0) ? 1u : 0u);
             }
             mma_commit(empty(s));
         }
@@ -228,8 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // ---- epilogue: the accumulator of weight row n0 + tid, every activation row of the block
     const bool got = mbar_wait(done, 0);
     fence_after_sync();
-    const bool good = got && ok;
-    if (!good && a.d_status) atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TIMEOUT));
+    // one verdict for the whole CTA (the collective TMEM loads below need every lane of a warp)
+    const bool good = __syncthreads_and(got && ok) != 0;
+    if (!good && tid == 0 && a.d_status) atomicCAS(a.d_status, int(GDN_OK), int(GDN_ERR_TIMEOUT));
+    const int n_acc = kb1 - kb0 > 1 ? 2 : 1;                 // the odd stages' accumulator holds a sum only if used
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int n = n0 + tid;
     const uint32_t taddr = tmem + ((uint32_t)(32 * wid) << 16);
@@ -237,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         if (good)
             for (int c0 = 0; c0 < a.Mt; c0 += 16) {
                 float v[16];
-                tmem_ld16(taddr + c0, v);
+                tmem_ld16_sum(taddr + c0, n_acc, a.Mt, v);
                 if (n < a.N)
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
@@ -252,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const uint32_t dst = map_cluster(sbase, 0) + (uint32_t)((split - 1) * a.Mt * kTileN + tid) * 4u;
             for (int c0 = 0; c0 < a.Mt; c0 += 16) {
                 float v[16];
-                tmem_ld16(taddr + c0, v);
+                tmem_ld16_sum(taddr + c0, n_acc, a.Mt, v);
 #pragma unroll
                 for (int q = 0; q < 16; ++q) st_cluster_f32(dst + (uint32_t)((c0 + q) * kTileN) * 4u, good ? v[q] : 0.f);
             }
@@ -262,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const float *red = reinterpret_cast<const float *>(sm + (sbase - smem_u32(sm)));
             for (int c0 = 0; c0 < a.Mt; c0 += 16) {
                 float v[16];
-                tmem_ld16(taddr + c0, v);
+                tmem_ld16_sum(taddr + c0, n_acc, a.Mt, v);
                 if (n < a.N)
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
@@ -276,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     fence_before_sync();
     __syncthreads();
-    if (wid == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kMaxMt));
+    if (wid == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(2 * kMaxMt));
 }
 
 }  // namespace
