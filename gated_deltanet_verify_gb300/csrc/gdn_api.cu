@@ -182,7 +182,8 @@ static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, con
                        float *conv_state, float *cap_state, float *cap_conv, void *out, int *d_status,
                        void *stream, int mode = gdn::kChain, const int32_t *d_trim = nullptr,
                        const void *qkv_prev = nullptr, const void *alpha_prev = nullptr,
-                       const void *beta_prev = nullptr, long long ld_act = 0) {
+                       const void *beta_prev = nullptr, long long ld_act = 0, const void *l2_next = nullptr,
+                       size_t l2_next_bytes = 0) {
     g_err.clear();
     int rc = check_common(dims);
     if (rc) return rc;
@@ -222,6 +223,8 @@ static int verify_impl(const gdn_dims *dims, const gdn_layer_params *params, con
     a.T = d.n_tokens; a.Ts = d.n_tokens; a.Tm = Tm; a.C = int(conv_channels(&d)); a.r = r; a.P = P;
     a.ld_qkv = a.C; a.ld_z = (long long)d.n_v_heads * d.d_v; a.ld_ab = d.n_v_heads;
     if (ld_act) a.ld_qkv = a.ld_z = a.ld_ab = ld_act;     // column blocks of one activation matrix
+    a.l2_next = l2_next;
+    a.l2_next_bytes = l2_next ? l2_next_bytes : 0;
     a.rms_eps = d.rms_eps; a.l2_eps = d.l2_eps; a.q_scale = d.q_scale;
     a.conv_w = params->conv_w; a.A_log = params->A_log; a.dt_bias = params->dt_bias; a.norm_w = params->norm_w;
     a.qkv = qkv; a.z = z; a.alpha = alpha; a.beta_raw = beta_raw;
@@ -626,8 +629,11 @@ int gdn_layer_verify(const gdn_dims *dims, const gdn_layer_params *params, const
     // the verify reads q|k|v, z, alpha and beta_raw as column blocks of the activation matrix
     const long long C = conv_channels(dims), V = (long long)d.n_v_heads * d.d_v;
     unsigned char *z = act + C * 2, *alpha = act + (C + V) * 2, *beta = alpha + size_t(d.n_v_heads) * 2;
+    // the verify also warms L2 with the output projection's weights (read by the next launch)
+    const size_t w_out_bytes = size_t(w->n_embd) * size_t(V) * 2;
     if ((rc = verify_impl(dims, params, act, z, alpha, beta, nullptr, state, conv_state, cap_state, cap_conv, out,
-                          d_status, stream, gdn::kChain, nullptr, nullptr, nullptr, nullptr, ld)))
+                          d_status, stream, gdn::kChain, nullptr, nullptr, nullptr, nullptr, ld, w->w_out,
+                          reinterpret_cast<uintptr_t>(w->w_out) % 16 ? 0 : w_out_bytes & ~size_t(15))))
         return rc;
     return project_out(dims, w, out, y, d_status, stream);
 }

@@ -42,6 +42,10 @@ struct VerifyArgs {
                                       // previous batch's rollback folded into a verify
     const void *qkv_prev, *alpha_prev, *beta_prev;   // lazy verify: the pending batch (same layouts)
     int mode;                         // VerifyMode
+    // optional: a region the next kernel in the stream streams (the layer call's output-projection
+    // weights), brought into L2 by bulk prefetches once each CTA's own loads have landed (NULL: none)
+    const void *l2_next;
+    size_t l2_next_bytes;
     // buffer extents in bytes, for the bounds checks of a checked build
     size_t ext_qkv, ext_z, ext_ab, ext_state, ext_conv_state, ext_cap_state, ext_cap_conv, ext_out;
     size_t ext_conv_w, ext_head, ext_norm_w, ext_parent, ext_trim;

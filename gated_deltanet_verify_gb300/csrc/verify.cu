@@ -544,6 +544,18 @@ __global__ void __launch_bounds__(kMaxThreads, MINB) verify_kernel(const __grid_
     cp_async_wait_all();
     mbar_wait_cta(loadbar, 0, a.d_status);      // the batch's activation boxes
     __syncthreads();
+    if (a.l2_next && tid == 0) {
+        // this CTA's share of the region the next launch streams, into L2 while this launch runs (bulk
+        // prefetches return nothing to the SM and are not waited for); 16-byte aligned shares of <= 64 KB
+        const size_t n_cta = size_t(gridDim.x) * gridDim.y, idx = size_t(blockIdx.y) * gridDim.x + blockIdx.x;
+        const size_t share = ((a.l2_next_bytes + n_cta - 1) / n_cta + 15) & ~size_t(15);
+        const size_t beg = idx * share, end = beg + share < a.l2_next_bytes ? beg + share : a.l2_next_bytes;
+        const char *base = static_cast<const char *>(a.l2_next);
+        for (size_t o = beg; o < end; o += 65536) {
+            const uint32_t n = uint32_t(end - o < 65536 ? end - o : 65536);
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(base + o), "r"(n) : "memory");
+        }
+    }
     // cluster phase 1: this CTA has read the old conv state (the copies above have
     // landed) and initialised its mbarrier (published by fence.mbarrier_init)
     cluster_arrive_relaxed();
