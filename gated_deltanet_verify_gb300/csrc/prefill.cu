@@ -77,6 +77,7 @@ constexpr uint32_t kTmemSlot = kMisc + 16;     // 4 B
 constexpr uint32_t kFlagOk = kMisc + 20;       // 4 B: result of a ring-flag wait, broadcast to the CTA
 constexpr uint32_t kZBar = kMisc + 24;         // 8 B: gate (z) tile copy
 constexpr uint32_t kItem = kMisc + 32;         // 4 B: work item claimed by a preparation CTA, broadcast
+constexpr uint32_t kMbar2 = kMisc + 40;        // 8 B: tensor-core completion of the second issuing thread
 constexpr uint32_t kLogG = kMisc + 48;         // 64 floats each
 constexpr uint32_t kBeta = kLogG + 256;
 constexpr uint32_t kGam = kBeta + 256;
@@ -369,7 +370,7 @@ __device__ __forceinline__ Ring ring_of(const PrefillArgs &a, int s, int h) {
 struct Ctx {
     unsigned char *sm;
     int tid, lane, wid, tl, half;
-    uint32_t tmem, tq, mbar, phase;
+    uint32_t tmem, tq, mbar, phase, mbar2, phase2;
     bool timed_out;
 
     __device__ __forceinline__ void commit_wait() {
@@ -378,6 +379,20 @@ struct Ctx {
         for (int it = 0; it < kSpinLimit && !ok; ++it) ok = mbar_try(mbar, phase & 1u);
         if (!ok) timed_out = true;
         phase ^= 1u;
+        fence_after_sync();
+    }
+    // two independent products issued by two threads (0 and 32): one MMA-issuing thread paces its MMAs
+    // ~150-200 cycles apart whatever their size (measured), so two threads finish two products in about
+    // the time of one
+    __device__ __forceinline__ void commit_wait2() {
+        if (tid == 0) mma_commit(mbar);
+        if (tid == 32) mma_commit(mbar2);
+        bool ok = timed_out, ok2 = timed_out;
+        for (int it = 0; it < kSpinLimit && !ok; ++it) ok = mbar_try(mbar, phase & 1u);
+        for (int it = 0; it < kSpinLimit && !ok2; ++it) ok2 = mbar_try(mbar2, phase2 & 1u);
+        if (!ok || !ok2) timed_out = true;
+        phase ^= 1u;
+        phase2 ^= 1u;
         fence_after_sync();
     }
     __device__ __forceinline__ void publish() {      // generic smem writes -> visible to the tensor core
@@ -802,11 +817,9 @@ __device__ __forceinline__ void prepare(const PrefillArgs &a, Ctx &x) {
             }
             if (wid >= 6) build_a12();
             x.publish();
-            if (tid == 0) {
-                mma3(tmem + kColWT, sRA, sRA + 32 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
-                mma3(tmem + kColUT, sRA + 64 * 1024, sRA + 96 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
-            }
-            x.commit_wait();
+            if (tid == 0) mma3(tmem + kColWT, sRA, sRA + 32 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
+            else if (tid == 32) mma3(tmem + kColUT, sRA + 64 * 1024, sRA + 96 * 1024, sRB, sRB + 16 * 1024, 64, 64, false);
+            x.commit_wait2();
 
             // the A region is free: fetch the next tile (next head's v, or the next chunk's q, k) and gates
             if (hi + 1 < R) {
@@ -983,10 +996,8 @@ __device__ __forceinline__ void advance_state(const PrefillArgs &a, Ctx &x, int 
         if (tid == 0) st_release(ring.empty + slot, c + 1);     // the slot's bytes are all on chip
         x.publish();
         // O2^T = U^T P^T (its own accumulator);  D2 = U^T (diag(Gamma_C / Gamma) K)
-        if (tid == 0) {
-            mma3_ts(tmem + kSO2, tmem + kSX, tmem + kSUlo, sRB, sRB + 16 * 1024, 64, 64, false);
-            mma3_ts(tmem + kSShi, tmem + kSX, tmem + kSUlo, sRA, sRA + 32 * 1024, 64, 128, false);
-        }
+        if (tid == 0) mma3_ts(tmem + kSO2, tmem + kSX, tmem + kSUlo, sRB, sRB + 16 * 1024, 64, 64, false);
+        else if (tid == 32) mma3_ts(tmem + kSShi, tmem + kSX, tmem + kSUlo, sRA, sRA + 32 * 1024, 64, 128, false);
         float zg[32];
         if constexpr (sizeof(Act) == 2) {
             x.wait_bar(zbar, z_phase);
@@ -1000,7 +1011,7 @@ __device__ __forceinline__ void advance_state(const PrefillArgs &a, Ctx &x, int 
                 zg[q] = t < n ? to_f32(z[((size_t)s * L + t0 + t) * Hv * kD + (size_t)h * kD + tl]) : 0.f;
             }
         }
-        x.commit_wait();
+        x.commit_wait2();
 
         // ---------------- outputs (gated RMSNorm) and the state update
         {
@@ -1073,6 +1084,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     x.tid = threadIdx.x; x.lane = x.tid & 31; x.wid = x.tid >> 5;
     x.tl = x.tid & 127; x.half = x.tid >> 7;           // TMEM lane of this thread, column half
     x.phase = 0;
+    x.phase2 = 0;
     x.timed_out = false;
     const int n_prep = a.n_prep;
     const bool prep = (int)blockIdx.x < n_prep;
@@ -1085,8 +1097,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
     x.mbar = smem_u32(sm + kMbar);
+    x.mbar2 = smem_u32(sm + kMbar2);
     if (x.tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(x.mbar));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(x.mbar2));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(sm + kRawBar)));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(sm + kZBar)));
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
