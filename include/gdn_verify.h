@@ -315,7 +315,8 @@ int gdn_project_out(const gdn_dims *dims, const gdn_proj_weights *w, const void 
  * back with gdn_rollback as usual.  workspace: gdn_layer_workspace_bytes,
  * 256-byte aligned; the activation matrix sits at its start (row stride
  * gdn_proj_in_ld) and the block's output [B*T][H_v*d_v] right after it (at
- * the next 256-byte boundary).
+ * the next 256-byte boundary).  While it runs, the verify also brings
+ * w_out into L2 (bulk prefetches; nothing is written) for the output GEMM.
  */
 int gdn_layer_verify(const gdn_dims *dims, const gdn_layer_params *params, const gdn_proj_weights *w,
                      const void *x, float *state, float *conv_state, float *cap_state, float *cap_conv,
