@@ -180,6 +180,10 @@ def test_project_calls_alone():
     dict(n_slots=3, n_tokens=7, n_embd=200),                 # ragged M (21), K not a multiple of 64
     dict(n_slots=20, n_tokens=15, n_embd=136),               # 300 rows: two blocks of activation rows
     dict(n_slots=1, n_tokens=16, n_qk_heads=16, n_v_heads=48, d_k=128, d_v=128, n_embd=1024),   # split K on out
+    # two K blocks split two ways: every split holds one stage, so only the even stages' MMA thread has work
+    dict(n_slots=2, n_tokens=8, n_qk_heads=2, n_v_heads=8, d_k=32, d_v=32, n_embd=256),
+    # 256 activation rows in one block: both accumulators fill the 512 tensor-memory columns
+    dict(n_slots=16, n_tokens=16, n_embd=128),
 ])
 def test_projection_gemm_shapes(kw):
     # both projections on their own against the fp64 product, over the tilings the GEMM kernel uses: weight
