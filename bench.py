@@ -817,12 +817,13 @@ def describe(shape) -> str:
 
 # steps a per-config entry times at least (about 10 ms of device work or more)
 MIN_STEPS = {"layer_verify": 1000, "multislot_verify": 64, "prefill": 20, "proj_verify": 500, "tree_verify": 1000,
-             "rolled_verify": 1000}
+             "rolled_verify": 1000, "lazy_verify": 1000}
 HEADLINE = "stack_verify"                                   # 48 layers x 8 slots: the largest configuration
 # one layer at one slot, 32 slots, the 8192-token prefill, the layer with its projections around the block
-# (hidden 5120, the library's GEMM), and at one slot the draft-tree verify and the verify with the previous
-# step's rollback folded in
-PER_CONFIG = ("layer_verify", "multislot_verify", "prefill", "proj_verify", "tree_verify", "rolled_verify")
+# (hidden 5120, the library's GEMM), and at one slot the draft-tree verify, the verify with the previous
+# step's rollback folded in, and the lazy-capture verify
+PER_CONFIG = ("layer_verify", "multislot_verify", "prefill", "proj_verify", "tree_verify", "rolled_verify",
+              "lazy_verify")
 
 
 def measure(name, steps, warmup, device, world, l2, clocks, with_e2e, graph_len_max=64):
